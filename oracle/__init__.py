@@ -1,0 +1,165 @@
+"""Plain CPU oracle of the tile-binned 2-D splat rasterizer.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the bench's CPU
+baseline leg use it; the product package never imports it.  The C source
+(oracle.c, raster.inc) shares no code with the CUDA path.
+
+Parity status: binning, forward and backward are pinned by
+tests/test_oracle_pins.py (closed forms, brute force, the pages' printed
+constants and pass counts, finite differences).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = [os.path.join(_HERE, "oracle.c"), os.path.join(_HERE, "raster.inc"),
+        os.path.join(_HERE, "oracle.h")]
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-Wall", "-Wextra",
+          "-shared", "-fPIC"]
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (plain C, no GPU)."""
+    newest = max(os.path.getmtime(p) for p in _SRC)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
+        os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, os.path.join(_HERE, "oracle.c"), "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    P = ctypes.c_void_p
+    i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    lib.orc_tile_rect.argtypes = [P, ctypes.c_float, i32, i32, P]
+    lib.orc_tile_rect.restype = ctypes.c_int
+    lib.orc_count_pairs.argtypes = [P, P, i32, i32, i32]
+    lib.orc_count_pairs.restype = i64
+    lib.orc_bin.argtypes = [P, P, i32, i32, i32, P, P, P, i64]
+    lib.orc_bin.restype = i64
+    lib.orc_radix_passes_4bit.argtypes = [ctypes.c_uint64]
+    lib.orc_radix_passes_4bit.restype = i32
+    for sfx in ("f32", "f64"):
+        fw = getattr(lib, f"orc_forward_{sfx}")
+        fw.argtypes = [P, P, P, i32, i32, P, P, P, P, f64, P]
+        fw.restype = None
+        bw = getattr(lib, f"orc_backward_{sfx}")
+        bw.argtypes = [P, i32, P, P, i32, i32, P, P, P, f64, P]
+        bw.restype = None
+    for name in ("orc_forward_untiled_f32", "orc_forward_untiled_noskip_f32"):
+        fn = getattr(lib, name)
+        fn.argtypes = [P, P, i32, i32, i32, P, P, P]
+        fn.restype = None
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def tiles(width: int, height: int):
+    return (width + 15) // 16, (height + 15) // 16
+
+
+def tile_rect(splat, depth, width, height):
+    lib = _load()
+    s = _f32(splat).reshape(9)
+    r = np.zeros(4, dtype=np.int32)
+    tx, ty = tiles(width, height)
+    ok = lib.orc_tile_rect(_ptr(s), ctypes.c_float(depth), tx, ty, _ptr(r))
+    return tuple(int(v) for v in r) if ok else None
+
+
+def count_pairs(splats, depths, width, height) -> int:
+    lib = _load()
+    s, d = _f32(splats).reshape(-1, 9), _f32(depths).reshape(-1)
+    return int(lib.orc_count_pairs(_ptr(s), _ptr(d), s.shape[0], width, height))
+
+
+def bin_splats(splats, depths, width, height):
+    """Returns (keys u64[P], idx u32[P], ranges u32[T, 2])."""
+    lib = _load()
+    s, d = _f32(splats).reshape(-1, 9), _f32(depths).reshape(-1)
+    p = count_pairs(s, d, width, height)
+    tx, ty = tiles(width, height)
+    keys = np.zeros(max(p, 1), dtype=np.uint64)
+    idx = np.zeros(max(p, 1), dtype=np.uint32)
+    ranges = np.zeros((tx * ty, 2), dtype=np.uint32)
+    got = lib.orc_bin(_ptr(s), _ptr(d), s.shape[0], width, height, _ptr(keys), _ptr(idx),
+                      _ptr(ranges), p)
+    assert got == p
+    return keys[:p], idx[:p], ranges
+
+
+def radix_passes_4bit(num_tiles: int) -> int:
+    return int(_load().orc_radix_passes_4bit(num_tiles))
+
+
+def forward(splats, idx, ranges, width, height, *, f64=False, eps_alpha=0.0):
+    """Tiled forward.  Returns dict(out [H*W,4], final_T, last, margin, counters)."""
+    lib = _load()
+    dt = np.float64 if f64 else np.float32
+    s = np.ascontiguousarray(splats, dtype=dt).reshape(-1, 9)
+    ix = np.ascontiguousarray(idx, dtype=np.uint32)
+    rg = np.ascontiguousarray(ranges, dtype=np.uint32)
+    npx = width * height
+    out = np.zeros((npx, 4), dtype=dt)
+    final_t = np.zeros(npx, dtype=dt)
+    last = np.zeros(npx, dtype=np.uint32)
+    margin = np.zeros(npx, dtype=np.float32)
+    cnt = np.zeros(3, dtype=np.int64)
+    fn = lib.orc_forward_f64 if f64 else lib.orc_forward_f32
+    fn(_ptr(s), _ptr(ix), _ptr(rg), width, height, _ptr(out), _ptr(final_t), _ptr(last),
+       _ptr(margin), float(eps_alpha), _ptr(cnt))
+    return {"out": out, "final_T": final_t, "last": last, "margin": margin,
+            "counters": {"n_eval": int(cnt[0]), "n_exp": int(cnt[1]), "n_contrib": int(cnt[2])}}
+
+
+def forward_untiled(splats, depths, width, height, *, sigma_skip=True):
+    lib = _load()
+    s, d = _f32(splats).reshape(-1, 9), _f32(depths).reshape(-1)
+    npx = width * height
+    out = np.zeros((npx, 4), dtype=np.float32)
+    final_t = np.zeros(npx, dtype=np.float32)
+    last = np.zeros(npx, dtype=np.uint32)
+    fn = lib.orc_forward_untiled_f32 if sigma_skip else lib.orc_forward_untiled_noskip_f32
+    fn(_ptr(s), _ptr(d), s.shape[0], width, height, _ptr(out), _ptr(final_t), _ptr(last))
+    return {"out": out, "final_T": final_t, "last": last}
+
+
+def backward(splats, idx, ranges, width, height, dl_dout, *, f64=False, eps_alpha=0.0):
+    """Returns dict(grad float64 [N,9], knife bool [N], counters)."""
+    lib = _load()
+    dt = np.float64 if f64 else np.float32
+    s = np.ascontiguousarray(splats, dtype=dt).reshape(-1, 9)
+    ix = np.ascontiguousarray(idx, dtype=np.uint32)
+    rg = np.ascontiguousarray(ranges, dtype=np.uint32)
+    g = np.ascontiguousarray(dl_dout, dtype=dt).reshape(-1, 4)
+    n = s.shape[0]
+    grad = np.zeros((n, 9), dtype=np.float64)
+    knife = np.zeros(n, dtype=np.uint8)
+    cnt = np.zeros(3, dtype=np.int64)
+    fn = lib.orc_backward_f64 if f64 else lib.orc_backward_f32
+    fn(_ptr(s), n, _ptr(ix), _ptr(rg), width, height, _ptr(g), _ptr(grad), _ptr(knife),
+       float(eps_alpha), _ptr(cnt))
+    return {"grad": grad, "knife": knife.astype(bool),
+            "counters": {"n_eval": int(cnt[0]), "n_exp": int(cnt[1]), "n_contrib": int(cnt[2])}}

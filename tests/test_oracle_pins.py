@@ -1,0 +1,400 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test ties one oracle function to a value the pages print, a closed form,
+a brute-force or library route, or finite differences, chosen so that a
+dropped term, a wrong sign or index, or a transposed operand fails at least
+one of them.  No GPU is used here.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from conftest import read_page_constants
+
+f32 = np.float32
+
+
+def iso(x, y, std, rgb=(0.2, 0.5, 0.8), o=0.5):
+    """A round splat: conic a = c = 1/std^2, b = 0."""
+    a = 1.0 / (std * std)
+    return [x, y, a, 0.0, a, rgb[0], rgb[1], rgb[2], o]
+
+
+def arr(rows):
+    return np.asarray(rows, dtype=np.float32).reshape(-1, 9)
+
+
+# --------------------------------------------------------------------------
+# Printed constants and formulas
+# --------------------------------------------------------------------------
+
+def test_page_constants_and_exp_skip_identity():
+    rows = {(n, arg): v for n, v, arg in read_page_constants()}
+    # The pages print exp(-5.55) ~ 0.003887 < 1/255 ~ 0.003922 as the reason the
+    # sigma >= 5.55 skip can never change a result.
+    assert math.exp(-5.55) == pytest.approx(rows[("exp_neg_5_55", None)], abs=5e-7)
+    assert 1.0 / 255.0 == pytest.approx(rows[("inv_255", None)], abs=5e-7)
+    e = np.exp(-np.float32(5.55), dtype=np.float32)
+    assert e < np.float32(1.0) / np.float32(255.0)
+    # Any color_a <= 1 at sigma >= 5.55 gives alpha below the 1/255 cut.
+    assert np.float32(1.0) * e < np.float32(1.0) / np.float32(255.0)
+    assert rows[("alpha_cap", None)] == 0.999
+
+
+def test_radix_pass_count_formula():
+    rows = [(v, arg) for n, v, arg in read_page_constants() if n == "radix_passes_4bit"]
+    assert len(rows) == 3
+    for passes, tiles in rows:
+        assert oracle.radix_passes_4bit(int(tiles)) == int(passes)
+
+
+def test_record_and_output_sizes():
+    rows = {(n, arg): v for n, v, arg in read_page_constants()}
+    assert len(gen.SPLAT_FIELDS) * 4 == rows[("splat2d_bytes", None)]
+    assert 256 * len(gen.SPLAT_FIELDS) * 4 == rows[("local_batch_bytes", 256.0)]
+    # out float4 + final_T f32 + last_contrib u32, as the oracle returns them.
+    w = gen.tiny()
+    _, idx, ranges = oracle.bin_splats(w.splats, w.depths, w.width, w.height)
+    r = oracle.forward(w.splats, idx, ranges, w.width, w.height)
+    per_px = r["out"].itemsize * r["out"].shape[1] + r["final_T"].itemsize + r["last"].itemsize
+    assert per_px == rows[("output_bytes_px", None)]
+    assert per_px * 640000 == rows[("output_bytes_frame", 640000.0)]
+
+
+# --------------------------------------------------------------------------
+# Tile rectangle
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("x,y,std,expect", [
+    (40.0, 40.0, 2.0, (2, 2, 2, 2)),       # box [34,46]^2 inside tile 2
+    (30.0, 17.0, 2.0, (1, 0, 2, 1)),       # x [24,36] -> 1..2, y [11,23] -> 0..1
+    (-3.0, 10.0, 2.0, (0, 0, 0, 1)),       # x [-9,3] clamps to tile 0; y [4,16] -> 0..1
+    (69.9, 10.0, 2.0, (3, 0, 3, 1)),       # x [63.9,75.9]: starts in the last tile
+    (70.0, 10.0, 2.0, None),               # x [64,76]: right of the image
+    (-20.0, 10.0, 2.0, None),              # x [-26,-14]: left of the image
+    (32.0, 32.0, 100.0, (0, 0, 3, 3)),     # covers everything
+])
+def test_tile_rect_closed_form(x, y, std, expect):
+    assert oracle.tile_rect(iso(x, y, std), 1.0, 64, 64) == expect
+
+
+def test_tile_rect_anisotropic_closed_form():
+    # Axis-aligned ellipse with std 1 along x and 10 along y: Sigma = diag(1, 100),
+    # conic = diag(1, 0.01); box half-extents 3 and 30.
+    s = [40.0, 40.0, 1.0, 0.0, 0.01, 0.1, 0.1, 0.1, 0.5]
+    assert oracle.tile_rect(s, 2.0, 64, 64) == (2, 0, 2, 3)  # x [37,43], y [10,70]
+    # Rotated 90 degrees: std 10 along x.
+    s = [40.0, 40.0, 0.01, 0.0, 1.0, 0.1, 0.1, 0.1, 0.5]
+    assert oracle.tile_rect(s, 2.0, 64, 64) == (0, 2, 3, 2)
+
+
+@pytest.mark.parametrize("splat,depth", [
+    ([10.0, 10.0, 1.0, 1.0, 1.0, 0.5, 0.5, 0.5, 0.5], 1.0),       # det = 0
+    ([10.0, 10.0, -1.0, 0.0, -1.0, 0.5, 0.5, 0.5, 0.5], 1.0),     # negative definite
+    ([10.0, 10.0, 1.0, 2.0, 1.0, 0.5, 0.5, 0.5, 0.5], 1.0),       # indefinite
+    ([10.0, 10.0, 1.0, 0.0, 1.0, 0.5, 0.5, 0.5, 0.5], 0.0),       # depth 0
+    ([10.0, 10.0, 1.0, 0.0, 1.0, 0.5, 0.5, 0.5, 0.5], -2.0),      # depth < 0
+    ([10.0, 10.0, 1.0, 0.0, 1.0, 0.5, 0.5, 0.5, 0.5], float("nan")),
+    ([float("inf"), 10.0, 1.0, 0.0, 1.0, 0.5, 0.5, 0.5, 0.5], 1.0),
+    ([10.0, 10.0, 1.0, 0.0, 1.0, float("nan"), 0.5, 0.5, 0.5], 1.0),
+])
+def test_tile_rect_culls(splat, depth):
+    assert oracle.tile_rect(splat, depth, 64, 64) is None
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_tile_rect_against_double_precision_route(name):
+    """The same box from numpy's float64 matrix inverse of the conic."""
+    w = gen.make(name)
+    tx, ty = oracle.tiles(w.width, w.height)
+    boundary_cases = 0
+    for i in range(w.n):
+        s = w.splats[i].astype(np.float64)
+        cov = np.linalg.inv(np.array([[s[2], s[3]], [s[3], s[4]]]))
+        rx, ry = 3.0 * math.sqrt(cov[0, 0]), 3.0 * math.sqrt(cov[1, 1])
+        lo = np.array([s[0] - rx, s[1] - ry]) / 16.0
+        hi = np.array([s[0] + rx, s[1] + ry]) / 16.0
+        r = (max(0, math.floor(lo[0])), max(0, math.floor(lo[1])),
+             min(tx - 1, math.floor(hi[0])), min(ty - 1, math.floor(hi[1])))
+        want = r if (r[0] <= r[2] and r[1] <= r[3]) else None
+        got = oracle.tile_rect(w.splats[i], w.depths[i], w.width, w.height)
+        if got != want:
+            # Only a box edge within float rounding of a tile boundary may differ.
+            edges = np.concatenate([lo, hi]) * 16.0
+            dist = np.min(np.abs(edges - 16.0 * np.round(edges / 16.0)))
+            assert dist < 1e-3 * max(1.0, np.max(np.abs(edges))), (i, got, want)
+            boundary_cases += 1
+    assert boundary_cases <= 2
+
+
+# --------------------------------------------------------------------------
+# Binning: emission + sort + ranges against numpy's lexsort
+# --------------------------------------------------------------------------
+
+def _numpy_binning(splats, depths, width, height):
+    tx, ty = oracle.tiles(width, height)
+    keys, idx = [], []
+    for i in range(splats.shape[0]):
+        r = oracle.tile_rect(splats[i], depths[i], width, height)
+        if r is None:
+            continue
+        dbits = int(np.asarray(depths[i], dtype=np.float32).view(np.uint32))
+        for y in range(r[1], r[3] + 1):
+            for x in range(r[0], r[2] + 1):
+                keys.append(((y * tx + x) << 32) | dbits)
+                idx.append(i)
+    keys = np.asarray(keys, dtype=np.uint64)
+    idx = np.asarray(idx, dtype=np.uint32)
+    order = np.lexsort((idx, keys))
+    keys, idx = keys[order], idx[order]
+    tile = (keys >> np.uint64(32)).astype(np.int64)
+    ranges = np.zeros((tx * ty, 2), dtype=np.uint32)
+    t_all = np.arange(tx * ty)
+    starts = np.searchsorted(tile, t_all, side="left")
+    ends = np.searchsorted(tile, t_all, side="right")
+    nz = ends > starts
+    ranges[nz, 0], ranges[nz, 1] = starts[nz], ends[nz]
+    return keys, idx, ranges
+
+
+def _random_splats(n, width, height, seed, depth_levels=None):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    s = np.zeros((n, 9), dtype=np.float32)
+    s[:, 0] = rng.uniform(-10, width + 10, n)
+    s[:, 1] = rng.uniform(-10, height + 10, n)
+    std = rng.uniform(0.5, 12.0, n)
+    s[:, 2] = 1.0 / std ** 2
+    s[:, 3] = rng.uniform(-0.3, 0.3, n) / std ** 2
+    s[:, 4] = 1.0 / std ** 2
+    s[:, 5:8] = rng.uniform(0, 1, (n, 3))
+    s[:, 8] = rng.uniform(0, 1, n)
+    if depth_levels:
+        d = rng.integers(1, depth_levels + 1, n).astype(np.float32)
+    else:
+        d = rng.uniform(0.5, 20.0, n).astype(np.float32)
+    return s, d
+
+
+@pytest.mark.parametrize("n,seed,levels", [(0, 0, None), (1, 1, None), (255, 2, None),
+                                           (256, 3, None), (257, 4, None), (1234, 5, None),
+                                           (5000, 6, 8)])
+def test_binning_matches_lexsort(n, seed, levels):
+    s, d = _random_splats(n, 100, 70, seed, levels)
+    k, i, r = oracle.bin_splats(s, d, 100, 70)
+    k2, i2, r2 = _numpy_binning(s, d, 100, 70)
+    assert np.array_equal(k, k2)
+    assert np.array_equal(i, i2)
+    assert np.array_equal(r, r2)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_binning_invariants(name):
+    w = gen.make(name)
+    k, i, r = oracle.bin_splats(w.splats, w.depths, w.width, w.height)
+    k2, i2, r2 = _numpy_binning(w.splats, w.depths, w.width, w.height)
+    assert np.array_equal(k, k2) and np.array_equal(i, i2) and np.array_equal(r, r2)
+    assert np.all(np.diff(k.astype(np.float64)) >= 0)
+    # ranges partition [0, P) in tile order
+    nz = r[:, 1] > r[:, 0]
+    assert r[nz, 1].max() == len(k) and (r[nz, 1] - r[nz, 0]).sum() == len(k)
+
+
+# --------------------------------------------------------------------------
+# Forward: closed forms
+# --------------------------------------------------------------------------
+
+def _fwd(splats, depths, width=32, height=32, f64=False):
+    s = arr(splats)
+    d = np.asarray(depths, dtype=np.float32)
+    _, idx, ranges = oracle.bin_splats(s, d, width, height)
+    return oracle.forward(s, idx, ranges, width, height, f64=f64), s
+
+
+def test_forward_single_splat_at_mean():
+    r, _ = _fwd([iso(10.0, 12.0, 3.0, (0.25, 0.5, 0.75), 0.5)], [1.0])
+    p = 12 * 32 + 10
+    assert r["out"][p].tolist() == [0.125, 0.25, 0.375, 0.5]
+    assert r["final_T"][p] == 0.5 and r["last"][p] == 1
+
+
+def test_forward_single_splat_offset_closed_form():
+    # sigma = 1/2 (a dx^2 + c dy^2) + b dx dy with a = 0.5, b = 0.1, c = 0.25
+    s = [10.0, 12.0, 0.5, 0.1, 0.25, 0.25, 0.5, 0.75, 0.8]
+    r, _ = _fwd([s], [1.0])
+    for px, py in [(11, 12), (12, 13), (8, 10), (10, 15)]:
+        dx, dy = px - 10.0, py - 12.0
+        sig = 0.5 * (0.5 * dx * dx + 0.25 * dy * dy) + 0.1 * dx * dy
+        alpha = min(0.999, 0.8 * math.exp(-sig))
+        p = py * 32 + px
+        if alpha < 1.0 / 255.0:
+            assert r["last"][p] == 0 and r["final_T"][p] == 1.0
+        else:
+            assert r["final_T"][p] == pytest.approx(1.0 - alpha, abs=1e-6)
+            assert r["out"][p][:3] == pytest.approx([0.25 * alpha, 0.5 * alpha, 0.75 * alpha], abs=1e-6)
+
+
+def test_forward_two_splats_depth_order():
+    # Index 0 is behind (depth 5), index 1 in front (depth 1).
+    back = iso(16.0, 16.0, 4.0, (1.0, 0.0, 0.0), 0.6)
+    front = iso(16.0, 16.0, 4.0, (0.0, 0.0, 1.0), 0.3)
+    r, _ = _fwd([back, front], [5.0, 1.0])
+    p = 16 * 32 + 16
+    a1, a2 = 0.3, 0.6
+    assert r["out"][p][:3] == pytest.approx([a2 * (1 - a1), 0.0, a1], abs=1e-7)
+    assert r["final_T"][p] == pytest.approx((1 - a1) * (1 - a2), abs=1e-7)
+    assert r["last"][p] == 2
+
+
+def test_forward_termination_rule():
+    # Two opaque splats: alpha = 0.999 -> T = 1e-3; the second would give
+    # T = 1e-6 < 1e-4, so it is not composited and the pixel stops.
+    a = iso(16.0, 16.0, 4.0, (0.5, 0.25, 1.0), 1.0)
+    b = iso(16.0, 16.0, 4.0, (1.0, 1.0, 1.0), 1.0)
+    r, _ = _fwd([a, b], [1.0, 2.0])
+    p = 16 * 32 + 16
+    c = f32(0.999)
+    assert r["out"][p][:3].tolist() == [f32(0.5) * c, f32(0.25) * c, f32(1.0) * c]
+    assert r["final_T"][p] == f32(1.0) - c
+    assert r["last"][p] == 1
+
+
+def test_forward_alpha_cut():
+    # color_a just under / over 1/255 at the splat's centre.
+    lo = iso(16.0, 16.0, 4.0, (1, 1, 1), float(np.nextafter(f32(1 / 255), f32(0))))
+    hi = iso(16.0, 16.0, 4.0, (1, 1, 1), float(f32(1.0) / f32(255.0)))
+    p = 16 * 32 + 16
+    r, _ = _fwd([lo], [1.0])
+    assert r["last"][p] == 0 and r["final_T"][p] == 1.0
+    r, _ = _fwd([hi], [1.0])
+    assert r["last"][p] == 1 and r["final_T"][p] < 1.0
+
+
+def test_forward_empty_and_off_image():
+    r, _ = _fwd([iso(-100.0, 5.0, 2.0)], [1.0])
+    assert np.all(r["out"] == 0) and np.all(r["final_T"] == 1) and np.all(r["last"] == 0)
+    r = oracle.forward(np.zeros((0, 9), np.float32), np.zeros(0, np.uint32),
+                       np.zeros((4, 2), np.uint32), 32, 32)
+    assert np.all(r["final_T"] == 1)
+
+
+# --------------------------------------------------------------------------
+# Forward: brute force and the exp-skip identity
+# --------------------------------------------------------------------------
+
+def _fixtures():
+    return [gen.tiny(), gen.small(), gen.overlap_fixture(32), gen.overlap_fixture(24)]
+
+
+@pytest.mark.parametrize("wi", range(4))
+def test_tiled_equals_untiled_bit_exact(wi):
+    w = _fixtures()[wi]
+    _, idx, ranges = oracle.bin_splats(w.splats, w.depths, w.width, w.height)
+    t = oracle.forward(w.splats, idx, ranges, w.width, w.height)
+    u = oracle.forward_untiled(w.splats, w.depths, w.width, w.height)
+    for key in ("out", "final_T", "last"):
+        assert np.array_equal(t[key], u[key]), key
+
+
+@pytest.mark.parametrize("wi", range(4))
+def test_sigma_skip_changes_nothing(wi):
+    """The pages' W1b argument: with color_a <= 1 the sigma >= 5.55 skip only
+    drops evaluations the alpha < 1/255 test drops anyway."""
+    w = _fixtures()[wi]
+    a = oracle.forward_untiled(w.splats, w.depths, w.width, w.height, sigma_skip=True)
+    b = oracle.forward_untiled(w.splats, w.depths, w.width, w.height, sigma_skip=False)
+    for key in ("out", "final_T", "last"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_f32_forward_agrees_with_f64_instantiation():
+    w = gen.small()
+    _, idx, ranges = oracle.bin_splats(w.splats, w.depths, w.width, w.height)
+    a = oracle.forward(w.splats, idx, ranges, w.width, w.height, eps_alpha=1e-6)
+    b = oracle.forward(w.splats, idx, ranges, w.width, w.height, f64=True)
+    ok = a["margin"] >= 1.0
+    assert ok.mean() > 0.999
+    assert np.max(np.abs(a["out"][ok] - b["out"][ok])) < 1e-5
+    assert np.array_equal(a["last"][ok], b["last"][ok])
+
+
+# --------------------------------------------------------------------------
+# Backward: finite differences of the double forward
+# --------------------------------------------------------------------------
+
+def _loss(splats64, idx, ranges, w, h, g):
+    r = oracle.forward(splats64, idx, ranges, w, h, f64=True)
+    return float(np.sum(r["out"][:, :3] * g[:, :3])), r["last"]
+
+
+def _fd_check(wl, splat_ids, rel_tol=2e-4):
+    s32 = wl.splats
+    _, idx, ranges = oracle.bin_splats(s32, wl.depths, wl.width, wl.height)
+    s64 = s32.astype(np.float64)
+    g = wl.dl_dout.astype(np.float64)
+    bw = oracle.backward(s64, idx, ranges, wl.width, wl.height, g, f64=True, eps_alpha=1e-7)
+    grad, knife = bw["grad"], bw["knife"]
+    checked = 0
+    for j in splat_ids:
+        if knife[j]:
+            continue
+        for k in range(9):
+            base = s64[j, k]
+            h = 1e-6 * max(abs(base), 1e-2) if k in (2, 3, 4) else 1e-5
+            sp = s64.copy()
+            sp[j, k] = base + h
+            lp, last_p = _loss(sp, idx, ranges, wl.width, wl.height, g)
+            sp[j, k] = base - h
+            lm, last_m = _loss(sp, idx, ranges, wl.width, wl.height, g)
+            if not np.array_equal(last_p, last_m):
+                continue  # the perturbation crosses a threshold: not differentiable there
+            fd = (lp - lm) / (2 * h)
+            scale = max(abs(fd), abs(grad[j, k]), 1e-3)
+            assert abs(fd - grad[j, k]) <= rel_tol * scale, (j, k, fd, grad[j, k])
+            checked += 1
+    return checked
+
+
+def test_backward_finite_differences_overlap32():
+    wl = gen.overlap_fixture(32)
+    assert _fd_check(wl, range(wl.n)) > 0.9 * wl.n * 9
+
+
+def test_backward_finite_differences_overlap24_oob():
+    wl = gen.overlap_fixture(24)
+    assert _fd_check(wl, range(wl.n)) > 0.9 * wl.n * 9
+
+
+def test_backward_finite_differences_tiny():
+    wl = gen.tiny()
+    ids = np.random.Generator(np.random.PCG64(11)).choice(wl.n, 24, replace=False)
+    assert _fd_check(wl, ids) > 0.8 * len(ids) * 9
+
+
+def test_backward_single_pixel_support():
+    """dL/dout nonzero at one pixel: only splats composited there get gradient."""
+    wl = gen.overlap_fixture(32)
+    _, idx, ranges = oracle.bin_splats(wl.splats, wl.depths, wl.width, wl.height)
+    g = np.zeros_like(wl.dl_dout)
+    p = 15 * 32 + 17
+    g[p, :3] = [0.3, -1.2, 0.7]
+    bw = oracle.backward(wl.splats, idx, ranges, wl.width, wl.height, g)
+    fw = oracle.forward(wl.splats, idx, ranges, wl.width, wl.height)
+    tile = (15 // 16) * 2 + 17 // 16
+    st = ranges[tile, 0]
+    seen = set(idx[st:st + fw["last"][p]].tolist())
+    nz = set(np.nonzero(np.any(bw["grad"] != 0, axis=1))[0].tolist())
+    assert nz <= seen and len(nz) > 0
+
+
+def test_f32_backward_agrees_with_f64_instantiation():
+    w = gen.small()
+    _, idx, ranges = oracle.bin_splats(w.splats, w.depths, w.width, w.height)
+    a = oracle.backward(w.splats, idx, ranges, w.width, w.height, w.dl_dout, eps_alpha=1e-6)
+    b = oracle.backward(w.splats, idx, ranges, w.width, w.height, w.dl_dout, f64=True)
+    ok = ~a["knife"]
+    assert ok.mean() > 0.8
+    d = np.abs(a["grad"][ok] - b["grad"][ok])
+    assert np.all(d <= 1e-4 + 1e-4 * np.abs(b["grad"][ok]))
