@@ -1,0 +1,433 @@
+"""Benchmark: bin + forward + backward per iteration on the 800x800, 409,660-splat
+Lego-shaped synthetic set (seed 3), one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--config NAME]
+
+GPU arm: inputs resident in HBM, warm arena, L2 flushed (256 MB write) between
+timed steps, each step bracketed by CUDA events on the launching stream, per
+stage (bin / forward / backward) events as well.  e2e: the same steps with the
+inputs copied from pinned host memory and the gradients and image copied back
+inside the timed region.  N > 1 (torchrun): independent replicas, one per
+GPU, the slowest rank's time counts.
+
+Reference arm (--impl reference): the CPU oracle, unchanged, on the host
+cores, on the same workload; each step bins the splats of one band of tile
+rows and runs the forward and backward there, and the step time is scaled to
+the full frame by pixel count; successive steps walk the bands.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+
+METRIC = "rasterize bin+fwd+bwd ms/iter @800×800, 409,660 splats; % of roofline"
+FLUSH_BYTES = 256 << 20
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+SFU_LANES_PER_SM = 16
+
+# Algorithmic FP32 operations per unit (the counts come from the oracle's counters).
+#   forward, per examined (pixel, splat): dx, dy, 5 for sigma, 2 range compares   = 9
+#            per sigma-in-range evaluation: exponent scale, o*e, min, alpha cut    = 4  (+1 SFU exp)
+#            per composited splat: 1-alpha, T(1-alpha), stop test, alpha*T, 3 FMA = 7
+#   backward, per replayed (pixel, splat) below last_contributor                  = 9
+#            per sigma-in-range evaluation                                          = 4  (+1 SFU exp)
+#            per composited splat: 1/(1-alpha) (+1 SFU), T_j, alpha T_j, 3 rgb grads,
+#            dL/dalpha (9), S update (3), clamp select, dL/dcolor_a, dL/dsigma,
+#            5 conic/mean grads (12), and the 9 additions that accumulate them   = 44
+FWD_OPS = {"n_eval": 9, "n_exp": 4, "n_contrib": 7}
+BWD_OPS = {"n_eval": 9, "n_exp": 4, "n_contrib": 44}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="gsr", choices=["gsr", "reference"])
+    p.add_argument("--config", default="lego_final", choices=sorted(gen.CONFIGS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max over ranks (a scalar timing exchange, not a data-path collective)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "sm_max_mhz": float(d.get("sm_max_mhz", 2070.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def workload_label(wl):
+    return f"{wl.name}: {wl.width}x{wl.height}, {wl.n:,} Splat2D, seed {wl.recipe.get('seed')}"
+
+
+# --------------------------------------------------------------------------
+# Clock sampling
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "sm_max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
+                             "hw_slowdown": parts[5], "hw_thermal": parts[6],
+                             "sw_thermal": parts[7], "sw_power_cap": parts[8]})
+            except ValueError:
+                continue
+        return rows
+
+    @staticmethod
+    def summarize(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r["power"] is None or r["power"] > 0] or rows
+        reasons = []
+        for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power_cap", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in loaded):
+                reasons.append(name)
+        return {"sm_mhz": float(np.median([r["sm"] for r in loaded])),
+                "sm_max_mhz": float(max(r["sm_max"] for r in loaded)),
+                "reasons": reasons, "samples": len(loaded)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle (the cpu_baseline leg and the reference arm)
+# --------------------------------------------------------------------------
+
+def cpu_baseline(wl):
+    """The oracle, as it stands, on the whole workload once: binning, forward,
+    backward.  Returns the timing and the oracle's evaluation counters."""
+    import oracle
+    t0 = time.perf_counter()
+    keys, idx, ranges = oracle.bin_splats(wl.splats, wl.depths, wl.width, wl.height)
+    t1 = time.perf_counter()
+    f = oracle.forward(wl.splats, idx, ranges, wl.width, wl.height)
+    t2 = time.perf_counter()
+    b = oracle.backward(wl.splats, idx, ranges, wl.width, wl.height, wl.dl_dout)
+    t3 = time.perf_counter()
+    return {"ms": (t3 - t0) * 1e3, "bin_ms": (t1 - t0) * 1e3, "fwd_ms": (t2 - t1) * 1e3,
+            "bwd_ms": (t3 - t2) * 1e3, "pairs": int(len(keys)),
+            "fwd_counters": f["counters"], "bwd_counters": b["counters"]}
+
+
+def band_workload(wl, band, bands):
+    """Tile-row band `band` of `bands` as its own image (means shifted up)."""
+    tiles_y = (wl.height + 15) // 16
+    per = (tiles_y + bands - 1) // bands
+    y0 = min(band * per, tiles_y) * 16
+    y1 = min((band + 1) * per * 16, wl.height)
+    s = wl.splats.copy()
+    s[:, 1] -= np.float32(y0)
+    dl = wl.dl_dout.reshape(wl.height, wl.width, 4)[y0:y1].reshape(-1, 4)
+    return gen.from_arrays(f"{wl.name}[rows {y0}:{y1}]", wl.width, y1 - y0, s, wl.depths, dl), y1 - y0
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    wl = gen.make(args.config)
+    bands = 8
+    steps_ms = []
+
+    def one(k):
+        sub, rows = band_workload(wl, k % bands, bands)
+        t0 = time.perf_counter()
+        keys, idx, ranges = oracle.bin_splats(sub.splats, sub.depths, sub.width, sub.height)
+        f = oracle.forward(sub.splats, idx, ranges, sub.width, sub.height)
+        oracle.backward(sub.splats, idx, ranges, sub.width, sub.height, sub.dl_dout)
+        dt = time.perf_counter() - t0
+        del f
+        return dt * 1e3 * wl.height / max(rows, 1)
+
+    for k in range(args.warmup):
+        one(k)
+    for k in range(args.steps):
+        steps_ms.append(one(args.warmup + k))
+    value = float(np.mean(steps_ms))
+    cores = 1
+    line = {"metric": METRIC, "value": value, "unit": "ms/iter", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": value,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": workload_label(wl), "splats": wl.n, "width": wl.width,
+                       "height": wl.height, "parallelism": "single process, host cores"},
+            "cpu_baseline": {"value": value, "unit": "ms/iter", "cores": cores, "kind": "oracle",
+                             "sample": f"per step one of {bands} tile-row bands (binning of the "
+                                       "band's splats, forward, backward), scaled to the full "
+                                       "frame by rows; steps walk the bands"},
+            "e2e": {"value": value, "unit": "ms/iter", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def roofline_for(kind, counters, pairs, wl, ms, peaks, sm_mhz):
+    """Algorithmic work of one launch against the FP32 / SFU / HBM peaks."""
+    ops = FWD_OPS if kind == "forward" else BWD_OPS
+    fp32 = sum(ops[k] * counters[k] for k in ops)
+    sfu = counters["n_exp"] + (counters["n_contrib"] if kind == "backward" else 0)
+    px = wl.width * wl.height
+    if kind == "forward":
+        bytes_ = pairs * (36 + 4) + px * 24
+    else:
+        bytes_ = pairs * (36 + 4) + px * (16 + 4 + 4) + wl.n * 36 * 2
+    clk = peaks["sm_max_mhz"] * 1e6
+    fp32_peak = SM_COUNT * FP32_LANES_PER_SM * clk
+    sfu_peak = SM_COUNT * SFU_LANES_PER_SM * clk
+    hbm_peak = peaks["hbm_gbs"] * 1e9
+    t = {"alu": fp32 / fp32_peak, "sfu": sfu / sfu_peak, "hbm": bytes_ / hbm_peak}
+    bound = max(t, key=t.get)
+    sec = ms * 1e-3
+    if bound == "hbm":
+        achieved, peak, unit = bytes_ / sec / 1e9, peaks["hbm_gbs"], "GB/s"
+    elif bound == "alu":
+        achieved, peak, unit = fp32 / sec / 1e9, fp32_peak / 1e9, "Gop/s (fp32 lane ops)"
+    else:
+        achieved, peak, unit = sfu / sec / 1e9, sfu_peak / 1e9, "Gop/s (sfu lane ops)"
+    return {"kernel": kind, "bound": "alu" if bound in ("alu", "sfu") else "hbm",
+            "pipe": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": None,
+            "peak_source": f"{peaks['source']} HBM; FP32/SFU = {SM_COUNT} SMs x "
+                           f"{FP32_LANES_PER_SM}/{SFU_LANES_PER_SM} lanes x {peaks['sm_max_mhz']:.0f} MHz",
+            "algorithmic": {"fp32_ops": fp32, "sfu_ops": sfu, "bytes": bytes_},
+            "frac_at_sampled_clock": (achieved / peak) * (peaks["sm_max_mhz"] / sm_mhz)
+            if (sm_mhz and bound != "hbm") else None}
+
+
+def gpu_arm(args):
+    import torch
+
+    import gaussian_splatting_tile_bin_gb300 as gsr
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = gen.make(args.config)
+    ctx = gsr.Context(local)
+    stream = torch.cuda.current_stream(dev)
+
+    sp = torch.from_numpy(wl.splats).to(dev)
+    dp = torch.from_numpy(wl.depths).to(dev)
+    dl = torch.from_numpy(wl.dl_dout).to(dev)
+    npx = wl.width * wl.height
+    out = torch.empty((npx, 4), dtype=torch.float32, device=dev)
+    fT = torch.empty((npx,), dtype=torch.float32, device=dev)
+    last = torch.empty((npx,), dtype=torch.int32, device=dev)
+    grad = torch.empty((wl.n, 9), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(evs):
+        evs[0].record(stream)
+        bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+        evs[1].record(stream)
+        gsr.rasterize_forward(ctx, sp, bins, out, fT, last)
+        evs[2].record(stream)
+        gsr.rasterize_backward(ctx, sp, bins, dl, fT, last, grad)
+        evs[3].record(stream)
+        return bins
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    # Warm-up: W steps, then more untimed steps until ~1.5 s has passed so the
+    # clock sampler sees the GPU under this load before the timed region.
+    t_warm = time.perf_counter()
+    k = 0
+    while k < args.warmup or time.perf_counter() - t_warm < 1.5:
+        flush.fill_(float(k))
+        step(new_events())
+        k += 1
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+
+    launches0 = ctx.launch_count()
+    evs = [new_events() for _ in range(args.steps)]
+    wall0 = time.perf_counter()
+    pairs = 0
+    for i in range(args.steps):
+        flush.fill_(float(i))      # L2 flush between timed steps (outside the events)
+        pairs = step(evs[i]).num_pairs
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    launches = ctx.launch_count() - launches0
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+
+    bin_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
+    fwd_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
+    bwd_ms = np.array([e[2].elapsed_time(e[3]) for e in evs])
+    tot_ms = np.array([e[0].elapsed_time(e[3]) for e in evs])
+
+    # e2e: inputs from pinned host memory, gradients + image back, per step.
+    e2e = None
+    if not args.no_e2e:
+        h_sp = torch.from_numpy(wl.splats).pin_memory()
+        h_dp = torch.from_numpy(wl.depths).pin_memory()
+        h_dl = torch.from_numpy(wl.dl_dout).pin_memory()
+        h_grad = torch.empty((wl.n, 9), dtype=torch.float32).pin_memory()
+        h_out = torch.empty((npx, 4), dtype=torch.float32).pin_memory()
+
+        def e2e_step(e0, e1):
+            e0.record(stream)
+            sp.copy_(h_sp, non_blocking=True)
+            dp.copy_(h_dp, non_blocking=True)
+            dl.copy_(h_dl, non_blocking=True)
+            step(new_events())
+            h_grad.copy_(grad, non_blocking=True)
+            h_out.copy_(out, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+
+        for i in range(max(3, args.warmup // 2)):
+            e2e_step(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        e2e_ms = []
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e2e_step(a, b)
+            e2e_ms.append(a.elapsed_time(b))
+        h2d = (wl.splats.nbytes + wl.depths.nbytes + wl.dl_dout.nbytes)
+        d2h = wl.n * 9 * 4 + npx * 16
+        e2e_val = reduce_max(float(np.sum(e2e_ms)), world, dev) / (args.steps * world)
+        e2e = {"value": e2e_val, "unit": "ms/iter", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    rows = sampler.stop()
+    clocks = ClockSampler.summarize(rows)
+
+    total = reduce_max(float(tot_ms.sum()), world, dev)
+    value = total / (args.steps * world)
+    peaks = measured_peaks()
+
+    line = {"metric": METRIC, "value": value, "unit": "ms/iter", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(tot_ms.mean()),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": workload_label(wl), "splats": wl.n, "width": wl.width,
+                       "height": wl.height, "pairs": int(pairs),
+                       "l2": "flushed between timed steps (256 MB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "stages_ms": {"bin": float(bin_ms.mean()), "forward": float(fwd_ms.mean()),
+                          "backward": float(bwd_ms.mean()),
+                          "bin_median": float(np.median(bin_ms)),
+                          "forward_median": float(np.median(fwd_ms)),
+                          "backward_median": float(np.median(bwd_ms))},
+            "wall_s": wall, "gpu_launches": int(launches), "clocks": clocks}
+    if e2e:
+        line["e2e"] = e2e
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(wl)
+        line["cpu_baseline"] = {"value": cb["ms"], "unit": "ms/iter", "cores": 1, "kind": "oracle",
+                                "sample": "the whole workload once (binning, forward, backward), "
+                                          "single thread",
+                                "stages_ms": {"bin": cb["bin_ms"], "forward": cb["fwd_ms"],
+                                              "backward": cb["bwd_ms"]}}
+        rf = roofline_for("forward", cb["fwd_counters"], cb["pairs"], wl, float(fwd_ms.mean()), peaks,
+                          clocks.get("sm_mhz"))
+        rb = roofline_for("backward", cb["bwd_counters"], cb["pairs"], wl, float(bwd_ms.mean()),
+                          peaks, clocks.get("sm_mhz"))
+        dom = rb if bwd_ms.mean() >= fwd_ms.mean() else rf
+        line["roofline"] = dom
+        line["roofline_other"] = rf if dom is rb else rb
+        line["counters"] = {"forward": cb["fwd_counters"], "backward": cb["bwd_counters"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,203 @@
+// api.cu -- the extern "C" surface of libgsr.so: argument checks, the device
+// guard, error reporting and the context / arena lifetime.  The operations
+// themselves live in bin.cu and raster.cu.
+#include <new>
+#include <string>
+
+#include "internal.cuh"
+
+namespace gsr {
+
+int fail(gsr_ctx *ctx, int code, const std::string &msg)
+{
+    if (ctx) ctx->err = msg;
+    return code;
+}
+
+int cuda_check(gsr_ctx *ctx, cudaError_t e, const char *what)
+{
+    if (e == cudaSuccess) return GSR_OK;
+    return fail(ctx, GSR_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+namespace {
+
+// Makes the context's device current for the lifetime of the guard.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            cudaGetLastError();
+            prev = -1;
+        }
+        if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_bins(gsr_ctx *ctx, const gsr_bins *bins, int32_t n)
+{
+    if (!bins) return fail(ctx, GSR_ERR_INVALID_ARG, "bins is NULL");
+    if (bins->n != n) return fail(ctx, GSR_ERR_INVALID_ARG, "n differs from the n the bins were built from");
+    if (bins->width < 1 || bins->height < 1 || bins->width > GSR_MAX_IMAGE_SIDE ||
+        bins->height > GSR_MAX_IMAGE_SIDE)
+        return fail(ctx, GSR_ERR_INVALID_ARG, "bins carry an invalid image size");
+    if (bins->tiles_x != (bins->width + GSR_TILE - 1) / GSR_TILE ||
+        bins->tiles_y != (bins->height + GSR_TILE - 1) / GSR_TILE)
+        return fail(ctx, GSR_ERR_INVALID_ARG, "bins carry an inconsistent tile grid");
+    if (!bins->tile_ranges || (bins->num_pairs > 0 && !bins->sorted_idx))
+        return fail(ctx, GSR_ERR_INVALID_ARG, "bins hold NULL arrays");
+    return GSR_OK;
+}
+
+}  // namespace
+}  // namespace gsr
+
+using namespace gsr;
+
+extern "C" {
+
+int gsr_create(gsr_ctx **out, int device)
+{
+    if (!out) return GSR_ERR_INVALID_ARG;
+    *out = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess) {
+        cudaGetLastError();
+        return GSR_ERR_CUDA;
+    }
+    if (device < 0 || device >= count) return GSR_ERR_INVALID_ARG;
+    gsr_ctx *ctx = new (std::nothrow) gsr_ctx();
+    if (!ctx) return GSR_ERR_OOM;
+    ctx->device = device;
+    *out = ctx;
+    return GSR_OK;
+}
+
+void gsr_destroy(gsr_ctx *ctx)
+{
+    if (!ctx) return;
+    {
+        DeviceGuard g(ctx->device);
+        for (int b = 0; b < 3; ++b) {
+            cudaFree(ctx->pairs.k[b]);
+            cudaFree(ctx->pairs.v[b]);
+        }
+        cudaFree(ctx->counts);
+        cudaFree(ctx->blk_sums);
+        cudaFree(ctx->ranges);
+        cudaFree(ctx->radix_counts);
+        cudaFree(ctx->radix_totals);
+        cudaFree(ctx->scalars);
+        cudaFree(ctx->plan);
+        if (ctx->host_total) cudaFreeHost(ctx->host_total);
+    }
+    delete ctx;
+}
+
+const char *gsr_last_error(const gsr_ctx *ctx) { return ctx ? ctx->err.c_str() : "NULL context"; }
+
+int gsr_set_option(gsr_ctx *ctx, int option, int value)
+{
+    if (!ctx) return GSR_ERR_INVALID_ARG;
+    if (value != 0 && value != 1) return fail(ctx, GSR_ERR_INVALID_ARG, "option value must be 0 or 1");
+    switch (option) {
+    case GSR_OPT_BWD_WARP_SKIP: ctx->opt_warp_skip = value; return GSR_OK;
+    case GSR_OPT_BWD_LAST_CONTRIB: ctx->opt_last_contrib = value; return GSR_OK;
+    default: return fail(ctx, GSR_ERR_INVALID_ARG, "unknown option " + std::to_string(option));
+    }
+}
+
+uint64_t gsr_launch_count(const gsr_ctx *ctx) { return ctx ? ctx->launches : 0; }
+
+int gsr_bin_splats(gsr_ctx *ctx, const gsr_splat2d *splats, const float *depths, int32_t n,
+                   int32_t width, int32_t height, void *stream, gsr_bins *out)
+{
+    if (!ctx) return GSR_ERR_INVALID_ARG;
+    ctx->err.clear();
+    if (!out) return fail(ctx, GSR_ERR_INVALID_ARG, "out is NULL");
+    if (n < 0 || n > GSR_MAX_SPLATS) return fail(ctx, GSR_ERR_INVALID_ARG, "n out of range");
+    if (width < 1 || height < 1 || width > GSR_MAX_IMAGE_SIDE || height > GSR_MAX_IMAGE_SIDE)
+        return fail(ctx, GSR_ERR_INVALID_ARG, "width/height out of range");
+    if (n > 0 && (!splats || !depths)) return fail(ctx, GSR_ERR_INVALID_ARG, "splats/depths is NULL");
+    if (!aligned(splats, 4) || !aligned(depths, 4))
+        return fail(ctx, GSR_ERR_INVALID_ARG, "splats/depths must be 4-byte aligned");
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, GSR_ERR_CUDA, "cannot select the context's device");
+    return gsr::bin_splats(ctx, reinterpret_cast<const float *>(splats), depths, n, width, height,
+                           (cudaStream_t)stream, out);
+}
+
+int gsr_rasterize_forward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n, const gsr_bins *bins,
+                          float *out_rgbw, float *final_T, uint32_t *last_contrib, void *stream)
+{
+    if (!ctx) return GSR_ERR_INVALID_ARG;
+    ctx->err.clear();
+    int rc = check_bins(ctx, bins, n);
+    if (rc) return rc;
+    if (!out_rgbw || !final_T || !last_contrib)
+        return fail(ctx, GSR_ERR_INVALID_ARG, "an output pointer is NULL");
+    if (bins->num_pairs > 0 && !splats) return fail(ctx, GSR_ERR_INVALID_ARG, "splats is NULL");
+    if (!aligned(out_rgbw, 16) || !aligned(final_T, 4) || !aligned(last_contrib, 4) ||
+        !aligned(splats, 4))
+        return fail(ctx, GSR_ERR_INVALID_ARG, "misaligned buffer (out_rgbw needs 16 bytes)");
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, GSR_ERR_CUDA, "cannot select the context's device");
+    return gsr::rasterize_forward(ctx, reinterpret_cast<const float *>(splats), bins, out_rgbw, final_T,
+                                  last_contrib, (cudaStream_t)stream);
+}
+
+int gsr_rasterize_backward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n, const gsr_bins *bins,
+                           const float *dl_dout, const float *final_T, const uint32_t *last_contrib,
+                           float *grad, void *stream)
+{
+    if (!ctx) return GSR_ERR_INVALID_ARG;
+    ctx->err.clear();
+    int rc = check_bins(ctx, bins, n);
+    if (rc) return rc;
+    if (!dl_dout || !final_T || !last_contrib || (n > 0 && !grad))
+        return fail(ctx, GSR_ERR_INVALID_ARG, "an input/output pointer is NULL");
+    if (bins->num_pairs > 0 && !splats) return fail(ctx, GSR_ERR_INVALID_ARG, "splats is NULL");
+    if (!aligned(dl_dout, 16) || !aligned(final_T, 4) || !aligned(last_contrib, 4) ||
+        !aligned(grad, 4) || !aligned(splats, 4))
+        return fail(ctx, GSR_ERR_INVALID_ARG, "misaligned buffer (dl_dout needs 16 bytes)");
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, GSR_ERR_CUDA, "cannot select the context's device");
+    if (n == 0) return GSR_OK;
+    return gsr::rasterize_backward(ctx, reinterpret_cast<const float *>(splats), n, bins, dl_dout,
+                                   final_T, last_contrib, grad, (cudaStream_t)stream);
+}
+
+int gsr_get_bin_stats(gsr_ctx *ctx, gsr_bin_stats *out)
+{
+    if (!ctx || !out) return GSR_ERR_INVALID_ARG;
+    ctx->err.clear();
+    DeviceGuard g(ctx->device);
+    out->num_pairs = ctx->last_pairs;
+    out->key_digits = ctx->last_key_digits;
+    out->capacity = ctx->cap_pairs;
+    out->radix_passes = 0;
+    out->digit_mask = 0;
+    if (!ctx->plan || ctx->last_pairs == 0) return GSR_OK;
+    int rc = cuda_check(ctx, cudaStreamSynchronize(ctx->last_stream), "cudaStreamSynchronize");
+    if (rc) return rc;
+    RadixPlan plan;
+    rc = cuda_check(ctx, cudaMemcpy(&plan, ctx->plan, sizeof plan, cudaMemcpyDeviceToHost), "cudaMemcpy");
+    if (rc) return rc;
+    out->radix_passes = plan.num_exec;
+    for (int d = 0; d < kMaxDigits; ++d)
+        if (plan.exec[d]) out->digit_mask |= 1u << d;
+    return GSR_OK;
+}
+
+}  // extern "C"
+
+static_assert(sizeof(gsr_splat2d) == 36, "Splat2D is 9 floats");

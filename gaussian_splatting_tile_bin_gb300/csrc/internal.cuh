@@ -1,0 +1,83 @@
+// internal.cuh -- definitions shared by the translation units of libgsr.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "gsr.h"
+
+namespace gsr {
+
+constexpr int kTile = GSR_TILE;           // 16x16 pixels per tile
+constexpr int kTilePixels = kTile * kTile;
+constexpr int kBinBlock = 256;            // splats per block in count / emit
+constexpr int kRadixThreads = 256;        // 8 warps
+constexpr int kRadixItems = 8;            // keys per thread per radix tile
+constexpr int kRadixTile = kRadixThreads * kRadixItems;
+constexpr int kMaxDigits = 8;             // 8-bit digits of a 64-bit key
+
+// Which of the three key/value buffers each executed radix pass reads and
+// writes.  Buffer 0 holds the emitted pairs, buffer 1 the sorted result,
+// buffer 2 is scratch.  Written on the device after emission.
+struct RadixPlan {
+    int num_exec;
+    int exec[kMaxDigits];
+    int src[kMaxDigits];
+    int dst[kMaxDigits];
+};
+
+struct PairBuffers {
+    uint64_t *k[3];
+    uint32_t *v[3];
+};
+
+}  // namespace gsr
+
+struct gsr_ctx {
+    int device = 0;
+    std::string err;
+    uint64_t launches = 0;
+    int opt_warp_skip = 1;
+    int opt_last_contrib = 1;
+
+    // Grow-only arena.
+    size_t cap_pairs = 0;
+    gsr::PairBuffers pairs = {};
+    size_t cap_splats = 0;
+    uint32_t *counts = nullptr;                 // [cap_splats] tile count per splat
+    size_t cap_blocks = 0;
+    unsigned long long *blk_sums = nullptr;     // [2 * cap_blocks]: sums, then offsets
+    unsigned long long *blk_offs = nullptr;     // blk_sums + cap_blocks
+    size_t cap_tiles = 0;
+    uint32_t *ranges = nullptr;                 // [2 * cap_tiles]
+    size_t cap_radix_tiles = 0;
+    uint32_t *radix_counts = nullptr;           // [256 * cap_radix_tiles]
+    uint32_t *radix_totals = nullptr;           // [kMaxDigits * 256]
+    unsigned long long *scalars = nullptr;      // [0] pair total, [1] AND of keys, [2] OR of keys
+    gsr::RadixPlan *plan = nullptr;
+    unsigned long long *host_total = nullptr;   // pinned
+
+    // Last binning, for gsr_get_bin_stats.
+    cudaStream_t last_stream = nullptr;
+    uint32_t last_pairs = 0;
+    int last_key_digits = 0;
+};
+
+namespace gsr {
+
+// Records a CUDA error on the context; returns GSR_ERR_CUDA (or GSR_OK).
+int cuda_check(gsr_ctx *ctx, cudaError_t e, const char *what);
+int fail(gsr_ctx *ctx, int code, const std::string &msg);
+
+// Host sides of the three operations (validated arguments).
+int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n, int32_t width,
+               int32_t height, cudaStream_t stream, gsr_bins *out);
+int rasterize_forward(gsr_ctx *ctx, const float *splats, const gsr_bins *bins, float *out_rgbw,
+                      float *final_T, uint32_t *last_contrib, cudaStream_t stream);
+int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_bins *bins,
+                       const float *dl_dout, const float *final_T, const uint32_t *last_contrib,
+                       float *grad, cudaStream_t stream);
+
+}  // namespace gsr

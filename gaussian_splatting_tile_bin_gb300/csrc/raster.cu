@@ -1,0 +1,284 @@
+// raster.cu -- forward and backward tile rasterization.
+//
+// One 256-thread CTA per 16x16 tile, one thread per pixel ("forward/adam
+// audit" (p3-forward-adam-audit), sections (a), (b), (e): 256-thread group per
+// tile staging local_batch[256] Splat2D records).  Each batch of the tile's
+// sorted range is staged in shared memory in a compute-ready form (mean, half
+// conic, colour, and a per-splat sigma bound); every thread then walks the batch.
+//
+// Both kernels evaluate a splat at a pixel through the same two inline
+// functions (splat_sigma, splat_alpha), so the backward takes exactly the
+// forward's skip and stop decisions.
+#include "internal.cuh"
+
+namespace gsr {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kAlphaMin = 1.0f / 255.0f;  // "W1 warp sparse skip + exp-skip", body
+constexpr float kAlphaMax = 0.999f;         // "A.9 f16 forward", snippet
+constexpr float kSigmaSkip = 5.55f;         // "W1 warp sparse skip + exp-skip", section 1, W1b
+constexpr float kTMin = 1e-4f;              // stop once the transmittance would fall below this
+// ln(255) plus a margin far above the rounding of the exponent path: a lane whose
+// sigma exceeds ln(color_a) + this cannot reach alpha >= 1/255.
+constexpr float kLn255Margin = 5.5412636f + 1e-3f;
+
+// Staged splat, three 16-byte vectors per batch slot.
+//   geo = (mean_x, mean_y, a / 2, b)
+//   aux = (c / 2, color_a, sigma bound, splat index as bits)
+//   rgb = (r, g, b, 0)
+// The sigma bound is min(5.55, ln(color_a) + ln 255 + margin): an evaluation
+// with sigma at or above it is skipped without computing an exponential.  At
+// 5.55 the bound is the pages' exact skip; below it only lanes whose exact alpha
+// test would fail are dropped, so the decisions are those of the exact test.
+struct StagedBatch {
+    float4 geo[kTilePixels];
+    float4 aux[kTilePixels];
+    float4 rgb[kTilePixels];
+};
+
+__device__ __forceinline__ void stage_splat(StagedBatch &sb, int slot, const float *__restrict__ splats,
+                                            uint32_t idx)
+{
+    const float *s = splats + 9 * (size_t)idx;
+    const float mx = __ldg(s + 0), my = __ldg(s + 1);
+    const float a = __ldg(s + 2), b = __ldg(s + 3), c = __ldg(s + 4);
+    const float r = __ldg(s + 5), g = __ldg(s + 6), bl = __ldg(s + 7);
+    const float o = __ldg(s + 8);
+    const float bound = fminf(kSigmaSkip, __logf(o) + kLn255Margin);
+    sb.geo[slot] = make_float4(mx, my, 0.5f * a, b);
+    sb.aux[slot] = make_float4(0.5f * c, o, bound, __uint_as_float(idx));
+    sb.rgb[slot] = make_float4(r, g, bl, 0.0f);
+}
+
+// sigma = 1/2 (a dx^2 + c dy^2) + b dx dy = dx (a/2 dx + b dy) + c/2 dy dy
+__device__ __forceinline__ float splat_sigma(const float4 geo, const float half_c, float px, float py,
+                                             float &dx, float &dy)
+{
+    dx = px - geo.x;
+    dy = py - geo.y;
+    const float t = __fmaf_rn(geo.w, dy, __fmul_rn(geo.z, dx));
+    return __fmaf_rn(dx, t, __fmul_rn(__fmul_rn(half_c, dy), dy));
+}
+
+// alpha = min(0.999, color_a exp(-sigma)); also returns exp(-sigma) and the
+// unclamped product for the backward.
+__device__ __forceinline__ float splat_alpha(float sigma, float o, float &e, float &raw)
+{
+    e = __expf(-sigma);
+    raw = __fmul_rn(o, e);
+    return fminf(kAlphaMax, raw);
+}
+
+__device__ __forceinline__ int pixel_x(int tid) { return tid & (kTile - 1); }
+__device__ __forceinline__ int pixel_y(int tid) { return tid >> 4; }
+
+// --- forward ---------------------------------------------------------------
+
+__global__ void __launch_bounds__(kTilePixels)
+k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
+          const uint2 *__restrict__ ranges, int width, int height, int tiles_x,
+          float4 *__restrict__ out_rgbw, float *__restrict__ final_T, uint32_t *__restrict__ last_out)
+{
+    __shared__ StagedBatch sb;
+    const int tile = blockIdx.x;
+    const int tx = tile % tiles_x, ty = tile / tiles_x;
+    const int x = tx * kTile + pixel_x(threadIdx.x);
+    const int y = ty * kTile + pixel_y(threadIdx.x);
+    const bool inside = x < width && y < height;
+    const float px = (float)x, py = (float)y;
+    const uint2 range = ranges[tile];
+
+    float T = 1.0f;
+    float3 C = make_float3(0.0f, 0.0f, 0.0f);
+    uint32_t last = 0;
+    bool done = !inside;
+
+    for (uint32_t bstart = range.x; bstart < range.y; bstart += kTilePixels) {
+        // Every pixel of the tile has stopped: no later splat can change it.
+        if (__syncthreads_count(done) == kTilePixels) break;
+        const uint32_t pos = bstart + threadIdx.x;
+        if (pos < range.y) stage_splat(sb, threadIdx.x, splats, __ldg(sorted_idx + pos));
+        __syncthreads();
+        const int cnt = (int)min(range.y - bstart, (uint32_t)kTilePixels);
+        if (!done) {
+            for (int j = 0; j < cnt; ++j) {
+                const float4 geo = sb.geo[j];
+                const float4 aux = sb.aux[j];
+                float dx, dy;
+                const float sigma = splat_sigma(geo, aux.x, px, py, dx, dy);
+                if (!(sigma >= 0.0f) || !(sigma < aux.z)) continue;
+                float e, raw;
+                const float alpha = splat_alpha(sigma, aux.y, e, raw);
+                if (alpha < kAlphaMin) continue;
+                const float next_T = T * (1.0f - alpha);
+                if (next_T < kTMin) {
+                    done = true;
+                    break;
+                }
+                const float w = alpha * T;
+                const float4 c = sb.rgb[j];
+                C.x = __fmaf_rn(c.x, w, C.x);
+                C.y = __fmaf_rn(c.y, w, C.y);
+                C.z = __fmaf_rn(c.z, w, C.z);
+                T = next_T;
+                last = bstart - range.x + (uint32_t)j + 1u;
+            }
+        }
+    }
+    if (inside) {
+        const size_t p = (size_t)y * width + x;
+        out_rgbw[p] = make_float4(C.x, C.y, C.z, 1.0f - T);
+        final_T[p] = T;
+        last_out[p] = last;
+    }
+}
+
+// --- backward --------------------------------------------------------------
+
+template <bool kWarpSkip, bool kLastContrib>
+__global__ void __launch_bounds__(kTilePixels)
+k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
+           const uint2 *__restrict__ ranges, int width, int height, int tiles_x,
+           const float4 *__restrict__ dl_dout, const float *__restrict__ final_T,
+           const uint32_t *__restrict__ last_in, float *__restrict__ grad)
+{
+    __shared__ StagedBatch sb;
+    __shared__ uint32_t s_wmax[kTilePixels / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tile = blockIdx.x;
+    const int tx = tile % tiles_x, ty = tile / tiles_x;
+    const int x = tx * kTile + pixel_x(threadIdx.x);
+    const int y = ty * kTile + pixel_y(threadIdx.x);
+    const bool inside = x < width && y < height;
+    const float px = (float)x, py = (float)y;
+    const uint2 range = ranges[tile];
+    const uint32_t len = range.y - range.x;
+
+    float T = 1.0f;
+    uint32_t L = 0;
+    float3 g = make_float3(0.0f, 0.0f, 0.0f);
+    if (inside) {
+        const size_t p = (size_t)y * width + x;
+        T = final_T[p];
+        L = min(last_in[p], len);  // a caller's stale last_contrib cannot reach past the range
+        const float4 d = dl_dout[p];
+        g = make_float3(d.x, d.y, d.z);
+    }
+    // Positions at or beyond a pixel's last_contributor were never composited
+    // there; a warp stops at its largest, the CTA at the largest of its warps.
+    uint32_t warp_end = len;
+    uint32_t cta_end = len;
+    if (kLastContrib) {
+        warp_end = __reduce_max_sync(kFull, L);
+        if (lane == 0) s_wmax[warp] = warp_end;
+        __syncthreads();
+        cta_end = 0;
+#pragma unroll
+        for (int w = 0; w < kTilePixels / 32; ++w) cta_end = max(cta_end, s_wmax[w]);
+    }
+    float3 S = make_float3(0.0f, 0.0f, 0.0f);
+
+    for (int bend = (int)cta_end; bend > 0; bend -= kTilePixels) {
+        const int bstart = max(0, bend - kTilePixels);
+        const int cnt = bend - bstart;
+        __syncthreads();
+        if (threadIdx.x < cnt)
+            stage_splat(sb, threadIdx.x, splats, __ldg(sorted_idx + range.x + bstart + threadIdx.x));
+        __syncthreads();
+        const int jhi = min(cnt, (int)warp_end - bstart) - 1;
+        for (int j = jhi; j >= 0; --j) {
+            const uint32_t rel = (uint32_t)(bstart + j);
+            bool contrib = false;
+            float v[9];
+#pragma unroll
+            for (int k = 0; k < 9; ++k) v[k] = 0.0f;
+            if (rel < L) {
+                const float4 geo = sb.geo[j];
+                const float4 aux = sb.aux[j];
+                float dx, dy;
+                const float sigma = splat_sigma(geo, aux.x, px, py, dx, dy);
+                if (sigma >= 0.0f && sigma < aux.z) {
+                    float e, raw;
+                    const float alpha = splat_alpha(sigma, aux.y, e, raw);
+                    if (alpha >= kAlphaMin) {
+                        contrib = true;
+                        const float4 c = sb.rgb[j];
+                        const float inv = __fdividef(1.0f, 1.0f - alpha);
+                        const float Tj = T * inv;  // transmittance in front of this splat
+                        const float aT = alpha * Tj;
+                        v[5] = g.x * aT;
+                        v[6] = g.y * aT;
+                        v[7] = g.z * aT;
+                        float dA = g.x * (c.x * Tj - S.x * inv);
+                        dA = __fmaf_rn(g.y, c.y * Tj - S.y * inv, dA);
+                        dA = __fmaf_rn(g.z, c.z * Tj - S.z * inv, dA);
+                        S.x = __fmaf_rn(c.x, aT, S.x);
+                        S.y = __fmaf_rn(c.y, aT, S.y);
+                        S.z = __fmaf_rn(c.z, aT, S.z);
+                        const float dRaw = raw < kAlphaMax ? dA : 0.0f;
+                        v[8] = dRaw * e;
+                        const float dSig = -dRaw * raw;
+                        const float a = 2.0f * geo.z, b = geo.w, cc = 2.0f * aux.x;
+                        v[0] = -dSig * __fmaf_rn(a, dx, b * dy);
+                        v[1] = -dSig * __fmaf_rn(b, dx, cc * dy);
+                        v[2] = dSig * (0.5f * dx * dx);
+                        v[3] = dSig * (dx * dy);
+                        v[4] = dSig * (0.5f * dy * dy);
+                        T = Tj;
+                    }
+                }
+            }
+            // "W1 warp sparse skip": with no contributing lane every sum is +0.
+            if (kWarpSkip && !__any_sync(kFull, contrib)) continue;
+#pragma unroll
+            for (int k = 0; k < 9; ++k) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(kFull, v[k], o);
+            }
+            if (lane == 0) {
+                const uint32_t idx = __float_as_uint(sb.aux[j].w);
+                float *gr = grad + 9 * (size_t)idx;
+#pragma unroll
+                for (int k = 0; k < 9; ++k) atomicAdd(gr + k, v[k]);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+int rasterize_forward(gsr_ctx *ctx, const float *splats, const gsr_bins *bins, float *out_rgbw,
+                      float *final_T, uint32_t *last_contrib, cudaStream_t stream)
+{
+    const int num_tiles = bins->tiles_x * bins->tiles_y;
+    k_forward<<<num_tiles, kTilePixels, 0, stream>>>(
+        splats, bins->sorted_idx, reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width,
+        bins->height, bins->tiles_x, reinterpret_cast<float4 *>(out_rgbw), final_T, last_contrib);
+    ++ctx->launches;
+    return cuda_check(ctx, cudaGetLastError(), "forward launch");
+}
+
+int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_bins *bins,
+                       const float *dl_dout, const float *final_T, const uint32_t *last_contrib,
+                       float *grad, cudaStream_t stream)
+{
+    int rc = cuda_check(ctx, cudaMemsetAsync(grad, 0, (size_t)n * 9 * sizeof(float), stream),
+                        "cudaMemsetAsync");
+    if (rc) return rc;
+    const int num_tiles = bins->tiles_x * bins->tiles_y;
+    auto launch = [&](auto kernel) {
+        kernel<<<num_tiles, kTilePixels, 0, stream>>>(
+            splats, bins->sorted_idx, reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width,
+            bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
+            last_contrib, grad);
+    };
+    if (ctx->opt_warp_skip && ctx->opt_last_contrib) launch(k_backward<true, true>);
+    else if (ctx->opt_warp_skip) launch(k_backward<true, false>);
+    else if (ctx->opt_last_contrib) launch(k_backward<false, true>);
+    else launch(k_backward<false, false>);
+    ++ctx->launches;
+    return cuda_check(ctx, cudaGetLastError(), "backward launch");
+}
+
+}  // namespace gsr

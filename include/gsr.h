@@ -1,0 +1,182 @@
+/*
+ * gsr.h -- C ABI of libgsr.so, a tile-binned 2-D Gaussian splat rasterizer for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Three entry points make one training iteration of the rasterizer:
+ *   gsr_bin_splats          pairs each splat with the 16x16 tiles its 3-sigma box
+ *                           touches and sorts the pairs by (tile, depth)
+ *   gsr_rasterize_forward   front-to-back alpha compositing, one CTA per tile
+ *   gsr_rasterize_backward  back-to-front replay giving d/d{mean, conic, rgb, color_a}
+ *
+ * The operations follow a 3D Gaussian Splatting trainer's findings pages:
+ *   - "C0 resident arena + C1 pass skip" (p2-c0-resident-binning), section 2 table:
+ *     pair keys (tile_id << 32) | depth_bits, a stable radix sort whose
+ *     constant-digit passes are skipped, per-tile ranges, a grow-only arena;
+ *   - "forward/adam audit" (p3-forward-adam-audit), sections (a), (b), (e), 3:
+ *     one 256-thread group per 16x16 tile staging a batch of 256 Splat2D
+ *     records, outputs rgb + final_T + last_contributor (24 B/pixel);
+ *   - "A.9 f16 forward" (a-9-f16-forward-negative), implementation snippet:
+ *     alpha = min(0.999, color_a exp(-sigma)), T <- T (1 - alpha), fp32 throughout;
+ *   - "W1 warp sparse skip + exp-skip" (p2-w1-warp-sparse-skip), section 1: the
+ *     sigma >= 5.55 skip, the all-lanes-idle warp skip before the reduction;
+ *   - "M3 per-splat backward" (p3-per-splat-backward), section 1: 9 gradient
+ *     components per splat, no background, no rgb clamp, alpha-clamp rule
+ *     raw < 0.999.
+ *
+ * Conventions shared by every call
+ *   - All array arguments are DEVICE pointers owned by the caller, except the
+ *     arrays inside gsr_bins, which belong to the context's arena.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream).  gsr_bin_splats synchronises that stream once to
+ *     read the pair count; the raster calls return without synchronising.
+ *   - The calling thread's current CUDA device is switched to the context's
+ *     device for the duration of a call and restored afterwards.
+ *   - Every call returns GSR_OK or an error code; gsr_last_error() gives the text.
+ *     No C++ exception crosses this interface.  A context is not thread-safe.
+ *   - Pixel centres sit at integer coordinates (px, py); image sizes need not be
+ *     multiples of 16 (pixels outside the image neither write nor contribute).
+ */
+#ifndef GSR_H
+#define GSR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* One splat after projection: 9 floats, 36 bytes, in this order
+ * ("forward/adam audit", section 3, staging read: Splat2D = 9 float = 36 B).
+ * The conic (a, b, c) is the inverse 2-D covariance: sigma(d) =
+ * 1/2 (a dx^2 + c dy^2) + b dx dy.  color_a is expected in [0, 1]. */
+typedef struct gsr_splat2d {
+    float mean_x, mean_y;
+    float conic_a, conic_b, conic_c;
+    float color_r, color_g, color_b;
+    float color_a;
+} gsr_splat2d;
+
+#define GSR_TILE 16
+#define GSR_MAX_IMAGE_SIDE (1 << 19)   /* width and height limit */
+#define GSR_MAX_SPLATS (1 << 28)       /* n limit */
+#define GSR_MAX_PAIRS 0x7fffffffu      /* tile-pair limit (indices are uint32) */
+
+enum {
+    GSR_OK = 0,
+    GSR_ERR_INVALID_ARG = 1,    /* null pointer, bad size or misaligned buffer */
+    GSR_ERR_CUDA = 2,           /* a CUDA runtime call or launch failed */
+    GSR_ERR_OOM = 3,            /* the arena could not grow */
+    GSR_ERR_TOO_MANY_PAIRS = 4  /* more than GSR_MAX_PAIRS tile pairs */
+};
+
+/* Per-call variant switches (A/B and equivalence tests; defaults are 1). */
+enum {
+    GSR_OPT_BWD_WARP_SKIP = 1,   /* skip the reduction when no lane contributes */
+    GSR_OPT_BWD_LAST_CONTRIB = 2 /* stop each warp at its largest last_contributor */
+};
+
+typedef struct gsr_ctx gsr_ctx;
+
+/* Result of gsr_bin_splats.  The device arrays live in the context's arena and
+ * stay valid until the next gsr_bin_splats or gsr_destroy on that context. */
+typedef struct gsr_bins {
+    const uint64_t *keys;        /* device, [num_pairs], ascending (tile << 32 | depth bits);
+                                    equal keys are ordered by splat index */
+    const uint32_t *sorted_idx;  /* device, [num_pairs], splat index of each key */
+    const uint32_t *tile_ranges; /* device, [2 * tiles_x * tiles_y]: {start, end} per tile,
+                                    {0, 0} for an empty tile */
+    uint32_t num_pairs;          /* host copy of the pair count */
+    int32_t n;                   /* splat count the bins were built from */
+    int32_t width, height;       /* image size in pixels */
+    int32_t tiles_x, tiles_y;    /* ceil(width / 16), ceil(height / 16) */
+} gsr_bins;
+
+/* Creates a context on CUDA device `device`.  Allocates nothing on the GPU
+ * until the first gsr_bin_splats.  *out receives the context (NULL on error). */
+int gsr_create(gsr_ctx **out, int device);
+
+/* Frees the context and its arena.  Safe on NULL.  Waits for nothing: the
+ * caller must make sure no enqueued work still uses the arena. */
+void gsr_destroy(gsr_ctx *ctx);
+
+/* Text of the last error on this context ("" if none).  Owned by the context. */
+const char *gsr_last_error(const gsr_ctx *ctx);
+
+/* Sets a GSR_OPT_* switch (value 0 or 1).  GSR_ERR_INVALID_ARG for an unknown option. */
+int gsr_set_option(gsr_ctx *ctx, int option, int value);
+
+/* Number of kernels this context has launched since it was created. */
+uint64_t gsr_launch_count(const gsr_ctx *ctx);
+
+/* Bins n splats for a width x height image
+ * ("C0 resident arena + C1 pass skip", section 2 table, C0 and C1).
+ *
+ *   splats  device, [n] gsr_splat2d (4-byte aligned)
+ *   depths  device, [n] float; view-space depth, ordered front (small) to back
+ *   out     host struct, filled on success
+ *
+ * A splat emits one pair per tile of its 3-sigma box, rx = 3 sqrt(c / det),
+ * ry = 3 sqrt(a / det), det = a c - b^2, tile range floor((mean -+ r) / 16)
+ * clamped to the grid; it emits nothing when a field or its depth is not
+ * finite, depth <= 0, a <= 0 or det <= 0, or its box misses the image.  The
+ * arena grows (never shrinks) to max(65536, 16 n, 1.5 x previous pairs) pairs
+ * as needed.  n == 0 is valid and gives empty bins.
+ * Errors: GSR_ERR_INVALID_ARG (null ctx/out, n < 0 or > GSR_MAX_SPLATS,
+ * width/height outside [1, GSR_MAX_IMAGE_SIDE], null splats/depths with n > 0),
+ * GSR_ERR_TOO_MANY_PAIRS, GSR_ERR_OOM, GSR_ERR_CUDA. */
+int gsr_bin_splats(gsr_ctx *ctx, const gsr_splat2d *splats, const float *depths, int32_t n,
+                   int32_t width, int32_t height, void *stream, gsr_bins *out);
+
+/* Forward rasterization over bins made by gsr_bin_splats from the same splats
+ * ("forward/adam audit", sections (a), (b), 3; "A.9 f16 forward", snippet;
+ * "W1 warp sparse skip + exp-skip", section 1, W1b).
+ *
+ * For each pixel, front to back over its tile's sorted range: sigma as above
+ * with d = pixel - mean; skip sigma < 0 or sigma >= 5.55;
+ * alpha = min(0.999, color_a exp(-sigma)); skip alpha < 1/255;
+ * next_T = T (1 - alpha); if next_T < 1e-4 the pixel stops without this splat;
+ * otherwise C += rgb alpha T, T = next_T.
+ *
+ *   out_rgbw      device, [height * width] float4 (16-byte aligned): C and 1 - final_T
+ *   final_T       device, [height * width] float
+ *   last_contrib  device, [height * width] uint32: 1 + position of the last composited
+ *                 splat within the tile's range, 0 if none
+ * Errors: GSR_ERR_INVALID_ARG (null pointer, misaligned out_rgbw, n differs from
+ * bins->n), GSR_ERR_CUDA. */
+int gsr_rasterize_forward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n,
+                          const gsr_bins *bins, float *out_rgbw, float *final_T,
+                          uint32_t *last_contrib, void *stream);
+
+/* Backward rasterization: gradient of L = sum_pixels dl_dout.rgb . out.rgb with
+ * respect to every Splat2D field ("M3 per-splat backward", section 1;
+ * "W1 warp sparse skip + exp-skip", section 1, W1a).  Each pixel replays its
+ * composited splats back to front from final_T, recovering the transmittance in
+ * front of splat j as T / (1 - alpha_j).  The w channel of dl_dout is ignored.
+ *
+ *   dl_dout       device, [height * width] float4 (16-byte aligned)
+ *   final_T, last_contrib   the forward's outputs for the same bins
+ *   grad          device, [n * 9] float, overwritten; row i holds d/d of splat i's
+ *                 fields in gsr_splat2d order
+ * Gradients are accumulated with float atomics, so the last bits may differ
+ * between runs.  Errors: as gsr_rasterize_forward. */
+int gsr_rasterize_backward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n,
+                           const gsr_bins *bins, const float *dl_dout, const float *final_T,
+                           const uint32_t *last_contrib, float *grad, void *stream);
+
+/* Statistics of the last gsr_bin_splats (synchronises its stream).
+ * radix_passes: passes the sort executed; digit_mask: bit d set when 8-bit digit
+ * d of the keys varied (pass d executed); capacity: arena capacity in pairs. */
+typedef struct gsr_bin_stats {
+    uint32_t num_pairs;
+    int32_t radix_passes;
+    uint32_t digit_mask;
+    int32_t key_digits;
+    uint64_t capacity;
+} gsr_bin_stats;
+int gsr_get_bin_stats(gsr_ctx *ctx, gsr_bin_stats *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GSR_H */

@@ -1,0 +1,95 @@
+"""The C ABI without a GPU: the library builds, loads, exports every declared
+symbol, its structs match the binding, and argument checks fail cleanly."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gsr.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gsr_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gaussian_splatting_tile_bin_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert {"gsr_bin_splats", "gsr_rasterize_forward", "gsr_rasterize_backward"} <= set(names)
+    nm = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True)
+    exported = set(re.findall(r"\bT (gsr_\w+)", nm.stdout))
+    for name in names:
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # Nothing from the oracle or an unnamed extra entry point leaks out.
+    assert exported == set(names)
+
+
+def test_struct_layouts_match_binding(tmp_path):
+    from gaussian_splatting_tile_bin_gb300 import _abi  # noqa: F401  (loads without a GPU)
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gsr.h"\n'
+                   'int main(void){printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(gsr_splat2d),'
+                   ' sizeof(gsr_bins), offsetof(gsr_bins, num_pairs), offsetof(gsr_bins, tiles_y),'
+                   ' sizeof(gsr_bin_stats), offsetof(gsr_bin_stats, capacity)); return 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(v) for v in subprocess.check_output([str(exe)]).split()]
+    want = [36, ctypes.sizeof(_abi._Bins), _abi._Bins.num_pairs.offset, _abi._Bins.tiles_y.offset,
+            ctypes.sizeof(_abi._BinStats), _abi._BinStats.capacity.offset]
+    assert got == want
+
+
+def test_null_and_invalid_arguments(lib):
+    P = ctypes.c_void_p
+    lib.gsr_create.argtypes = [ctypes.POINTER(P), ctypes.c_int]
+    assert lib.gsr_create(None, 0) == 1
+    lib.gsr_set_option.argtypes = [P, ctypes.c_int, ctypes.c_int]
+    assert lib.gsr_set_option(None, 1, 1) == 1
+    lib.gsr_bin_splats.argtypes = [P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P]
+    assert lib.gsr_bin_splats(None, None, None, 0, 16, 16, None, None) == 1
+    lib.gsr_rasterize_forward.argtypes = [P, P, ctypes.c_int32, P, P, P, P, P]
+    assert lib.gsr_rasterize_forward(None, None, 0, None, None, None, None, None) == 1
+    lib.gsr_rasterize_backward.argtypes = [P, P, ctypes.c_int32, P, P, P, P, P, P]
+    assert lib.gsr_rasterize_backward(None, None, 0, None, None, None, None, None, None) == 1
+    lib.gsr_get_bin_stats.argtypes = [P, P]
+    assert lib.gsr_get_bin_stats(None, None) == 1
+    lib.gsr_launch_count.argtypes = [P]
+    lib.gsr_launch_count.restype = ctypes.c_uint64
+    assert lib.gsr_launch_count(None) == 0
+    lib.gsr_last_error.argtypes = [P]
+    lib.gsr_last_error.restype = ctypes.c_char_p
+    assert lib.gsr_last_error(None) == b"NULL context"
+    lib.gsr_destroy.argtypes = [P]
+    lib.gsr_destroy(None)
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    """The product path has no CPU fallback: a missing libgsr.so is an ImportError."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "abi_copy", os.path.join(ROOT, "gaussian_splatting_tile_bin_gb300", "_abi.py"))
+    mod = importlib.util.module_from_spec(spec)
+    monkeypatch.setattr(os.path, "exists", lambda p: False if p.endswith("libgsr.so") else True)
+    with pytest.raises(ImportError):
+        spec.loader.exec_module(mod)
+
+
+def test_package_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "gaussian_splatting_tile_bin_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f

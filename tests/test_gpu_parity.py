@@ -1,0 +1,243 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Binning must match bit for bit (sorted keys, sorted indices, tile ranges);
+forward pixels within 1e-5 absolute; gradients within 1e-4 + 1e-4 |ref|.
+A pixel or splat may differ beyond that only where the oracle flags a
+threshold decision (alpha vs 1/255, T vs 1e-4, the 0.999 clamp, the sign of
+sigma) within the rounding uncertainty of the two implementations.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gen
+from gpu_helpers import (check_backward, check_bins, check_forward, run_gpu, run_oracle, to_dev,
+                         varying_digit_mask)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gsr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gaussian_splatting_tile_bin_gb300 as g
+    return g
+
+
+@pytest.fixture(scope="module")
+def ctx(gsr):
+    c = gsr.Context(0)
+    yield c
+    c.close()
+
+
+def _full(gsr, ctx, wl, backward=True):
+    g = run_gpu(gsr, ctx, wl, backward)
+    o = run_oracle(wl, backward)
+    check_bins(g, o)
+    fs = check_forward(g, o)
+    bs = check_backward(g, o) if backward else None
+    return g, o, fs, bs
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "lego_early", "lego_final"])
+def test_config_parity(gsr, ctx, name):
+    g, o, fs, bs = _full(gsr, ctx, gen.make(name))
+    print(name, "pairs", g["num_pairs"], "forward", fs, "backward", bs)
+
+
+def test_stress_parity(gsr, ctx):
+    wl = gen.stress()
+    g, o, fs, bs = _full(gsr, ctx, wl)
+    print("stress pairs", g["num_pairs"], "forward", fs, "backward", bs)
+
+
+@pytest.mark.parametrize("size", [32, 24])
+def test_overlap_fixtures(gsr, ctx, size):
+    _full(gsr, ctx, gen.overlap_fixture(size))
+
+
+def _random(n, w, h, seed, levels=None, big=0):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    s = np.zeros((n, 9), dtype=np.float32)
+    s[:, 0] = rng.uniform(-20, w + 20, n)
+    s[:, 1] = rng.uniform(-20, h + 20, n)
+    std = rng.uniform(0.4, 10.0, n)
+    if big:
+        std[:big] = rng.uniform(max(w, h) * 0.5, max(w, h) * 2.0, big)
+    s[:, 2] = 1.0 / std ** 2
+    s[:, 3] = rng.uniform(-0.4, 0.4, n) / std ** 2
+    s[:, 4] = 1.0 / std ** 2
+    s[:, 5:8] = rng.uniform(0, 1, (n, 3))
+    s[:, 8] = rng.uniform(0.0, 1.0, n)
+    d = (rng.integers(1, levels + 1, n) if levels else rng.uniform(0.5, 30.0, n)).astype(np.float32)
+    return gen.from_arrays(f"rand{n}", w, h, s, d, seed=seed + 100)
+
+
+@pytest.mark.parametrize("n", [0, 1, 255, 256, 257, 1234])
+def test_sizes(gsr, ctx, n):
+    _full(gsr, ctx, _random(n, 96, 80, n))
+
+
+def test_tie_heavy_depths(gsr, ctx):
+    # 8 distinct depths over 5000 splats: equal keys must come out in splat order.
+    _full(gsr, ctx, _random(5000, 128, 128, 9, levels=8))
+
+
+@pytest.mark.parametrize("w,h", [(100, 70), (1, 1), (17, 33), (16, 16), (257, 15)])
+def test_ragged_images(gsr, ctx, w, h):
+    _full(gsr, ctx, _random(600, w, h, w * 1000 + h))
+
+
+def test_huge_splats_long_lists(gsr, ctx):
+    # A few splats cover every tile; every tile list holds thousands of entries.
+    _full(gsr, ctx, _random(3000, 160, 144, 5, big=40))
+
+
+def test_culled_splats(gsr, ctx):
+    wl = _random(400, 64, 64, 3)
+    s, d = wl.splats, wl.depths
+    s[0, 2] = -1.0                  # a <= 0
+    s[1, 3] = 10.0                  # indefinite (det <= 0)
+    d[2] = 0.0                      # depth 0
+    d[3] = -1.0                     # behind
+    s[4, 0] = np.nan                # non-finite field
+    s[5, 8] = np.inf
+    d[6] = np.inf
+    s[7, 0:2] = [-500.0, -500.0]    # off image
+    g, o, _, _ = _full(gsr, ctx, wl)
+    assert not np.isin(np.arange(8), g["idx"]).any()
+
+
+def test_all_culled_and_empty(gsr, ctx):
+    wl = _random(50, 48, 48, 4)
+    wl.depths[:] = -1.0
+    g = run_gpu(gsr, ctx, wl)
+    assert g["num_pairs"] == 0
+    assert np.all(g["ranges"] == 0)
+    assert np.all(g["out"] == 0) and np.all(g["final_T"] == 1) and np.all(g["last"] == 0)
+    assert np.all(g["grad"] == 0)
+    g = run_gpu(gsr, ctx, _random(0, 40, 40, 0))
+    assert g["num_pairs"] == 0 and g["grad"].shape == (0, 9)
+
+
+def test_radix_pass_skip(gsr, ctx):
+    """Constant 8-bit digits are skipped; the stats report which ran
+    ("C0 resident arena + C1 pass skip", section 2, C1)."""
+    wl = gen.lego_final()
+    g = run_gpu(gsr, ctx, wl, backward=False)
+    st = ctx.bin_stats()
+    o = run_oracle(wl, backward=False)
+    assert st["key_digits"] == 6                      # 32 + 12 tile bits for 2500 tiles
+    assert st["digit_mask"] == varying_digit_mask(o["keys"], 6)
+    assert not (st["digit_mask"] >> 3) & 1            # depths in [2,6) share their top byte
+    assert st["radix_passes"] == bin(st["digit_mask"]).count("1")
+    check_bins(g, o)
+
+
+def test_no_pass_needed(gsr, ctx):
+    # One tile, one depth: every digit is constant; the emitted order is the result.
+    s = np.tile(np.array([[8.0, 8.0, 1.0, 0.0, 1.0, 0.5, 0.5, 0.5, 0.5]], np.float32), (300, 1))
+    wl = gen.from_arrays("flat", 16, 16, s, np.full(300, 2.0, np.float32))
+    g = run_gpu(gsr, ctx, wl)
+    assert ctx.bin_stats()["radix_passes"] == 0
+    o = run_oracle(wl)
+    check_bins(g, o)
+    check_forward(g, o)
+    check_backward(g, o)
+
+
+def test_arena_grows_and_reuses(gsr, ctx):
+    caps = []
+    for name in ["tiny", "lego_early", "small", "lego_early"]:
+        wl = gen.make(name)
+        g = run_gpu(gsr, ctx, wl, backward=False)
+        check_bins(g, run_oracle(wl, backward=False))
+        caps.append(ctx.bin_stats()["capacity"])
+    assert caps == sorted(caps)          # grow-only
+    assert caps[-1] == caps[1]           # reused, not regrown
+
+
+def test_backward_variants_single_pixel_bit_equal(gsr, ctx):
+    """dL/dout nonzero at one pixel: one nonzero term per splat, so every
+    backward variant must give the same bits ("W1 warp sparse skip + exp-skip",
+    section 1, parity (2))."""
+    wl = gen.overlap_fixture(32)
+    dl = np.zeros_like(wl.dl_dout)
+    dl[15 * 32 + 17, :3] = [0.3, -1.2, 0.7]
+    wl.dl_dout = dl
+    results = []
+    for skip in (1, 0):
+        for lc in (1, 0):
+            ctx.set_option("bwd_warp_skip", skip)
+            ctx.set_option("bwd_last_contrib", lc)
+            results.append(run_gpu(gsr, ctx, wl)["grad"])
+    ctx.set_option("bwd_warp_skip", 1)
+    ctx.set_option("bwd_last_contrib", 1)
+    for r in results[1:]:
+        assert np.array_equal(r.view(np.uint32), results[0].view(np.uint32))
+    assert np.any(results[0] != 0)
+    check_backward({"grad": results[0]}, run_oracle(wl))
+
+
+def test_backward_variants_agree(gsr, ctx):
+    wl = gen.small()
+    o = run_oracle(wl)
+    for skip in (0, 1):
+        for lc in (0, 1):
+            ctx.set_option("bwd_warp_skip", skip)
+            ctx.set_option("bwd_last_contrib", lc)
+            check_backward(run_gpu(gsr, ctx, wl), o)
+    ctx.set_option("bwd_warp_skip", 1)
+    ctx.set_option("bwd_last_contrib", 1)
+
+
+def test_self_noise(gsr, ctx):
+    """Run-to-run spread of the atomically accumulated gradients (the pages'
+    self-noise protocol: 20 repeats, "M3 per-splat backward", section 2)."""
+    wl = gen.small()
+    sp, dp, dl = to_dev(wl.splats), to_dev(wl.depths), to_dev(wl.dl_dout)
+    bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+    out, t, last = gsr.rasterize_forward(ctx, sp, bins)
+    runs = [gsr.rasterize_backward(ctx, sp, bins, dl, t, last).cpu().numpy() for _ in range(20)]
+    ref = runs[0]
+    worst = max(float(np.max(np.abs(r - ref) / (np.abs(ref) + 1e-3))) for r in runs[1:])
+    print("self-noise max_rel", worst)
+    assert worst < 1e-4
+
+
+def test_forward_deterministic(gsr, ctx):
+    wl = gen.lego_early()
+    a = run_gpu(gsr, ctx, wl, backward=False)
+    b = run_gpu(gsr, ctx, wl, backward=False)
+    for k in ("keys", "idx", "ranges", "out", "final_T", "last"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_invalid_arguments(gsr, ctx):
+    dev = "cuda:0"
+    sp = torch.zeros((4, 9), dtype=torch.float32, device=dev)
+    dp = torch.ones(4, dtype=torch.float32, device=dev)
+    with pytest.raises(gsr.GsrError) as e:
+        gsr.bin_splats(ctx, sp, dp, 0, 16)
+    assert e.value.code == 1
+    with pytest.raises(gsr.GsrError):
+        gsr.bin_splats(ctx, sp, dp, 16, (1 << 19) + 1)
+    bins = gsr.bin_splats(ctx, sp, dp, 16, 16)
+    with pytest.raises(gsr.GsrError):   # n differs from the bins'
+        gsr.rasterize_forward(ctx, sp[:3], bins)
+    base = torch.zeros(256 * 4 + 1, dtype=torch.float32, device=dev)
+    misaligned = base[1:].view(256, 4)
+    with pytest.raises(gsr.GsrError) as e:
+        gsr.rasterize_forward(ctx, sp, bins, out_rgbw=misaligned)
+    assert e.value.code == 1
+    with pytest.raises(ValueError):
+        gsr.bin_splats(ctx, sp.double(), dp, 16, 16)
+
+
+def test_launch_count(gsr, ctx):
+    wl = gen.tiny()
+    before = ctx.launch_count()
+    run_gpu(gsr, ctx, wl)
+    assert ctx.launch_count() > before + 5
