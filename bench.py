@@ -59,6 +59,8 @@ def parse_args(argv=None):
     p.add_argument("--config", default="lego_final", choices=sorted(gen.CONFIGS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--min-warm-s", type=float, default=1.5,
+                   help="keep warming up until this many seconds passed (clock sampling)")
     return p.parse_args(argv)
 
 
@@ -310,7 +312,7 @@ def gpu_arm(args):
     # clock sampler sees the GPU under this load before the timed region.
     t_warm = time.perf_counter()
     k = 0
-    while k < args.warmup or time.perf_counter() - t_warm < 1.5:
+    while k < args.warmup or time.perf_counter() - t_warm < args.min_warm_s:
         flush.fill_(float(k))
         step(new_events())
         k += 1

@@ -98,6 +98,7 @@ void gsr_destroy(gsr_ctx *ctx)
         cudaFree(ctx->radix_totals);
         cudaFree(ctx->scalars);
         cudaFree(ctx->plan);
+        cudaFree(ctx->grad_acc);
         if (ctx->host_total) cudaFreeHost(ctx->host_total);
     }
     delete ctx;

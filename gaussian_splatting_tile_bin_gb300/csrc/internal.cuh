@@ -58,6 +58,8 @@ struct gsr_ctx {
     unsigned long long *scalars = nullptr;      // [0] pair total, [1] AND of keys, [2] OR of keys
     gsr::RadixPlan *plan = nullptr;
     unsigned long long *host_total = nullptr;   // pinned
+    size_t cap_grad_acc = 0;
+    double *grad_acc = nullptr;                 // [9 * cap] backward accumulator
 
     // Last binning, for gsr_get_bin_stats.
     cudaStream_t last_stream = nullptr;

@@ -9,12 +9,15 @@
 // Both kernels evaluate a splat at a pixel through the same two inline
 // functions (splat_sigma, splat_alpha), so the backward takes exactly the
 // forward's skip and stop decisions.
+#include <algorithm>
+
 #include "internal.cuh"
 
 namespace gsr {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int SM_BLOCKS_CAP = 152 * 16;     // grid-stride cap for elementwise passes
 constexpr float kAlphaMin = 1.0f / 255.0f;  // "W1 warp sparse skip + exp-skip", body
 constexpr float kAlphaMax = 0.999f;         // "A.9 f16 forward", snippet
 constexpr float kSigmaSkip = 5.55f;         // "W1 warp sparse skip + exp-skip", section 1, W1b
@@ -24,8 +27,8 @@ constexpr float kTMin = 1e-4f;              // stop once the transmittance would
 constexpr float kLn255Margin = 5.5412636f + 1e-3f;
 
 // Staged splat, three 16-byte vectors per batch slot.
-//   geo = (mean_x, mean_y, a / 2, b)
-//   aux = (c / 2, color_a, sigma bound, splat index as bits)
+//   geo = (mean_x, mean_y, a, b)
+//   aux = (c, color_a, sigma bound, splat index as bits)
 //   rgb = (r, g, b, 0)
 // The sigma bound is min(5.55, ln(color_a) + ln 255 + margin): an evaluation
 // with sigma at or above it is skipped without computing an exponential.  At
@@ -46,26 +49,31 @@ __device__ __forceinline__ void stage_splat(StagedBatch &sb, int slot, const flo
     const float r = __ldg(s + 5), g = __ldg(s + 6), bl = __ldg(s + 7);
     const float o = __ldg(s + 8);
     const float bound = fminf(kSigmaSkip, __logf(o) + kLn255Margin);
-    sb.geo[slot] = make_float4(mx, my, 0.5f * a, b);
-    sb.aux[slot] = make_float4(0.5f * c, o, bound, __uint_as_float(idx));
+    sb.geo[slot] = make_float4(mx, my, a, b);
+    sb.aux[slot] = make_float4(c, o, bound, __uint_as_float(idx));
     sb.rgb[slot] = make_float4(r, g, bl, 0.0f);
 }
 
-// sigma = 1/2 (a dx^2 + c dy^2) + b dx dy = dx (a/2 dx + b dy) + c/2 dy dy
-__device__ __forceinline__ float splat_sigma(const float4 geo, const float half_c, float px, float py,
+// sigma = 1/2 (a dx^2 + c dy^2) + b dx dy, evaluated in exactly that order with
+// one rounding per operation (no contraction), so every implementation that
+// follows the formula's order gets the same bits.
+__device__ __forceinline__ float splat_sigma(const float4 geo, const float c, float px, float py,
                                              float &dx, float &dy)
 {
-    dx = px - geo.x;
-    dy = py - geo.y;
-    const float t = __fmaf_rn(geo.w, dy, __fmul_rn(geo.z, dx));
-    return __fmaf_rn(dx, t, __fmul_rn(__fmul_rn(half_c, dy), dy));
+    dx = __fsub_rn(px, geo.x);
+    dy = __fsub_rn(py, geo.y);
+    const float q = __fadd_rn(__fmul_rn(__fmul_rn(geo.z, dx), dx), __fmul_rn(__fmul_rn(c, dy), dy));
+    return __fadd_rn(__fmul_rn(0.5f, q), __fmul_rn(__fmul_rn(geo.w, dx), dy));
 }
 
-// alpha = min(0.999, color_a exp(-sigma)); also returns exp(-sigma) and the
-// unclamped product for the backward.
+// alpha = min(0.999, color_a exp(-sigma)) ("A.9 f16 forward", snippet); also
+// returns exp(-sigma) and the unclamped product for the backward.  expf is the
+// accurate exponential (within 2 ulp): a deep pixel's colour error grows with the
+// sum of its alphas times the per-splat alpha error, and the 1e-5 forward
+// tolerance leaves no room for the approximate one.
 __device__ __forceinline__ float splat_alpha(float sigma, float o, float &e, float &raw)
 {
-    e = __expf(-sigma);
+    e = expf(-sigma);
     raw = __fmul_rn(o, e);
     return fminf(kAlphaMax, raw);
 }
@@ -111,16 +119,16 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
                 float e, raw;
                 const float alpha = splat_alpha(sigma, aux.y, e, raw);
                 if (alpha < kAlphaMin) continue;
-                const float next_T = T * (1.0f - alpha);
+                const float next_T = __fmul_rn(T, __fsub_rn(1.0f, alpha));
                 if (next_T < kTMin) {
                     done = true;
                     break;
                 }
-                const float w = alpha * T;
+                const float w = __fmul_rn(alpha, T);
                 const float4 c = sb.rgb[j];
-                C.x = __fmaf_rn(c.x, w, C.x);
-                C.y = __fmaf_rn(c.y, w, C.y);
-                C.z = __fmaf_rn(c.z, w, C.z);
+                C.x = __fadd_rn(C.x, __fmul_rn(c.x, w));
+                C.y = __fadd_rn(C.y, __fmul_rn(c.y, w));
+                C.z = __fadd_rn(C.z, __fmul_rn(c.z, w));
                 T = next_T;
                 last = bstart - range.x + (uint32_t)j + 1u;
             }
@@ -128,7 +136,7 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
     }
     if (inside) {
         const size_t p = (size_t)y * width + x;
-        out_rgbw[p] = make_float4(C.x, C.y, C.z, 1.0f - T);
+        out_rgbw[p] = make_float4(C.x, C.y, C.z, __fsub_rn(1.0f, T));
         final_T[p] = T;
         last_out[p] = last;
     }
@@ -141,7 +149,7 @@ __global__ void __launch_bounds__(kTilePixels)
 k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
            const uint2 *__restrict__ ranges, int width, int height, int tiles_x,
            const float4 *__restrict__ dl_dout, const float *__restrict__ final_T,
-           const uint32_t *__restrict__ last_in, float *__restrict__ grad)
+           const uint32_t *__restrict__ last_in, double *__restrict__ grad_acc)
 {
     __shared__ StagedBatch sb;
     __shared__ uint32_t s_wmax[kTilePixels / 32];
@@ -204,8 +212,13 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                     if (alpha >= kAlphaMin) {
                         contrib = true;
                         const float4 c = sb.rgb[j];
-                        const float inv = __fdividef(1.0f, 1.0f - alpha);
-                        const float Tj = T * inv;  // transmittance in front of this splat
+                        const float one_m = __fsub_rn(1.0f, alpha);
+                        const float inv = __fdividef(1.0f, one_m);
+                        // Transmittance in front of this splat: the forward's
+                        // T_j (1 - alpha) undone with one correctly rounded division,
+                        // so a pixel replayed through hundreds of splats drifts by at
+                        // most a rounding per splat.
+                        const float Tj = __fdiv_rn(T, one_m);
                         const float aT = alpha * Tj;
                         v[5] = g.x * aT;
                         v[6] = g.y * aT;
@@ -219,7 +232,7 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                         const float dRaw = raw < kAlphaMax ? dA : 0.0f;
                         v[8] = dRaw * e;
                         const float dSig = -dRaw * raw;
-                        const float a = 2.0f * geo.z, b = geo.w, cc = 2.0f * aux.x;
+                        const float a = geo.z, b = geo.w, cc = aux.x;
                         v[0] = -dSig * __fmaf_rn(a, dx, b * dy);
                         v[1] = -dSig * __fmaf_rn(b, dx, cc * dy);
                         v[2] = dSig * (0.5f * dx * dx);
@@ -236,14 +249,24 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(kFull, v[k], o);
             }
+            // One atomic per warp, splat and field, accumulated in double: a
+            // large splat sums thousands of warp partials of both signs, and in
+            // float their order alone moves the result by more than 1e-4.
             if (lane == 0) {
                 const uint32_t idx = __float_as_uint(sb.aux[j].w);
-                float *gr = grad + 9 * (size_t)idx;
+                double *gr = grad_acc + 9 * (size_t)idx;
 #pragma unroll
-                for (int k = 0; k < 9; ++k) atomicAdd(gr + k, v[k]);
+                for (int k = 0; k < 9; ++k) atomicAdd(gr + k, (double)v[k]);
             }
         }
     }
+}
+
+__global__ void k_grad_to_float(const double *__restrict__ acc, float *__restrict__ grad, size_t count)
+{
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count;
+         i += (size_t)gridDim.x * blockDim.x)
+        grad[i] = (float)acc[i];
 }
 
 }  // namespace
@@ -263,7 +286,18 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
                        const float *dl_dout, const float *final_T, const uint32_t *last_contrib,
                        float *grad, cudaStream_t stream)
 {
-    int rc = cuda_check(ctx, cudaMemsetAsync(grad, 0, (size_t)n * 9 * sizeof(float), stream),
+    const size_t count = (size_t)n * 9;
+    if (count > ctx->cap_grad_acc || !ctx->grad_acc) {
+        if (ctx->grad_acc) cudaFree(ctx->grad_acc);
+        ctx->grad_acc = nullptr;
+        ctx->cap_grad_acc = 0;
+        if (cudaMalloc(&ctx->grad_acc, count * sizeof(double)) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the gradient accumulator");
+        }
+        ctx->cap_grad_acc = count;
+    }
+    int rc = cuda_check(ctx, cudaMemsetAsync(ctx->grad_acc, 0, count * sizeof(double), stream),
                         "cudaMemsetAsync");
     if (rc) return rc;
     const int num_tiles = bins->tiles_x * bins->tiles_y;
@@ -271,14 +305,18 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
         kernel<<<num_tiles, kTilePixels, 0, stream>>>(
             splats, bins->sorted_idx, reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width,
             bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
-            last_contrib, grad);
+            last_contrib, ctx->grad_acc);
     };
     if (ctx->opt_warp_skip && ctx->opt_last_contrib) launch(k_backward<true, true>);
     else if (ctx->opt_warp_skip) launch(k_backward<true, false>);
     else if (ctx->opt_last_contrib) launch(k_backward<false, true>);
     else launch(k_backward<false, false>);
     ++ctx->launches;
-    return cuda_check(ctx, cudaGetLastError(), "backward launch");
+    if ((rc = cuda_check(ctx, cudaGetLastError(), "backward launch"))) return rc;
+    const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)SM_BLOCKS_CAP);
+    k_grad_to_float<<<blocks, 256, 0, stream>>>(ctx->grad_acc, grad, count);
+    ++ctx->launches;
+    return cuda_check(ctx, cudaGetLastError(), "gradient conversion launch");
 }
 
 }  // namespace gsr

@@ -55,10 +55,10 @@ def _load():
     lib.orc_radix_passes_4bit.restype = i32
     for sfx in ("f32", "f64"):
         fw = getattr(lib, f"orc_forward_{sfx}")
-        fw.argtypes = [P, P, P, i32, i32, P, P, P, P, f64, P]
+        fw.argtypes = [P, P, P, i32, i32, P, P, P, P, f64, f64, P]
         fw.restype = None
         bw = getattr(lib, f"orc_backward_{sfx}")
-        bw.argtypes = [P, i32, P, P, i32, i32, P, P, P, f64, P]
+        bw.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, f64, f64, P]
         bw.restype = None
     for name in ("orc_forward_untiled_f32", "orc_forward_untiled_noskip_f32"):
         fn = getattr(lib, name)
@@ -114,7 +114,7 @@ def radix_passes_4bit(num_tiles: int) -> int:
     return int(_load().orc_radix_passes_4bit(num_tiles))
 
 
-def forward(splats, idx, ranges, width, height, *, f64=False, eps_alpha=0.0):
+def forward(splats, idx, ranges, width, height, *, f64=False, eps_alpha=0.0, sigma_ulps=8.0):
     """Tiled forward.  Returns dict(out [H*W,4], final_T, last, margin, counters)."""
     lib = _load()
     dt = np.float64 if f64 else np.float32
@@ -129,7 +129,7 @@ def forward(splats, idx, ranges, width, height, *, f64=False, eps_alpha=0.0):
     cnt = np.zeros(3, dtype=np.int64)
     fn = lib.orc_forward_f64 if f64 else lib.orc_forward_f32
     fn(_ptr(s), _ptr(ix), _ptr(rg), width, height, _ptr(out), _ptr(final_t), _ptr(last),
-       _ptr(margin), float(eps_alpha), _ptr(cnt))
+       _ptr(margin), float(eps_alpha), float(sigma_ulps), _ptr(cnt))
     return {"out": out, "final_T": final_t, "last": last, "margin": margin,
             "counters": {"n_eval": int(cnt[0]), "n_exp": int(cnt[1]), "n_contrib": int(cnt[2])}}
 
@@ -146,8 +146,10 @@ def forward_untiled(splats, depths, width, height, *, sigma_skip=True):
     return {"out": out, "final_T": final_t, "last": last}
 
 
-def backward(splats, idx, ranges, width, height, dl_dout, *, f64=False, eps_alpha=0.0):
-    """Returns dict(grad float64 [N,9], knife bool [N], counters)."""
+def backward(splats, idx, ranges, width, height, dl_dout, *, f64=False, eps_alpha=0.0,
+             sigma_ulps=8.0):
+    """Returns dict(grad float64 [N,9], gabs float64 [N,9] (sum of |per-pixel term|),
+    knife bool [N], counters)."""
     lib = _load()
     dt = np.float64 if f64 else np.float32
     s = np.ascontiguousarray(splats, dtype=dt).reshape(-1, 9)
@@ -156,10 +158,11 @@ def backward(splats, idx, ranges, width, height, dl_dout, *, f64=False, eps_alph
     g = np.ascontiguousarray(dl_dout, dtype=dt).reshape(-1, 4)
     n = s.shape[0]
     grad = np.zeros((n, 9), dtype=np.float64)
+    gabs = np.zeros((n, 9), dtype=np.float64)
     knife = np.zeros(n, dtype=np.uint8)
     cnt = np.zeros(3, dtype=np.int64)
     fn = lib.orc_backward_f64 if f64 else lib.orc_backward_f32
-    fn(_ptr(s), n, _ptr(ix), _ptr(rg), width, height, _ptr(g), _ptr(grad), _ptr(knife),
-       float(eps_alpha), _ptr(cnt))
-    return {"grad": grad, "knife": knife.astype(bool),
+    fn(_ptr(s), n, _ptr(ix), _ptr(rg), width, height, _ptr(g), _ptr(grad), _ptr(gabs), _ptr(knife),
+       float(eps_alpha), float(sigma_ulps), _ptr(cnt))
+    return {"grad": grad, "gabs": gabs, "knife": knife.astype(bool),
             "counters": {"n_eval": int(cnt[0]), "n_exp": int(cnt[1]), "n_contrib": int(cnt[2])}}

@@ -232,7 +232,7 @@ static void forward_untiled(const float *splats, const float *depths, int32_t n,
                 uint32_t i = order[k].idx;
                 const int32_t *r = rects + 4 * (int64_t)i;
                 if (!alive[i] || tx < r[0] || tx > r[2] || ty < r[1] || ty > r[3]) continue;
-                composite_f32(&st, splats + 9 * (int64_t)i, (float)px, (float)py, pos, 0.0,
+                composite_f32(&st, splats + 9 * (int64_t)i, (float)px, (float)py, pos, 0.0, 0.0,
                               cnt, skip_sigma, NULL);
                 ++pos;
             }

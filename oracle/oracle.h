@@ -57,14 +57,17 @@ int32_t orc_radix_passes_4bit(uint64_t num_tiles);
  * w = 1 - final_T); final_T, last (1 + position of the last composited splat
  * within the tile's range, 0 if none).  margin (nullable): per pixel, the
  * smallest ratio of a threshold decision's distance to its rounding
- * uncertainty, given eps_alpha = the relative uncertainty of one alpha.
+ * uncertainty, given eps_alpha = the relative uncertainty of one exponential
+ * and sigma_ulps = the half-ulps of uncertainty of sigma's terms.
  * counters (nullable): 3 int64. */
 void orc_forward_f32(const float *splats, const uint32_t *idx, const uint32_t *ranges,
                      int32_t width, int32_t height, float *out_rgbw, float *final_T,
-                     uint32_t *last, float *margin, double eps_alpha, int64_t *counters);
+                     uint32_t *last, float *margin, double eps_alpha, double sigma_ulps,
+                     int64_t *counters);
 void orc_forward_f64(const double *splats, const uint32_t *idx, const uint32_t *ranges,
                      int32_t width, int32_t height, double *out_rgbw, double *final_T,
-                     uint32_t *last, float *margin, double eps_alpha, int64_t *counters);
+                     uint32_t *last, float *margin, double eps_alpha, double sigma_ulps,
+                     int64_t *counters);
 
 /* Brute-force forward without tile lists: every pixel walks all splats in
  * (depth_bits, index) order and admits a splat iff its tile rectangle holds the
@@ -81,16 +84,17 @@ void orc_forward_untiled_noskip_f32(const float *splats, const float *depths, in
 
 /* Backward: gradient of L = sum_p sum_ch dl_dout[p][ch] * out[p][ch] (ch = rgb;
  * w carries no gradient) with respect to the 9 Splat2D fields, accumulated in
- * double into grad[n*9] (overwritten).  knife (nullable, n bytes): set for each
+ * double into grad[n*9] (overwritten).  gabs (nullable, n*9): the sums of the
+ * absolute values of the per-pixel terms of each gradient.  knife (nullable, n bytes): set for each
  * splat examined at a pixel whose margin is below 1, or composited with its
  * unclamped alpha within its uncertainty of the 0.999 cap. */
 void orc_backward_f32(const float *splats, int32_t n, const uint32_t *idx,
                       const uint32_t *ranges, int32_t width, int32_t height,
-                      const float *dl_dout, double *grad, uint8_t *knife,
-                      double eps_alpha, int64_t *counters);
+                      const float *dl_dout, double *grad, double *gabs, uint8_t *knife,
+                      double eps_alpha, double sigma_ulps, int64_t *counters);
 void orc_backward_f64(const double *splats, int32_t n, const uint32_t *idx,
                       const uint32_t *ranges, int32_t width, int32_t height,
-                      const double *dl_dout, double *grad, uint8_t *knife,
-                      double eps_alpha, int64_t *counters);
+                      const double *dl_dout, double *grad, double *gabs, uint8_t *knife,
+                      double eps_alpha, double sigma_ulps, int64_t *counters);
 
 #endif

@@ -5,13 +5,21 @@ import torch
 
 import oracle
 
-# Relative uncertainty of one alpha between the two sides' exponentials
-# (the kernel's ex2.approx-based exp and its exponent rounding against the
-# oracle's correctly rounded one), with a safety factor of about three.
-EPS_ALPHA = 2e-6
+# Relative uncertainty of one exponential between the two sides: the kernel's
+# expf is within 2 ulp, the oracle's correctly rounded, so 2.5 ulp apart at
+# most; doubled.  The kernel evaluates sigma in the oracle's operation order
+# with one rounding per operation, so sigma itself carries no uncertainty.
+EPS_ALPHA = 6e-7
+SIGMA_ULPS = 0.0
 FWD_TOL = 1e-5          # absolute, per channel of out_rgbw and final_T
-GRAD_ATOL = 1e-4        # |g - g_ref| <= GRAD_ATOL + GRAD_RTOL |g_ref|
+GRAD_ATOL = 1e-4        # |g - g_ref| <= GRAD_ATOL + GRAD_RTOL |g_ref| + GRAD_COND sum|t|
 GRAD_RTOL = 1e-4
+# A gradient is a sum of per-pixel terms t.  A float evaluation of each term
+# carries a few roundings, so its error is bounded by about k u sum|t|
+# (u = 2^-24).  When the terms cancel (sum|t| >> |sum t|, condition numbers of
+# 1e4 and more occur for the conic of large elongated splats) that bound, not
+# 1e-4, is what any float implementation can promise; k = 8.
+GRAD_COND = 8 * 2.0 ** -24
 
 
 def to_dev(a, dev="cuda:0"):
@@ -38,11 +46,12 @@ def run_gpu(gsr, ctx, wl, backward=True, dev="cuda:0"):
 
 def run_oracle(wl, backward=True):
     keys, idx, ranges = oracle.bin_splats(wl.splats, wl.depths, wl.width, wl.height)
-    f = oracle.forward(wl.splats, idx, ranges, wl.width, wl.height, eps_alpha=EPS_ALPHA)
+    f = oracle.forward(wl.splats, idx, ranges, wl.width, wl.height, eps_alpha=EPS_ALPHA,
+                       sigma_ulps=SIGMA_ULPS)
     res = {"keys": keys, "idx": idx, "ranges": ranges, "fwd": f}
     if backward:
         res["bwd"] = oracle.backward(wl.splats, idx, ranges, wl.width, wl.height, wl.dl_dout,
-                                     eps_alpha=EPS_ALPHA)
+                                     eps_alpha=EPS_ALPHA, sigma_ulps=SIGMA_ULPS)
     return res
 
 
@@ -73,7 +82,9 @@ def check_backward(g, o, max_knife_frac=5e-3):
     b = o["bwd"]
     ref = b["grad"]
     diff = np.abs(g["grad"].astype(np.float64) - ref)
-    bad = np.any(diff > GRAD_ATOL + GRAD_RTOL * np.abs(ref), axis=1)
+    plain_tol = GRAD_ATOL + GRAD_RTOL * np.abs(ref)
+    bad = np.any(diff > plain_tol + GRAD_COND * b["gabs"], axis=1)
+    cond_used = int(np.sum(diff > plain_tol))
     unexplained = np.nonzero(bad & ~b["knife"])[0]
     assert unexplained.size == 0, (
         f"{unexplained.size} splats' gradients differ away from knife-edges; first "
@@ -83,7 +94,8 @@ def check_backward(g, o, max_knife_frac=5e-3):
     rel = diff[ok] / (np.abs(ref[ok]) + 1e-3)
     return {"max_abs": float(diff[ok].max()) if ok.any() else 0.0,
             "max_rel": float(rel.max()) if ok.any() else 0.0,
-            "knife_splats": int(b["knife"].sum()), "knife_diff_splats": int(bad.sum())}
+            "knife_splats": int(b["knife"].sum()), "knife_diff_splats": int(bad.sum()),
+            "components_beyond_1e-4_within_cond_bound": cond_used}
 
 
 def varying_digit_mask(keys, digits):

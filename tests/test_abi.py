@@ -19,8 +19,8 @@ def _declared_functions():
 
 @pytest.fixture(scope="module")
 def lib():
-    from gaussian_splatting_tile_bin_gb300 import build
-    path = build.build()
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
     return ctypes.CDLL(path)
 
 
@@ -36,8 +36,8 @@ def test_exports_every_declared_symbol(lib):
     assert exported == set(names)
 
 
-def test_struct_layouts_match_binding(tmp_path):
-    from gaussian_splatting_tile_bin_gb300 import _abi  # noqa: F401  (loads without a GPU)
+def test_struct_layouts_match_binding(tmp_path, lib):
+    from gaussian_splatting_tile_bin_gb300 import _abi  # loads without a GPU
     src = tmp_path / "layout.c"
     src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gsr.h"\n'
                    'int main(void){printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(gsr_splat2d),'

@@ -200,11 +200,15 @@ def test_self_noise(gsr, ctx):
     sp, dp, dl = to_dev(wl.splats), to_dev(wl.depths), to_dev(wl.dl_dout)
     bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
     out, t, last = gsr.rasterize_forward(ctx, sp, bins)
-    runs = [gsr.rasterize_backward(ctx, sp, bins, dl, t, last).cpu().numpy() for _ in range(20)]
+    runs = [gsr.rasterize_backward(ctx, sp, bins, dl, t, last).cpu().numpy().astype(np.float64)
+            for _ in range(20)]
     ref = runs[0]
-    worst = max(float(np.max(np.abs(r - ref) / (np.abs(ref) + 1e-3))) for r in runs[1:])
-    print("self-noise max_rel", worst)
-    assert worst < 1e-4
+    # Spread in units of the parity tolerance (1e-4 + 1e-4 |g|): atomics may
+    # reorder the sums but must stay far inside it.
+    worst = max(float(np.max(np.abs(r - ref) / (1e-4 + 1e-4 * np.abs(ref)))) for r in runs[1:])
+    max_rel = max(float(np.max(np.abs(r - ref) / np.maximum(np.abs(ref), 1e-6))) for r in runs[1:])
+    print("self-noise: max |d| / tolerance", worst, "max_rel", max_rel)
+    assert worst < 0.1
 
 
 def test_forward_deterministic(gsr, ctx):
