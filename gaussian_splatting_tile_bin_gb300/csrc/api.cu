@@ -177,6 +177,32 @@ int gsr_rasterize_backward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n, c
                                    final_T, last_contrib, grad, (cudaStream_t)stream);
 }
 
+int gsr_rasterize_backward_noalloc(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n,
+                                   const gsr_bins *bins, const float *dl_dout, const float *final_T,
+                                   const uint32_t *last_contrib, float *grad, void *stream)
+{
+    if (!ctx) return GSR_ERR_INVALID_ARG;
+    ctx->err.clear();
+    if (n < 0 || n > GSR_NOALLOC_MAX_SPLATS)
+        return fail(ctx, GSR_ERR_INVALID_ARG,
+                    "n = " + std::to_string(n) + " is outside [0, GSR_NOALLOC_MAX_SPLATS = " +
+                        std::to_string(GSR_NOALLOC_MAX_SPLATS) + "]");
+    int rc = check_bins(ctx, bins, n);
+    if (rc) return rc;
+    if (!dl_dout || !final_T || !last_contrib || (n > 0 && !grad))
+        return fail(ctx, GSR_ERR_INVALID_ARG, "an input/output pointer is NULL");
+    if (bins->num_pairs > 0 && !splats) return fail(ctx, GSR_ERR_INVALID_ARG, "splats is NULL");
+    if (!aligned(dl_dout, 16) || !aligned(final_T, 4) || !aligned(last_contrib, 4) ||
+        !aligned(grad, 4) || !aligned(splats, 4))
+        return fail(ctx, GSR_ERR_INVALID_ARG, "misaligned buffer (dl_dout needs 16 bytes)");
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, GSR_ERR_CUDA, "cannot select the context's device");
+    if (n == 0) return GSR_OK;
+    return gsr::rasterize_backward_noalloc(ctx, reinterpret_cast<const float *>(splats), n, bins,
+                                           dl_dout, final_T, last_contrib, grad,
+                                           (cudaStream_t)stream);
+}
+
 int gsr_get_bin_stats(gsr_ctx *ctx, gsr_bin_stats *out)
 {
     if (!ctx || !out) return GSR_ERR_INVALID_ARG;

@@ -81,5 +81,8 @@ int rasterize_forward(gsr_ctx *ctx, const float *splats, const gsr_bins *bins, f
 int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_bins *bins,
                        const float *dl_dout, const float *final_T, const uint32_t *last_contrib,
                        float *grad, cudaStream_t stream);
+int rasterize_backward_noalloc(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_bins *bins,
+                               const float *dl_dout, const float *final_T,
+                               const uint32_t *last_contrib, float *grad, cudaStream_t stream);
 
 }  // namespace gsr

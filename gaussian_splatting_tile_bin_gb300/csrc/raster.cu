@@ -10,6 +10,7 @@
 // functions (splat_sigma, splat_alpha), so the backward takes exactly the
 // forward's skip and stop decisions.
 #include <algorithm>
+#include <string>
 
 #include "internal.cuh"
 
@@ -315,6 +316,66 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
     if ((rc = cuda_check(ctx, cudaGetLastError(), "backward launch"))) return rc;
     const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)SM_BLOCKS_CAP);
     k_grad_to_float<<<blocks, 256, 0, stream>>>(ctx->grad_acc, grad, count);
+    ++ctx->launches;
+    return cuda_check(ctx, cudaGetLastError(), "gradient conversion launch");
+}
+
+// --- backward without allocation ---------------------------------------------
+//
+// For callers that cannot call cudaMalloc, rasterize_backward_noalloc runs the
+// same backward kernels with the double-precision accumulator in this fixed
+// device array instead of the context's arena.  Every GPU that loads the
+// library holds the array until the process exits.
+
+namespace {
+
+__device__ __align__(256) double g_noalloc_grad_acc[(size_t)GSR_NOALLOC_MAX_SPLATS * 9];
+
+// Device address of g_noalloc_grad_acc, looked up once per device (the array's
+// name in host code is only a stand-in, not a device pointer).
+double *g_noalloc_ptr[64] = {};
+
+}  // namespace
+
+int rasterize_backward_noalloc(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_bins *bins,
+                               const float *dl_dout, const float *final_T,
+                               const uint32_t *last_contrib, float *grad, cudaStream_t stream)
+{
+    if (n > GSR_NOALLOC_MAX_SPLATS)
+        return fail(ctx, GSR_ERR_INVALID_ARG,
+                    "n = " + std::to_string(n) + " exceeds GSR_NOALLOC_MAX_SPLATS (" +
+                        std::to_string(GSR_NOALLOC_MAX_SPLATS) + ")");
+    if (ctx->device < 0 || ctx->device >= 64)
+        return fail(ctx, GSR_ERR_INVALID_ARG, "device ordinal out of range for the fixed scratch table");
+    double *acc = g_noalloc_ptr[ctx->device];
+    if (!acc) {
+        // First call on this device (the device is current here): find the
+        // array's device address.
+        void *p = nullptr;
+        int rc = cuda_check(ctx, cudaGetSymbolAddress(&p, g_noalloc_grad_acc), "cudaGetSymbolAddress");
+        if (rc) return rc;
+        acc = static_cast<double *>(p);
+        g_noalloc_ptr[ctx->device] = acc;
+    }
+    const size_t count = (size_t)n * 9;
+    // The array keeps the previous call's sums: clear the part this call uses.
+    int rc = cuda_check(ctx, cudaMemsetAsync(acc, 0, count * sizeof(double), stream), "cudaMemsetAsync");
+    if (rc) return rc;
+    const int num_tiles = bins->tiles_x * bins->tiles_y;
+    auto launch = [&](auto kernel) {
+        kernel<<<num_tiles, kTilePixels, 0, stream>>>(
+            splats, bins->sorted_idx, reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width,
+            bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
+            last_contrib, acc);
+    };
+    if (ctx->opt_warp_skip && ctx->opt_last_contrib) launch(k_backward<true, true>);
+    else if (ctx->opt_warp_skip) launch(k_backward<true, false>);
+    else if (ctx->opt_last_contrib) launch(k_backward<false, true>);
+    else launch(k_backward<false, false>);
+    ++ctx->launches;
+    if ((rc = cuda_check(ctx, cudaGetLastError(), "backward launch"))) return rc;
+    const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)SM_BLOCKS_CAP);
+    k_grad_to_float<<<blocks, 256, 0, stream>>>(acc, grad, count);
     ++ctx->launches;
     return cuda_check(ctx, cudaGetLastError(), "gradient conversion launch");
 }

@@ -163,6 +163,29 @@ int gsr_rasterize_backward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n,
                            const gsr_bins *bins, const float *dl_dout, const float *final_T,
                            const uint32_t *last_contrib, float *grad, void *stream);
 
+/* Backward rasterization that allocates nothing.  The paper has no counterpart
+ * to this entry point; it exists for callers that cannot call cudaMalloc, for
+ * example code whose device memory is all reserved up front by another
+ * allocator, or loops that must not stall: cudaMalloc may synchronise the
+ * device, and it may fail in the middle of a step.
+ *
+ * Same arguments, result and errors as gsr_rasterize_backward, computed by the
+ * same kernels.  Its double-precision accumulator is a fixed device array of
+ * GSR_NOALLOC_MAX_SPLATS * 9 doubles (9 MiB), compiled into the library: every
+ * GPU that loads libgsr.so holds it until the process exits.  The caller
+ * still owns all inputs and outputs, and the bins come from gsr_bin_splats as
+ * usual (which does use the context's arena).
+ *   - n > GSR_NOALLOC_MAX_SPLATS is rejected with GSR_ERR_INVALID_ARG.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - All calls on a device share the one array, and each call clears the part
+ *     it uses before accumulating.  Calls whose work overlaps on the GPU (other
+ *     streams, other contexts, other threads) race on it: order them. */
+#define GSR_NOALLOC_MAX_SPLATS (1 << 17)
+int gsr_rasterize_backward_noalloc(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n,
+                                   const gsr_bins *bins, const float *dl_dout, const float *final_T,
+                                   const uint32_t *last_contrib, float *grad, void *stream);
+
 /* Statistics of the last gsr_bin_splats (synchronises its stream).
  * radix_passes: passes the sort executed; digit_mask: bit d set when 8-bit digit
  * d of the keys varied (pass d executed); capacity: arena capacity in pairs. */
