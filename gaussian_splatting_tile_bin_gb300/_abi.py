@@ -12,10 +12,11 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "lib", "libgsr.so")
+# GSR_LIBRARY selects another build of the same library (A/B of build flags).
+LIB_PATH = os.environ.get("GSR_LIBRARY") or os.path.join(_PKG, "lib", "libgsr.so")
 
 GSR_OK, GSR_ERR_INVALID_ARG, GSR_ERR_CUDA, GSR_ERR_OOM, GSR_ERR_TOO_MANY_PAIRS = range(5)
-OPTIONS = {"bwd_warp_skip": 1, "bwd_last_contrib": 2}
+OPTIONS = {"bwd_warp_skip": 1, "bwd_last_contrib": 2, "warp_cull": 3}
 
 
 class GsrError(RuntimeError):

@@ -41,6 +41,7 @@ struct gsr_ctx {
     uint64_t launches = 0;
     int opt_warp_skip = 1;
     int opt_last_contrib = 1;
+    int opt_warp_cull = 1;
 
     // Grow-only arena.
     size_t cap_pairs = 0;

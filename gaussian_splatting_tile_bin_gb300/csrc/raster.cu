@@ -3,22 +3,38 @@
 // One 256-thread CTA per 16x16 tile, one thread per pixel ("forward/adam
 // audit" (p3-forward-adam-audit), sections (a), (b), (e): 256-thread group per
 // tile staging local_batch[256] Splat2D records).  Each batch of the tile's
-// sorted range is staged in shared memory in a compute-ready form (mean, half
-// conic, colour, and a per-splat sigma bound); every thread then walks the batch.
+// sorted range is staged in shared memory in a compute-ready form.
 //
-// Both kernels evaluate a splat at a pixel through the same two inline
-// functions (splat_sigma, splat_alpha), so the backward takes exactly the
-// forward's skip and stop decisions.
+// Warps own 8x4-pixel blocks of the tile.  When a splat is staged, the thread
+// that stages it also marks which of the 8 blocks the splat can reach at all:
+// the set {sigma < bound} is an ellipse, and its bounding box (grown by a
+// margin that covers float rounding) is tested against each block.  A warp
+// walks only the splats marked for it, found 32 at a time with a ballot.  A
+// skipped evaluation could only have been skipped by the per-pixel tests as
+// well, so the results are bit-identical with and without this culling.
+//
+// Both kernels evaluate a splat at a pixel through the same inline functions
+// (splat_sigma, splat_alpha), so the backward takes exactly the forward's skip
+// and stop decisions.
 #include <algorithm>
 #include <string>
 
 #include "internal.cuh"
+
+// Resident CTAs per SM the raster kernels are compiled for (register budget).
+#ifndef GSR_FWD_MIN_BLOCKS
+#define GSR_FWD_MIN_BLOCKS 1
+#endif
+#ifndef GSR_BWD_MIN_BLOCKS
+#define GSR_BWD_MIN_BLOCKS 1
+#endif
 
 namespace gsr {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int SM_BLOCKS_CAP = 152 * 16;     // grid-stride cap for elementwise passes
+constexpr int kWarps = kTilePixels / 32;
 constexpr float kAlphaMin = 1.0f / 255.0f;  // "W1 warp sparse skip + exp-skip", body
 constexpr float kAlphaMax = 0.999f;         // "A.9 f16 forward", snippet
 constexpr float kSigmaSkip = 5.55f;         // "W1 warp sparse skip + exp-skip", section 1, W1b
@@ -27,7 +43,7 @@ constexpr float kTMin = 1e-4f;              // stop once the transmittance would
 // sigma exceeds ln(color_a) + this cannot reach alpha >= 1/255.
 constexpr float kLn255Margin = 5.5412636f + 1e-3f;
 
-// Staged splat, three 16-byte vectors per batch slot.
+// Staged splat, three 16-byte vectors per batch slot, plus the warp mask.
 //   geo = (mean_x, mean_y, a, b)
 //   aux = (c, color_a, sigma bound, splat index as bits)
 //   rgb = (r, g, b, 0)
@@ -39,10 +55,48 @@ struct StagedBatch {
     float4 geo[kTilePixels];
     float4 aux[kTilePixels];
     float4 rgb[kTilePixels];
+    uint32_t mask[kTilePixels];  // bit w: warp w's 8x4 block may see sigma < bound
 };
 
+// Warp w covers the 8x4 block (w & 1, w >> 1) of the tile; lane l the pixel
+// (l & 7, l >> 3) inside it.
+__device__ __forceinline__ int pixel_x(int tid) { return ((tid >> 5) & 1) * 8 + (tid & 7); }
+__device__ __forceinline__ int pixel_y(int tid) { return (tid >> 6) * 4 + ((tid >> 3) & 3); }
+
+// Which 8x4 blocks of the tile at (x0, y0) the ellipse {sigma < bound} can reach.
+// Its half-extents are sqrt(2 bound Sigma_xx) and sqrt(2 bound Sigma_yy).  The
+// computed sigma may be off by a few roundings of its terms, at most
+// 8u (|a| + |c| + 2|b|) / lambda_min relative, so the box is grown by four
+// times that (plus 1e-3 relative and 1e-3 px); a conic too ill-conditioned
+// for that bound to be small is not culled at all.
+template <bool kCull>
+__device__ __forceinline__ uint32_t block_mask(float mx, float my, float a, float b, float c,
+                                               float bound, int x0, int y0)
+{
+    if (!kCull) return 0xffu;
+    if (!(bound > 0.0f)) return 0u;
+    const float det = a * c - b * b;
+    const float half_tr = 0.5f * (a + c);
+    const float lam_min = half_tr - sqrtf(0.25f * (a - c) * (a - c) + b * b);
+    const float rel = 2e-6f * (fabsf(a) + fabsf(c) + 2.0f * fabsf(b)) / lam_min + 1e-3f;
+    if (!(det > 0.0f) || !(lam_min > 0.0f) || !(rel < 0.25f)) return 0xffu;
+    const float grow = 1.0f + rel;
+    const float rx = sqrtf(2.0f * bound * (c / det)) * grow + 1e-3f;
+    const float ry = sqrtf(2.0f * bound * (a / det)) * grow + 1e-3f;
+    uint32_t m = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const float bx0 = (float)(x0 + (w & 1) * 8), by0 = (float)(y0 + (w >> 1) * 4);
+        const bool hit = (mx - rx <= bx0 + 7.0f) && (mx + rx >= bx0) && (my - ry <= by0 + 3.0f) &&
+                         (my + ry >= by0);
+        m |= hit ? (1u << w) : 0u;
+    }
+    return m;
+}
+
+template <bool kCull>
 __device__ __forceinline__ void stage_splat(StagedBatch &sb, int slot, const float *__restrict__ splats,
-                                            uint32_t idx)
+                                            uint32_t idx, int x0, int y0)
 {
     const float *s = splats + 9 * (size_t)idx;
     const float mx = __ldg(s + 0), my = __ldg(s + 1);
@@ -53,6 +107,7 @@ __device__ __forceinline__ void stage_splat(StagedBatch &sb, int slot, const flo
     sb.geo[slot] = make_float4(mx, my, a, b);
     sb.aux[slot] = make_float4(c, o, bound, __uint_as_float(idx));
     sb.rgb[slot] = make_float4(r, g, bl, 0.0f);
+    sb.mask[slot] = block_mask<kCull>(mx, my, a, b, c, bound, x0, y0);
 }
 
 // sigma = 1/2 (a dx^2 + c dy^2) + b dx dy, evaluated in exactly that order with
@@ -79,21 +134,41 @@ __device__ __forceinline__ float splat_alpha(float sigma, float o, float &e, flo
     return fminf(kAlphaMax, raw);
 }
 
-__device__ __forceinline__ int pixel_x(int tid) { return tid & (kTile - 1); }
-__device__ __forceinline__ int pixel_y(int tid) { return tid >> 4; }
+// float -> double with integer operations only (this GPU's FP64 pipe is narrow
+// and the conversion would otherwise run there).  Subnormal floats become 0.
+__device__ __forceinline__ double widen(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    const uint32_t e = (u >> 23) & 0xffu;
+    const uint32_t hi_sign = u & 0x80000000u;
+    uint32_t hi, lo;
+    if (e == 0u) {
+        hi = hi_sign;
+        lo = 0u;
+    } else {
+        const uint32_t e64 = (e == 0xffu) ? 0x7ffu : e + 896u;
+        const uint32_t m = u & 0x7fffffu;
+        hi = hi_sign | (e64 << 20) | (m >> 3);
+        lo = m << 29;
+    }
+    return __hiloint2double((int)hi, (int)lo);
+}
 
 // --- forward ---------------------------------------------------------------
 
-__global__ void __launch_bounds__(kTilePixels)
+template <bool kCull>
+__global__ void __launch_bounds__(kTilePixels, GSR_FWD_MIN_BLOCKS)
 k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
           const uint2 *__restrict__ ranges, int width, int height, int tiles_x,
           float4 *__restrict__ out_rgbw, float *__restrict__ final_T, uint32_t *__restrict__ last_out)
 {
     __shared__ StagedBatch sb;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t wbit = 1u << warp;
     const int tile = blockIdx.x;
-    const int tx = tile % tiles_x, ty = tile / tiles_x;
-    const int x = tx * kTile + pixel_x(threadIdx.x);
-    const int y = ty * kTile + pixel_y(threadIdx.x);
+    const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
+    const int x = x0 + pixel_x(threadIdx.x);
+    const int y = y0 + pixel_y(threadIdx.x);
     const bool inside = x < width && y < height;
     const float px = (float)x, py = (float)y;
     const uint2 range = ranges[tile];
@@ -107,11 +182,16 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
         // Every pixel of the tile has stopped: no later splat can change it.
         if (__syncthreads_count(done) == kTilePixels) break;
         const uint32_t pos = bstart + threadIdx.x;
-        if (pos < range.y) stage_splat(sb, threadIdx.x, splats, __ldg(sorted_idx + pos));
+        if (pos < range.y) stage_splat<kCull>(sb, threadIdx.x, splats, __ldg(sorted_idx + pos), x0, y0);
         __syncthreads();
         const int cnt = (int)min(range.y - bstart, (uint32_t)kTilePixels);
-        if (!done) {
-            for (int j = 0; j < cnt; ++j) {
+        if (__all_sync(kFull, done)) continue;
+        for (int c0 = 0; c0 < cnt; c0 += 32) {
+            uint32_t m = __ballot_sync(kFull, c0 + lane < cnt && (sb.mask[c0 + lane] & wbit));
+            while (m) {
+                const int j = c0 + __ffs(m) - 1;
+                m &= m - 1;
+                if (done) continue;
                 const float4 geo = sb.geo[j];
                 const float4 aux = sb.aux[j];
                 float dx, dy;
@@ -123,7 +203,7 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
                 const float next_T = __fmul_rn(T, __fsub_rn(1.0f, alpha));
                 if (next_T < kTMin) {
                     done = true;
-                    break;
+                    continue;
                 }
                 const float w = __fmul_rn(alpha, T);
                 const float4 c = sb.rgb[j];
@@ -133,6 +213,7 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
                 T = next_T;
                 last = bstart - range.x + (uint32_t)j + 1u;
             }
+            if (__all_sync(kFull, done)) break;
         }
     }
     if (inside) {
@@ -145,20 +226,52 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
 
 // --- backward --------------------------------------------------------------
 
-template <bool kWarpSkip, bool kLastContrib>
-__global__ void __launch_bounds__(kTilePixels)
+// Sums the 9 per-lane values over the warp and adds the totals to acc[0..8] in
+// one atomic instruction: a transposed butterfly leaves component k (k < 8) in
+// lanes 4k..4k+3 after 7 shuffles, component 8 takes a plain butterfly, and
+// lanes 4k and lane 1 issue the adds.
+__device__ __forceinline__ void warp_reduce_add9(float (&v)[9], double *__restrict__ acc, int lane)
+{
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+    float w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = h16 ? v[i] : v[i + 4];
+        const float keep = h16 ? v[i + 4] : v[i];
+        w[i] = keep + __shfl_xor_sync(kFull, send, 16);
+    }
+    float x2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = h8 ? w[i] : w[i + 2];
+        const float keep = h8 ? w[i + 2] : w[i];
+        x2[i] = keep + __shfl_xor_sync(kFull, send, 8);
+    }
+    float y = (h4 ? x2[1] : x2[0]) + __shfl_xor_sync(kFull, h4 ? x2[0] : x2[1], 4);
+    y += __shfl_xor_sync(kFull, y, 2);
+    y += __shfl_xor_sync(kFull, y, 1);
+    float z = v[8];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
+    if ((lane & 3) == 0) atomicAdd(acc + (lane >> 2), widen(y));
+    else if (lane == 1) atomicAdd(acc + 8, widen(z));
+}
+
+template <bool kWarpSkip, bool kLastContrib, bool kCull>
+__global__ void __launch_bounds__(kTilePixels, GSR_BWD_MIN_BLOCKS)
 k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
            const uint2 *__restrict__ ranges, int width, int height, int tiles_x,
            const float4 *__restrict__ dl_dout, const float *__restrict__ final_T,
            const uint32_t *__restrict__ last_in, double *__restrict__ grad_acc)
 {
     __shared__ StagedBatch sb;
-    __shared__ uint32_t s_wmax[kTilePixels / 32];
+    __shared__ uint32_t s_wmax[kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t wbit = 1u << warp;
     const int tile = blockIdx.x;
-    const int tx = tile % tiles_x, ty = tile / tiles_x;
-    const int x = tx * kTile + pixel_x(threadIdx.x);
-    const int y = ty * kTile + pixel_y(threadIdx.x);
+    const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
+    const int x = x0 + pixel_x(threadIdx.x);
+    const int y = y0 + pixel_y(threadIdx.x);
     const bool inside = x < width && y < height;
     const float px = (float)x, py = (float)y;
     const uint2 range = ranges[tile];
@@ -184,7 +297,7 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
         __syncthreads();
         cta_end = 0;
 #pragma unroll
-        for (int w = 0; w < kTilePixels / 32; ++w) cta_end = max(cta_end, s_wmax[w]);
+        for (int w = 0; w < kWarps; ++w) cta_end = max(cta_end, s_wmax[w]);
     }
     float3 S = make_float3(0.0f, 0.0f, 0.0f);
 
@@ -193,71 +306,66 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
         const int cnt = bend - bstart;
         __syncthreads();
         if (threadIdx.x < cnt)
-            stage_splat(sb, threadIdx.x, splats, __ldg(sorted_idx + range.x + bstart + threadIdx.x));
+            stage_splat<kCull>(sb, threadIdx.x, splats, __ldg(sorted_idx + range.x + bstart + threadIdx.x),
+                               x0, y0);
         __syncthreads();
-        const int jhi = min(cnt, (int)warp_end - bstart) - 1;
-        for (int j = jhi; j >= 0; --j) {
-            const uint32_t rel = (uint32_t)(bstart + j);
-            bool contrib = false;
-            float v[9];
+        const int jlim = min(cnt, (int)warp_end - bstart);  // this warp's positions: j < jlim
+        for (int c0 = ((jlim - 1) >> 5) << 5; c0 >= 0 && jlim > 0; c0 -= 32) {
+            uint32_t m = __ballot_sync(kFull, c0 + lane < jlim && (sb.mask[c0 + lane] & wbit));
+            while (m) {
+                const int bit = 31 - __clz(m);
+                m &= ~(1u << bit);
+                const int j = c0 + bit;
+                const uint32_t rel = (uint32_t)(bstart + j);
+                bool contrib = false;
+                float v[9];
 #pragma unroll
-            for (int k = 0; k < 9; ++k) v[k] = 0.0f;
-            if (rel < L) {
-                const float4 geo = sb.geo[j];
-                const float4 aux = sb.aux[j];
-                float dx, dy;
-                const float sigma = splat_sigma(geo, aux.x, px, py, dx, dy);
-                if (sigma >= 0.0f && sigma < aux.z) {
-                    float e, raw;
-                    const float alpha = splat_alpha(sigma, aux.y, e, raw);
-                    if (alpha >= kAlphaMin) {
-                        contrib = true;
-                        const float4 c = sb.rgb[j];
-                        const float one_m = __fsub_rn(1.0f, alpha);
-                        const float inv = __fdividef(1.0f, one_m);
-                        // Transmittance in front of this splat: the forward's
-                        // T_j (1 - alpha) undone with one correctly rounded division,
-                        // so a pixel replayed through hundreds of splats drifts by at
-                        // most a rounding per splat.
-                        const float Tj = __fdiv_rn(T, one_m);
-                        const float aT = alpha * Tj;
-                        v[5] = g.x * aT;
-                        v[6] = g.y * aT;
-                        v[7] = g.z * aT;
-                        float dA = g.x * (c.x * Tj - S.x * inv);
-                        dA = __fmaf_rn(g.y, c.y * Tj - S.y * inv, dA);
-                        dA = __fmaf_rn(g.z, c.z * Tj - S.z * inv, dA);
-                        S.x = __fmaf_rn(c.x, aT, S.x);
-                        S.y = __fmaf_rn(c.y, aT, S.y);
-                        S.z = __fmaf_rn(c.z, aT, S.z);
-                        const float dRaw = raw < kAlphaMax ? dA : 0.0f;
-                        v[8] = dRaw * e;
-                        const float dSig = -dRaw * raw;
-                        const float a = geo.z, b = geo.w, cc = aux.x;
-                        v[0] = -dSig * __fmaf_rn(a, dx, b * dy);
-                        v[1] = -dSig * __fmaf_rn(b, dx, cc * dy);
-                        v[2] = dSig * (0.5f * dx * dx);
-                        v[3] = dSig * (dx * dy);
-                        v[4] = dSig * (0.5f * dy * dy);
-                        T = Tj;
+                for (int k = 0; k < 9; ++k) v[k] = 0.0f;
+                if (rel < L) {
+                    const float4 geo = sb.geo[j];
+                    const float4 aux = sb.aux[j];
+                    float dx, dy;
+                    const float sigma = splat_sigma(geo, aux.x, px, py, dx, dy);
+                    if (sigma >= 0.0f && sigma < aux.z) {
+                        float e, raw;
+                        const float alpha = splat_alpha(sigma, aux.y, e, raw);
+                        if (alpha >= kAlphaMin) {
+                            contrib = true;
+                            const float4 c = sb.rgb[j];
+                            const float one_m = __fsub_rn(1.0f, alpha);
+                            const float inv = __fdividef(1.0f, one_m);
+                            // Transmittance in front of this splat: the forward's
+                            // T_j (1 - alpha) undone with one correctly rounded
+                            // division, so a pixel replayed through hundreds of
+                            // splats drifts by at most a rounding per splat.
+                            const float Tj = __fdiv_rn(T, one_m);
+                            const float aT = alpha * Tj;
+                            v[5] = g.x * aT;
+                            v[6] = g.y * aT;
+                            v[7] = g.z * aT;
+                            float dA = g.x * (c.x * Tj - S.x * inv);
+                            dA = __fmaf_rn(g.y, c.y * Tj - S.y * inv, dA);
+                            dA = __fmaf_rn(g.z, c.z * Tj - S.z * inv, dA);
+                            S.x = __fmaf_rn(c.x, aT, S.x);
+                            S.y = __fmaf_rn(c.y, aT, S.y);
+                            S.z = __fmaf_rn(c.z, aT, S.z);
+                            const float dRaw = raw < kAlphaMax ? dA : 0.0f;
+                            v[8] = dRaw * e;
+                            const float dSig = -dRaw * raw;
+                            const float a = geo.z, b = geo.w, cc = aux.x;
+                            v[0] = -dSig * __fmaf_rn(a, dx, b * dy);
+                            v[1] = -dSig * __fmaf_rn(b, dx, cc * dy);
+                            v[2] = dSig * (0.5f * dx * dx);
+                            v[3] = dSig * (dx * dy);
+                            v[4] = dSig * (0.5f * dy * dy);
+                            T = Tj;
+                        }
                     }
                 }
-            }
-            // "W1 warp sparse skip": with no contributing lane every sum is +0.
-            if (kWarpSkip && !__any_sync(kFull, contrib)) continue;
-#pragma unroll
-            for (int k = 0; k < 9; ++k) {
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(kFull, v[k], o);
-            }
-            // One atomic per warp, splat and field, accumulated in double: a
-            // large splat sums thousands of warp partials of both signs, and in
-            // float their order alone moves the result by more than 1e-4.
-            if (lane == 0) {
+                // "W1 warp sparse skip": with no contributing lane every sum is +0.
+                if (kWarpSkip && !__any_sync(kFull, contrib)) continue;
                 const uint32_t idx = __float_as_uint(sb.aux[j].w);
-                double *gr = grad_acc + 9 * (size_t)idx;
-#pragma unroll
-                for (int k = 0; k < 9; ++k) atomicAdd(gr + k, (double)v[k]);
+                warp_reduce_add9(v, grad_acc + 9 * (size_t)idx, lane);
             }
         }
     }
@@ -270,15 +378,51 @@ __global__ void k_grad_to_float(const double *__restrict__ acc, float *__restric
         grad[i] = (float)acc[i];
 }
 
+template <bool kSkip, bool kLc>
+void launch_backward_cull(bool cull, int grid, cudaStream_t stream, const float *splats,
+                          const gsr_bins *bins, const float *dl_dout, const float *final_T,
+                          const uint32_t *last_contrib, double *acc)
+{
+    auto go = [&](auto kernel) {
+        kernel<<<grid, kTilePixels, 0, stream>>>(
+            splats, bins->sorted_idx, reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width,
+            bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
+            last_contrib, acc);
+    };
+    if (cull) go(k_backward<kSkip, kLc, true>);
+    else go(k_backward<kSkip, kLc, false>);
+}
+
+// The backward kernel variant the context's options select, accumulating into acc.
+void launch_backward(const gsr_ctx *ctx, cudaStream_t stream, const float *splats, const gsr_bins *bins,
+                     const float *dl_dout, const float *final_T, const uint32_t *last_contrib,
+                     double *acc)
+{
+    const int grid = bins->tiles_x * bins->tiles_y;
+    const bool cull = ctx->opt_warp_cull != 0;
+    if (ctx->opt_warp_skip && ctx->opt_last_contrib)
+        launch_backward_cull<true, true>(cull, grid, stream, splats, bins, dl_dout, final_T, last_contrib, acc);
+    else if (ctx->opt_warp_skip)
+        launch_backward_cull<true, false>(cull, grid, stream, splats, bins, dl_dout, final_T, last_contrib, acc);
+    else if (ctx->opt_last_contrib)
+        launch_backward_cull<false, true>(cull, grid, stream, splats, bins, dl_dout, final_T, last_contrib, acc);
+    else
+        launch_backward_cull<false, false>(cull, grid, stream, splats, bins, dl_dout, final_T, last_contrib, acc);
+}
+
 }  // namespace
 
 int rasterize_forward(gsr_ctx *ctx, const float *splats, const gsr_bins *bins, float *out_rgbw,
                       float *final_T, uint32_t *last_contrib, cudaStream_t stream)
 {
     const int num_tiles = bins->tiles_x * bins->tiles_y;
-    k_forward<<<num_tiles, kTilePixels, 0, stream>>>(
-        splats, bins->sorted_idx, reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width,
-        bins->height, bins->tiles_x, reinterpret_cast<float4 *>(out_rgbw), final_T, last_contrib);
+    auto go = [&](auto kernel) {
+        kernel<<<num_tiles, kTilePixels, 0, stream>>>(
+            splats, bins->sorted_idx, reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width,
+            bins->height, bins->tiles_x, reinterpret_cast<float4 *>(out_rgbw), final_T, last_contrib);
+    };
+    if (ctx->opt_warp_cull) go(k_forward<true>);
+    else go(k_forward<false>);
     ++ctx->launches;
     return cuda_check(ctx, cudaGetLastError(), "forward launch");
 }
@@ -301,17 +445,7 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
     int rc = cuda_check(ctx, cudaMemsetAsync(ctx->grad_acc, 0, count * sizeof(double), stream),
                         "cudaMemsetAsync");
     if (rc) return rc;
-    const int num_tiles = bins->tiles_x * bins->tiles_y;
-    auto launch = [&](auto kernel) {
-        kernel<<<num_tiles, kTilePixels, 0, stream>>>(
-            splats, bins->sorted_idx, reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width,
-            bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
-            last_contrib, ctx->grad_acc);
-    };
-    if (ctx->opt_warp_skip && ctx->opt_last_contrib) launch(k_backward<true, true>);
-    else if (ctx->opt_warp_skip) launch(k_backward<true, false>);
-    else if (ctx->opt_last_contrib) launch(k_backward<false, true>);
-    else launch(k_backward<false, false>);
+    launch_backward(ctx, stream, splats, bins, dl_dout, final_T, last_contrib, ctx->grad_acc);
     ++ctx->launches;
     if ((rc = cuda_check(ctx, cudaGetLastError(), "backward launch"))) return rc;
     const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)SM_BLOCKS_CAP);
@@ -361,17 +495,7 @@ int rasterize_backward_noalloc(gsr_ctx *ctx, const float *splats, int32_t n, con
     // The array keeps the previous call's sums: clear the part this call uses.
     int rc = cuda_check(ctx, cudaMemsetAsync(acc, 0, count * sizeof(double), stream), "cudaMemsetAsync");
     if (rc) return rc;
-    const int num_tiles = bins->tiles_x * bins->tiles_y;
-    auto launch = [&](auto kernel) {
-        kernel<<<num_tiles, kTilePixels, 0, stream>>>(
-            splats, bins->sorted_idx, reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width,
-            bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
-            last_contrib, acc);
-    };
-    if (ctx->opt_warp_skip && ctx->opt_last_contrib) launch(k_backward<true, true>);
-    else if (ctx->opt_warp_skip) launch(k_backward<true, false>);
-    else if (ctx->opt_last_contrib) launch(k_backward<false, true>);
-    else launch(k_backward<false, false>);
+    launch_backward(ctx, stream, splats, bins, dl_dout, final_T, last_contrib, acc);
     ++ctx->launches;
     if ((rc = cuda_check(ctx, cudaGetLastError(), "backward launch"))) return rc;
     const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)SM_BLOCKS_CAP);

@@ -193,6 +193,24 @@ def test_backward_variants_agree(gsr, ctx):
     ctx.set_option("bwd_last_contrib", 1)
 
 
+@pytest.mark.parametrize("name", ["lego_early", "stress"])
+def test_warp_culling_changes_nothing(gsr, ctx, name):
+    """Warps skip splats whose alpha >= 1/255 ellipse misses their pixel block;
+    the per-pixel tests would have skipped every one of those evaluations, so
+    the forward must be bit-identical with culling off, and the backward
+    identical up to the order of its double-precision sums."""
+    wl = gen.make(name)
+    on = run_gpu(gsr, ctx, wl)
+    ctx.set_option("warp_cull", 0)
+    try:
+        off = run_gpu(gsr, ctx, wl)
+    finally:
+        ctx.set_option("warp_cull", 1)
+    for k in ("out", "final_T", "last"):
+        assert np.array_equal(on[k], off[k]), k
+    assert np.allclose(on["grad"], off["grad"], rtol=1e-6, atol=1e-9)
+
+
 def test_self_noise(gsr, ctx):
     """Run-to-run spread of the atomically accumulated gradients (the pages'
     self-noise protocol: 20 repeats, "M3 per-splat backward", section 2)."""
