@@ -92,6 +92,10 @@ void gsr_destroy(gsr_ctx *ctx)
             cudaFree(ctx->pairs.v[b]);
         }
         cudaFree(ctx->counts);
+        for (int b = 0; b < 3; ++b) {
+            cudaFree(ctx->depth.k[b]);
+            cudaFree(ctx->depth.v[b]);
+        }
         cudaFree(ctx->blk_sums);
         cudaFree(ctx->ranges);
         cudaFree(ctx->radix_counts);
@@ -217,12 +221,13 @@ int gsr_get_bin_stats(gsr_ctx *ctx, gsr_bin_stats *out)
     if (!ctx->plan || ctx->last_pairs == 0) return GSR_OK;
     int rc = cuda_check(ctx, cudaStreamSynchronize(ctx->last_stream), "cudaStreamSynchronize");
     if (rc) return rc;
-    RadixPlan plan;
-    rc = cuda_check(ctx, cudaMemcpy(&plan, ctx->plan, sizeof plan, cudaMemcpyDeviceToHost), "cudaMemcpy");
+    RadixPlan plan[2];
+    rc = cuda_check(ctx, cudaMemcpy(plan, ctx->plan, sizeof plan, cudaMemcpyDeviceToHost), "cudaMemcpy");
     if (rc) return rc;
-    out->radix_passes = plan.num_exec;
+    // The depth sort runs the low four digits, the tile sort the rest.
+    out->radix_passes = plan[0].num_exec + plan[1].num_exec;
     for (int d = 0; d < kMaxDigits; ++d)
-        if (plan.exec[d]) out->digit_mask |= 1u << d;
+        if (plan[0].exec[d] || plan[1].exec[d]) out->digit_mask |= 1u << d;
     return GSR_OK;
 }
 

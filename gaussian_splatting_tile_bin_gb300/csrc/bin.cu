@@ -1,14 +1,23 @@
-// bin.cu -- tile binning: per-splat tile counts, a block scan, load-balanced
-// pair emission, a stable LSD radix sort with 8-bit digits that skips every
-// pass whose digit is the same in all keys, and per-tile range extraction.
+// bin.cu -- tile binning.
 //
 // Follows "C0 resident arena + C1 pass skip" (p2-c0-resident-binning),
-// section 2 table: key = (tile_id << 32) | depth_bits; a stable radix sort; a
-// pass over a digit every key shares is the identity and is skipped (the page
-// derives the skip from num_tiles for 4-bit digits; here the constant digits
-// are found on the device from the AND and OR of all keys, which also catches
-// constant depth-exponent digits); ranges extracted from the sorted keys; all
-// buffers kept in a grow-only arena.
+// section 2 table: each splat emits a key (tile_id << 32) | depth_bits per tile
+// it touches, the pairs are sorted by key with a stable radix sort whose passes
+// over constant digits are skipped, per-tile ranges are extracted from the
+// sorted keys, and every buffer lives in a grow-only arena.
+//
+// The sorted order is (tile, depth bits, splat index).  It is produced in two
+// stages that give exactly the same keys and indices as sorting the pairs on
+// the whole key:
+//   1. the splats that emit at least one pair are compacted and sorted stably
+//      by their depth bits (LSD, 8-bit digits, 4 passes at most over the
+//      splats instead of over the pairs);
+//   2. the pairs are emitted in that depth order (a splat's own pairs in
+//      row-major tile order), so they are already ordered by (depth, index)
+//      within every tile, and a stable LSD sort on the tile digits alone
+//      finishes the job.
+// In both sorts a digit that every key shares is found on the device from the
+// AND and the OR of all keys, and its pass is skipped.
 //
 // The tile rectangle is computed with round-to-nearest intrinsics only (no
 // contraction), so every splat's rectangle is the IEEE single-precision result
@@ -21,6 +30,17 @@ namespace gsr {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+
+// ctx->scalars slots.
+enum {
+    kScalarPairs = 0,      // total tile pairs
+    kScalarEmitting = 1,   // splats with at least one pair
+    kScalarDepthAnd = 2,   // AND / OR of the emitting splats' depth bits
+    kScalarDepthOr = 3,
+    kScalarKeyAnd = 4,     // AND / OR of the emitted keys
+    kScalarKeyOr = 5,
+    kScalarCount = 8
+};
 
 // The 3-sigma box of splat i as an inclusive tile rectangle (x0, y0, x1, y1).
 // false when the splat is culled.
@@ -62,14 +82,6 @@ __device__ __forceinline__ bool splat_tile_rect(const float *__restrict__ splats
     return true;
 }
 
-template <typename T>
-__device__ __forceinline__ T warp_sum(T v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
-}
-
 // Exclusive scan over a 256-thread block; returns the exclusive prefix and the
 // block total in *total.  `ws` must hold 8 elements.
 template <typename T>
@@ -96,44 +108,80 @@ __device__ __forceinline__ T block_exclusive_scan_256(T v, T *ws, T *total)
     return warp_off + incl - v;
 }
 
+// AND and OR of one value per thread over a 256-thread block, folded into
+// acc[0] (AND) and acc[1] (OR) by thread 0.  Threads pass ~0 / 0 to abstain.
+__device__ __forceinline__ void block_and_or_into(unsigned long long a, unsigned long long o,
+                                                  unsigned long long *s_and, unsigned long long *s_or,
+                                                  unsigned long long *acc)
+{
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) {
+        a &= __shfl_xor_sync(kFull, a, k);
+        o |= __shfl_xor_sync(kFull, o, k);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s_and[threadIdx.x >> 5] = a;
+        s_or[threadIdx.x >> 5] = o;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long ta = ~0ull, to = 0ull;
+        for (int w = 0; w < 8; ++w) {
+            ta &= s_and[w];
+            to |= s_or[w];
+        }
+        if (ta != ~0ull) atomicAnd(acc, ta);
+        if (to != 0ull) atomicOr(acc + 1, to);
+    }
+}
+
+__global__ void k_init_scalars(unsigned long long *__restrict__ scalars)
+{
+    if (threadIdx.x != 0) return;
+    for (int k = 0; k < kScalarCount; ++k) scalars[k] = 0ull;
+    scalars[kScalarDepthAnd] = ~0ull;
+    scalars[kScalarKeyAnd] = ~0ull;
+}
+
 // --- count -----------------------------------------------------------------
 
+// Per splat: tile count.  Per block: the pair total, the number of emitting
+// splats, and the AND / OR of their depth bits.
 __global__ void __launch_bounds__(kBinBlock)
 k_count(const float *__restrict__ splats, const float *__restrict__ depths, int n, int tiles_x,
-        int tiles_y, uint32_t *__restrict__ counts, unsigned long long *__restrict__ blk_sums)
+        int tiles_y, uint32_t *__restrict__ counts, unsigned long long *__restrict__ blk_pairs,
+        unsigned long long *__restrict__ blk_emitting, unsigned long long *__restrict__ scalars)
 {
+    __shared__ unsigned long long s_and[8], s_or[8];
+    __shared__ unsigned long long ws[8];
     const int i = blockIdx.x * kBinBlock + threadIdx.x;
-    uint32_t c = 0;
+    uint32_t c = 0, db = 0;
     if (i < n) {
         int4 r;
-        uint32_t db;
         if (splat_tile_rect(splats, depths, i, tiles_x, tiles_y, r, db))
             c = (uint32_t)(r.z - r.x + 1) * (uint32_t)(r.w - r.y + 1);
         counts[i] = c;
     }
-    __shared__ unsigned long long ws[8];
-    unsigned long long v = warp_sum<unsigned long long>(c);
-    if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = v;
-    __syncthreads();
+    unsigned long long pairs_total, emit_total;
+    block_exclusive_scan_256<unsigned long long>(c, ws, &pairs_total);
+    block_exclusive_scan_256<unsigned long long>(c > 0 ? 1ull : 0ull, ws, &emit_total);
     if (threadIdx.x == 0) {
-        unsigned long long t = 0;
-        for (int w = 0; w < 8; ++w) t += ws[w];
-        blk_sums[blockIdx.x] = t;
+        blk_pairs[blockIdx.x] = pairs_total;
+        blk_emitting[blockIdx.x] = emit_total;
     }
+    block_and_or_into(c > 0 ? (unsigned long long)db : ~0ull, c > 0 ? (unsigned long long)db : 0ull,
+                      s_and, s_or, scalars + kScalarDepthAnd);
 }
 
-// One block: exclusive scan of the per-block sums, the pair total, and the
-// AND/OR accumulators reset for the emission.
-__global__ void __launch_bounds__(1024)
-k_scan_blocks(const unsigned long long *__restrict__ blk_sums, int nblk,
-              unsigned long long *__restrict__ blk_offs, unsigned long long *__restrict__ scalars)
+// Exclusive scan in place of vals[0, num) by one 1024-thread block; returns the total.
+__device__ unsigned long long block_scan_inplace_1024(unsigned long long *__restrict__ vals, int num,
+                                                      unsigned long long *ws)
 {
-    __shared__ unsigned long long ws[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     unsigned long long carry = 0;
-    for (int base = 0; base < nblk; base += 1024) {
+    for (int base = 0; base < num; base += 1024) {
         const int i = base + threadIdx.x;
-        unsigned long long v = i < nblk ? blk_sums[i] : 0ull;
+        unsigned long long v = i < num ? vals[i] : 0ull;
         unsigned long long incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -148,44 +196,108 @@ k_scan_blocks(const unsigned long long *__restrict__ blk_sums, int nblk,
             sum += ws[w];
         }
         __syncthreads();
-        if (i < nblk) blk_offs[i] = carry + off + incl - v;
+        if (i < num) vals[i] = carry + off + incl - v;
         carry += sum;
     }
+    return carry;
+}
+
+__global__ void __launch_bounds__(1024)
+k_scan_u64(unsigned long long *__restrict__ vals, int num)
+{
+    __shared__ unsigned long long ws[32];
+    block_scan_inplace_1024(vals, num, ws);
+}
+
+// One block: the pair total (a plain sum) and the exclusive scan of the
+// per-block emitting counts with their total.
+__global__ void __launch_bounds__(1024)
+k_count_totals(const unsigned long long *__restrict__ blk_pairs, unsigned long long *__restrict__ blk_emitting,
+               int nblk, unsigned long long *__restrict__ scalars)
+{
+    __shared__ unsigned long long ws[32];
+    unsigned long long s = 0;
+    for (int i = threadIdx.x; i < nblk; i += 1024) s += blk_pairs[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+    if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = s;
+    __syncthreads();
+    unsigned long long t = 0;
+    for (int w = 0; w < 32; ++w) t += ws[w];
+    __syncthreads();
+    const unsigned long long m = block_scan_inplace_1024(blk_emitting, nblk, ws);
     if (threadIdx.x == 0) {
-        scalars[0] = carry;
-        scalars[1] = ~0ull;
-        scalars[2] = 0ull;
+        scalars[kScalarPairs] = t;
+        scalars[kScalarEmitting] = m;
     }
+}
+
+// Writes (depth bits, splat index) of every emitting splat, in splat order.
+__global__ void __launch_bounds__(kBinBlock)
+k_compact(const uint32_t *__restrict__ counts, const float *__restrict__ depths, int n,
+          const unsigned long long *__restrict__ blk_emit_offs, uint32_t *__restrict__ dkeys,
+          uint32_t *__restrict__ didx)
+{
+    __shared__ uint32_t ws[8];
+    const int i = blockIdx.x * kBinBlock + threadIdx.x;
+    const bool emits = i < n && counts[i] > 0;
+    uint32_t total;
+    const uint32_t excl = block_exclusive_scan_256<uint32_t>(emits ? 1u : 0u, ws, &total);
+    if (emits) {
+        const size_t pos = (size_t)blk_emit_offs[blockIdx.x] + excl;
+        dkeys[pos] = __float_as_uint(__ldg(depths + i));
+        didx[pos] = (uint32_t)i;
+    }
+}
+
+// Per block of 256 depth-sorted splats: their pair total.
+__global__ void __launch_bounds__(kBinBlock)
+k_sorted_sums(const uint32_t *__restrict__ sorted_idx, const uint32_t *__restrict__ counts, int m,
+              unsigned long long *__restrict__ blk_sorted)
+{
+    __shared__ unsigned long long ws[8];
+    const int k = blockIdx.x * kBinBlock + threadIdx.x;
+    const uint32_t c = k < m ? counts[sorted_idx[k]] : 0u;
+    unsigned long long total;
+    block_exclusive_scan_256<unsigned long long>(c, ws, &total);
+    if (threadIdx.x == 0) blk_sorted[blockIdx.x] = total;
 }
 
 // --- emit ------------------------------------------------------------------
 
-// Each block re-derives the rectangles of its 256 splats, scans their counts
-// and writes its contiguous slice of pairs with all 256 threads, so a splat
-// with thousands of tiles does not serialise on one thread.  Within a splat the
-// pairs go in row-major tile order; across splats in splat order.
+// Each block takes 256 consecutive depth-sorted splats, re-derives their
+// rectangles, scans their counts and writes its contiguous slice of pairs with
+// all 256 threads, so a splat with thousands of tiles does not serialise on one
+// thread.  Within a splat the pairs go in row-major tile order; across splats in
+// depth order.  Also folds the AND / OR of the keys for the tile sort's plan.
 __global__ void __launch_bounds__(kBinBlock)
-k_emit(const float *__restrict__ splats, const float *__restrict__ depths, int n, int tiles_x,
-       int tiles_y, const unsigned long long *__restrict__ blk_offs, uint64_t *__restrict__ keys,
+k_emit(const float *__restrict__ splats, const float *__restrict__ depths,
+       const uint32_t *__restrict__ sorted_idx, int m, int tiles_x, int tiles_y,
+       const unsigned long long *__restrict__ blk_offs, uint64_t *__restrict__ keys,
        uint32_t *__restrict__ vals, unsigned long long *__restrict__ scalars)
 {
     __shared__ uint32_t s_off[kBinBlock];
     __shared__ int4 s_rect[kBinBlock];
     __shared__ uint32_t s_db[kBinBlock];
+    __shared__ uint32_t s_idx[kBinBlock];
     __shared__ uint32_t ws[8];
     __shared__ unsigned long long s_and[8], s_or[8];
 
-    const int i = blockIdx.x * kBinBlock + threadIdx.x;
+    const int k = blockIdx.x * kBinBlock + threadIdx.x;
     uint32_t c = 0;
     int4 r = make_int4(0, 0, -1, -1);
-    uint32_t db = 0;
-    if (i < n && splat_tile_rect(splats, depths, i, tiles_x, tiles_y, r, db))
-        c = (uint32_t)(r.z - r.x + 1) * (uint32_t)(r.w - r.y + 1);
+    uint32_t db = 0, i = 0;
+    if (k < m) {
+        i = sorted_idx[k];
+        if (splat_tile_rect(splats, depths, (int)i, tiles_x, tiles_y, r, db))
+            c = (uint32_t)(r.z - r.x + 1) * (uint32_t)(r.w - r.y + 1);
+    }
     uint32_t total;
     const uint32_t excl = block_exclusive_scan_256<uint32_t>(c, ws, &total);
     s_off[threadIdx.x] = excl;
     s_rect[threadIdx.x] = r;
     s_db[threadIdx.x] = db;
+    s_idx[threadIdx.x] = i;
     __syncthreads();
 
     const unsigned long long base = blk_offs[blockIdx.x];
@@ -207,57 +319,28 @@ k_emit(const float *__restrict__ splats, const float *__restrict__ depths, int n
         const uint64_t tile = (uint64_t)ty * (uint64_t)tiles_x + tx;
         const uint64_t key = (tile << 32) | (uint64_t)s_db[lo];
         keys[base + q] = key;
-        vals[base + q] = (uint32_t)(blockIdx.x * kBinBlock + lo);
+        vals[base + q] = s_idx[lo];
         acc_and &= key;
         acc_or |= key;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        acc_and &= __shfl_xor_sync(kFull, acc_and, o);
-        acc_or |= __shfl_xor_sync(kFull, acc_or, o);
-    }
-    if ((threadIdx.x & 31) == 0) {
-        s_and[threadIdx.x >> 5] = acc_and;
-        s_or[threadIdx.x >> 5] = acc_or;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0 && total > 0) {
-        unsigned long long a = ~0ull, o = 0ull;
-        for (int w = 0; w < 8; ++w) {
-            a &= s_and[w];
-            o |= s_or[w];
-        }
-        atomicAnd(&scalars[1], a);
-        atomicOr(&scalars[2], o);
-    }
+    block_and_or_into(acc_and, acc_or, s_and, s_or, scalars + kScalarKeyAnd);
 }
 
 // --- radix sort --------------------------------------------------------------
 
-// Buffer b of the three (a select, so the kernel parameter block is not copied
-// to local memory for dynamic indexing).
-__device__ __forceinline__ uint64_t *keys_of(const PairBuffers &p, int b)
-{
-    return b == 0 ? p.k[0] : (b == 1 ? p.k[1] : p.k[2]);
-}
-__device__ __forceinline__ uint32_t *vals_of(const PairBuffers &p, int b)
-{
-    return b == 0 ? p.v[0] : (b == 1 ? p.v[1] : p.v[2]);
-}
-
-// Decides which 8-bit digits vary and chains the executed passes so that the
-// last one writes buffer 1: pass j of k reads the previous pass's output (the
-// emitted buffer 0 for the first) and writes buffer 1 when k - 1 - j is even,
-// buffer 2 otherwise.
-__global__ void k_radix_plan(const unsigned long long *__restrict__ scalars, int digits,
+// Decides which 8-bit digits in [d_lo, d_hi) vary (from acc[0] = AND, acc[1] =
+// OR of the keys) and chains the executed passes so that the last one writes
+// buffer 1: pass j of k reads the previous pass's output (buffer 0 for the
+// first) and writes buffer 1 when k - 1 - j is even, buffer 2 otherwise.
+__global__ void k_radix_plan(const unsigned long long *__restrict__ acc, int d_lo, int d_hi,
                              RadixPlan *__restrict__ plan)
 {
     if (threadIdx.x != 0) return;
-    const unsigned long long diff = scalars[1] ^ scalars[2];
+    const unsigned long long diff = acc[0] ^ acc[1];
     int list[kMaxDigits];
     int k = 0;
     for (int d = 0; d < kMaxDigits; ++d) {
-        const bool ex = d < digits && ((diff >> (8 * d)) & 0xffull) != 0ull;
+        const bool ex = d >= d_lo && d < d_hi && ((diff >> (8 * d)) & 0xffull) != 0ull;
         plan->exec[d] = ex ? 1 : 0;
         plan->src[d] = 0;
         plan->dst[d] = 0;
@@ -274,14 +357,28 @@ __global__ void k_radix_plan(const unsigned long long *__restrict__ scalars, int
     plan->num_exec = k;
 }
 
+// Buffer b of the three (a select, so the kernel parameter block is not copied
+// to local memory for dynamic indexing).
+template <typename K>
+__device__ __forceinline__ K *keys_of(const SortBuffers<K> &p, int b)
+{
+    return b == 0 ? p.k[0] : (b == 1 ? p.k[1] : p.k[2]);
+}
+template <typename K>
+__device__ __forceinline__ uint32_t *vals_of(const SortBuffers<K> &p, int b)
+{
+    return b == 0 ? p.v[0] : (b == 1 ? p.v[1] : p.v[2]);
+}
+
 // Per radix tile: how many keys carry each digit value.  counts is
 // digit-major, [256][ntiles]; totals[digit] accumulates over tiles.
+template <typename K>
 __global__ void __launch_bounds__(kRadixThreads)
-k_radix_upsweep(const RadixPlan *__restrict__ plan, int d, PairBuffers bufs, uint32_t num,
+k_radix_upsweep(const RadixPlan *__restrict__ plan, int d, SortBuffers<K> bufs, uint32_t num,
                 int ntiles, uint32_t *__restrict__ counts, uint32_t *__restrict__ totals)
 {
     if (!plan->exec[d]) return;
-    const uint64_t *__restrict__ keys = keys_of(bufs, plan->src[d]);
+    const K *__restrict__ keys = keys_of(bufs, plan->src[d]);
     __shared__ uint32_t h[256];
     h[threadIdx.x] = 0;
     __syncthreads();
@@ -308,7 +405,7 @@ k_radix_scan(const RadixPlan *__restrict__ plan, int d, int ntiles, uint32_t *__
     if (!plan->exec[d]) return;
     __shared__ uint32_t ws[8];
     const uint32_t digit = blockIdx.x;
-    uint32_t dummy, base;
+    uint32_t base;
     {
         const uint32_t x = threadIdx.x < digit ? totals[threadIdx.x] : 0u;
         block_exclusive_scan_256<uint32_t>(x, ws, &base);
@@ -323,7 +420,6 @@ k_radix_scan(const RadixPlan *__restrict__ plan, int d, int ntiles, uint32_t *__
         if (i < ntiles) row[i] = carry + e;
         carry += sum;
     }
-    (void)dummy;
 }
 
 // Stable scatter of one radix tile.  Warp w owns keys [w*256, w*256+256) of
@@ -331,15 +427,16 @@ k_radix_scan(const RadixPlan *__restrict__ plan, int d, int ntiles, uint32_t *__
 // equal digits are ranked by lane (match.any), across rounds by per-warp digit
 // counters, across warps by a per-digit prefix over the 8 warps, across tiles
 // by the scanned counts.  This reproduces input order among equal digits.
+template <typename K>
 __global__ void __launch_bounds__(kRadixThreads)
-k_radix_downsweep(const RadixPlan *__restrict__ plan, int d, PairBuffers bufs, uint32_t num,
+k_radix_downsweep(const RadixPlan *__restrict__ plan, int d, SortBuffers<K> bufs, uint32_t num,
                   int ntiles, const uint32_t *__restrict__ offsets)
 {
     if (!plan->exec[d]) return;
     const int src = plan->src[d], dst = plan->dst[d];
-    const uint64_t *__restrict__ kin = keys_of(bufs, src);
+    const K *__restrict__ kin = keys_of(bufs, src);
     const uint32_t *__restrict__ vin = vals_of(bufs, src);
-    uint64_t *__restrict__ kout = keys_of(bufs, dst);
+    K *__restrict__ kout = keys_of(bufs, dst);
     uint32_t *__restrict__ vout = vals_of(bufs, dst);
 
     __shared__ uint32_t wcnt[8][256];
@@ -352,14 +449,14 @@ k_radix_downsweep(const RadixPlan *__restrict__ plan, int d, PairBuffers bufs, u
     const int shift = 8 * d;
     const uint32_t lanemask_lt = (1u << lane) - 1u;
     const uint32_t base = blockIdx.x * kRadixTile + warp * (32 * kRadixItems);
-    uint64_t key[kRadixItems];
+    K key[kRadixItems];
     uint32_t val[kRadixItems];
     uint32_t rank[kRadixItems];
 #pragma unroll
     for (int k = 0; k < kRadixItems; ++k) {
         const uint32_t i = base + k * 32 + lane;
         const bool valid = i < num;
-        key[k] = valid ? kin[i] : 0ull;
+        key[k] = valid ? kin[i] : (K)0;
         val[k] = valid ? vin[i] : 0u;
         const uint32_t digit = valid ? ((uint32_t)(key[k] >> shift) & 0xffu) : 0x100u;
         const uint32_t peers = __match_any_sync(kFull, digit);
@@ -394,10 +491,10 @@ k_radix_downsweep(const RadixPlan *__restrict__ plan, int d, PairBuffers bufs, u
     }
 }
 
-// When every digit was constant no pass ran and the emitted order is already
+// When every digit was constant no pass ran and the input order is already
 // sorted; copy it to the result buffer.
-__global__ void k_copy_if_unsorted(const RadixPlan *__restrict__ plan, PairBuffers bufs,
-                                   uint32_t num)
+template <typename K>
+__global__ void k_copy_if_unsorted(const RadixPlan *__restrict__ plan, SortBuffers<K> bufs, uint32_t num)
 {
     if (plan->num_exec != 0) return;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < num; i += gridDim.x * blockDim.x) {
@@ -447,7 +544,28 @@ int grow(gsr_ctx *ctx, T **ptr, size_t *cap, size_t need, size_t elems_per, cons
     return GSR_OK;
 }
 
-}  // namespace
+template <typename K>
+int grow_sort_buffers(gsr_ctx *ctx, SortBuffers<K> &b, size_t *cap, size_t need, const char *what)
+{
+    if (need <= *cap && b.k[0]) return GSR_OK;
+    for (int j = 0; j < 3; ++j) {
+        if (b.k[j]) cudaFree(b.k[j]);
+        if (b.v[j]) cudaFree(b.v[j]);
+        b.k[j] = nullptr;
+        b.v[j] = nullptr;
+    }
+    *cap = 0;
+    need = std::max<size_t>(need, 1);
+    for (int j = 0; j < 3; ++j) {
+        if (cudaMalloc(&b.k[j], need * sizeof(K)) != cudaSuccess ||
+            cudaMalloc(&b.v[j], need * sizeof(uint32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(ctx, GSR_ERR_OOM, std::string("cudaMalloc failed for ") + what);
+        }
+    }
+    *cap = need;
+    return GSR_OK;
+}
 
 #define GSR_LAUNCHED(ctx)                                                     \
     do {                                                                      \
@@ -455,6 +573,37 @@ int grow(gsr_ctx *ctx, T **ptr, size_t *cap, size_t need, size_t elems_per, cons
         int _rc = cuda_check((ctx), cudaGetLastError(), "kernel launch");     \
         if (_rc) return _rc;                                                  \
     } while (0)
+
+// Stable LSD sort of bufs buffer 0 into buffer 1 over the digits in
+// [d_lo, d_hi) that vary (acc: AND / OR of the keys on the device).
+template <typename K>
+int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int d_lo, int d_hi,
+               const unsigned long long *acc, RadixPlan *plan, cudaStream_t stream)
+{
+    const int ntiles = (int)((num + kRadixTile - 1) / kRadixTile);
+    int rc;
+    if ((rc = grow(ctx, &ctx->radix_counts, &ctx->cap_radix_tiles, (size_t)std::max(ntiles, 1), 256,
+                   "radix counts")))
+        return rc;
+    k_radix_plan<<<1, 32, 0, stream>>>(acc, d_lo, d_hi, plan);
+    GSR_LAUNCHED(ctx);
+    for (int d = d_lo; d < d_hi; ++d) {
+        uint32_t *totals = ctx->radix_totals + 256 * d;
+        k_radix_upsweep<K><<<ntiles, kRadixThreads, 0, stream>>>(plan, d, bufs, num, ntiles,
+                                                                 ctx->radix_counts, totals);
+        GSR_LAUNCHED(ctx);
+        k_radix_scan<<<256, kRadixThreads, 0, stream>>>(plan, d, ntiles, ctx->radix_counts, totals);
+        GSR_LAUNCHED(ctx);
+        k_radix_downsweep<K><<<ntiles, kRadixThreads, 0, stream>>>(plan, d, bufs, num, ntiles,
+                                                                   ctx->radix_counts);
+        GSR_LAUNCHED(ctx);
+    }
+    k_copy_if_unsorted<K><<<std::min(ntiles, 1024), 256, 0, stream>>>(plan, bufs, num);
+    GSR_LAUNCHED(ctx);
+    return GSR_OK;
+}
+
+}  // namespace
 
 int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n, int32_t width,
                int32_t height, cudaStream_t stream, gsr_bins *out)
@@ -468,43 +617,57 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
 
     // Fixed-size scratch, allocated once.
     if (!ctx->scalars) {
-        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->scalars, 4 * sizeof(unsigned long long)), "cudaMalloc")))
+        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->scalars, kScalarCount * sizeof(unsigned long long)),
+                             "cudaMalloc")))
             return rc;
         if ((rc = cuda_check(ctx, cudaMalloc(&ctx->radix_totals, kMaxDigits * 256 * sizeof(uint32_t)),
                              "cudaMalloc")))
             return rc;
-        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->plan, sizeof(RadixPlan)), "cudaMalloc"))) return rc;
-        if ((rc = cuda_check(ctx, cudaHostAlloc(&ctx->host_total, sizeof(unsigned long long),
+        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->plan, 2 * sizeof(RadixPlan)), "cudaMalloc"))) return rc;
+        if ((rc = cuda_check(ctx, cudaHostAlloc(&ctx->host_total, 2 * sizeof(unsigned long long),
                                                 cudaHostAllocDefault),
                              "cudaHostAlloc")))
             return rc;
     }
     const int nblk = (n + kBinBlock - 1) / kBinBlock;
-    if ((rc = grow(ctx, &ctx->counts, &ctx->cap_splats, (size_t)n, 1, "counts"))) return rc;
-    // Block sums and block offsets share one buffer: [0, cap) and [cap, 2 cap).
-    if ((rc = grow(ctx, &ctx->blk_sums, &ctx->cap_blocks, (size_t)nblk, 2, "block sums"))) return rc;
-    ctx->blk_offs = ctx->blk_sums + ctx->cap_blocks;
+    if (!ctx->depth.k[0] || (size_t)n > ctx->cap_splats) {
+        size_t cap = 0;
+        if ((rc = grow_sort_buffers(ctx, ctx->depth, &cap, (size_t)n, "depth sort buffers"))) return rc;
+        ctx->cap_splats = 0;  // regrow counts below to the same capacity
+        if ((rc = grow(ctx, &ctx->counts, &ctx->cap_splats, cap, 1, "counts"))) return rc;
+    }
+    // Three per-block arrays: [0, c) pair sums, [c, 2c) emitting counts then
+    // offsets, [2c, 3c) pair sums in depth order then offsets.
+    if ((rc = grow(ctx, &ctx->blk_sums, &ctx->cap_blocks, (size_t)nblk, 3, "block sums"))) return rc;
+    unsigned long long *blk_pairs = ctx->blk_sums;
+    unsigned long long *blk_emit = ctx->blk_sums + ctx->cap_blocks;
+    unsigned long long *blk_sorted = ctx->blk_sums + 2 * ctx->cap_blocks;
     if ((rc = grow(ctx, &ctx->ranges, &ctx->cap_tiles, num_tiles, 2, "tile ranges"))) return rc;
 
-    // 1. count + scan, then read the pair total.
-    uint64_t total = 0;
+    // 1. counts, totals; read the pair total and the emitting count.
+    uint64_t total = 0, emitting = 0;
+    k_init_scalars<<<1, 32, 0, stream>>>(ctx->scalars);
+    GSR_LAUNCHED(ctx);
     if (n > 0) {
         k_count<<<nblk, kBinBlock, 0, stream>>>(splats, depths, n, tiles_x, tiles_y, ctx->counts,
-                                                ctx->blk_sums);
+                                                blk_pairs, blk_emit, ctx->scalars);
         GSR_LAUNCHED(ctx);
-        k_scan_blocks<<<1, 1024, 0, stream>>>(ctx->blk_sums, nblk, ctx->blk_offs, ctx->scalars);
+        k_count_totals<<<1, 1024, 0, stream>>>(blk_pairs, blk_emit, nblk, ctx->scalars);
         GSR_LAUNCHED(ctx);
-        if ((rc = cuda_check(ctx, cudaMemcpyAsync(ctx->host_total, ctx->scalars, sizeof(unsigned long long),
+        if ((rc = cuda_check(ctx, cudaMemcpyAsync(ctx->host_total, ctx->scalars,
+                                                  2 * sizeof(unsigned long long),
                                                   cudaMemcpyDeviceToHost, stream),
                              "cudaMemcpyAsync")))
             return rc;
         if ((rc = cuda_check(ctx, cudaStreamSynchronize(stream), "cudaStreamSynchronize"))) return rc;
-        total = *ctx->host_total;
+        total = ctx->host_total[0];
+        emitting = ctx->host_total[1];
     }
     if (total > (uint64_t)GSR_MAX_PAIRS)
         return fail(ctx, GSR_ERR_TOO_MANY_PAIRS,
                     "tile-pair count " + std::to_string(total) + " exceeds GSR_MAX_PAIRS");
     const uint32_t num = (uint32_t)total;
+    const int m = (int)emitting;
 
     // 2. grow the pair buffers: max(65536, 16 n, 1.5 x pairs).
     if (num > ctx->cap_pairs || !ctx->pairs.k[0]) {
@@ -512,65 +675,51 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         cap = std::max<size_t>(cap, (size_t)num + num / 2);
         cap = std::min<size_t>(cap, (size_t)GSR_MAX_PAIRS);
         cap = std::max<size_t>(cap, num);
-        for (int b = 0; b < 3; ++b) {
-            if (ctx->pairs.k[b]) cudaFree(ctx->pairs.k[b]);
-            if (ctx->pairs.v[b]) cudaFree(ctx->pairs.v[b]);
-            ctx->pairs.k[b] = nullptr;
-            ctx->pairs.v[b] = nullptr;
-        }
-        ctx->cap_pairs = 0;
-        for (int b = 0; b < 3; ++b) {
-            if (cudaMalloc(&ctx->pairs.k[b], cap * sizeof(uint64_t)) != cudaSuccess ||
-                cudaMalloc(&ctx->pairs.v[b], cap * sizeof(uint32_t)) != cudaSuccess) {
-                cudaGetLastError();
-                return fail(ctx, GSR_ERR_OOM,
-                            "cudaMalloc failed for " + std::to_string(cap) + " tile pairs");
-            }
+        size_t have = 0;
+        if ((rc = grow_sort_buffers(ctx, ctx->pairs, &have, cap, "tile pairs"))) {
+            ctx->cap_pairs = 0;
+            return rc;
         }
         ctx->cap_pairs = cap;
     }
-    const int ntiles = (int)((num + kRadixTile - 1) / kRadixTile);
-    if ((rc = grow(ctx, &ctx->radix_counts, &ctx->cap_radix_tiles, (size_t)std::max(ntiles, 1), 256,
-                   "radix counts")))
-        return rc;
 
     if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->ranges, 0, num_tiles * 2 * sizeof(uint32_t), stream),
                          "cudaMemsetAsync")))
         return rc;
 
     if (num > 0) {
-        // 3. emission.
-        k_emit<<<nblk, kBinBlock, 0, stream>>>(splats, depths, n, tiles_x, tiles_y, ctx->blk_offs,
-                                               ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars);
-        GSR_LAUNCHED(ctx);
-        // 4. radix sort over the digits the keys can occupy; constant ones skip on the device.
-        k_radix_plan<<<1, 32, 0, stream>>>(ctx->scalars, digits, ctx->plan);
-        GSR_LAUNCHED(ctx);
         if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->radix_totals, 0,
                                                   kMaxDigits * 256 * sizeof(uint32_t), stream),
                              "cudaMemsetAsync")))
             return rc;
-        for (int d = 0; d < digits; ++d) {
-            uint32_t *totals = ctx->radix_totals + 256 * d;
-            k_radix_upsweep<<<ntiles, kRadixThreads, 0, stream>>>(ctx->plan, d, ctx->pairs, num, ntiles,
-                                                                  ctx->radix_counts, totals);
-            GSR_LAUNCHED(ctx);
-            k_radix_scan<<<256, kRadixThreads, 0, stream>>>(ctx->plan, d, ntiles, ctx->radix_counts,
-                                                            totals);
-            GSR_LAUNCHED(ctx);
-            k_radix_downsweep<<<ntiles, kRadixThreads, 0, stream>>>(ctx->plan, d, ctx->pairs, num,
-                                                                    ntiles, ctx->radix_counts);
-            GSR_LAUNCHED(ctx);
-        }
-        k_copy_if_unsorted<<<std::min(ntiles, 1024), 256, 0, stream>>>(ctx->plan, ctx->pairs, num);
+        // 3. depth sort of the emitting splats.
+        k_compact<<<nblk, kBinBlock, 0, stream>>>(ctx->counts, depths, n, blk_emit, ctx->depth.k[0],
+                                                  ctx->depth.v[0]);
         GSR_LAUNCHED(ctx);
-        // 5. per-tile ranges.
+        if ((rc = radix_sort<uint32_t>(ctx, ctx->depth, (uint32_t)m, 0, 4,
+                                       ctx->scalars + kScalarDepthAnd, ctx->plan, stream)))
+            return rc;
+        // 4. pair offsets in depth order, emission.
+        const int mblk = (m + kBinBlock - 1) / kBinBlock;
+        k_sorted_sums<<<mblk, kBinBlock, 0, stream>>>(ctx->depth.v[1], ctx->counts, m, blk_sorted);
+        GSR_LAUNCHED(ctx);
+        k_scan_u64<<<1, 1024, 0, stream>>>(blk_sorted, mblk);
+        GSR_LAUNCHED(ctx);
+        k_emit<<<mblk, kBinBlock, 0, stream>>>(splats, depths, ctx->depth.v[1], m, tiles_x, tiles_y,
+                                               blk_sorted, ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars);
+        GSR_LAUNCHED(ctx);
+        // 5. stable sort on the tile digits only.
+        if ((rc = radix_sort<uint64_t>(ctx, ctx->pairs, num, 4, digits, ctx->scalars + kScalarKeyAnd,
+                                       ctx->plan + 1, stream)))
+            return rc;
+        // 6. per-tile ranges.
         k_extract_ranges<<<(num + 255) / 256, 256, 0, stream>>>(ctx->pairs.k[1], num, ctx->ranges);
         GSR_LAUNCHED(ctx);
     }
 
     ctx->last_stream = stream;
     ctx->last_pairs = num;
+    ctx->last_emitting = (uint32_t)m;
     ctx->last_key_digits = digits;
     out->keys = ctx->pairs.k[1];
     out->sorted_idx = ctx->pairs.v[1];

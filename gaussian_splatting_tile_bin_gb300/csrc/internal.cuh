@@ -19,8 +19,8 @@ constexpr int kRadixTile = kRadixThreads * kRadixItems;
 constexpr int kMaxDigits = 8;             // 8-bit digits of a 64-bit key
 
 // Which of the three key/value buffers each executed radix pass reads and
-// writes.  Buffer 0 holds the emitted pairs, buffer 1 the sorted result,
-// buffer 2 is scratch.  Written on the device after emission.
+// writes.  Buffer 0 holds the unsorted input, buffer 1 the sorted result,
+// buffer 2 is scratch.  Written on the device once the keys are known.
 struct RadixPlan {
     int num_exec;
     int exec[kMaxDigits];
@@ -28,10 +28,13 @@ struct RadixPlan {
     int dst[kMaxDigits];
 };
 
-struct PairBuffers {
-    uint64_t *k[3];
+template <typename K>
+struct SortBuffers {
+    K *k[3];
     uint32_t *v[3];
 };
+using PairBuffers = SortBuffers<uint64_t>;   // (tile << 32 | depth bits, splat index)
+using DepthBuffers = SortBuffers<uint32_t>;  // (depth bits, splat index)
 
 }  // namespace gsr
 
@@ -48,16 +51,17 @@ struct gsr_ctx {
     gsr::PairBuffers pairs = {};
     size_t cap_splats = 0;
     uint32_t *counts = nullptr;                 // [cap_splats] tile count per splat
+    gsr::DepthBuffers depth = {};               // [cap_splats] x 3: depth sort of emitting splats
     size_t cap_blocks = 0;
-    unsigned long long *blk_sums = nullptr;     // [2 * cap_blocks]: sums, then offsets
-    unsigned long long *blk_offs = nullptr;     // blk_sums + cap_blocks
+    unsigned long long *blk_sums = nullptr;     // [4 * cap_blocks]: see bin.cu
+    unsigned long long *blk_offs = nullptr;
     size_t cap_tiles = 0;
     uint32_t *ranges = nullptr;                 // [2 * cap_tiles]
     size_t cap_radix_tiles = 0;
     uint32_t *radix_counts = nullptr;           // [256 * cap_radix_tiles]
     uint32_t *radix_totals = nullptr;           // [kMaxDigits * 256]
-    unsigned long long *scalars = nullptr;      // [0] pair total, [1] AND of keys, [2] OR of keys
-    gsr::RadixPlan *plan = nullptr;
+    unsigned long long *scalars = nullptr;      // see bin.cu (kScalar*)
+    gsr::RadixPlan *plan = nullptr;             // [2]: depth sort, tile sort
     unsigned long long *host_total = nullptr;   // pinned
     size_t cap_grad_acc = 0;
     double *grad_acc = nullptr;                 // [9 * cap] backward accumulator
@@ -66,6 +70,7 @@ struct gsr_ctx {
     cudaStream_t last_stream = nullptr;
     uint32_t last_pairs = 0;
     int last_key_digits = 0;
+    uint32_t last_emitting = 0;                 // splats with at least one pair
 };
 
 namespace gsr {

@@ -189,8 +189,10 @@ int gsr_rasterize_backward_noalloc(gsr_ctx *ctx, const gsr_splat2d *splats, int3
                                    const uint32_t *last_contrib, float *grad, void *stream);
 
 /* Statistics of the last gsr_bin_splats (synchronises its stream).
- * radix_passes: passes the sort executed; digit_mask: bit d set when 8-bit digit
- * d of the keys varied (pass d executed); capacity: arena capacity in pairs. */
+ * radix_passes: radix passes executed (the depth sort of the emitting splats
+ * runs key digits 0-3, the tile sort of the pairs digits 4 and up); digit_mask:
+ * bit d set when 8-bit digit d of the keys varied (its pass executed);
+ * capacity: arena capacity in pairs. */
 typedef struct gsr_bin_stats {
     uint32_t num_pairs;
     int32_t radix_passes;
