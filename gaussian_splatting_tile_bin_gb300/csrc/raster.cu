@@ -28,6 +28,10 @@
 #ifndef GSR_BWD_MIN_BLOCKS
 #define GSR_BWD_MIN_BLOCKS 1
 #endif
+// Splats staged per thread and batch: a batch holds 256 x this many splats.
+#ifndef GSR_STAGE_PER_THREAD
+#define GSR_STAGE_PER_THREAD 2
+#endif
 
 namespace gsr {
 namespace {
@@ -35,6 +39,7 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int SM_BLOCKS_CAP = 152 * 16;     // grid-stride cap for elementwise passes
 constexpr int kWarps = kTilePixels / 32;
+constexpr int kBatch = kTilePixels * GSR_STAGE_PER_THREAD;  // splats per staged batch
 constexpr float kAlphaMin = 1.0f / 255.0f;  // "W1 warp sparse skip + exp-skip", body
 constexpr float kAlphaMax = 0.999f;         // "A.9 f16 forward", snippet
 constexpr float kSigmaSkip = 5.55f;         // "W1 warp sparse skip + exp-skip", section 1, W1b
@@ -52,10 +57,10 @@ constexpr float kLn255Margin = 5.5412636f + 1e-3f;
 // 5.55 the bound is the pages' exact skip; below it only lanes whose exact alpha
 // test would fail are dropped, so the decisions are those of the exact test.
 struct StagedBatch {
-    float4 geo[kTilePixels];
-    float4 aux[kTilePixels];
-    float4 rgb[kTilePixels];
-    uint32_t mask[kTilePixels];  // bit w: warp w's 8x4 block may see sigma < bound
+    float4 geo[kBatch];
+    float4 aux[kBatch];
+    float4 rgb[kBatch];
+    uint32_t mask[kBatch];  // bit w: warp w's 8x4 block may see sigma < bound
 };
 
 // Warp w covers the 8x4 block (w & 1, w >> 1) of the tile; lane l the pixel
@@ -134,26 +139,6 @@ __device__ __forceinline__ float splat_alpha(float sigma, float o, float &e, flo
     return fminf(kAlphaMax, raw);
 }
 
-// float -> double with integer operations only (this GPU's FP64 pipe is narrow
-// and the conversion would otherwise run there).  Subnormal floats become 0.
-__device__ __forceinline__ double widen(float f)
-{
-    const uint32_t u = __float_as_uint(f);
-    const uint32_t e = (u >> 23) & 0xffu;
-    const uint32_t hi_sign = u & 0x80000000u;
-    uint32_t hi, lo;
-    if (e == 0u) {
-        hi = hi_sign;
-        lo = 0u;
-    } else {
-        const uint32_t e64 = (e == 0xffu) ? 0x7ffu : e + 896u;
-        const uint32_t m = u & 0x7fffffu;
-        hi = hi_sign | (e64 << 20) | (m >> 3);
-        lo = m << 29;
-    }
-    return __hiloint2double((int)hi, (int)lo);
-}
-
 // --- forward ---------------------------------------------------------------
 
 template <bool kCull>
@@ -178,13 +163,17 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
     uint32_t last = 0;
     bool done = !inside;
 
-    for (uint32_t bstart = range.x; bstart < range.y; bstart += kTilePixels) {
+    for (uint32_t bstart = range.x; bstart < range.y; bstart += kBatch) {
         // Every pixel of the tile has stopped: no later splat can change it.
         if (__syncthreads_count(done) == kTilePixels) break;
-        const uint32_t pos = bstart + threadIdx.x;
-        if (pos < range.y) stage_splat<kCull>(sb, threadIdx.x, splats, __ldg(sorted_idx + pos), x0, y0);
+#pragma unroll
+        for (int q = 0; q < GSR_STAGE_PER_THREAD; ++q) {
+            const int slot = q * kTilePixels + threadIdx.x;
+            const uint32_t pos = bstart + slot;
+            if (pos < range.y) stage_splat<kCull>(sb, slot, splats, __ldg(sorted_idx + pos), x0, y0);
+        }
         __syncthreads();
-        const int cnt = (int)min(range.y - bstart, (uint32_t)kTilePixels);
+        const int cnt = (int)min(range.y - bstart, (uint32_t)kBatch);
         if (__all_sync(kFull, done)) continue;
         for (int c0 = 0; c0 < cnt; c0 += 32) {
             uint32_t m = __ballot_sync(kFull, c0 + lane < cnt && (sb.mask[c0 + lane] & wbit));
@@ -229,7 +218,8 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
 // Sums the 9 per-lane values over the warp and adds the totals to acc[0..8] in
 // one atomic instruction: a transposed butterfly leaves component k (k < 8) in
 // lanes 4k..4k+3 after 7 shuffles, component 8 takes a plain butterfly, and
-// lanes 4k and lane 1 issue the adds.
+// lanes 4k and lane 1 widen their sums to double and issue the adds (9 lanes
+// share one conversion instruction on the narrow FP64 pipe).
 __device__ __forceinline__ void warp_reduce_add9(float (&v)[9], double *__restrict__ acc, int lane)
 {
     const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
@@ -253,8 +243,8 @@ __device__ __forceinline__ void warp_reduce_add9(float (&v)[9], double *__restri
     float z = v[8];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
-    if ((lane & 3) == 0) atomicAdd(acc + (lane >> 2), widen(y));
-    else if (lane == 1) atomicAdd(acc + 8, widen(z));
+    if ((lane & 3) == 0) atomicAdd(acc + (lane >> 2), (double)y);
+    else if (lane == 1) atomicAdd(acc + 8, (double)z);
 }
 
 template <bool kWarpSkip, bool kLastContrib, bool kCull>
@@ -301,13 +291,16 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
     }
     float3 S = make_float3(0.0f, 0.0f, 0.0f);
 
-    for (int bend = (int)cta_end; bend > 0; bend -= kTilePixels) {
-        const int bstart = max(0, bend - kTilePixels);
+    for (int bend = (int)cta_end; bend > 0; bend -= kBatch) {
+        const int bstart = max(0, bend - kBatch);
         const int cnt = bend - bstart;
         __syncthreads();
-        if (threadIdx.x < cnt)
-            stage_splat<kCull>(sb, threadIdx.x, splats, __ldg(sorted_idx + range.x + bstart + threadIdx.x),
-                               x0, y0);
+#pragma unroll
+        for (int q = 0; q < GSR_STAGE_PER_THREAD; ++q) {
+            const int slot = q * kTilePixels + threadIdx.x;
+            if (slot < cnt)
+                stage_splat<kCull>(sb, slot, splats, __ldg(sorted_idx + range.x + bstart + slot), x0, y0);
+        }
         __syncthreads();
         const int jlim = min(cnt, (int)warp_end - bstart);  // this warp's positions: j < jlim
         for (int c0 = ((jlim - 1) >> 5) << 5; c0 >= 0 && jlim > 0; c0 -= 32) {
@@ -335,10 +328,12 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                             const float one_m = __fsub_rn(1.0f, alpha);
                             const float inv = __fdividef(1.0f, one_m);
                             // Transmittance in front of this splat: the forward's
-                            // T_j (1 - alpha) undone with one correctly rounded
-                            // division, so a pixel replayed through hundreds of
-                            // splats drifts by at most a rounding per splat.
-                            const float Tj = __fdiv_rn(T, one_m);
+                            // T_j (1 - alpha) undone by T / (1 - alpha), a reciprocal
+                            // refined by one Newton step on the exact residual (an
+                            // FMA), so a pixel replayed through hundreds of splats
+                            // drifts by about a rounding per splat.
+                            float Tj = T * inv;
+                            Tj = __fmaf_rn(inv, __fmaf_rn(-one_m, Tj, T), Tj);
                             const float aT = alpha * Tj;
                             v[5] = g.x * aT;
                             v[6] = g.y * aT;
