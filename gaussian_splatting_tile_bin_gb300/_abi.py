@@ -33,8 +33,10 @@ class _Bins(ctypes.Structure):
 
 
 class _BinStats(ctypes.Structure):
-    _fields_ = [("num_pairs", ctypes.c_uint32), ("radix_passes", ctypes.c_int32),
-                ("digit_mask", ctypes.c_uint32), ("key_digits", ctypes.c_int32),
+    _fields_ = [("num_pairs", ctypes.c_uint32), ("emitting", ctypes.c_uint32),
+                ("radix_passes", ctypes.c_int32), ("depth_pass_mask", ctypes.c_uint32),
+                ("tile_pass_mask", ctypes.c_uint32), ("tile_digit_bits", ctypes.c_int32),
+                ("tile_digits", ctypes.c_int32), ("lookback_timeouts", ctypes.c_uint32),
                 ("capacity", ctypes.c_uint64)]
 
 
@@ -100,9 +102,7 @@ class Context:
     def bin_stats(self) -> dict:
         st = _BinStats()
         self._check(lib.gsr_get_bin_stats(self._h, ctypes.byref(st)))
-        return {"num_pairs": st.num_pairs, "radix_passes": st.radix_passes,
-                "digit_mask": st.digit_mask, "key_digits": st.key_digits,
-                "capacity": int(st.capacity)}
+        return {name: (int(getattr(st, name))) for name, _ in _BinStats._fields_}
 
     def close(self):
         if getattr(self, "_h", None):

@@ -98,10 +98,10 @@ void gsr_destroy(gsr_ctx *ctx)
         }
         cudaFree(ctx->blk_sums);
         cudaFree(ctx->ranges);
-        cudaFree(ctx->radix_counts);
-        cudaFree(ctx->radix_totals);
+        cudaFree(ctx->radix_status);
+        cudaFree(ctx->radix_hist);
+        cudaFree(ctx->radix_err);
         cudaFree(ctx->scalars);
-        cudaFree(ctx->plan);
         cudaFree(ctx->grad_acc);
         if (ctx->host_total) cudaFreeHost(ctx->host_total);
     }
@@ -213,21 +213,26 @@ int gsr_get_bin_stats(gsr_ctx *ctx, gsr_bin_stats *out)
     if (!ctx || !out) return GSR_ERR_INVALID_ARG;
     ctx->err.clear();
     DeviceGuard g(ctx->device);
+    *out = gsr_bin_stats{};
     out->num_pairs = ctx->last_pairs;
-    out->key_digits = ctx->last_key_digits;
+    out->emitting = ctx->last_emitting;
     out->capacity = ctx->cap_pairs;
-    out->radix_passes = 0;
-    out->digit_mask = 0;
-    if (!ctx->plan || ctx->last_pairs == 0) return GSR_OK;
-    int rc = cuda_check(ctx, cudaStreamSynchronize(ctx->last_stream), "cudaStreamSynchronize");
+    if (ctx->last_stream || ctx->scalars) {
+        int rc = cuda_check(ctx, cudaStreamSynchronize(ctx->last_stream), "cudaStreamSynchronize");
+        if (rc) return rc;
+    }
+    int tile_bits = 0, tile_digits = 0;
+    int rc = gsr::bin_pass_masks(ctx, &out->depth_pass_mask, &out->tile_pass_mask, &tile_bits, &tile_digits);
     if (rc) return rc;
-    RadixPlan plan[2];
-    rc = cuda_check(ctx, cudaMemcpy(plan, ctx->plan, sizeof plan, cudaMemcpyDeviceToHost), "cudaMemcpy");
-    if (rc) return rc;
-    // The depth sort runs the low four digits, the tile sort the rest.
-    out->radix_passes = plan[0].num_exec + plan[1].num_exec;
-    for (int d = 0; d < kMaxDigits; ++d)
-        if (plan[0].exec[d] || plan[1].exec[d]) out->digit_mask |= 1u << d;
+    out->tile_digit_bits = tile_bits;
+    out->tile_digits = tile_digits;
+    out->radix_passes = __builtin_popcount(out->depth_pass_mask) + __builtin_popcount(out->tile_pass_mask);
+    if (ctx->radix_err) {
+        unsigned long long e = 0;
+        rc = cuda_check(ctx, cudaMemcpy(&e, ctx->radix_err, sizeof e, cudaMemcpyDeviceToHost), "cudaMemcpy");
+        if (rc) return rc;
+        out->lookback_timeouts = (uint32_t)e;
+    }
     return GSR_OK;
 }
 

@@ -135,6 +135,46 @@ __device__ __forceinline__ void block_and_or_into(unsigned long long a, unsigned
     }
 }
 
+// Radix digits: the key bits [key_lo, key_hi) split into num_fields digits of
+// equal width, at most 8 bits each.
+__host__ __device__ __forceinline__ int num_fields(int key_lo, int key_hi)
+{
+    return (key_hi - key_lo + 7) / 8;
+}
+
+__host__ __device__ __forceinline__ void field_geom(int key_lo, int key_hi, int nfields, int f, int &shift,
+                                                    int &width)
+{
+    const int w = (key_hi - key_lo + nfields - 1) / nfields;
+    shift = key_lo + f * w;
+    width = key_hi - shift < w ? key_hi - shift : w;
+}
+
+// Digit f of the keys varies iff its bits differ between the AND and the OR of
+// all keys.
+__host__ __device__ __forceinline__ bool field_varies(unsigned long long and_or_diff, int shift, int width)
+{
+    return width > 0 && ((and_or_diff >> shift) & ((1ull << width) - 1ull)) != 0ull;
+}
+
+// Position of field among the executed passes (-1 if skipped) and their number.
+__host__ __device__ __forceinline__ int field_pass(unsigned long long diff, int key_lo, int key_hi, int field,
+                                                  int *executed)
+{
+    const int nf = num_fields(key_lo, key_hi);
+    int k = 0, j = -1;
+    for (int f = 0; f < nf; ++f) {
+        int sh, w;
+        field_geom(key_lo, key_hi, nf, f, sh, w);
+        if (field_varies(diff, sh, w)) {
+            if (f == field) j = k;
+            ++k;
+        }
+    }
+    *executed = k;
+    return j;
+}
+
 __global__ void k_init_scalars(unsigned long long *__restrict__ scalars)
 {
     if (threadIdx.x != 0) return;
@@ -232,22 +272,32 @@ k_count_totals(const unsigned long long *__restrict__ blk_pairs, unsigned long l
     }
 }
 
-// Writes (depth bits, splat index) of every emitting splat, in splat order.
+// Writes (depth bits, splat index) of every emitting splat, in splat order,
+// and adds their four 8-bit depth digits to the depth sort's digit totals.
 __global__ void __launch_bounds__(kBinBlock)
 k_compact(const uint32_t *__restrict__ counts, const float *__restrict__ depths, int n,
           const unsigned long long *__restrict__ blk_emit_offs, uint32_t *__restrict__ dkeys,
-          uint32_t *__restrict__ didx)
+          uint32_t *__restrict__ didx, uint32_t *__restrict__ hist)
 {
     __shared__ uint32_t ws[8];
+    __shared__ uint32_t h[4][256];
+    for (int k = threadIdx.x; k < 4 * 256; k += kBinBlock) (&h[0][0])[k] = 0;
     const int i = blockIdx.x * kBinBlock + threadIdx.x;
     const bool emits = i < n && counts[i] > 0;
     uint32_t total;
     const uint32_t excl = block_exclusive_scan_256<uint32_t>(emits ? 1u : 0u, ws, &total);
     if (emits) {
         const size_t pos = (size_t)blk_emit_offs[blockIdx.x] + excl;
-        dkeys[pos] = __float_as_uint(__ldg(depths + i));
+        const uint32_t db = __float_as_uint(__ldg(depths + i));
+        dkeys[pos] = db;
         didx[pos] = (uint32_t)i;
+#pragma unroll
+        for (int f = 0; f < 4; ++f) atomicAdd(&h[f][(db >> (8 * f)) & 0xffu], 1u);
     }
+    __syncthreads();
+#pragma unroll
+    for (int f = 0; f < 4; ++f)
+        if (h[f][threadIdx.x]) atomicAdd(&hist[f * 256 + threadIdx.x], h[f][threadIdx.x]);
 }
 
 // Per block of 256 depth-sorted splats: their pair total.
@@ -274,8 +324,10 @@ __global__ void __launch_bounds__(kBinBlock)
 k_emit(const float *__restrict__ splats, const float *__restrict__ depths,
        const uint32_t *__restrict__ sorted_idx, int m, int tiles_x, int tiles_y,
        const unsigned long long *__restrict__ blk_offs, uint64_t *__restrict__ keys,
-       uint32_t *__restrict__ vals, unsigned long long *__restrict__ scalars)
+       uint32_t *__restrict__ vals, unsigned long long *__restrict__ scalars, int key_hi,
+       uint32_t *__restrict__ hist)
 {
+    __shared__ uint32_t h[4][256];
     __shared__ uint32_t s_off[kBinBlock];
     __shared__ int4 s_rect[kBinBlock];
     __shared__ uint32_t s_db[kBinBlock];
@@ -283,6 +335,8 @@ k_emit(const float *__restrict__ splats, const float *__restrict__ depths,
     __shared__ uint32_t ws[8];
     __shared__ unsigned long long s_and[8], s_or[8];
 
+    for (int q = threadIdx.x; q < 4 * 256; q += kBinBlock) (&h[0][0])[q] = 0;
+    const int nf = num_fields(32, key_hi);
     const int k = blockIdx.x * kBinBlock + threadIdx.x;
     uint32_t c = 0;
     int4 r = make_int4(0, 0, -1, -1);
@@ -322,39 +376,49 @@ k_emit(const float *__restrict__ splats, const float *__restrict__ depths,
         vals[base + q] = s_idx[lo];
         acc_and &= key;
         acc_or |= key;
+        for (int f = 0; f < nf; ++f) {
+            int sh, w;
+            field_geom(32, key_hi, nf, f, sh, w);
+            atomicAdd(&h[f][(uint32_t)(key >> sh) & ((1u << w) - 1u)], 1u);
+        }
     }
     block_and_or_into(acc_and, acc_or, s_and, s_or, scalars + kScalarKeyAnd);
+    for (int f = 0; f < nf; ++f)
+        if (h[f][threadIdx.x]) atomicAdd(&hist[f * 256 + threadIdx.x], h[f][threadIdx.x]);
 }
 
 // --- radix sort --------------------------------------------------------------
+//
+// A stable LSD sort over the key bits [key_lo, key_hi), split into nfields
+// digits of equal width (at most 8 bits).  Each digit takes one kernel launch
+// (single-pass, decoupled look-back): a CTA claims the next 2048-key tile in
+// launch order, ranks its keys stably by digit, publishes its per-digit counts,
+// then adds up the counts of the tiles before it (walking back until a tile has
+// published its inclusive prefix) and scatters through shared memory so each
+// digit's keys leave in contiguous runs.  The digit totals come from the kernel
+// that produced the keys.  A digit every key shares is skipped; the executed
+// passes chain buffer 0 -> ... -> buffer 1.
 
-// Decides which 8-bit digits in [d_lo, d_hi) vary (from acc[0] = AND, acc[1] =
-// OR of the keys) and chains the executed passes so that the last one writes
-// buffer 1: pass j of k reads the previous pass's output (buffer 0 for the
-// first) and writes buffer 1 when k - 1 - j is even, buffer 2 otherwise.
-__global__ void k_radix_plan(const unsigned long long *__restrict__ acc, int d_lo, int d_hi,
-                             RadixPlan *__restrict__ plan)
+constexpr int kOsThreads = 256;
+constexpr int kOsItems = 8;
+constexpr int kOsTile = kOsThreads * kOsItems;
+constexpr unsigned long long kStatusAggregate = 1ull << 62;
+constexpr unsigned long long kStatusInclusive = 2ull << 62;
+constexpr unsigned long long kStatusValue = (1ull << 62) - 1;
+// A look-back wait gives up after this many polls (far beyond any real wait)
+// and records the timeout instead of hanging the GPU.
+constexpr int kLookbackSpinLimit = 1 << 22;
+
+__device__ __forceinline__ unsigned long long load_relaxed(const unsigned long long *p)
 {
-    if (threadIdx.x != 0) return;
-    const unsigned long long diff = acc[0] ^ acc[1];
-    int list[kMaxDigits];
-    int k = 0;
-    for (int d = 0; d < kMaxDigits; ++d) {
-        const bool ex = d >= d_lo && d < d_hi && ((diff >> (8 * d)) & 0xffull) != 0ull;
-        plan->exec[d] = ex ? 1 : 0;
-        plan->src[d] = 0;
-        plan->dst[d] = 0;
-        if (ex) list[k++] = d;
-    }
-    int prev = 0;
-    for (int j = 0; j < k; ++j) {
-        const int d = list[j];
-        const int dst = ((k - 1 - j) % 2 == 0) ? 1 : 2;
-        plan->src[d] = prev;
-        plan->dst[d] = dst;
-        prev = dst;
-    }
-    plan->num_exec = k;
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void store_relaxed(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Buffer b of the three (a select, so the kernel parameter block is not copied
@@ -370,95 +434,58 @@ __device__ __forceinline__ uint32_t *vals_of(const SortBuffers<K> &p, int b)
     return b == 0 ? p.v[0] : (b == 1 ? p.v[1] : p.v[2]);
 }
 
-// Per radix tile: how many keys carry each digit value.  counts is
-// digit-major, [256][ntiles]; totals[digit] accumulates over tiles.
 template <typename K>
-__global__ void __launch_bounds__(kRadixThreads)
-k_radix_upsweep(const RadixPlan *__restrict__ plan, int d, SortBuffers<K> bufs, uint32_t num,
-                int ntiles, uint32_t *__restrict__ counts, uint32_t *__restrict__ totals)
+__global__ void __launch_bounds__(kOsThreads)
+k_onesweep(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__restrict__ and_or, int key_lo,
+           int key_hi, int field, const uint32_t *__restrict__ hist, unsigned long long *__restrict__ status,
+           uint32_t *__restrict__ tile_counter, unsigned long long *__restrict__ err)
 {
-    if (!plan->exec[d]) return;
-    const K *__restrict__ keys = keys_of(bufs, plan->src[d]);
-    __shared__ uint32_t h[256];
-    h[threadIdx.x] = 0;
-    __syncthreads();
-    const int shift = 8 * d;
-    const uint32_t base = blockIdx.x * kRadixTile;
-#pragma unroll
-    for (int k = 0; k < kRadixItems; ++k) {
-        const uint32_t i = base + k * kRadixThreads + threadIdx.x;
-        if (i < num) atomicAdd(&h[(uint32_t)(keys[i] >> shift) & 0xffu], 1u);
-    }
-    __syncthreads();
-    const uint32_t c = h[threadIdx.x];
-    counts[(size_t)threadIdx.x * ntiles + blockIdx.x] = c;
-    if (c) atomicAdd(&totals[threadIdx.x], c);
-}
-
-// One block per digit value: the global start of the digit (sum of the totals
-// of smaller digits) plus an exclusive scan of that digit's per-tile counts,
-// written in place.
-__global__ void __launch_bounds__(kRadixThreads)
-k_radix_scan(const RadixPlan *__restrict__ plan, int d, int ntiles, uint32_t *__restrict__ counts,
-             const uint32_t *__restrict__ totals)
-{
-    if (!plan->exec[d]) return;
-    __shared__ uint32_t ws[8];
-    const uint32_t digit = blockIdx.x;
-    uint32_t base;
-    {
-        const uint32_t x = threadIdx.x < digit ? totals[threadIdx.x] : 0u;
-        block_exclusive_scan_256<uint32_t>(x, ws, &base);
-    }
-    uint32_t *row = counts + (size_t)digit * ntiles;
-    uint32_t carry = base;
-    for (int start = 0; start < ntiles; start += kRadixThreads) {
-        const int i = start + threadIdx.x;
-        const uint32_t c = i < ntiles ? row[i] : 0u;
-        uint32_t sum;
-        const uint32_t e = block_exclusive_scan_256<uint32_t>(c, ws, &sum);
-        if (i < ntiles) row[i] = carry + e;
-        carry += sum;
-    }
-}
-
-// Stable scatter of one radix tile.  Warp w owns keys [w*256, w*256+256) of
-// the tile and walks them in 8 rounds of 32 consecutive keys; within a round
-// equal digits are ranked by lane (match.any), across rounds by per-warp digit
-// counters, across warps by a per-digit prefix over the 8 warps, across tiles
-// by the scanned counts.  This reproduces input order among equal digits.
-template <typename K>
-__global__ void __launch_bounds__(kRadixThreads)
-k_radix_downsweep(const RadixPlan *__restrict__ plan, int d, SortBuffers<K> bufs, uint32_t num,
-                  int ntiles, const uint32_t *__restrict__ offsets)
-{
-    if (!plan->exec[d]) return;
-    const int src = plan->src[d], dst = plan->dst[d];
+    const unsigned long long diff = and_or[0] ^ and_or[1];
+    int executed;
+    const int j = field_pass(diff, key_lo, key_hi, field, &executed);
+    if (j < 0) return;
+    const int nf = num_fields(key_lo, key_hi);
+    int shift, width;
+    field_geom(key_lo, key_hi, nf, field, shift, width);
+    const int dst = ((executed - 1 - j) % 2 == 0) ? 1 : 2;
+    const int src = (j == 0) ? 0 : (((executed - j) % 2 == 0) ? 1 : 2);
+    const uint32_t radix = 1u << width, dmask = radix - 1u;
     const K *__restrict__ kin = keys_of(bufs, src);
     const uint32_t *__restrict__ vin = vals_of(bufs, src);
     K *__restrict__ kout = keys_of(bufs, dst);
     uint32_t *__restrict__ vout = vals_of(bufs, dst);
 
-    __shared__ uint32_t wcnt[8][256];
-    __shared__ uint32_t toff[256];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int k = threadIdx.x; k < 8 * 256; k += kRadixThreads) (&wcnt[0][0])[k] = 0;
-    toff[threadIdx.x] = offsets[(size_t)threadIdx.x * ntiles + blockIdx.x];
-    __syncthreads();
+    __shared__ uint32_t wcnt[8][256];   // per-warp digit counts, then per-warp prefixes
+    __shared__ uint32_t s_cnt[256];     // this tile's digit counts
+    __shared__ uint32_t s_lstart[256];  // local start of each digit's run in the staged tile
+    __shared__ uint32_t s_goff[256];    // global start of each digit's run
+    __shared__ uint32_t ws[8];
+    __shared__ K s_keys[kOsTile];
+    __shared__ uint32_t s_vals[kOsTile];
+    __shared__ uint32_t s_tile;
 
-    const int shift = 8 * d;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int k = tid; k < 8 * 256; k += kOsThreads) (&wcnt[0][0])[k] = 0;
+    if (tid == 0) s_tile = atomicAdd(tile_counter, 1u);
+    __syncthreads();
+    const uint32_t tile = s_tile;
+    const uint32_t tbase = tile * kOsTile;
+    const uint32_t tcount = min((uint32_t)kOsTile, num - tbase);
+
+    // Stable rank inside the tile: warp w owns keys [w*256, w*256+256) and
+    // walks them in 8 rounds of 32; equal digits are ranked by lane within a
+    // round (match.any) and by per-warp counters across rounds.
     const uint32_t lanemask_lt = (1u << lane) - 1u;
-    const uint32_t base = blockIdx.x * kRadixTile + warp * (32 * kRadixItems);
-    K key[kRadixItems];
-    uint32_t val[kRadixItems];
-    uint32_t rank[kRadixItems];
+    const uint32_t wbase = warp * (32 * kOsItems);
+    K key[kOsItems];
+    uint32_t val[kOsItems], rank[kOsItems];
 #pragma unroll
-    for (int k = 0; k < kRadixItems; ++k) {
-        const uint32_t i = base + k * 32 + lane;
-        const bool valid = i < num;
-        key[k] = valid ? kin[i] : (K)0;
-        val[k] = valid ? vin[i] : 0u;
-        const uint32_t digit = valid ? ((uint32_t)(key[k] >> shift) & 0xffu) : 0x100u;
+    for (int k = 0; k < kOsItems; ++k) {
+        const uint32_t i = wbase + k * 32 + lane;
+        const bool valid = i < tcount;
+        key[k] = valid ? kin[tbase + i] : (K)0;
+        val[k] = valid ? vin[tbase + i] : 0u;
+        const uint32_t digit = valid ? ((uint32_t)(key[k] >> shift) & dmask) : 0x100u;
         const uint32_t peers = __match_any_sync(kFull, digit);
         const uint32_t prior = valid ? wcnt[warp][digit] : 0u;
         __syncwarp();
@@ -469,34 +496,80 @@ k_radix_downsweep(const RadixPlan *__restrict__ plan, int d, SortBuffers<K> bufs
     }
     __syncthreads();
     {
-        const int v = threadIdx.x;
         uint32_t run = 0;
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
-            const uint32_t t = wcnt[w][v];
-            wcnt[w][v] = run;
+            const uint32_t t = wcnt[w][tid];
+            wcnt[w][tid] = run;
             run += t;
+        }
+        s_cnt[tid] = run;
+    }
+    uint32_t total;
+    const uint32_t lstart = block_exclusive_scan_256<uint32_t>(s_cnt[tid], ws, &total);
+    s_lstart[tid] = lstart;
+    uint32_t htotal;
+    const uint32_t gstart = block_exclusive_scan_256<uint32_t>(tid < (int)radix ? hist[tid] : 0u, ws, &htotal);
+
+    // Publish this tile's counts, add up the tiles before it, publish the prefix.
+    if (tid < (int)radix) {
+        const uint32_t c = s_cnt[tid];
+        unsigned long long *mine = status + (size_t)tile * 256 + tid;
+        unsigned long long prefix = 0;
+        if (tile == 0) {
+            store_relaxed(mine, kStatusInclusive | c);
+        } else {
+            store_relaxed(mine, kStatusAggregate | c);
+            for (int t = (int)tile - 1; t >= 0; --t) {
+                const unsigned long long *p = status + (size_t)t * 256 + tid;
+                unsigned long long v = load_relaxed(p);
+                int spins = 0;
+                while ((v >> 62) == 0ull) {
+                    if (++spins > kLookbackSpinLimit) {
+                        atomicAdd(err, 1ull);
+                        v = kStatusInclusive;
+                        break;
+                    }
+                    __nanosleep(32);
+                    v = load_relaxed(p);
+                }
+                prefix += v & kStatusValue;
+                if ((v & ~kStatusValue) == kStatusInclusive) break;
+            }
+            store_relaxed(mine, kStatusInclusive | (prefix + c));
+        }
+        s_goff[tid] = gstart + (uint32_t)prefix;
+    }
+    // Stage the tile in digit order, then write each digit's run contiguously.
+#pragma unroll
+    for (int k = 0; k < kOsItems; ++k) {
+        const uint32_t i = wbase + k * 32 + lane;
+        if (i < tcount) {
+            const uint32_t digit = (uint32_t)(key[k] >> shift) & dmask;
+            const uint32_t lpos = s_lstart[digit] + wcnt[warp][digit] + rank[k];
+            s_keys[lpos] = key[k];
+            s_vals[lpos] = val[k];
         }
     }
     __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kRadixItems; ++k) {
-        const uint32_t i = base + k * 32 + lane;
-        if (i < num) {
-            const uint32_t digit = (uint32_t)(key[k] >> shift) & 0xffu;
-            const uint32_t pos = toff[digit] + wcnt[warp][digit] + rank[k];
-            kout[pos] = key[k];
-            vout[pos] = val[k];
-        }
+    for (uint32_t i = tid; i < tcount; i += kOsThreads) {
+        const K kk = s_keys[i];
+        const uint32_t digit = (uint32_t)(kk >> shift) & dmask;
+        const uint32_t gpos = s_goff[digit] + (i - s_lstart[digit]);
+        kout[gpos] = kk;
+        vout[gpos] = s_vals[i];
     }
 }
 
-// When every digit was constant no pass ran and the input order is already
-// sorted; copy it to the result buffer.
+// When no digit varied no pass ran and the input order is already sorted;
+// copy it to the result buffer.
 template <typename K>
-__global__ void k_copy_if_unsorted(const RadixPlan *__restrict__ plan, SortBuffers<K> bufs, uint32_t num)
+__global__ void k_copy_if_unsorted(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__restrict__ and_or,
+                                   int key_lo, int key_hi)
 {
-    if (plan->num_exec != 0) return;
+    int executed;
+    field_pass(and_or[0] ^ and_or[1], key_lo, key_hi, -1, &executed);
+    if (executed != 0) return;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < num; i += gridDim.x * blockDim.x) {
         bufs.k[1][i] = bufs.k[0][i];
         bufs.v[1][i] = bufs.v[0][i];
@@ -574,31 +647,22 @@ int grow_sort_buffers(gsr_ctx *ctx, SortBuffers<K> &b, size_t *cap, size_t need,
         if (_rc) return _rc;                                                  \
     } while (0)
 
-// Stable LSD sort of bufs buffer 0 into buffer 1 over the digits in
-// [d_lo, d_hi) that vary (acc: AND / OR of the keys on the device).
+// Stable LSD sort of bufs buffer 0 into buffer 1 over the key bits
+// [key_lo, key_hi); and_or, hist, status, counter: the sort's device scratch.
 template <typename K>
-int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int d_lo, int d_hi,
-               const unsigned long long *acc, RadixPlan *plan, cudaStream_t stream)
+int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int key_hi,
+               const unsigned long long *and_or, const uint32_t *hist, unsigned long long *status,
+               uint32_t *counters, cudaStream_t stream)
 {
-    const int ntiles = (int)((num + kRadixTile - 1) / kRadixTile);
-    int rc;
-    if ((rc = grow(ctx, &ctx->radix_counts, &ctx->cap_radix_tiles, (size_t)std::max(ntiles, 1), 256,
-                   "radix counts")))
-        return rc;
-    k_radix_plan<<<1, 32, 0, stream>>>(acc, d_lo, d_hi, plan);
-    GSR_LAUNCHED(ctx);
-    for (int d = d_lo; d < d_hi; ++d) {
-        uint32_t *totals = ctx->radix_totals + 256 * d;
-        k_radix_upsweep<K><<<ntiles, kRadixThreads, 0, stream>>>(plan, d, bufs, num, ntiles,
-                                                                 ctx->radix_counts, totals);
-        GSR_LAUNCHED(ctx);
-        k_radix_scan<<<256, kRadixThreads, 0, stream>>>(plan, d, ntiles, ctx->radix_counts, totals);
-        GSR_LAUNCHED(ctx);
-        k_radix_downsweep<K><<<ntiles, kRadixThreads, 0, stream>>>(plan, d, bufs, num, ntiles,
-                                                                   ctx->radix_counts);
+    const int ntiles = (int)((num + kOsTile - 1) / kOsTile);
+    const int nf = num_fields(key_lo, key_hi);
+    for (int f = 0; f < nf; ++f) {
+        k_onesweep<K><<<ntiles, kOsThreads, 0, stream>>>(bufs, num, and_or, key_lo, key_hi, f, hist + 256 * f,
+                                                         status + (size_t)f * ntiles * 256, counters + f,
+                                                         ctx->radix_err);
         GSR_LAUNCHED(ctx);
     }
-    k_copy_if_unsorted<K><<<std::min(ntiles, 1024), 256, 0, stream>>>(plan, bufs, num);
+    k_copy_if_unsorted<K><<<std::min(ntiles, 1024), 256, 0, stream>>>(bufs, num, and_or, key_lo, key_hi);
     GSR_LAUNCHED(ctx);
     return GSR_OK;
 }
@@ -612,22 +676,27 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     const int tiles_x = (width + kTile - 1) / kTile;
     const int tiles_y = (height + kTile - 1) / kTile;
     const size_t num_tiles = (size_t)tiles_x * tiles_y;
-    const int key_bits = 32 + bits_for(num_tiles - 1);
-    const int digits = (key_bits + 7) / 8;
+    const int key_hi = 32 + bits_for(num_tiles - 1);  // keys occupy bits [0, key_hi)
+    const int digits = (key_hi + 7) / 8;
 
     // Fixed-size scratch, allocated once.
     if (!ctx->scalars) {
         if ((rc = cuda_check(ctx, cudaMalloc(&ctx->scalars, kScalarCount * sizeof(unsigned long long)),
                              "cudaMalloc")))
             return rc;
-        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->radix_totals, kMaxDigits * 256 * sizeof(uint32_t)),
+        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->radix_hist, (8 * 256 + 8) * sizeof(uint32_t)),
                              "cudaMalloc")))
             return rc;
-        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->plan, 2 * sizeof(RadixPlan)), "cudaMalloc"))) return rc;
-        if ((rc = cuda_check(ctx, cudaHostAlloc(&ctx->host_total, 2 * sizeof(unsigned long long),
+        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->radix_err, sizeof(unsigned long long)), "cudaMalloc")))
+            return rc;
+        if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->radix_err, 0, sizeof(unsigned long long), stream),
+                             "cudaMemsetAsync")))
+            return rc;
+        if ((rc = cuda_check(ctx, cudaHostAlloc(&ctx->host_total, 4 * sizeof(unsigned long long),
                                                 cudaHostAllocDefault),
                              "cudaHostAlloc")))
             return rc;
+        ctx->host_total[2] = 0;
     }
     const int nblk = (n + kBinBlock - 1) / kBinBlock;
     if (!ctx->depth.k[0] || (size_t)n > ctx->cap_splats) {
@@ -663,6 +732,15 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         total = ctx->host_total[0];
         emitting = ctx->host_total[1];
     }
+    // A look-back wait of an earlier call on this context that gave up (its
+    // copy has landed: the stream was synchronised above or by the caller).
+    if (ctx->host_total[2] != 0) {
+        ctx->host_total[2] = 0;
+        cudaMemsetAsync(ctx->radix_err, 0, sizeof(unsigned long long), stream);
+        return fail(ctx, GSR_ERR_CUDA,
+                    "a radix look-back wait timed out in an earlier gsr_bin_splats on this context; "
+                    "its bins were invalid");
+    }
     if (total > (uint64_t)GSR_MAX_PAIRS)
         return fail(ctx, GSR_ERR_TOO_MANY_PAIRS,
                     "tile-pair count " + std::to_string(total) + " exceeds GSR_MAX_PAIRS");
@@ -682,22 +760,39 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         }
         ctx->cap_pairs = cap;
     }
+    // Look-back status words: 256 per 2048-key tile and digit, for the depth
+    // sort's 4 digits and the tile sort's digits.
+    const int dtiles = (m + kOsTile - 1) / kOsTile;
+    const int ptiles = (int)((num + kOsTile - 1) / kOsTile);
+    const int tile_fields = num_fields(32, key_hi);
+    const size_t status_need = (size_t)256 * (4 * (size_t)dtiles + (size_t)tile_fields * ptiles);
+    if ((rc = grow(ctx, &ctx->radix_status, &ctx->cap_status, std::max<size_t>(status_need, 1), 1,
+                   "radix status")))
+        return rc;
 
     if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->ranges, 0, num_tiles * 2 * sizeof(uint32_t), stream),
                          "cudaMemsetAsync")))
         return rc;
 
     if (num > 0) {
-        if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->radix_totals, 0,
-                                                  kMaxDigits * 256 * sizeof(uint32_t), stream),
+        if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->radix_hist, 0, (8 * 256 + 8) * sizeof(uint32_t), stream),
                              "cudaMemsetAsync")))
             return rc;
+        if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->radix_status, 0,
+                                                  status_need * sizeof(unsigned long long), stream),
+                             "cudaMemsetAsync")))
+            return rc;
+        uint32_t *hist_depth = ctx->radix_hist;
+        uint32_t *hist_tile = ctx->radix_hist + 4 * 256;
+        uint32_t *counters = ctx->radix_hist + 8 * 256;
+        unsigned long long *status_depth = ctx->radix_status;
+        unsigned long long *status_tile = ctx->radix_status + (size_t)256 * 4 * dtiles;
         // 3. depth sort of the emitting splats.
         k_compact<<<nblk, kBinBlock, 0, stream>>>(ctx->counts, depths, n, blk_emit, ctx->depth.k[0],
-                                                  ctx->depth.v[0]);
+                                                  ctx->depth.v[0], hist_depth);
         GSR_LAUNCHED(ctx);
-        if ((rc = radix_sort<uint32_t>(ctx, ctx->depth, (uint32_t)m, 0, 4,
-                                       ctx->scalars + kScalarDepthAnd, ctx->plan, stream)))
+        if ((rc = radix_sort<uint32_t>(ctx, ctx->depth, (uint32_t)m, 0, 32, ctx->scalars + kScalarDepthAnd,
+                                       hist_depth, status_depth, counters, stream)))
             return rc;
         // 4. pair offsets in depth order, emission.
         const int mblk = (m + kBinBlock - 1) / kBinBlock;
@@ -705,22 +800,37 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         GSR_LAUNCHED(ctx);
         k_scan_u64<<<1, 1024, 0, stream>>>(blk_sorted, mblk);
         GSR_LAUNCHED(ctx);
-        k_emit<<<mblk, kBinBlock, 0, stream>>>(splats, depths, ctx->depth.v[1], m, tiles_x, tiles_y,
-                                               blk_sorted, ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars);
+        k_emit<<<mblk, kBinBlock, 0, stream>>>(splats, depths, ctx->depth.v[1], m, tiles_x, tiles_y, blk_sorted,
+                                               ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars, key_hi,
+                                               hist_tile);
         GSR_LAUNCHED(ctx);
         // 5. stable sort on the tile digits only.
-        if ((rc = radix_sort<uint64_t>(ctx, ctx->pairs, num, 4, digits, ctx->scalars + kScalarKeyAnd,
-                                       ctx->plan + 1, stream)))
-            return rc;
+        if (key_hi > 32) {
+            if ((rc = radix_sort<uint64_t>(ctx, ctx->pairs, num, 32, key_hi, ctx->scalars + kScalarKeyAnd,
+                                           hist_tile, status_tile, counters + 4, stream)))
+                return rc;
+        } else {
+            // One tile: the emitted order is already sorted.
+            if ((rc = cuda_check(ctx, cudaMemcpyAsync(ctx->pairs.k[1], ctx->pairs.k[0], (size_t)num * 8,
+                                                      cudaMemcpyDeviceToDevice, stream), "cudaMemcpyAsync")) ||
+                (rc = cuda_check(ctx, cudaMemcpyAsync(ctx->pairs.v[1], ctx->pairs.v[0], (size_t)num * 4,
+                                                      cudaMemcpyDeviceToDevice, stream), "cudaMemcpyAsync")))
+                return rc;
+        }
         // 6. per-tile ranges.
         k_extract_ranges<<<(num + 255) / 256, 256, 0, stream>>>(ctx->pairs.k[1], num, ctx->ranges);
         GSR_LAUNCHED(ctx);
+        // The look-back error word comes back with the next synchronisation.
+        if ((rc = cuda_check(ctx, cudaMemcpyAsync(ctx->host_total + 2, ctx->radix_err, sizeof(unsigned long long),
+                                                  cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync")))
+            return rc;
     }
 
     ctx->last_stream = stream;
     ctx->last_pairs = num;
     ctx->last_emitting = (uint32_t)m;
     ctx->last_key_digits = digits;
+    ctx->last_key_hi = key_hi;
     out->keys = ctx->pairs.k[1];
     out->sorted_idx = ctx->pairs.v[1];
     out->tile_ranges = ctx->ranges;
@@ -730,6 +840,31 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     out->height = height;
     out->tiles_x = tiles_x;
     out->tiles_y = tiles_y;
+    return GSR_OK;
+}
+
+// Which radix digits the last binning sorted (host side of the same rule the
+// kernels apply to the AND / OR of the keys).
+int bin_pass_masks(gsr_ctx *ctx, uint32_t *depth_mask, uint32_t *tile_mask, int *tile_digit_bits,
+                   int *tile_digits)
+{
+    *depth_mask = *tile_mask = 0;
+    *tile_digits = num_fields(32, ctx->last_key_hi);
+    *tile_digit_bits = *tile_digits ? (ctx->last_key_hi - 32 + *tile_digits - 1) / *tile_digits : 0;
+    if (!ctx->scalars || ctx->last_pairs == 0) return GSR_OK;
+    unsigned long long sc[kScalarCount];
+    int rc = cuda_check(ctx, cudaMemcpy(sc, ctx->scalars, sizeof sc, cudaMemcpyDeviceToHost), "cudaMemcpy");
+    if (rc) return rc;
+    for (int f = 0; f < 4; ++f) {
+        int sh, w;
+        field_geom(0, 32, 4, f, sh, w);
+        if (field_varies(sc[kScalarDepthAnd] ^ sc[kScalarDepthOr], sh, w)) *depth_mask |= 1u << f;
+    }
+    for (int f = 0; f < *tile_digits; ++f) {
+        int sh, w;
+        field_geom(32, ctx->last_key_hi, *tile_digits, f, sh, w);
+        if (field_varies(sc[kScalarKeyAnd] ^ sc[kScalarKeyOr], sh, w)) *tile_mask |= 1u << f;
+    }
     return GSR_OK;
 }
 

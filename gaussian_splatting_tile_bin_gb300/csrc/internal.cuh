@@ -18,16 +18,8 @@ constexpr int kRadixItems = 8;            // keys per thread per radix tile
 constexpr int kRadixTile = kRadixThreads * kRadixItems;
 constexpr int kMaxDigits = 8;             // 8-bit digits of a 64-bit key
 
-// Which of the three key/value buffers each executed radix pass reads and
-// writes.  Buffer 0 holds the unsorted input, buffer 1 the sorted result,
-// buffer 2 is scratch.  Written on the device once the keys are known.
-struct RadixPlan {
-    int num_exec;
-    int exec[kMaxDigits];
-    int src[kMaxDigits];
-    int dst[kMaxDigits];
-};
-
+// The three key/value buffers of a radix sort: buffer 0 holds the unsorted
+// input, buffer 1 the sorted result, buffer 2 is ping-pong scratch.
 template <typename K>
 struct SortBuffers {
     K *k[3];
@@ -57,12 +49,12 @@ struct gsr_ctx {
     unsigned long long *blk_offs = nullptr;
     size_t cap_tiles = 0;
     uint32_t *ranges = nullptr;                 // [2 * cap_tiles]
-    size_t cap_radix_tiles = 0;
-    uint32_t *radix_counts = nullptr;           // [256 * cap_radix_tiles]
-    uint32_t *radix_totals = nullptr;           // [kMaxDigits * 256]
+    size_t cap_status = 0;
+    unsigned long long *radix_status = nullptr; // [cap_status] look-back status words
+    uint32_t *radix_hist = nullptr;             // [8 * 256 + 8]: digit totals, tile counters
+    unsigned long long *radix_err = nullptr;    // [1] look-back waits that gave up
     unsigned long long *scalars = nullptr;      // see bin.cu (kScalar*)
-    gsr::RadixPlan *plan = nullptr;             // [2]: depth sort, tile sort
-    unsigned long long *host_total = nullptr;   // pinned
+    unsigned long long *host_total = nullptr;   // pinned: [0] pairs, [1] emitting, [2] look-back errors
     size_t cap_grad_acc = 0;
     double *grad_acc = nullptr;                 // [9 * cap] backward accumulator
 
@@ -71,6 +63,7 @@ struct gsr_ctx {
     uint32_t last_pairs = 0;
     int last_key_digits = 0;
     uint32_t last_emitting = 0;                 // splats with at least one pair
+    int last_key_hi = 32;                       // keys occupied bits [0, last_key_hi)
 };
 
 namespace gsr {
@@ -82,6 +75,8 @@ int fail(gsr_ctx *ctx, int code, const std::string &msg);
 // Host sides of the three operations (validated arguments).
 int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n, int32_t width,
                int32_t height, cudaStream_t stream, gsr_bins *out);
+int bin_pass_masks(gsr_ctx *ctx, uint32_t *depth_mask, uint32_t *tile_mask, int *tile_digit_bits,
+                   int *tile_digits);
 int rasterize_forward(gsr_ctx *ctx, const float *splats, const gsr_bins *bins, float *out_rgbw,
                       float *final_T, uint32_t *last_contrib, cudaStream_t stream);
 int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_bins *bins,

@@ -98,12 +98,18 @@ def check_backward(g, o, max_knife_frac=5e-3):
             "components_beyond_1e-4_within_cond_bound": cond_used}
 
 
-def varying_digit_mask(keys, digits):
-    """Bit d set when 8-bit digit d is not the same in every key (from the oracle's keys)."""
-    if len(keys) == 0:
+def varying_digit_mask(keys, lo, hi, ndigits):
+    """Bit f set when digit f of the key bits [lo, hi), split into ndigits equal
+    digits, is not the same in every key (computed from the oracle's keys)."""
+    if len(keys) == 0 or ndigits == 0:
         return 0
     k = keys.astype(np.uint64)
-    andv = np.bitwise_and.reduce(k)
-    orv = np.bitwise_or.reduce(k)
-    diff = int(andv ^ orv)
-    return sum(1 << d for d in range(digits) if (diff >> (8 * d)) & 0xFF)
+    diff = int(np.bitwise_and.reduce(k) ^ np.bitwise_or.reduce(k))
+    w = (hi - lo + ndigits - 1) // ndigits
+    mask = 0
+    for f in range(ndigits):
+        sh = lo + f * w
+        width = min(w, hi - sh)
+        if (diff >> sh) & ((1 << width) - 1):
+            mask |= 1 << f
+    return mask

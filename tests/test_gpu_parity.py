@@ -123,17 +123,30 @@ def test_all_culled_and_empty(gsr, ctx):
 
 
 def test_radix_pass_skip(gsr, ctx):
-    """Constant 8-bit digits are skipped; the stats report which ran
-    ("C0 resident arena + C1 pass skip", section 2, C1)."""
+    """Digits every key shares are skipped ("C0 resident arena + C1 pass skip",
+    section 2, C1); the stats report which ran."""
     wl = gen.lego_final()
     g = run_gpu(gsr, ctx, wl, backward=False)
     st = ctx.bin_stats()
     o = run_oracle(wl, backward=False)
-    assert st["key_digits"] == 6                      # 32 + 12 tile bits for 2500 tiles
-    assert st["digit_mask"] == varying_digit_mask(o["keys"], 6)
-    assert not (st["digit_mask"] >> 3) & 1            # depths in [2,6) share their top byte
-    assert st["radix_passes"] == bin(st["digit_mask"]).count("1")
     check_bins(g, o)
+    # 2500 tiles: 12 tile bits, sorted as two 6-bit digits.
+    assert (st["tile_digits"], st["tile_digit_bits"]) == (2, 6)
+    assert st["depth_pass_mask"] == varying_digit_mask(o["keys"], 0, 32, 4)
+    assert st["tile_pass_mask"] == varying_digit_mask(o["keys"], 32, 44, 2)
+    assert not (st["depth_pass_mask"] >> 3) & 1      # depths in [2,6) share their top byte
+    assert st["radix_passes"] == bin(st["depth_pass_mask"]).count("1") + bin(st["tile_pass_mask"]).count("1")
+    assert st["lookback_timeouts"] == 0
+    assert st["emitting"] == len(np.unique(o["idx"]))
+
+
+def test_stress_tile_digits(gsr, ctx):
+    wl = gen.stress()
+    run_gpu(gsr, ctx, wl, backward=False)
+    st = ctx.bin_stats()
+    # 120 x 68 = 8160 tiles: 13 tile bits as a 7-bit and a 6-bit digit.
+    assert (st["tile_digits"], st["tile_digit_bits"]) == (2, 7)
+    assert st["lookback_timeouts"] == 0
 
 
 def test_no_pass_needed(gsr, ctx):
