@@ -36,8 +36,7 @@ class _BinStats(ctypes.Structure):
     _fields_ = [("num_pairs", ctypes.c_uint32), ("emitting", ctypes.c_uint32),
                 ("radix_passes", ctypes.c_int32), ("depth_pass_mask", ctypes.c_uint32),
                 ("tile_pass_mask", ctypes.c_uint32), ("tile_digit_bits", ctypes.c_int32),
-                ("tile_digits", ctypes.c_int32), ("lookback_timeouts", ctypes.c_uint32),
-                ("capacity", ctypes.c_uint64)]
+                ("tile_digits", ctypes.c_int32), ("capacity", ctypes.c_uint64)]
 
 
 def _load():

@@ -98,9 +98,8 @@ void gsr_destroy(gsr_ctx *ctx)
         }
         cudaFree(ctx->blk_sums);
         cudaFree(ctx->ranges);
-        cudaFree(ctx->radix_status);
-        cudaFree(ctx->radix_hist);
-        cudaFree(ctx->radix_err);
+        cudaFree(ctx->radix_counts);
+        cudaFree(ctx->radix_totals);
         cudaFree(ctx->scalars);
         cudaFree(ctx->grad_acc);
         if (ctx->host_total) cudaFreeHost(ctx->host_total);
@@ -227,12 +226,6 @@ int gsr_get_bin_stats(gsr_ctx *ctx, gsr_bin_stats *out)
     out->tile_digit_bits = tile_bits;
     out->tile_digits = tile_digits;
     out->radix_passes = __builtin_popcount(out->depth_pass_mask) + __builtin_popcount(out->tile_pass_mask);
-    if (ctx->radix_err) {
-        unsigned long long e = 0;
-        rc = cuda_check(ctx, cudaMemcpy(&e, ctx->radix_err, sizeof e, cudaMemcpyDeviceToHost), "cudaMemcpy");
-        if (rc) return rc;
-        out->lookback_timeouts = (uint32_t)e;
-    }
     return GSR_OK;
 }
 

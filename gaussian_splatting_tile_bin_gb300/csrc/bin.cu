@@ -15,7 +15,9 @@
 //   2. the pairs are emitted in that depth order (a splat's own pairs in
 //      row-major tile order), so they are already ordered by (depth, index)
 //      within every tile, and a stable LSD sort on the tile digits alone
-//      finishes the job.
+//      finishes the job.  The tile field is split into digits of equal width
+//      (two 6-bit digits for 2500 tiles), which keeps the buckets few and the
+//      scattered runs long.
 // In both sorts a digit that every key shares is found on the device from the
 // AND and the OR of all keys, and its pass is skipped.
 //
@@ -135,6 +137,18 @@ __device__ __forceinline__ void block_and_or_into(unsigned long long a, unsigned
     }
 }
 
+// Lanes in `members` whose `width`-bit digit equals this lane's, from one
+// ballot per bit.  Every lane of the warp calls this together.
+__device__ __forceinline__ uint32_t digit_peers(uint32_t members, uint32_t digit, int width)
+{
+    uint32_t peers = members;
+    for (int b = 0; b < width; ++b) {
+        const uint32_t bal = __ballot_sync(kFull, (digit >> b) & 1u);
+        peers &= ((digit >> b) & 1u) ? bal : ~bal;
+    }
+    return peers;
+}
+
 // Radix digits: the key bits [key_lo, key_hi) split into num_fields digits of
 // equal width, at most 8 bits each.
 __host__ __device__ __forceinline__ int num_fields(int key_lo, int key_hi)
@@ -157,7 +171,10 @@ __host__ __device__ __forceinline__ bool field_varies(unsigned long long and_or_
     return width > 0 && ((and_or_diff >> shift) & ((1ull << width) - 1ull)) != 0ull;
 }
 
-// Position of field among the executed passes (-1 if skipped) and their number.
+// Position of `field` among the executed passes (-1 if skipped); *executed
+// receives their number.  The executed passes chain buffer 0 -> ... -> 1:
+// pass j of k writes buffer 1 when k - 1 - j is even, buffer 2 otherwise, and
+// reads what pass j - 1 wrote (buffer 0 for the first).
 __host__ __device__ __forceinline__ int field_pass(unsigned long long diff, int key_lo, int key_hi, int field,
                                                   int *executed)
 {
@@ -272,32 +289,22 @@ k_count_totals(const unsigned long long *__restrict__ blk_pairs, unsigned long l
     }
 }
 
-// Writes (depth bits, splat index) of every emitting splat, in splat order,
-// and adds their four 8-bit depth digits to the depth sort's digit totals.
+// Writes (depth bits, splat index) of every emitting splat, in splat order.
 __global__ void __launch_bounds__(kBinBlock)
 k_compact(const uint32_t *__restrict__ counts, const float *__restrict__ depths, int n,
           const unsigned long long *__restrict__ blk_emit_offs, uint32_t *__restrict__ dkeys,
-          uint32_t *__restrict__ didx, uint32_t *__restrict__ hist)
+          uint32_t *__restrict__ didx)
 {
     __shared__ uint32_t ws[8];
-    __shared__ uint32_t h[4][256];
-    for (int k = threadIdx.x; k < 4 * 256; k += kBinBlock) (&h[0][0])[k] = 0;
     const int i = blockIdx.x * kBinBlock + threadIdx.x;
     const bool emits = i < n && counts[i] > 0;
     uint32_t total;
     const uint32_t excl = block_exclusive_scan_256<uint32_t>(emits ? 1u : 0u, ws, &total);
     if (emits) {
         const size_t pos = (size_t)blk_emit_offs[blockIdx.x] + excl;
-        const uint32_t db = __float_as_uint(__ldg(depths + i));
-        dkeys[pos] = db;
+        dkeys[pos] = __float_as_uint(__ldg(depths + i));
         didx[pos] = (uint32_t)i;
-#pragma unroll
-        for (int f = 0; f < 4; ++f) atomicAdd(&h[f][(db >> (8 * f)) & 0xffu], 1u);
     }
-    __syncthreads();
-#pragma unroll
-    for (int f = 0; f < 4; ++f)
-        if (h[f][threadIdx.x]) atomicAdd(&hist[f * 256 + threadIdx.x], h[f][threadIdx.x]);
 }
 
 // Per block of 256 depth-sorted splats: their pair total.
@@ -324,10 +331,8 @@ __global__ void __launch_bounds__(kBinBlock)
 k_emit(const float *__restrict__ splats, const float *__restrict__ depths,
        const uint32_t *__restrict__ sorted_idx, int m, int tiles_x, int tiles_y,
        const unsigned long long *__restrict__ blk_offs, uint64_t *__restrict__ keys,
-       uint32_t *__restrict__ vals, unsigned long long *__restrict__ scalars, int key_hi,
-       uint32_t *__restrict__ hist)
+       uint32_t *__restrict__ vals, unsigned long long *__restrict__ scalars)
 {
-    __shared__ uint32_t h[4][256];
     __shared__ uint32_t s_off[kBinBlock];
     __shared__ int4 s_rect[kBinBlock];
     __shared__ uint32_t s_db[kBinBlock];
@@ -335,8 +340,6 @@ k_emit(const float *__restrict__ splats, const float *__restrict__ depths,
     __shared__ uint32_t ws[8];
     __shared__ unsigned long long s_and[8], s_or[8];
 
-    for (int q = threadIdx.x; q < 4 * 256; q += kBinBlock) (&h[0][0])[q] = 0;
-    const int nf = num_fields(32, key_hi);
     const int k = blockIdx.x * kBinBlock + threadIdx.x;
     uint32_t c = 0;
     int4 r = make_int4(0, 0, -1, -1);
@@ -376,50 +379,26 @@ k_emit(const float *__restrict__ splats, const float *__restrict__ depths,
         vals[base + q] = s_idx[lo];
         acc_and &= key;
         acc_or |= key;
-        for (int f = 0; f < nf; ++f) {
-            int sh, w;
-            field_geom(32, key_hi, nf, f, sh, w);
-            atomicAdd(&h[f][(uint32_t)(key >> sh) & ((1u << w) - 1u)], 1u);
-        }
     }
     block_and_or_into(acc_and, acc_or, s_and, s_or, scalars + kScalarKeyAnd);
-    for (int f = 0; f < nf; ++f)
-        if (h[f][threadIdx.x]) atomicAdd(&hist[f * 256 + threadIdx.x], h[f][threadIdx.x]);
 }
 
 // --- radix sort --------------------------------------------------------------
 //
-// A stable LSD sort over the key bits [key_lo, key_hi), split into nfields
-// digits of equal width (at most 8 bits).  Each digit takes one kernel launch
-// (single-pass, decoupled look-back): a CTA claims the next 2048-key tile in
-// launch order, ranks its keys stably by digit, publishes its per-digit counts,
-// then adds up the counts of the tiles before it (walking back until a tile has
-// published its inclusive prefix) and scatters through shared memory so each
-// digit's keys leave in contiguous runs.  The digit totals come from the kernel
-// that produced the keys.  A digit every key shares is skipped; the executed
-// passes chain buffer 0 -> ... -> buffer 1.
+// A stable LSD sort over the key bits [key_lo, key_hi), one pass per varying
+// digit, each pass three kernels with no waits between CTAs:
+//   upsweep  : per 2048-key radix tile, the count of each digit value, written
+//              digit-major, counts[digit][tile], and added to totals[digit];
+//   scan     : one CTA per digit value: the digit's global start (the totals of
+//              all smaller digits) plus the exclusive scan of its row, written
+//              to offsets[digit][tile];
+//   downsweep: each tile ranks its keys stably by digit (ballot-built peer
+//              masks, per-warp counters), stages them in shared memory in digit
+//              order and writes every digit's keys as one contiguous run.
 
-constexpr int kOsThreads = 256;
-constexpr int kOsItems = 8;
-constexpr int kOsTile = kOsThreads * kOsItems;
-constexpr unsigned long long kStatusAggregate = 1ull << 62;
-constexpr unsigned long long kStatusInclusive = 2ull << 62;
-constexpr unsigned long long kStatusValue = (1ull << 62) - 1;
-// A look-back wait gives up after this many polls (far beyond any real wait)
-// and records the timeout instead of hanging the GPU.
-constexpr int kLookbackSpinLimit = 1 << 22;
-
-__device__ __forceinline__ unsigned long long load_relaxed(const unsigned long long *p)
-{
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void store_relaxed(unsigned long long *p, unsigned long long v)
-{
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
+constexpr int kRtThreads = 256;
+constexpr int kRtItems = 8;
+constexpr int kRtTile = kRtThreads * kRtItems;
 
 // Buffer b of the three (a select, so the kernel parameter block is not copied
 // to local memory for dynamic indexing).
@@ -434,59 +413,118 @@ __device__ __forceinline__ uint32_t *vals_of(const SortBuffers<K> &p, int b)
     return b == 0 ? p.v[0] : (b == 1 ? p.v[1] : p.v[2]);
 }
 
-template <typename K>
-__global__ void __launch_bounds__(kOsThreads)
-k_onesweep(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__restrict__ and_or, int key_lo,
-           int key_hi, int field, const uint32_t *__restrict__ hist, unsigned long long *__restrict__ status,
-           uint32_t *__restrict__ tile_counter, unsigned long long *__restrict__ err)
+struct PassGeom {
+    int shift, width, src, dst;
+};
+
+// Geometry of pass `field`, or false when the digit is constant (skipped).
+__device__ __forceinline__ bool pass_geom(const unsigned long long *and_or, int key_lo, int key_hi, int field,
+                                          PassGeom &g)
 {
-    const unsigned long long diff = and_or[0] ^ and_or[1];
     int executed;
-    const int j = field_pass(diff, key_lo, key_hi, field, &executed);
-    if (j < 0) return;
-    const int nf = num_fields(key_lo, key_hi);
-    int shift, width;
-    field_geom(key_lo, key_hi, nf, field, shift, width);
-    const int dst = ((executed - 1 - j) % 2 == 0) ? 1 : 2;
-    const int src = (j == 0) ? 0 : (((executed - j) % 2 == 0) ? 1 : 2);
+    const int j = field_pass(and_or[0] ^ and_or[1], key_lo, key_hi, field, &executed);
+    if (j < 0) return false;
+    field_geom(key_lo, key_hi, num_fields(key_lo, key_hi), field, g.shift, g.width);
+    g.dst = ((executed - 1 - j) % 2 == 0) ? 1 : 2;
+    g.src = (j == 0) ? 0 : (((executed - j) % 2 == 0) ? 1 : 2);
+    return true;
+}
+
+template <typename K>
+__global__ void __launch_bounds__(kRtThreads)
+k_radix_upsweep(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__restrict__ and_or, int key_lo,
+                int key_hi, int field, int ntiles, uint32_t *__restrict__ counts, uint32_t *__restrict__ totals)
+{
+    PassGeom g;
+    if (!pass_geom(and_or, key_lo, key_hi, field, g)) return;
+    const K *__restrict__ keys = keys_of(bufs, g.src);
+    const uint32_t dmask = (1u << g.width) - 1u;
+    __shared__ uint32_t h[256];
+    h[threadIdx.x] = 0;
+    __syncthreads();
+    const uint32_t base = blockIdx.x * kRtTile;
+#pragma unroll
+    for (int k = 0; k < kRtItems; ++k) {
+        const uint32_t i = base + k * kRtThreads + threadIdx.x;
+        if (i < num) atomicAdd(&h[(uint32_t)(keys[i] >> g.shift) & dmask], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x <= (int)dmask) {
+        const uint32_t c = h[threadIdx.x];
+        counts[(size_t)threadIdx.x * ntiles + blockIdx.x] = c;
+        if (c) atomicAdd(&totals[threadIdx.x], c);
+    }
+}
+
+__global__ void __launch_bounds__(kRtThreads)
+k_radix_scan(const unsigned long long *__restrict__ and_or, int key_lo, int key_hi, int field, int ntiles,
+             const uint32_t *__restrict__ counts, const uint32_t *__restrict__ totals,
+             uint32_t *__restrict__ offsets)
+{
+    PassGeom g;
+    if (!pass_geom(and_or, key_lo, key_hi, field, g)) return;
+    const uint32_t digit = blockIdx.x;
+    if (digit >= (1u << g.width)) return;
+    __shared__ uint32_t ws[8];
+    // Global start of this digit: the totals of all smaller digits.
+    uint32_t base;
+    block_exclusive_scan_256<uint32_t>(threadIdx.x < digit ? totals[threadIdx.x] : 0u, ws, &base);
+    const uint32_t *row = counts + (size_t)digit * ntiles;
+    uint32_t *orow = offsets + (size_t)digit * ntiles;
+    uint32_t carry = base;
+    for (int start = 0; start < ntiles; start += kRtThreads) {
+        const int i = start + threadIdx.x;
+        const uint32_t c = i < ntiles ? row[i] : 0u;
+        uint32_t sum;
+        const uint32_t e = block_exclusive_scan_256<uint32_t>(c, ws, &sum);
+        if (i < ntiles) orow[i] = carry + e;
+        carry += sum;
+    }
+}
+
+template <typename K>
+__global__ void __launch_bounds__(kRtThreads)
+k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__restrict__ and_or, int key_lo,
+                  int key_hi, int field, int ntiles, const uint32_t *__restrict__ offsets)
+{
+    PassGeom g;
+    if (!pass_geom(and_or, key_lo, key_hi, field, g)) return;
+    const K *__restrict__ kin = keys_of(bufs, g.src);
+    const uint32_t *__restrict__ vin = vals_of(bufs, g.src);
+    K *__restrict__ kout = keys_of(bufs, g.dst);
+    uint32_t *__restrict__ vout = vals_of(bufs, g.dst);
+    const int shift = g.shift, width = g.width;
     const uint32_t radix = 1u << width, dmask = radix - 1u;
-    const K *__restrict__ kin = keys_of(bufs, src);
-    const uint32_t *__restrict__ vin = vals_of(bufs, src);
-    K *__restrict__ kout = keys_of(bufs, dst);
-    uint32_t *__restrict__ vout = vals_of(bufs, dst);
 
     __shared__ uint32_t wcnt[8][256];   // per-warp digit counts, then per-warp prefixes
-    __shared__ uint32_t s_cnt[256];     // this tile's digit counts
-    __shared__ uint32_t s_lstart[256];  // local start of each digit's run in the staged tile
+    __shared__ uint32_t s_lstart[256];  // start of each digit's run in the staged tile
     __shared__ uint32_t s_goff[256];    // global start of each digit's run
     __shared__ uint32_t ws[8];
-    __shared__ K s_keys[kOsTile];
-    __shared__ uint32_t s_vals[kOsTile];
-    __shared__ uint32_t s_tile;
+    __shared__ K s_keys[kRtTile];
+    __shared__ uint32_t s_vals[kRtTile];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int k = tid; k < 8 * 256; k += kOsThreads) (&wcnt[0][0])[k] = 0;
-    if (tid == 0) s_tile = atomicAdd(tile_counter, 1u);
+    for (int k = tid; k < 8 * 256; k += kRtThreads) (&wcnt[0][0])[k] = 0;
+    s_goff[tid] = tid < (int)radix ? offsets[(size_t)tid * ntiles + blockIdx.x] : 0u;
     __syncthreads();
-    const uint32_t tile = s_tile;
-    const uint32_t tbase = tile * kOsTile;
-    const uint32_t tcount = min((uint32_t)kOsTile, num - tbase);
+    const uint32_t tbase = blockIdx.x * kRtTile;
+    const uint32_t tcount = min((uint32_t)kRtTile, num - tbase);
 
-    // Stable rank inside the tile: warp w owns keys [w*256, w*256+256) and
-    // walks them in 8 rounds of 32; equal digits are ranked by lane within a
-    // round (match.any) and by per-warp counters across rounds.
+    // Warp w owns keys [w*256, w*256+256) of the tile and walks them in 8 rounds
+    // of 32; equal digits are ranked by lane within a round and by per-warp
+    // counters across rounds.
     const uint32_t lanemask_lt = (1u << lane) - 1u;
-    const uint32_t wbase = warp * (32 * kOsItems);
-    K key[kOsItems];
-    uint32_t val[kOsItems], rank[kOsItems];
+    const uint32_t wbase = warp * (32 * kRtItems);
+    K key[kRtItems];
+    uint32_t val[kRtItems], rank[kRtItems];
 #pragma unroll
-    for (int k = 0; k < kOsItems; ++k) {
+    for (int k = 0; k < kRtItems; ++k) {
         const uint32_t i = wbase + k * 32 + lane;
         const bool valid = i < tcount;
         key[k] = valid ? kin[tbase + i] : (K)0;
         val[k] = valid ? vin[tbase + i] : 0u;
-        const uint32_t digit = valid ? ((uint32_t)(key[k] >> shift) & dmask) : 0x100u;
-        const uint32_t peers = __match_any_sync(kFull, digit);
+        const uint32_t digit = (uint32_t)(key[k] >> shift) & dmask;
+        const uint32_t peers = digit_peers(__ballot_sync(kFull, valid), digit, width);
         const uint32_t prior = valid ? wcnt[warp][digit] : 0u;
         __syncwarp();
         const uint32_t before = __popc(peers & lanemask_lt);
@@ -495,54 +533,18 @@ k_onesweep(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__restri
         rank[k] = prior + before;
     }
     __syncthreads();
-    {
-        uint32_t run = 0;
+    uint32_t tot = 0;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const uint32_t t = wcnt[w][tid];
-            wcnt[w][tid] = run;
-            run += t;
-        }
-        s_cnt[tid] = run;
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t t = wcnt[w][tid];
+        wcnt[w][tid] = tot;
+        tot += t;
     }
-    uint32_t total;
-    const uint32_t lstart = block_exclusive_scan_256<uint32_t>(s_cnt[tid], ws, &total);
-    s_lstart[tid] = lstart;
-    uint32_t htotal;
-    const uint32_t gstart = block_exclusive_scan_256<uint32_t>(tid < (int)radix ? hist[tid] : 0u, ws, &htotal);
-
-    // Publish this tile's counts, add up the tiles before it, publish the prefix.
-    if (tid < (int)radix) {
-        const uint32_t c = s_cnt[tid];
-        unsigned long long *mine = status + (size_t)tile * 256 + tid;
-        unsigned long long prefix = 0;
-        if (tile == 0) {
-            store_relaxed(mine, kStatusInclusive | c);
-        } else {
-            store_relaxed(mine, kStatusAggregate | c);
-            for (int t = (int)tile - 1; t >= 0; --t) {
-                const unsigned long long *p = status + (size_t)t * 256 + tid;
-                unsigned long long v = load_relaxed(p);
-                int spins = 0;
-                while ((v >> 62) == 0ull) {
-                    if (++spins > kLookbackSpinLimit) {
-                        atomicAdd(err, 1ull);
-                        v = kStatusInclusive;
-                        break;
-                    }
-                    __nanosleep(32);
-                    v = load_relaxed(p);
-                }
-                prefix += v & kStatusValue;
-                if ((v & ~kStatusValue) == kStatusInclusive) break;
-            }
-            store_relaxed(mine, kStatusInclusive | (prefix + c));
-        }
-        s_goff[tid] = gstart + (uint32_t)prefix;
-    }
-    // Stage the tile in digit order, then write each digit's run contiguously.
+    uint32_t all;
+    s_lstart[tid] = block_exclusive_scan_256<uint32_t>(tot, ws, &all);
+    __syncthreads();
 #pragma unroll
-    for (int k = 0; k < kOsItems; ++k) {
+    for (int k = 0; k < kRtItems; ++k) {
         const uint32_t i = wbase + k * 32 + lane;
         if (i < tcount) {
             const uint32_t digit = (uint32_t)(key[k] >> shift) & dmask;
@@ -552,7 +554,7 @@ k_onesweep(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__restri
         }
     }
     __syncthreads();
-    for (uint32_t i = tid; i < tcount; i += kOsThreads) {
+    for (uint32_t i = tid; i < tcount; i += kRtThreads) {
         const K kk = s_keys[i];
         const uint32_t digit = (uint32_t)(kk >> shift) & dmask;
         const uint32_t gpos = s_goff[digit] + (i - s_lstart[digit]);
@@ -598,11 +600,17 @@ int bits_for(uint64_t v)
     return b;
 }
 
+// Growing the arena frees buffers that queued work (of this or an earlier call)
+// may still use: wait for the device first.  Growth is rare (grow-only arena).
+int drain_before_free(gsr_ctx *ctx) { return cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize"); }
+
 template <typename T>
 int grow(gsr_ctx *ctx, T **ptr, size_t *cap, size_t need, size_t elems_per, const char *what)
 {
     if (need <= *cap && *ptr) return GSR_OK;
     if (*ptr) {
+        int rc = drain_before_free(ctx);
+        if (rc) return rc;
         cudaFree(*ptr);
         *ptr = nullptr;
     }
@@ -621,6 +629,10 @@ template <typename K>
 int grow_sort_buffers(gsr_ctx *ctx, SortBuffers<K> &b, size_t *cap, size_t need, const char *what)
 {
     if (need <= *cap && b.k[0]) return GSR_OK;
+    if (b.k[0]) {
+        int rc = drain_before_free(ctx);
+        if (rc) return rc;
+    }
     for (int j = 0; j < 3; ++j) {
         if (b.k[j]) cudaFree(b.k[j]);
         if (b.v[j]) cudaFree(b.v[j]);
@@ -648,18 +660,27 @@ int grow_sort_buffers(gsr_ctx *ctx, SortBuffers<K> &b, size_t *cap, size_t need,
     } while (0)
 
 // Stable LSD sort of bufs buffer 0 into buffer 1 over the key bits
-// [key_lo, key_hi); and_or, hist, status, counter: the sort's device scratch.
+// [key_lo, key_hi); and_or: the device AND / OR of the keys.
 template <typename K>
 int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int key_hi,
-               const unsigned long long *and_or, const uint32_t *hist, unsigned long long *status,
-               uint32_t *counters, cudaStream_t stream)
+               const unsigned long long *and_or, uint32_t *totals, cudaStream_t stream)
 {
-    const int ntiles = (int)((num + kOsTile - 1) / kOsTile);
+    const int ntiles = (int)((num + kRtTile - 1) / kRtTile);
+    // [256][ntiles] counts, then [256][ntiles] offsets (sized by bin_splats).
+    uint32_t *counts = ctx->radix_counts;
+    uint32_t *offsets = ctx->radix_counts + (size_t)256 * ntiles;
     const int nf = num_fields(key_lo, key_hi);
     for (int f = 0; f < nf; ++f) {
-        k_onesweep<K><<<ntiles, kOsThreads, 0, stream>>>(bufs, num, and_or, key_lo, key_hi, f, hist + 256 * f,
-                                                         status + (size_t)f * ntiles * 256, counters + f,
-                                                         ctx->radix_err);
+        int sh, w;
+        field_geom(key_lo, key_hi, nf, f, sh, w);
+        uint32_t *tot = totals + 256 * f;
+        k_radix_upsweep<K><<<ntiles, kRtThreads, 0, stream>>>(bufs, num, and_or, key_lo, key_hi, f, ntiles,
+                                                              counts, tot);
+        GSR_LAUNCHED(ctx);
+        k_radix_scan<<<1 << w, kRtThreads, 0, stream>>>(and_or, key_lo, key_hi, f, ntiles, counts, tot, offsets);
+        GSR_LAUNCHED(ctx);
+        k_radix_downsweep<K><<<ntiles, kRtThreads, 0, stream>>>(bufs, num, and_or, key_lo, key_hi, f, ntiles,
+                                                                offsets);
         GSR_LAUNCHED(ctx);
     }
     k_copy_if_unsorted<K><<<std::min(ntiles, 1024), 256, 0, stream>>>(bufs, num, and_or, key_lo, key_hi);
@@ -677,26 +698,18 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     const int tiles_y = (height + kTile - 1) / kTile;
     const size_t num_tiles = (size_t)tiles_x * tiles_y;
     const int key_hi = 32 + bits_for(num_tiles - 1);  // keys occupy bits [0, key_hi)
-    const int digits = (key_hi + 7) / 8;
 
     // Fixed-size scratch, allocated once.
     if (!ctx->scalars) {
         if ((rc = cuda_check(ctx, cudaMalloc(&ctx->scalars, kScalarCount * sizeof(unsigned long long)),
                              "cudaMalloc")))
             return rc;
-        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->radix_hist, (8 * 256 + 8) * sizeof(uint32_t)),
-                             "cudaMalloc")))
-            return rc;
-        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->radix_err, sizeof(unsigned long long)), "cudaMalloc")))
-            return rc;
-        if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->radix_err, 0, sizeof(unsigned long long), stream),
-                             "cudaMemsetAsync")))
-            return rc;
-        if ((rc = cuda_check(ctx, cudaHostAlloc(&ctx->host_total, 4 * sizeof(unsigned long long),
+        if ((rc = cuda_check(ctx, cudaHostAlloc(&ctx->host_total, 2 * sizeof(unsigned long long),
                                                 cudaHostAllocDefault),
                              "cudaHostAlloc")))
             return rc;
-        ctx->host_total[2] = 0;
+        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->radix_totals, 2 * 4 * 256 * sizeof(uint32_t)), "cudaMalloc")))
+            return rc;
     }
     const int nblk = (n + kBinBlock - 1) / kBinBlock;
     if (!ctx->depth.k[0] || (size_t)n > ctx->cap_splats) {
@@ -732,15 +745,6 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         total = ctx->host_total[0];
         emitting = ctx->host_total[1];
     }
-    // A look-back wait of an earlier call on this context that gave up (its
-    // copy has landed: the stream was synchronised above or by the caller).
-    if (ctx->host_total[2] != 0) {
-        ctx->host_total[2] = 0;
-        cudaMemsetAsync(ctx->radix_err, 0, sizeof(unsigned long long), stream);
-        return fail(ctx, GSR_ERR_CUDA,
-                    "a radix look-back wait timed out in an earlier gsr_bin_splats on this context; "
-                    "its bins were invalid");
-    }
     if (total > (uint64_t)GSR_MAX_PAIRS)
         return fail(ctx, GSR_ERR_TOO_MANY_PAIRS,
                     "tile-pair count " + std::to_string(total) + " exceeds GSR_MAX_PAIRS");
@@ -760,39 +764,31 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         }
         ctx->cap_pairs = cap;
     }
-    // Look-back status words: 256 per 2048-key tile and digit, for the depth
-    // sort's 4 digits and the tile sort's digits.
-    const int dtiles = (m + kOsTile - 1) / kOsTile;
-    const int ptiles = (int)((num + kOsTile - 1) / kOsTile);
-    const int tile_fields = num_fields(32, key_hi);
-    const size_t status_need = (size_t)256 * (4 * (size_t)dtiles + (size_t)tile_fields * ptiles);
-    if ((rc = grow(ctx, &ctx->radix_status, &ctx->cap_status, std::max<size_t>(status_need, 1), 1,
-                   "radix status")))
-        return rc;
+
+    // Radix counts and offsets for the larger of the two sorts, allocated before
+    // any kernel that uses them is queued.
+    {
+        const size_t rtiles = std::max<size_t>((m + kRtTile - 1) / kRtTile, (num + kRtTile - 1) / kRtTile);
+        if ((rc = grow(ctx, &ctx->radix_counts, &ctx->cap_radix_tiles, std::max<size_t>(rtiles, 1), 512,
+                       "radix counts")))
+            return rc;
+    }
 
     if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->ranges, 0, num_tiles * 2 * sizeof(uint32_t), stream),
                          "cudaMemsetAsync")))
         return rc;
 
     if (num > 0) {
-        if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->radix_hist, 0, (8 * 256 + 8) * sizeof(uint32_t), stream),
+        // Digit totals: 4 digits x 256 values for each of the two sorts.
+        if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->radix_totals, 0, 2 * 4 * 256 * sizeof(uint32_t), stream),
                              "cudaMemsetAsync")))
             return rc;
-        if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->radix_status, 0,
-                                                  status_need * sizeof(unsigned long long), stream),
-                             "cudaMemsetAsync")))
-            return rc;
-        uint32_t *hist_depth = ctx->radix_hist;
-        uint32_t *hist_tile = ctx->radix_hist + 4 * 256;
-        uint32_t *counters = ctx->radix_hist + 8 * 256;
-        unsigned long long *status_depth = ctx->radix_status;
-        unsigned long long *status_tile = ctx->radix_status + (size_t)256 * 4 * dtiles;
         // 3. depth sort of the emitting splats.
         k_compact<<<nblk, kBinBlock, 0, stream>>>(ctx->counts, depths, n, blk_emit, ctx->depth.k[0],
-                                                  ctx->depth.v[0], hist_depth);
+                                                  ctx->depth.v[0]);
         GSR_LAUNCHED(ctx);
         if ((rc = radix_sort<uint32_t>(ctx, ctx->depth, (uint32_t)m, 0, 32, ctx->scalars + kScalarDepthAnd,
-                                       hist_depth, status_depth, counters, stream)))
+                                       ctx->radix_totals, stream)))
             return rc;
         // 4. pair offsets in depth order, emission.
         const int mblk = (m + kBinBlock - 1) / kBinBlock;
@@ -801,35 +797,31 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         k_scan_u64<<<1, 1024, 0, stream>>>(blk_sorted, mblk);
         GSR_LAUNCHED(ctx);
         k_emit<<<mblk, kBinBlock, 0, stream>>>(splats, depths, ctx->depth.v[1], m, tiles_x, tiles_y, blk_sorted,
-                                               ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars, key_hi,
-                                               hist_tile);
+                                               ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars);
         GSR_LAUNCHED(ctx);
         // 5. stable sort on the tile digits only.
         if (key_hi > 32) {
             if ((rc = radix_sort<uint64_t>(ctx, ctx->pairs, num, 32, key_hi, ctx->scalars + kScalarKeyAnd,
-                                           hist_tile, status_tile, counters + 4, stream)))
+                                           ctx->radix_totals + 4 * 256, stream)))
                 return rc;
         } else {
             // One tile: the emitted order is already sorted.
             if ((rc = cuda_check(ctx, cudaMemcpyAsync(ctx->pairs.k[1], ctx->pairs.k[0], (size_t)num * 8,
-                                                      cudaMemcpyDeviceToDevice, stream), "cudaMemcpyAsync")) ||
+                                                      cudaMemcpyDeviceToDevice, stream),
+                                 "cudaMemcpyAsync")) ||
                 (rc = cuda_check(ctx, cudaMemcpyAsync(ctx->pairs.v[1], ctx->pairs.v[0], (size_t)num * 4,
-                                                      cudaMemcpyDeviceToDevice, stream), "cudaMemcpyAsync")))
+                                                      cudaMemcpyDeviceToDevice, stream),
+                                 "cudaMemcpyAsync")))
                 return rc;
         }
         // 6. per-tile ranges.
         k_extract_ranges<<<(num + 255) / 256, 256, 0, stream>>>(ctx->pairs.k[1], num, ctx->ranges);
         GSR_LAUNCHED(ctx);
-        // The look-back error word comes back with the next synchronisation.
-        if ((rc = cuda_check(ctx, cudaMemcpyAsync(ctx->host_total + 2, ctx->radix_err, sizeof(unsigned long long),
-                                                  cudaMemcpyDeviceToHost, stream), "cudaMemcpyAsync")))
-            return rc;
     }
 
     ctx->last_stream = stream;
     ctx->last_pairs = num;
     ctx->last_emitting = (uint32_t)m;
-    ctx->last_key_digits = digits;
     ctx->last_key_hi = key_hi;
     out->keys = ctx->pairs.k[1];
     out->sorted_idx = ctx->pairs.v[1];

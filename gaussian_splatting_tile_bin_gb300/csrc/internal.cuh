@@ -49,19 +49,17 @@ struct gsr_ctx {
     unsigned long long *blk_offs = nullptr;
     size_t cap_tiles = 0;
     uint32_t *ranges = nullptr;                 // [2 * cap_tiles]
-    size_t cap_status = 0;
-    unsigned long long *radix_status = nullptr; // [cap_status] look-back status words
-    uint32_t *radix_hist = nullptr;             // [8 * 256 + 8]: digit totals, tile counters
-    unsigned long long *radix_err = nullptr;    // [1] look-back waits that gave up
+    size_t cap_radix_tiles = 0;
+    uint32_t *radix_counts = nullptr;           // [512 * cap_radix_tiles] digit counts and offsets
+    uint32_t *radix_totals = nullptr;           // [2 * 4 * 256] digit totals of both sorts
     unsigned long long *scalars = nullptr;      // see bin.cu (kScalar*)
-    unsigned long long *host_total = nullptr;   // pinned: [0] pairs, [1] emitting, [2] look-back errors
+    unsigned long long *host_total = nullptr;   // pinned: [0] pairs, [1] emitting
     size_t cap_grad_acc = 0;
     double *grad_acc = nullptr;                 // [9 * cap] backward accumulator
 
     // Last binning, for gsr_get_bin_stats.
     cudaStream_t last_stream = nullptr;
     uint32_t last_pairs = 0;
-    int last_key_digits = 0;
     uint32_t last_emitting = 0;                 // splats with at least one pair
     int last_key_hi = 32;                       // keys occupied bits [0, last_key_hi)
 };

@@ -428,7 +428,12 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
 {
     const size_t count = (size_t)n * 9;
     if (count > ctx->cap_grad_acc || !ctx->grad_acc) {
-        if (ctx->grad_acc) cudaFree(ctx->grad_acc);
+        if (ctx->grad_acc) {
+            // Queued work may still accumulate into the old buffer.
+            int rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+            if (rc) return rc;
+            cudaFree(ctx->grad_acc);
+        }
         ctx->grad_acc = nullptr;
         ctx->cap_grad_acc = 0;
         if (cudaMalloc(&ctx->grad_acc, count * sizeof(double)) != cudaSuccess) {

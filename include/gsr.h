@@ -194,10 +194,7 @@ int gsr_rasterize_backward_noalloc(gsr_ctx *ctx, const gsr_splat2d *splats, int3
  * split into tile_digits digits of tile_digit_bits bits each.  A digit that
  * every key shares is skipped ("C0 resident arena + C1 pass skip", section 2,
  * C1).  depth_pass_mask / tile_pass_mask: bit f set when digit f was sorted;
- * radix_passes: their total.  lookback_timeouts: single-pass look-back waits
- * that gave up (always 0 on a working GPU; a nonzero count means that call's
- * bins were invalid, and the next gsr_bin_splats on the context reports it).
- * capacity: arena capacity in pairs. */
+ * radix_passes: their total.  capacity: arena capacity in pairs. */
 typedef struct gsr_bin_stats {
     uint32_t num_pairs;
     uint32_t emitting;          /* splats with at least one pair */
@@ -206,7 +203,6 @@ typedef struct gsr_bin_stats {
     uint32_t tile_pass_mask;
     int32_t tile_digit_bits;
     int32_t tile_digits;
-    uint32_t lookback_timeouts;
     uint64_t capacity;
 } gsr_bin_stats;
 int gsr_get_bin_stats(gsr_ctx *ctx, gsr_bin_stats *out);
