@@ -49,6 +49,34 @@ SFU_LANES_PER_SM = 16
 FWD_OPS = {"n_eval": 9, "n_exp": 4, "n_contrib": 7}
 BWD_OPS = {"n_eval": 9, "n_exp": 4, "n_contrib": 44}
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch on the
+# 800x800, 409,660-splat workload, from one ncu capture (profiles/k_*_lego_final.md),
+# with the SHA-256 of the kernel sources it was taken on.  Once the sources
+# change, the figure no longer describes the kernel and is reported as null.
+NCU_TRAFFIC = {
+    "forward": {"bytes": 22_263_552 + 9_984, "workload": "lego_final"},
+    "backward": {"bytes": 50_600_960 + 173_568, "workload": "lego_final"},
+}
+NCU_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/raster.cu",
+               "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
+NCU_SOURCES_SHA256 = "eef0ff7a81583ced4e3d1dd1aec6b1a997659c5517f17f7e74c109cb790c612d"
+
+
+def raster_sources_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in NCU_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(hashlib.sha256(f.read()).digest())
+    return h.hexdigest()
+
+
+def ncu_traffic(kind: str, workload: str):
+    entry = NCU_TRAFFIC.get(kind)
+    if entry is None or entry["workload"] != workload or raster_sources_digest() != NCU_SOURCES_SHA256:
+        return None
+    return entry["bytes"]
+
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
@@ -260,7 +288,7 @@ def roofline_for(kind, counters, pairs, wl, ms, peaks, sm_mhz):
         achieved, peak, unit = sfu / sec / 1e9, sfu_peak / 1e9, "Gop/s (sfu lane ops)"
     return {"kernel": kind, "bound": "alu" if bound in ("alu", "sfu") else "hbm",
             "pipe": bound, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": None,
+            "frac": achieved / peak, "traffic": ncu_traffic(kind, wl.name),
             "peak_source": f"{peaks['source']} HBM; FP32/SFU = {SM_COUNT} SMs x "
                            f"{FP32_LANES_PER_SM}/{SFU_LANES_PER_SM} lanes x {peaks['sm_max_mhz']:.0f} MHz",
             "algorithmic": {"fp32_ops": fp32, "sfu_ops": sfu, "bytes": bytes_},
