@@ -111,6 +111,13 @@ def reduce_max(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def job_ms_per_iter(local_ms_sum: float, steps: int, world: int, device=None) -> float:
+    """Whole-job ms per iteration: every rank runs `steps` iterations of its own
+    replica, so the job finishes world x steps iterations in the slowest rank's
+    time."""
+    return reduce_max(local_ms_sum, world, device) / (steps * world)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -400,15 +407,14 @@ def gpu_arm(args):
             e2e_ms.append(a.elapsed_time(b))
         h2d = (wl.splats.nbytes + wl.depths.nbytes + wl.dl_dout.nbytes)
         d2h = wl.n * 9 * 4 + npx * 16
-        e2e_val = reduce_max(float(np.sum(e2e_ms)), world, dev) / (args.steps * world)
+        e2e_val = job_ms_per_iter(float(np.sum(e2e_ms)), args.steps, world, dev)
         e2e = {"value": e2e_val, "unit": "ms/iter", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h)}
 
     rows = sampler.stop()
     clocks = ClockSampler.summarize(rows)
 
-    total = reduce_max(float(tot_ms.sum()), world, dev)
-    value = total / (args.steps * world)
+    value = job_ms_per_iter(float(tot_ms.sum()), args.steps, world, dev)
     peaks = measured_peaks()
 
     line = {"metric": METRIC, "value": value, "unit": "ms/iter", "n_gpus": world,
