@@ -7,11 +7,12 @@
 //
 // Warps own 8x4-pixel blocks of the tile.  When a splat is staged, the thread
 // that stages it also marks which of the 8 blocks the splat can reach at all:
-// the set {sigma < bound} is an ellipse, and its bounding box (grown by a
-// margin that covers float rounding) is tested against each block.  A warp
-// walks only the splats marked for it, found 32 at a time with a ballot.  A
-// skipped evaluation could only have been skipped by the per-pixel tests as
-// well, so the results are bit-identical with and without this culling.
+// the set {sigma < bound} is an ellipse, and its axis-aligned and oriented
+// bounding boxes (grown by a margin that covers float rounding) are tested
+// against each block.  A warp walks only the splats marked for it, found 32 at
+// a time with a ballot.  A skipped evaluation could only have been skipped by
+// the per-pixel tests as well, so the results are bit-identical with and
+// without this culling.
 //
 // Both kernels evaluate a splat at a pixel through the same inline functions
 // (splat_sigma, splat_alpha), so the backward takes exactly the forward's skip
@@ -23,10 +24,10 @@
 
 // Resident CTAs per SM the raster kernels are compiled for (register budget).
 #ifndef GSR_FWD_MIN_BLOCKS
-#define GSR_FWD_MIN_BLOCKS 1
+#define GSR_FWD_MIN_BLOCKS 5
 #endif
 #ifndef GSR_BWD_MIN_BLOCKS
-#define GSR_BWD_MIN_BLOCKS 1
+#define GSR_BWD_MIN_BLOCKS 4
 #endif
 // Splats staged per thread and batch: a batch holds 256 x this many splats.
 #ifndef GSR_STAGE_PER_THREAD
@@ -69,11 +70,19 @@ __device__ __forceinline__ int pixel_x(int tid) { return ((tid >> 5) & 1) * 8 + 
 __device__ __forceinline__ int pixel_y(int tid) { return (tid >> 6) * 4 + ((tid >> 3) & 3); }
 
 // Which 8x4 blocks of the tile at (x0, y0) the ellipse {sigma < bound} can reach.
-// Its half-extents are sqrt(2 bound Sigma_xx) and sqrt(2 bound Sigma_yy).  The
-// computed sigma may be off by a few roundings of its terms, at most
-// 8u (|a| + |c| + 2|b|) / lambda_min relative, so the box is grown by four
-// times that (plus 1e-3 relative and 1e-3 px); a conic too ill-conditioned
-// for that bound to be small is not culled at all.
+//
+// A block is kept when it overlaps the ellipse's slab along each of four
+// directions: the x and y axes (the ellipse's bounding box) and its two
+// principal axes (its oriented bounding box).  For any direction u, the
+// ellipse {1/2 d^T Q d < bound} spans |d . u| <= sqrt(2 bound u^T Q^-1 u), so a
+// slab test is valid for whatever direction the rounded eigenvector gives, and
+// u need not be normalised (both sides scale with |u|).
+//
+// The computed sigma may be off by a few roundings of its terms, at most
+// 8u (|a| + |c| + 2|b|) / lambda_min relative, and the slab widths carry errors
+// of the same order, so every half-width is grown by far more than that
+// (plus 1e-3 relative and 1e-3 px); a conic too ill-conditioned for that bound
+// to be small is not culled at all.
 template <bool kCull>
 __device__ __forceinline__ uint32_t block_mask(float mx, float my, float a, float b, float c,
                                                float bound, int x0, int y0)
@@ -82,19 +91,44 @@ __device__ __forceinline__ uint32_t block_mask(float mx, float my, float a, floa
     if (!(bound > 0.0f)) return 0u;
     const float det = a * c - b * b;
     const float half_tr = 0.5f * (a + c);
-    const float lam_min = half_tr - sqrtf(0.25f * (a - c) * (a - c) + b * b);
+    const float rad = sqrtf(0.25f * (a - c) * (a - c) + b * b);
+    const float lam_min = half_tr - rad;
     const float rel = 2e-6f * (fabsf(a) + fabsf(c) + 2.0f * fabsf(b)) / lam_min + 1e-3f;
     if (!(det > 0.0f) || !(lam_min > 0.0f) || !(rel < 0.25f)) return 0xffu;
     const float grow = 1.0f + rel;
-    const float rx = sqrtf(2.0f * bound * (c / det)) * grow + 1e-3f;
-    const float ry = sqrtf(2.0f * bound * (a / det)) * grow + 1e-3f;
+    const float two_b_det = 2.0f * bound / det;
+    const float rx = sqrtf(two_b_det * c) * grow + 1e-3f;
+    const float ry = sqrtf(two_b_det * a) * grow + 1e-3f;
+    // Principal direction of the largest eigenvalue (a root of the
+    // characteristic polynomial), from the better-conditioned of the two
+    // forms; v is u rotated by 90 degrees.
+    const float lam_max = half_tr + rad;
+    const float ux = a >= c ? lam_max - c : b;
+    const float uy = a >= c ? b : lam_max - a;
+    const float vx = -uy, vy = ux;
+    // Half-widths of the ellipse's slabs along u and v, plus the half-extent of
+    // an 8x4 block (pixel centres x0..x0+7, y0..y0+3) along each.
+    // A quadratic form that rounds below zero, or overflows, gives NaN or
+    // infinity here, and the slab tests below then keep the block.
+    const float su = sqrtf(two_b_det * (c * ux * ux - 2.0f * b * ux * uy + a * uy * uy));
+    const float sv = sqrtf(two_b_det * (c * vx * vx - 2.0f * b * vx * vy + a * vy * vy));
+    const float nu = fabsf(ux) + fabsf(uy), nv = fabsf(vx) + fabsf(vy);
+    const float lim_u = su * grow + 3.5f * fabsf(ux) + 1.5f * fabsf(uy) + 1e-3f * nu;
+    const float lim_v = sv * grow + 3.5f * fabsf(vx) + 1.5f * fabsf(vy) + 1e-3f * nv;
+    // Block centre minus mean, projected on u and v, for block 0; the other
+    // blocks are offset by (8, 0) and (0, 4) steps.
+    const float cx = (float)x0 + 3.5f - mx, cy = (float)y0 + 1.5f - my;
+    const float pu0 = cx * ux + cy * uy, pv0 = cx * vx + cy * vy;
     uint32_t m = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
         const float bx0 = (float)(x0 + (w & 1) * 8), by0 = (float)(y0 + (w >> 1) * 4);
-        const bool hit = (mx - rx <= bx0 + 7.0f) && (mx + rx >= bx0) && (my - ry <= by0 + 3.0f) &&
+        const float ox = (float)((w & 1) * 8), oy = (float)((w >> 1) * 4);
+        const bool box = (mx - rx <= bx0 + 7.0f) && (mx + rx >= bx0) && (my - ry <= by0 + 3.0f) &&
                          (my + ry >= by0);
-        m |= hit ? (1u << w) : 0u;
+        const bool slab_u = !(fabsf(pu0 + ox * ux + oy * uy) > lim_u);  // NaN keeps the block
+        const bool slab_v = !(fabsf(pv0 + ox * vx + oy * vy) > lim_v);
+        m |= (box && slab_u && slab_v) ? (1u << w) : 0u;
     }
     return m;
 }

@@ -206,3 +206,27 @@ def from_arrays(name, width, height, splats, depths, dl_dout=None, seed=0) -> Wo
         dl_dout = np.zeros((width * height, 4), dtype=np.float32)
         dl_dout[:, 0:3] = rng.standard_normal((width * height, 3))
     return Workload(name, width, height, sp, dp, np.ascontiguousarray(dl_dout, dtype=np.float32))
+
+
+def elongated_fixture(seed: int = 8, n: int = 3000, size: int = 512) -> Workload:
+    """Thin, rotated splats of every size, some centred off-image.
+
+    Long-axis std log-uniform in [2, 150] px, aspect ratio log-uniform in
+    [1, 400], any orientation, a third of the splats at color_a in (0, 0.01)
+    so their alpha >= 1/255 ellipse is much smaller than their 3-sigma box.
+    Exercises the culling of staged splats against pixel blocks.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    means = rng.uniform(-0.2 * size, 1.2 * size, size=(n, 2))
+    depths = rng.uniform(1.0, 8.0, size=n)
+    s_long = np.exp(rng.uniform(np.log(2.0), np.log(150.0), size=n))
+    aspect = np.exp(rng.uniform(0.0, np.log(400.0), size=n))
+    s_short = np.maximum(s_long / aspect, 0.05)
+    theta = rng.uniform(0.0, np.pi, size=n)
+    rgb = rng.uniform(0.0, 1.0, size=(n, 3))
+    opac = _sigmoid(rng.normal(0.5, 1.5, size=n))
+    low = rng.permutation(n)[: n // 3]
+    opac[low] = rng.uniform(0.0, 0.01, size=low.size)
+    return _assemble("elongated", rng, size, size, means, depths, s_long, s_short, theta, rgb, opac,
+                     {"seed": seed, "aspect": "logU(1,400)", "long_std": "logU(2,150)"})
+

@@ -58,6 +58,12 @@ def test_overlap_fixtures(gsr, ctx, size):
     _full(gsr, ctx, gen.overlap_fixture(size))
 
 
+def test_elongated_parity(gsr, ctx):
+    """Thin rotated splats of every size: the oriented culling of staged splats
+    against pixel blocks must not drop an evaluation the oracle makes."""
+    _full(gsr, ctx, gen.elongated_fixture())
+
+
 def _random(n, w, h, seed, levels=None, big=0):
     rng = np.random.Generator(np.random.PCG64(seed))
     s = np.zeros((n, 9), dtype=np.float32)
@@ -204,13 +210,13 @@ def test_backward_variants_agree(gsr, ctx):
     ctx.set_option("bwd_last_contrib", 1)
 
 
-@pytest.mark.parametrize("name", ["lego_early", "stress"])
+@pytest.mark.parametrize("name", ["lego_early", "stress", "elongated"])
 def test_warp_culling_changes_nothing(gsr, ctx, name):
     """Warps skip splats whose alpha >= 1/255 ellipse misses their pixel block;
     the per-pixel tests would have skipped every one of those evaluations, so
     the forward must be bit-identical with culling off, and the backward
     identical up to the order of its double-precision sums."""
-    wl = gen.make(name)
+    wl = gen.elongated_fixture() if name == "elongated" else gen.make(name)
     on = run_gpu(gsr, ctx, wl)
     ctx.set_option("warp_cull", 0)
     try:
