@@ -117,6 +117,7 @@ int gsr_set_option(gsr_ctx *ctx, int option, int value)
     case GSR_OPT_BWD_WARP_SKIP: ctx->opt_warp_skip = value; return GSR_OK;
     case GSR_OPT_BWD_LAST_CONTRIB: ctx->opt_last_contrib = value; return GSR_OK;
     case GSR_OPT_WARP_CULL: ctx->opt_warp_cull = value; return GSR_OK;
+    case GSR_OPT_PDL: ctx->opt_pdl = value; return GSR_OK;
     default: return fail(ctx, GSR_ERR_INVALID_ARG, "unknown option " + std::to_string(option));
     }
 }

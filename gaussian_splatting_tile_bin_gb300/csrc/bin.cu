@@ -194,6 +194,7 @@ __host__ __device__ __forceinline__ int field_pass(unsigned long long diff, int 
 
 __global__ void k_init_scalars(unsigned long long *__restrict__ scalars)
 {
+    grid_dependency_begin();
     if (threadIdx.x != 0) return;
     for (int k = 0; k < kScalarCount; ++k) scalars[k] = 0ull;
     scalars[kScalarDepthAnd] = ~0ull;
@@ -209,6 +210,7 @@ k_count(const float *__restrict__ splats, const float *__restrict__ depths, int 
         int tiles_y, uint32_t *__restrict__ counts, unsigned long long *__restrict__ blk_pairs,
         unsigned long long *__restrict__ blk_emitting, unsigned long long *__restrict__ scalars)
 {
+    grid_dependency_begin();
     __shared__ unsigned long long s_and[8], s_or[8];
     __shared__ unsigned long long ws[8];
     const int i = blockIdx.x * kBinBlock + threadIdx.x;
@@ -262,6 +264,7 @@ __device__ unsigned long long block_scan_inplace_1024(unsigned long long *__rest
 __global__ void __launch_bounds__(1024)
 k_scan_u64(unsigned long long *__restrict__ vals, int num)
 {
+    grid_dependency_begin();
     __shared__ unsigned long long ws[32];
     block_scan_inplace_1024(vals, num, ws);
 }
@@ -272,6 +275,7 @@ __global__ void __launch_bounds__(1024)
 k_count_totals(const unsigned long long *__restrict__ blk_pairs, unsigned long long *__restrict__ blk_emitting,
                int nblk, unsigned long long *__restrict__ scalars)
 {
+    grid_dependency_begin();
     __shared__ unsigned long long ws[32];
     unsigned long long s = 0;
     for (int i = threadIdx.x; i < nblk; i += 1024) s += blk_pairs[i];
@@ -295,6 +299,7 @@ k_compact(const uint32_t *__restrict__ counts, const float *__restrict__ depths,
           const unsigned long long *__restrict__ blk_emit_offs, uint32_t *__restrict__ dkeys,
           uint32_t *__restrict__ didx)
 {
+    grid_dependency_begin();
     __shared__ uint32_t ws[8];
     const int i = blockIdx.x * kBinBlock + threadIdx.x;
     const bool emits = i < n && counts[i] > 0;
@@ -312,6 +317,7 @@ __global__ void __launch_bounds__(kBinBlock)
 k_sorted_sums(const uint32_t *__restrict__ sorted_idx, const uint32_t *__restrict__ counts, int m,
               unsigned long long *__restrict__ blk_sorted)
 {
+    grid_dependency_begin();
     __shared__ unsigned long long ws[8];
     const int k = blockIdx.x * kBinBlock + threadIdx.x;
     const uint32_t c = k < m ? counts[sorted_idx[k]] : 0u;
@@ -333,6 +339,7 @@ k_emit(const float *__restrict__ splats, const float *__restrict__ depths,
        const unsigned long long *__restrict__ blk_offs, uint64_t *__restrict__ keys,
        uint32_t *__restrict__ vals, unsigned long long *__restrict__ scalars)
 {
+    grid_dependency_begin();
     __shared__ uint32_t s_off[kBinBlock];
     __shared__ int4 s_rect[kBinBlock];
     __shared__ uint32_t s_db[kBinBlock];
@@ -417,26 +424,49 @@ struct PassGeom {
     int shift, width, src, dst;
 };
 
-// Geometry of pass `field`, or false when the digit is constant (skipped).
-__device__ __forceinline__ bool pass_geom(const unsigned long long *and_or, int key_lo, int key_hi, int field,
-                                          PassGeom &g)
+// Which digit a pass sorts on and how it learns whether the digit varies: from
+// the device AND / OR of the keys (and_or set; a constant digit's pass returns
+// at once), or from the plan the host made (and_or null; only passes over
+// varying digits are launched).
+struct PassSpec {
+    const unsigned long long *and_or;
+    int key_lo, key_hi, field;
+    PassGeom host;
+};
+
+// Geometry of pass `field` of `executed` varying digits, whose position among
+// them is j.
+__host__ __device__ __forceinline__ PassGeom plan_geom(int key_lo, int key_hi, int field, int j, int executed)
 {
-    int executed;
-    const int j = field_pass(and_or[0] ^ and_or[1], key_lo, key_hi, field, &executed);
-    if (j < 0) return false;
+    PassGeom g;
     field_geom(key_lo, key_hi, num_fields(key_lo, key_hi), field, g.shift, g.width);
     g.dst = ((executed - 1 - j) % 2 == 0) ? 1 : 2;
     g.src = (j == 0) ? 0 : (((executed - j) % 2 == 0) ? 1 : 2);
+    return g;
+}
+
+// Geometry of the pass, or false when its digit is constant (skipped).
+__device__ __forceinline__ bool pass_geom(const PassSpec &p, PassGeom &g)
+{
+    if (!p.and_or) {
+        g = p.host;
+        return true;
+    }
+    int executed;
+    const int j = field_pass(p.and_or[0] ^ p.and_or[1], p.key_lo, p.key_hi, p.field, &executed);
+    if (j < 0) return false;
+    g = plan_geom(p.key_lo, p.key_hi, p.field, j, executed);
     return true;
 }
 
 template <typename K>
 __global__ void __launch_bounds__(kRtThreads)
-k_radix_upsweep(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__restrict__ and_or, int key_lo,
-                int key_hi, int field, int ntiles, uint32_t *__restrict__ counts, uint32_t *__restrict__ totals)
+k_radix_upsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, uint32_t *__restrict__ counts,
+                uint32_t *__restrict__ totals)
 {
+    grid_dependency_begin();
     PassGeom g;
-    if (!pass_geom(and_or, key_lo, key_hi, field, g)) return;
+    if (!pass_geom(ps, g)) return;
     const K *__restrict__ keys = keys_of(bufs, g.src);
     const uint32_t dmask = (1u << g.width) - 1u;
     __shared__ uint32_t h[256];
@@ -457,12 +487,12 @@ k_radix_upsweep(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__r
 }
 
 __global__ void __launch_bounds__(kRtThreads)
-k_radix_scan(const unsigned long long *__restrict__ and_or, int key_lo, int key_hi, int field, int ntiles,
-             const uint32_t *__restrict__ counts, const uint32_t *__restrict__ totals,
+k_radix_scan(PassSpec ps, int ntiles, const uint32_t *__restrict__ counts, const uint32_t *__restrict__ totals,
              uint32_t *__restrict__ offsets)
 {
+    grid_dependency_begin();
     PassGeom g;
-    if (!pass_geom(and_or, key_lo, key_hi, field, g)) return;
+    if (!pass_geom(ps, g)) return;
     const uint32_t digit = blockIdx.x;
     if (digit >= (1u << g.width)) return;
     __shared__ uint32_t ws[8];
@@ -484,11 +514,11 @@ k_radix_scan(const unsigned long long *__restrict__ and_or, int key_lo, int key_
 
 template <typename K>
 __global__ void __launch_bounds__(kRtThreads)
-k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__restrict__ and_or, int key_lo,
-                  int key_hi, int field, int ntiles, const uint32_t *__restrict__ offsets)
+k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, const uint32_t *__restrict__ offsets)
 {
+    grid_dependency_begin();
     PassGeom g;
-    if (!pass_geom(and_or, key_lo, key_hi, field, g)) return;
+    if (!pass_geom(ps, g)) return;
     const K *__restrict__ kin = keys_of(bufs, g.src);
     const uint32_t *__restrict__ vin = vals_of(bufs, g.src);
     K *__restrict__ kout = keys_of(bufs, g.dst);
@@ -569,6 +599,7 @@ template <typename K>
 __global__ void k_copy_if_unsorted(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__restrict__ and_or,
                                    int key_lo, int key_hi)
 {
+    grid_dependency_begin();
     int executed;
     field_pass(and_or[0] ^ and_or[1], key_lo, key_hi, -1, &executed);
     if (executed != 0) return;
@@ -583,6 +614,7 @@ __global__ void k_copy_if_unsorted(SortBuffers<K> bufs, uint32_t num, const unsi
 __global__ void k_extract_ranges(const uint64_t *__restrict__ keys, uint32_t num,
                                  uint32_t *__restrict__ ranges)
 {
+    grid_dependency_begin();
     const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= num) return;
     const uint32_t t = (uint32_t)(keys[i] >> 32);
@@ -652,39 +684,60 @@ int grow_sort_buffers(gsr_ctx *ctx, SortBuffers<K> &b, size_t *cap, size_t need,
     return GSR_OK;
 }
 
-#define GSR_LAUNCHED(ctx)                                                     \
-    do {                                                                      \
-        ++(ctx)->launches;                                                    \
-        int _rc = cuda_check((ctx), cudaGetLastError(), "kernel launch");     \
-        if (_rc) return _rc;                                                  \
+#define GSR_LAUNCH(ctx, ...)                                                          \
+    do {                                                                              \
+        int _rc = cuda_check((ctx), launch_kernel((ctx), __VA_ARGS__), "kernel launch"); \
+        if (_rc) return _rc;                                                          \
     } while (0)
 
 // Stable LSD sort of bufs buffer 0 into buffer 1 over the key bits
-// [key_lo, key_hi); and_or: the device AND / OR of the keys.
+// [key_lo, key_hi).  and_or: the device AND / OR of the keys.  host_and_or:
+// the same two values already on the host, or null; with them only the passes
+// over varying digits are launched.
 template <typename K>
 int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int key_hi,
-               const unsigned long long *and_or, uint32_t *totals, cudaStream_t stream)
+               const unsigned long long *and_or, const unsigned long long *host_and_or, uint32_t *totals,
+               cudaStream_t stream)
 {
     const int ntiles = (int)((num + kRtTile - 1) / kRtTile);
     // [256][ntiles] counts, then [256][ntiles] offsets (sized by bin_splats).
     uint32_t *counts = ctx->radix_counts;
     uint32_t *offsets = ctx->radix_counts + (size_t)256 * ntiles;
     const int nf = num_fields(key_lo, key_hi);
+    int executed = nf;
+    if (host_and_or) {
+        field_pass(host_and_or[0] ^ host_and_or[1], key_lo, key_hi, -1, &executed);
+        if (executed == 0) {
+            // No digit varies: the input order is the sorted order.
+            int rc;
+            if ((rc = cuda_check(ctx, cudaMemcpyAsync(bufs.k[1], bufs.k[0], (size_t)num * sizeof(K),
+                                                      cudaMemcpyDeviceToDevice, stream), "cudaMemcpyAsync")) ||
+                (rc = cuda_check(ctx, cudaMemcpyAsync(bufs.v[1], bufs.v[0], (size_t)num * sizeof(uint32_t),
+                                                      cudaMemcpyDeviceToDevice, stream), "cudaMemcpyAsync")))
+                return rc;
+            return GSR_OK;
+        }
+    }
     for (int f = 0; f < nf; ++f) {
+        PassSpec ps = {and_or, key_lo, key_hi, f, {}};
+        if (host_and_or) {
+            const int j = field_pass(host_and_or[0] ^ host_and_or[1], key_lo, key_hi, f, &executed);
+            if (j < 0) continue;
+            ps.and_or = nullptr;
+            ps.host = plan_geom(key_lo, key_hi, f, j, executed);
+        }
         int sh, w;
         field_geom(key_lo, key_hi, nf, f, sh, w);
         uint32_t *tot = totals + 256 * f;
-        k_radix_upsweep<K><<<ntiles, kRtThreads, 0, stream>>>(bufs, num, and_or, key_lo, key_hi, f, ntiles,
-                                                              counts, tot);
-        GSR_LAUNCHED(ctx);
-        k_radix_scan<<<1 << w, kRtThreads, 0, stream>>>(and_or, key_lo, key_hi, f, ntiles, counts, tot, offsets);
-        GSR_LAUNCHED(ctx);
-        k_radix_downsweep<K><<<ntiles, kRtThreads, 0, stream>>>(bufs, num, and_or, key_lo, key_hi, f, ntiles,
-                                                                offsets);
-        GSR_LAUNCHED(ctx);
+        GSR_LAUNCH(ctx, k_radix_upsweep<K>, dim3(ntiles), dim3(kRtThreads), stream, bufs, num, ps, ntiles, counts,
+                   tot);
+        GSR_LAUNCH(ctx, k_radix_scan, dim3(1 << w), dim3(kRtThreads), stream, ps, ntiles, counts, tot, offsets);
+        GSR_LAUNCH(ctx, k_radix_downsweep<K>, dim3(ntiles), dim3(kRtThreads), stream, bufs, num, ps, ntiles,
+                   offsets);
     }
-    k_copy_if_unsorted<K><<<std::min(ntiles, 1024), 256, 0, stream>>>(bufs, num, and_or, key_lo, key_hi);
-    GSR_LAUNCHED(ctx);
+    if (!host_and_or)
+        GSR_LAUNCH(ctx, k_copy_if_unsorted<K>, dim3(std::min(ntiles, 1024)), dim3(256), stream, bufs, num, and_or,
+                   key_lo, key_hi);
     return GSR_OK;
 }
 
@@ -704,7 +757,7 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         if ((rc = cuda_check(ctx, cudaMalloc(&ctx->scalars, kScalarCount * sizeof(unsigned long long)),
                              "cudaMalloc")))
             return rc;
-        if ((rc = cuda_check(ctx, cudaHostAlloc(&ctx->host_total, 2 * sizeof(unsigned long long),
+        if ((rc = cuda_check(ctx, cudaHostAlloc(&ctx->host_total, 4 * sizeof(unsigned long long),
                                                 cudaHostAllocDefault),
                              "cudaHostAlloc")))
             return rc;
@@ -728,16 +781,15 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
 
     // 1. counts, totals; read the pair total and the emitting count.
     uint64_t total = 0, emitting = 0;
-    k_init_scalars<<<1, 32, 0, stream>>>(ctx->scalars);
-    GSR_LAUNCHED(ctx);
+    GSR_LAUNCH(ctx, k_init_scalars, dim3(1), dim3(32), stream, ctx->scalars);
     if (n > 0) {
-        k_count<<<nblk, kBinBlock, 0, stream>>>(splats, depths, n, tiles_x, tiles_y, ctx->counts,
-                                                blk_pairs, blk_emit, ctx->scalars);
-        GSR_LAUNCHED(ctx);
-        k_count_totals<<<1, 1024, 0, stream>>>(blk_pairs, blk_emit, nblk, ctx->scalars);
-        GSR_LAUNCHED(ctx);
+        GSR_LAUNCH(ctx, k_count, dim3(nblk), dim3(kBinBlock), stream, splats, depths, n, tiles_x, tiles_y,
+                   ctx->counts, blk_pairs, blk_emit, ctx->scalars);
+        GSR_LAUNCH(ctx, k_count_totals, dim3(1), dim3(1024), stream, blk_pairs, blk_emit, nblk, ctx->scalars);
+        // Pair total, emitting count and the AND / OR of the emitting splats'
+        // depth bits (scalar slots 0..3).
         if ((rc = cuda_check(ctx, cudaMemcpyAsync(ctx->host_total, ctx->scalars,
-                                                  2 * sizeof(unsigned long long),
+                                                  4 * sizeof(unsigned long long),
                                                   cudaMemcpyDeviceToHost, stream),
                              "cudaMemcpyAsync")))
             return rc;
@@ -784,25 +836,22 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
                              "cudaMemsetAsync")))
             return rc;
         // 3. depth sort of the emitting splats.
-        k_compact<<<nblk, kBinBlock, 0, stream>>>(ctx->counts, depths, n, blk_emit, ctx->depth.k[0],
-                                                  ctx->depth.v[0]);
-        GSR_LAUNCHED(ctx);
+        GSR_LAUNCH(ctx, k_compact, dim3(nblk), dim3(kBinBlock), stream, ctx->counts, depths, n, blk_emit,
+                   ctx->depth.k[0], ctx->depth.v[0]);
         if ((rc = radix_sort<uint32_t>(ctx, ctx->depth, (uint32_t)m, 0, 32, ctx->scalars + kScalarDepthAnd,
-                                       ctx->radix_totals, stream)))
+                                       ctx->host_total + 2, ctx->radix_totals, stream)))
             return rc;
         // 4. pair offsets in depth order, emission.
         const int mblk = (m + kBinBlock - 1) / kBinBlock;
-        k_sorted_sums<<<mblk, kBinBlock, 0, stream>>>(ctx->depth.v[1], ctx->counts, m, blk_sorted);
-        GSR_LAUNCHED(ctx);
-        k_scan_u64<<<1, 1024, 0, stream>>>(blk_sorted, mblk);
-        GSR_LAUNCHED(ctx);
-        k_emit<<<mblk, kBinBlock, 0, stream>>>(splats, depths, ctx->depth.v[1], m, tiles_x, tiles_y, blk_sorted,
-                                               ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars);
-        GSR_LAUNCHED(ctx);
+        GSR_LAUNCH(ctx, k_sorted_sums, dim3(mblk), dim3(kBinBlock), stream, ctx->depth.v[1], ctx->counts, m,
+                   blk_sorted);
+        GSR_LAUNCH(ctx, k_scan_u64, dim3(1), dim3(1024), stream, blk_sorted, mblk);
+        GSR_LAUNCH(ctx, k_emit, dim3(mblk), dim3(kBinBlock), stream, splats, depths, ctx->depth.v[1], m, tiles_x,
+                   tiles_y, blk_sorted, ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars);
         // 5. stable sort on the tile digits only.
         if (key_hi > 32) {
             if ((rc = radix_sort<uint64_t>(ctx, ctx->pairs, num, 32, key_hi, ctx->scalars + kScalarKeyAnd,
-                                           ctx->radix_totals + 4 * 256, stream)))
+                                           nullptr, ctx->radix_totals + 4 * 256, stream)))
                 return rc;
         } else {
             // One tile: the emitted order is already sorted.
@@ -815,8 +864,8 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
                 return rc;
         }
         // 6. per-tile ranges.
-        k_extract_ranges<<<(num + 255) / 256, 256, 0, stream>>>(ctx->pairs.k[1], num, ctx->ranges);
-        GSR_LAUNCHED(ctx);
+        GSR_LAUNCH(ctx, k_extract_ranges, dim3((num + 255) / 256), dim3(256), stream, ctx->pairs.k[1], num,
+                   ctx->ranges);
     }
 
     ctx->last_stream = stream;

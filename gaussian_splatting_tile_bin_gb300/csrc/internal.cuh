@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 #include "gsr.h"
 
@@ -13,10 +14,6 @@ namespace gsr {
 constexpr int kTile = GSR_TILE;           // 16x16 pixels per tile
 constexpr int kTilePixels = kTile * kTile;
 constexpr int kBinBlock = 256;            // splats per block in count / emit
-constexpr int kRadixThreads = 256;        // 8 warps
-constexpr int kRadixItems = 8;            // keys per thread per radix tile
-constexpr int kRadixTile = kRadixThreads * kRadixItems;
-constexpr int kMaxDigits = 8;             // 8-bit digits of a 64-bit key
 
 // The three key/value buffers of a radix sort: buffer 0 holds the unsorted
 // input, buffer 1 the sorted result, buffer 2 is ping-pong scratch.
@@ -37,6 +34,7 @@ struct gsr_ctx {
     int opt_warp_skip = 1;
     int opt_last_contrib = 1;
     int opt_warp_cull = 1;
+    int opt_pdl = 1;
 
     // Grow-only arena.
     size_t cap_pairs = 0;
@@ -45,17 +43,17 @@ struct gsr_ctx {
     uint32_t *counts = nullptr;                 // [cap_splats] tile count per splat
     gsr::DepthBuffers depth = {};               // [cap_splats] x 3: depth sort of emitting splats
     size_t cap_blocks = 0;
-    unsigned long long *blk_sums = nullptr;     // [4 * cap_blocks]: see bin.cu
-    unsigned long long *blk_offs = nullptr;
+    unsigned long long *blk_sums = nullptr;     // [3 * cap_blocks]: see bin.cu
     size_t cap_tiles = 0;
     uint32_t *ranges = nullptr;                 // [2 * cap_tiles]
     size_t cap_radix_tiles = 0;
     uint32_t *radix_counts = nullptr;           // [512 * cap_radix_tiles] digit counts and offsets
     uint32_t *radix_totals = nullptr;           // [2 * 4 * 256] digit totals of both sorts
     unsigned long long *scalars = nullptr;      // see bin.cu (kScalar*)
-    unsigned long long *host_total = nullptr;   // pinned: [0] pairs, [1] emitting
+    unsigned long long *host_total = nullptr;   // pinned: pairs, emitting, depth-bit AND / OR
     size_t cap_grad_acc = 0;
     double *grad_acc = nullptr;                 // [9 * cap] backward accumulator
+    bool grad_acc_zero = false;                 // grad_acc holds zeros when no call is in flight
 
     // Last binning, for gsr_get_bin_stats.
     cudaStream_t last_stream = nullptr;
@@ -65,6 +63,39 @@ struct gsr_ctx {
 };
 
 namespace gsr {
+
+// Programmatic dependent launch.  Every kernel of the library starts with this:
+// it lets the next grid in the stream begin launching (its CTAs take SM slots
+// as this grid's CTAs retire), then waits until every grid before it in the
+// stream has completed and its memory is visible.  No global memory is touched
+// before the wait, so each kernel sees exactly what stream order promises.
+__device__ __forceinline__ void grid_dependency_begin()
+{
+#if defined(__CUDA_ARCH__)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+
+// Launches `kernel` on `stream`, with programmatic stream serialisation when the
+// context allows it (GSR_OPT_PDL), and counts the launch.
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(gsr_ctx *ctx, void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t stream,
+                          Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = ctx->opt_pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    ++ctx->launches;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Records a CUDA error on the context; returns GSR_ERR_CUDA (or GSR_OK).
 int cuda_check(gsr_ctx *ctx, cudaError_t e, const char *what);

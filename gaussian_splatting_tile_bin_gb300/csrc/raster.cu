@@ -181,6 +181,7 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
           const uint2 *__restrict__ ranges, int width, int height, int tiles_x,
           float4 *__restrict__ out_rgbw, float *__restrict__ final_T, uint32_t *__restrict__ last_out)
 {
+    grid_dependency_begin();
     __shared__ StagedBatch sb;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t wbit = 1u << warp;
@@ -288,6 +289,7 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
            const float4 *__restrict__ dl_dout, const float *__restrict__ final_T,
            const uint32_t *__restrict__ last_in, double *__restrict__ grad_acc)
 {
+    grid_dependency_begin();
     __shared__ StagedBatch sb;
     __shared__ uint32_t s_wmax[kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -400,43 +402,49 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
     }
 }
 
-__global__ void k_grad_to_float(const double *__restrict__ acc, float *__restrict__ grad, size_t count)
+// grad = (float)acc, and acc back to zero for the next backward.
+__global__ void k_grad_to_float(double *__restrict__ acc, float *__restrict__ grad, size_t count)
 {
+    grid_dependency_begin();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count;
-         i += (size_t)gridDim.x * blockDim.x)
+         i += (size_t)gridDim.x * blockDim.x) {
         grad[i] = (float)acc[i];
+        acc[i] = 0.0;
+    }
 }
 
 template <bool kSkip, bool kLc>
-void launch_backward_cull(bool cull, int grid, cudaStream_t stream, const float *splats,
-                          const gsr_bins *bins, const float *dl_dout, const float *final_T,
-                          const uint32_t *last_contrib, double *acc)
+cudaError_t launch_backward_cull(gsr_ctx *ctx, bool cull, int grid, cudaStream_t stream, const float *splats,
+                                 const gsr_bins *bins, const float *dl_dout, const float *final_T,
+                                 const uint32_t *last_contrib, double *acc)
 {
     auto go = [&](auto kernel) {
-        kernel<<<grid, kTilePixels, 0, stream>>>(
-            splats, bins->sorted_idx, reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width,
-            bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
-            last_contrib, acc);
+        return launch_kernel(ctx, kernel, dim3(grid), dim3(kTilePixels), stream, splats, bins->sorted_idx,
+                             reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width, bins->height,
+                             bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T, last_contrib,
+                             acc);
     };
-    if (cull) go(k_backward<kSkip, kLc, true>);
-    else go(k_backward<kSkip, kLc, false>);
+    return cull ? go(k_backward<kSkip, kLc, true>) : go(k_backward<kSkip, kLc, false>);
 }
 
 // The backward kernel variant the context's options select, accumulating into acc.
-void launch_backward(const gsr_ctx *ctx, cudaStream_t stream, const float *splats, const gsr_bins *bins,
-                     const float *dl_dout, const float *final_T, const uint32_t *last_contrib,
-                     double *acc)
+cudaError_t launch_backward(gsr_ctx *ctx, cudaStream_t stream, const float *splats, const gsr_bins *bins,
+                            const float *dl_dout, const float *final_T, const uint32_t *last_contrib,
+                            double *acc)
 {
     const int grid = bins->tiles_x * bins->tiles_y;
     const bool cull = ctx->opt_warp_cull != 0;
     if (ctx->opt_warp_skip && ctx->opt_last_contrib)
-        launch_backward_cull<true, true>(cull, grid, stream, splats, bins, dl_dout, final_T, last_contrib, acc);
-    else if (ctx->opt_warp_skip)
-        launch_backward_cull<true, false>(cull, grid, stream, splats, bins, dl_dout, final_T, last_contrib, acc);
-    else if (ctx->opt_last_contrib)
-        launch_backward_cull<false, true>(cull, grid, stream, splats, bins, dl_dout, final_T, last_contrib, acc);
-    else
-        launch_backward_cull<false, false>(cull, grid, stream, splats, bins, dl_dout, final_T, last_contrib, acc);
+        return launch_backward_cull<true, true>(ctx, cull, grid, stream, splats, bins, dl_dout, final_T,
+                                                last_contrib, acc);
+    if (ctx->opt_warp_skip)
+        return launch_backward_cull<true, false>(ctx, cull, grid, stream, splats, bins, dl_dout, final_T,
+                                                 last_contrib, acc);
+    if (ctx->opt_last_contrib)
+        return launch_backward_cull<false, true>(ctx, cull, grid, stream, splats, bins, dl_dout, final_T,
+                                                 last_contrib, acc);
+    return launch_backward_cull<false, false>(ctx, cull, grid, stream, splats, bins, dl_dout, final_T,
+                                              last_contrib, acc);
 }
 
 }  // namespace
@@ -446,14 +454,11 @@ int rasterize_forward(gsr_ctx *ctx, const float *splats, const gsr_bins *bins, f
 {
     const int num_tiles = bins->tiles_x * bins->tiles_y;
     auto go = [&](auto kernel) {
-        kernel<<<num_tiles, kTilePixels, 0, stream>>>(
-            splats, bins->sorted_idx, reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width,
-            bins->height, bins->tiles_x, reinterpret_cast<float4 *>(out_rgbw), final_T, last_contrib);
+        return launch_kernel(ctx, kernel, dim3(num_tiles), dim3(kTilePixels), stream, splats, bins->sorted_idx,
+                             reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width, bins->height,
+                             bins->tiles_x, reinterpret_cast<float4 *>(out_rgbw), final_T, last_contrib);
     };
-    if (ctx->opt_warp_cull) go(k_forward<true>);
-    else go(k_forward<false>);
-    ++ctx->launches;
-    return cuda_check(ctx, cudaGetLastError(), "forward launch");
+    return cuda_check(ctx, ctx->opt_warp_cull ? go(k_forward<true>) : go(k_forward<false>), "forward launch");
 }
 
 int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_bins *bins,
@@ -461,31 +466,46 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
                        float *grad, cudaStream_t stream)
 {
     const size_t count = (size_t)n * 9;
+    int rc;
     if (count > ctx->cap_grad_acc || !ctx->grad_acc) {
         if (ctx->grad_acc) {
             // Queued work may still accumulate into the old buffer.
-            int rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-            if (rc) return rc;
+            if ((rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize"))) return rc;
             cudaFree(ctx->grad_acc);
         }
         ctx->grad_acc = nullptr;
         ctx->cap_grad_acc = 0;
-        if (cudaMalloc(&ctx->grad_acc, count * sizeof(double)) != cudaSuccess) {
+        const size_t cap = std::max<size_t>(count, 1);
+        if (cudaMalloc(&ctx->grad_acc, cap * sizeof(double)) != cudaSuccess) {
             cudaGetLastError();
             return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the gradient accumulator");
         }
-        ctx->cap_grad_acc = count;
+        ctx->cap_grad_acc = cap;
+        ctx->grad_acc_zero = false;
     }
-    int rc = cuda_check(ctx, cudaMemsetAsync(ctx->grad_acc, 0, count * sizeof(double), stream),
-                        "cudaMemsetAsync");
-    if (rc) return rc;
-    launch_backward(ctx, stream, splats, bins, dl_dout, final_T, last_contrib, ctx->grad_acc);
-    ++ctx->launches;
-    if ((rc = cuda_check(ctx, cudaGetLastError(), "backward launch"))) return rc;
-    const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)SM_BLOCKS_CAP);
-    k_grad_to_float<<<blocks, 256, 0, stream>>>(ctx->grad_acc, grad, count);
-    ++ctx->launches;
-    return cuda_check(ctx, cudaGetLastError(), "gradient conversion launch");
+    // The accumulator is zero between calls: the conversion kernel clears every
+    // element it reads.  Only a fresh buffer, or one a failed call left behind,
+    // is cleared here.
+    if (!ctx->grad_acc_zero) {
+        if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->grad_acc, 0, ctx->cap_grad_acc * sizeof(double), stream),
+                             "cudaMemsetAsync")))
+            return rc;
+        ctx->grad_acc_zero = true;
+    }
+    ctx->grad_acc_zero = false;
+    if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins, dl_dout, final_T, last_contrib,
+                                              ctx->grad_acc),
+                         "backward launch")))
+        return rc;
+    if (count > 0) {
+        const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)SM_BLOCKS_CAP);
+        if ((rc = cuda_check(ctx, launch_kernel(ctx, k_grad_to_float, dim3(blocks), dim3(256), stream,
+                                                ctx->grad_acc, grad, count),
+                             "gradient conversion launch")))
+            return rc;
+    }
+    ctx->grad_acc_zero = true;
+    return GSR_OK;
 }
 
 // --- backward without allocation ---------------------------------------------
@@ -529,13 +549,13 @@ int rasterize_backward_noalloc(gsr_ctx *ctx, const float *splats, int32_t n, con
     // The array keeps the previous call's sums: clear the part this call uses.
     int rc = cuda_check(ctx, cudaMemsetAsync(acc, 0, count * sizeof(double), stream), "cudaMemsetAsync");
     if (rc) return rc;
-    launch_backward(ctx, stream, splats, bins, dl_dout, final_T, last_contrib, acc);
-    ++ctx->launches;
-    if ((rc = cuda_check(ctx, cudaGetLastError(), "backward launch"))) return rc;
+    if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins, dl_dout, final_T, last_contrib, acc),
+                         "backward launch")))
+        return rc;
+    if (count == 0) return GSR_OK;
     const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)SM_BLOCKS_CAP);
-    k_grad_to_float<<<blocks, 256, 0, stream>>>(acc, grad, count);
-    ++ctx->launches;
-    return cuda_check(ctx, cudaGetLastError(), "gradient conversion launch");
+    return cuda_check(ctx, launch_kernel(ctx, k_grad_to_float, dim3(blocks), dim3(256), stream, acc, grad, count),
+                      "gradient conversion launch");
 }
 
 }  // namespace gsr

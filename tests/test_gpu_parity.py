@@ -228,6 +228,21 @@ def test_warp_culling_changes_nothing(gsr, ctx, name):
     assert np.allclose(on["grad"], off["grad"], rtol=1e-6, atol=1e-9)
 
 
+def test_dependent_launch_changes_nothing(gsr, ctx):
+    """Kernels launched with programmatic dependent launch wait for the grids
+    before them, so the results are those of plain stream order."""
+    wl = gen.lego_early()
+    on = run_gpu(gsr, ctx, wl)
+    ctx.set_option("pdl", 0)
+    try:
+        off = run_gpu(gsr, ctx, wl)
+    finally:
+        ctx.set_option("pdl", 1)
+    for k in ("keys", "idx", "ranges", "out", "final_T", "last"):
+        assert np.array_equal(on[k], off[k]), k
+    assert np.allclose(on["grad"], off["grad"], rtol=1e-6, atol=1e-9)
+
+
 def test_self_noise(gsr, ctx):
     """Run-to-run spread of the atomically accumulated gradients (the pages'
     self-noise protocol: 20 repeats, "M3 per-splat backward", section 2)."""
