@@ -91,7 +91,7 @@ void gsr_destroy(gsr_ctx *ctx)
             cudaFree(ctx->pairs.k[b]);
             cudaFree(ctx->pairs.v[b]);
         }
-        cudaFree(ctx->counts);
+        cudaFree(ctx->rects);
         for (int b = 0; b < 3; ++b) {
             cudaFree(ctx->depth.k[b]);
             cudaFree(ctx->depth.v[b]);

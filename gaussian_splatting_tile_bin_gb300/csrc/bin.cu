@@ -44,18 +44,10 @@ enum {
     kScalarCount = 8
 };
 
-// The 3-sigma box of splat i as an inclusive tile rectangle (x0, y0, x1, y1).
-// false when the splat is culled.
-__device__ __forceinline__ bool splat_tile_rect(const float *__restrict__ splats,
-                                                const float *__restrict__ depths, int i,
-                                                int tiles_x, int tiles_y, int4 &r,
-                                                uint32_t &depth_bits)
+// The 3-sigma box of a splat (its 9 fields v and its depth) as an inclusive
+// tile rectangle (x0, y0, x1, y1).  false when the splat is culled.
+__device__ __forceinline__ bool tile_rect(const float (&v)[9], float depth, int tiles_x, int tiles_y, int4 &r)
 {
-    const float *s = splats + 9 * (size_t)i;
-    float v[9];
-#pragma unroll
-    for (int k = 0; k < 9; ++k) v[k] = __ldg(s + k);
-    float depth = __ldg(depths + i);
     bool ok = isfinite(depth) && depth > 0.0f;
 #pragma unroll
     for (int k = 0; k < 9; ++k) ok = ok && isfinite(v[k]);
@@ -80,8 +72,23 @@ __device__ __forceinline__ bool splat_tile_rect(const float *__restrict__ splats
     y1 = min(y1, tiles_y - 1);
     if (x0 > x1 || y0 > y1) return false;
     r = make_int4(x0, y0, x1, y1);
-    depth_bits = __float_as_uint(depth);
     return true;
+}
+
+// A tile rectangle packed into 8 bytes: (x0 | y0 << 16, x1 | y1 << 16); tile
+// coordinates fit 16 bits (at most 32768 tiles per side).  A culled splat is
+// stored as x0 = 1 > x1 = 0.
+__device__ __forceinline__ uint2 pack_rect(bool ok, int4 r)
+{
+    return ok ? make_uint2((uint32_t)r.x | ((uint32_t)r.y << 16), (uint32_t)r.z | ((uint32_t)r.w << 16))
+              : make_uint2(1u, 0u);
+}
+
+__device__ __forceinline__ uint32_t rect_width(uint2 p) { return (p.y & 0xffffu) - (p.x & 0xffffu) + 1u; }
+__device__ __forceinline__ uint32_t rect_count(uint2 p)
+{
+    const uint32_t x0 = p.x & 0xffffu, x1 = p.y & 0xffffu, y0 = p.x >> 16, y1 = p.y >> 16;
+    return x0 <= x1 && y0 <= y1 ? (x1 - x0 + 1u) * (y1 - y0 + 1u) : 0u;
 }
 
 // Exclusive scan over a 256-thread block; returns the exclusive prefix and the
@@ -203,23 +210,41 @@ __global__ void k_init_scalars(unsigned long long *__restrict__ scalars)
 
 // --- count -----------------------------------------------------------------
 
-// Per splat: tile count.  Per block: the pair total, the number of emitting
-// splats, and the AND / OR of their depth bits.
+// Per splat: its tile rectangle.  Per block: the pair total, the number of
+// emitting splats, and the AND / OR of their depth bits.  The block's 256
+// records (9216 contiguous bytes) are read with coalesced 4-byte loads through
+// shared memory.
 __global__ void __launch_bounds__(kBinBlock)
 k_count(const float *__restrict__ splats, const float *__restrict__ depths, int n, int tiles_x,
-        int tiles_y, uint32_t *__restrict__ counts, unsigned long long *__restrict__ blk_pairs,
+        int tiles_y, uint2 *__restrict__ rects, unsigned long long *__restrict__ blk_pairs,
         unsigned long long *__restrict__ blk_emitting, unsigned long long *__restrict__ scalars)
 {
     grid_dependency_begin();
+    __shared__ float s_rec[kBinBlock * 9];
     __shared__ unsigned long long s_and[8], s_or[8];
     __shared__ unsigned long long ws[8];
-    const int i = blockIdx.x * kBinBlock + threadIdx.x;
+    const int first = blockIdx.x * kBinBlock;
+    const int nrec = min(kBinBlock, n - first);
+    const float *src = splats + 9 * (size_t)first;
+#pragma unroll
+    for (int k = 0; k < 9; ++k) {
+        const int e = k * kBinBlock + threadIdx.x;
+        if (e < nrec * 9) s_rec[e] = __ldg(src + e);
+    }
+    __syncthreads();
+    const int i = first + threadIdx.x;
     uint32_t c = 0, db = 0;
     if (i < n) {
-        int4 r;
-        if (splat_tile_rect(splats, depths, i, tiles_x, tiles_y, r, db))
-            c = (uint32_t)(r.z - r.x + 1) * (uint32_t)(r.w - r.y + 1);
-        counts[i] = c;
+        float v[9];
+#pragma unroll
+        for (int k = 0; k < 9; ++k) v[k] = s_rec[9 * threadIdx.x + k];
+        const float depth = __ldg(depths + i);
+        int4 r = make_int4(0, 0, 0, 0);
+        const bool ok = tile_rect(v, depth, tiles_x, tiles_y, r);
+        const uint2 pr = pack_rect(ok, r);
+        rects[i] = pr;
+        c = rect_count(pr);
+        db = __float_as_uint(depth);
     }
     unsigned long long pairs_total, emit_total;
     block_exclusive_scan_256<unsigned long long>(c, ws, &pairs_total);
@@ -295,14 +320,14 @@ k_count_totals(const unsigned long long *__restrict__ blk_pairs, unsigned long l
 
 // Writes (depth bits, splat index) of every emitting splat, in splat order.
 __global__ void __launch_bounds__(kBinBlock)
-k_compact(const uint32_t *__restrict__ counts, const float *__restrict__ depths, int n,
+k_compact(const uint2 *__restrict__ rects, const float *__restrict__ depths, int n,
           const unsigned long long *__restrict__ blk_emit_offs, uint32_t *__restrict__ dkeys,
           uint32_t *__restrict__ didx)
 {
     grid_dependency_begin();
     __shared__ uint32_t ws[8];
     const int i = blockIdx.x * kBinBlock + threadIdx.x;
-    const bool emits = i < n && counts[i] > 0;
+    const bool emits = i < n && rect_count(rects[i]) > 0;
     uint32_t total;
     const uint32_t excl = block_exclusive_scan_256<uint32_t>(emits ? 1u : 0u, ws, &total);
     if (emits) {
@@ -314,13 +339,13 @@ k_compact(const uint32_t *__restrict__ counts, const float *__restrict__ depths,
 
 // Per block of 256 depth-sorted splats: their pair total.
 __global__ void __launch_bounds__(kBinBlock)
-k_sorted_sums(const uint32_t *__restrict__ sorted_idx, const uint32_t *__restrict__ counts, int m,
+k_sorted_sums(const uint32_t *__restrict__ sorted_idx, const uint2 *__restrict__ rects, int m,
               unsigned long long *__restrict__ blk_sorted)
 {
     grid_dependency_begin();
     __shared__ unsigned long long ws[8];
     const int k = blockIdx.x * kBinBlock + threadIdx.x;
-    const uint32_t c = k < m ? counts[sorted_idx[k]] : 0u;
+    const uint32_t c = k < m ? rect_count(rects[sorted_idx[k]]) : 0u;
     unsigned long long total;
     block_exclusive_scan_256<unsigned long long>(c, ws, &total);
     if (threadIdx.x == 0) blk_sorted[blockIdx.x] = total;
@@ -328,58 +353,109 @@ k_sorted_sums(const uint32_t *__restrict__ sorted_idx, const uint32_t *__restric
 
 // --- emit ------------------------------------------------------------------
 
-// Each block takes 256 consecutive depth-sorted splats, re-derives their
-// rectangles, scans their counts and writes its contiguous slice of pairs with
-// all 256 threads, so a splat with thousands of tiles does not serialise on one
-// thread.  Within a splat the pairs go in row-major tile order; across splats in
-// depth order.  Also folds the AND / OR of the keys for the tile sort's plan.
+// Pairs per block that the start-bit index covers; a block with more pairs
+// (very large splats) finds each pair's splat by binary search instead.
+constexpr int kEmitIndexPairs = 16384;
+
+// Each block takes 256 consecutive depth-sorted splats, scans their counts and
+// writes its contiguous slice of pairs with all 256 threads, so a splat with
+// thousands of tiles does not serialise on one thread.  Within a splat the pairs
+// go in row-major tile order; across splats in depth order.  A pair finds its
+// splat as the rank of the last splat start at or before it (a bit per pair
+// marks the starts; every splat here has at least one pair).  Also folds the
+// AND / OR of the keys for the tile sort's plan.
 __global__ void __launch_bounds__(kBinBlock)
-k_emit(const float *__restrict__ splats, const float *__restrict__ depths,
-       const uint32_t *__restrict__ sorted_idx, int m, int tiles_x, int tiles_y,
-       const unsigned long long *__restrict__ blk_offs, uint64_t *__restrict__ keys,
+k_emit(const uint2 *__restrict__ rects, const float *__restrict__ depths, const uint32_t *__restrict__ sorted_idx,
+       int m, int tiles_x, const unsigned long long *__restrict__ blk_offs, uint64_t *__restrict__ keys,
        uint32_t *__restrict__ vals, unsigned long long *__restrict__ scalars)
 {
     grid_dependency_begin();
     __shared__ uint32_t s_off[kBinBlock];
-    __shared__ int4 s_rect[kBinBlock];
+    __shared__ uint32_t s_x0y0[kBinBlock];
+    __shared__ uint32_t s_w[kBinBlock];
+    __shared__ float s_invw[kBinBlock];
     __shared__ uint32_t s_db[kBinBlock];
     __shared__ uint32_t s_idx[kBinBlock];
+    __shared__ uint32_t s_bits[kEmitIndexPairs / 32];
+    __shared__ uint32_t s_rank[kEmitIndexPairs / 32];
     __shared__ uint32_t ws[8];
     __shared__ unsigned long long s_and[8], s_or[8];
 
     const int k = blockIdx.x * kBinBlock + threadIdx.x;
-    uint32_t c = 0;
-    int4 r = make_int4(0, 0, -1, -1);
-    uint32_t db = 0, i = 0;
+    uint32_t c = 0, i = 0;
+    uint2 pr = make_uint2(1u, 0u);
     if (k < m) {
         i = sorted_idx[k];
-        if (splat_tile_rect(splats, depths, (int)i, tiles_x, tiles_y, r, db))
-            c = (uint32_t)(r.z - r.x + 1) * (uint32_t)(r.w - r.y + 1);
+        pr = rects[i];
+        c = rect_count(pr);
     }
     uint32_t total;
     const uint32_t excl = block_exclusive_scan_256<uint32_t>(c, ws, &total);
+    const bool indexed = total <= (uint32_t)kEmitIndexPairs;
+    if (indexed)
+        for (uint32_t wi = threadIdx.x; wi < (total + 31) / 32; wi += kBinBlock) s_bits[wi] = 0u;
     s_off[threadIdx.x] = excl;
-    s_rect[threadIdx.x] = r;
-    s_db[threadIdx.x] = db;
+    s_x0y0[threadIdx.x] = pr.x;
+    const uint32_t w = c ? rect_width(pr) : 1u;
+    s_w[threadIdx.x] = w;
+    s_invw[threadIdx.x] = 1.0f / (float)w;
+    s_db[threadIdx.x] = k < m ? __float_as_uint(__ldg(depths + i)) : 0u;
     s_idx[threadIdx.x] = i;
     __syncthreads();
+    if (indexed) {
+        if (c) atomicOr(&s_bits[excl >> 5], 1u << (excl & 31));
+        __syncthreads();
+        // s_rank[w]: starts in the words before w (one warp scans the words).
+        if (threadIdx.x < 32) {
+            uint32_t carry = 0;
+            for (uint32_t w0 = 0; w0 < (total + 31) / 32; w0 += 32) {
+                const uint32_t wi = w0 + threadIdx.x;
+                const uint32_t cnt = wi < (total + 31) / 32 ? __popc(s_bits[wi]) : 0u;
+                uint32_t incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t t = __shfl_up_sync(kFull, incl, o);
+                    if ((int)threadIdx.x >= o) incl += t;
+                }
+                if (wi < (total + 31) / 32) s_rank[wi] = carry + incl - cnt;
+                carry += __shfl_sync(kFull, incl, 31);
+            }
+        }
+        __syncthreads();
+    }
 
     const unsigned long long base = blk_offs[blockIdx.x];
     unsigned long long acc_and = ~0ull, acc_or = 0ull;
     for (uint32_t q = threadIdx.x; q < total; q += kBinBlock) {
-        // Last splat t with s_off[t] <= q; it has a nonzero count.
-        int lo = 0, hi = kBinBlock - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_off[mid] <= q) lo = mid;
-            else hi = mid - 1;
+        int lo;
+        if (indexed) {
+            const uint32_t bits = s_bits[q >> 5] & (0xffffffffu >> (31 - (q & 31)));
+            lo = (int)(s_rank[q >> 5] + __popc(bits)) - 1;
+        } else {
+            // Last splat t with s_off[t] <= q; it has a nonzero count.
+            int l = 0, h = kBinBlock - 1;
+            while (l < h) {
+                const int mid = (l + h + 1) >> 1;
+                if (s_off[mid] <= q) l = mid;
+                else h = mid - 1;
+            }
+            lo = l;
         }
-        const int4 rr = s_rect[lo];
         const uint32_t local = q - s_off[lo];
-        const uint32_t w = (uint32_t)(rr.z - rr.x + 1);
-        const uint32_t dy = local / w;
-        const uint32_t ty = (uint32_t)rr.y + dy;
-        const uint32_t tx = (uint32_t)rr.x + (local - dy * w);
+        const uint32_t wd = s_w[lo];
+        // local / wd: below 2^22 a float reciprocal is within one of the
+        // quotient and one correction makes it exact.
+        uint32_t dy;
+        if (local < (1u << 22)) {
+            dy = (uint32_t)((float)local * s_invw[lo]);
+            if (dy * wd > local) --dy;
+            else if ((dy + 1u) * wd <= local) ++dy;
+        } else {
+            dy = local / wd;
+        }
+        const uint32_t xy = s_x0y0[lo];
+        const uint32_t ty = (xy >> 16) + dy;
+        const uint32_t tx = (xy & 0xffffu) + (local - dy * wd);
         const uint64_t tile = (uint64_t)ty * (uint64_t)tiles_x + tx;
         const uint64_t key = (tile << 32) | (uint64_t)s_db[lo];
         keys[base + q] = key;
@@ -403,9 +479,20 @@ k_emit(const float *__restrict__ splats, const float *__restrict__ depths,
 //              masks, per-warp counters), stages them in shared memory in digit
 //              order and writes every digit's keys as one contiguous run.
 
+// Keys per thread in a radix tile of the depth sort and of the pair sort.
+#ifndef GSR_RT_ITEMS_DEPTH
+#define GSR_RT_ITEMS_DEPTH 8
+#endif
+#ifndef GSR_RT_ITEMS_PAIRS
+#define GSR_RT_ITEMS_PAIRS 8
+#endif
+// Resident CTAs per SM the radix downsweep is compiled for (register budget).
+#ifndef GSR_RT_MIN_BLOCKS
+#define GSR_RT_MIN_BLOCKS 4
+#endif
 constexpr int kRtThreads = 256;
-constexpr int kRtItems = 8;
-constexpr int kRtTile = kRtThreads * kRtItems;
+constexpr int kRtItemsDepth = GSR_RT_ITEMS_DEPTH;
+constexpr int kRtItemsPairs = GSR_RT_ITEMS_PAIRS;
 
 // Buffer b of the three (a select, so the kernel parameter block is not copied
 // to local memory for dynamic indexing).
@@ -459,7 +546,7 @@ __device__ __forceinline__ bool pass_geom(const PassSpec &p, PassGeom &g)
     return true;
 }
 
-template <typename K>
+template <typename K, int kRtItems>
 __global__ void __launch_bounds__(kRtThreads)
 k_radix_upsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, uint32_t *__restrict__ counts,
                 uint32_t *__restrict__ totals)
@@ -472,7 +559,7 @@ k_radix_upsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, uint
     __shared__ uint32_t h[256];
     h[threadIdx.x] = 0;
     __syncthreads();
-    const uint32_t base = blockIdx.x * kRtTile;
+    const uint32_t base = blockIdx.x * (kRtThreads * kRtItems);
 #pragma unroll
     for (int k = 0; k < kRtItems; ++k) {
         const uint32_t i = base + k * kRtThreads + threadIdx.x;
@@ -496,24 +583,42 @@ k_radix_scan(PassSpec ps, int ntiles, const uint32_t *__restrict__ counts, const
     const uint32_t digit = blockIdx.x;
     if (digit >= (1u << g.width)) return;
     __shared__ uint32_t ws[8];
+    __shared__ uint32_t s_wsum[kRtThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // Global start of this digit: the totals of all smaller digits.
     uint32_t base;
     block_exclusive_scan_256<uint32_t>(threadIdx.x < digit ? totals[threadIdx.x] : 0u, ws, &base);
     const uint32_t *row = counts + (size_t)digit * ntiles;
     uint32_t *orow = offsets + (size_t)digit * ntiles;
+    // Warp w scans the segment [seg0, seg1) of the row: first its sum (all loads
+    // independent), then, after the warps' sums are exchanged, the segment in
+    // runs of 32 with a carried prefix.
+    const int per = ((ntiles + kRtThreads - 1) / kRtThreads) * 32;
+    const int seg0 = min(ntiles, warp * per), seg1 = min(ntiles, seg0 + per);
+    uint32_t part = 0;
+    for (int i = seg0 + lane; i < seg1; i += 32) part += row[i];
+    part = __reduce_add_sync(kFull, part);
+    if (lane == 0) s_wsum[warp] = part;
+    __syncthreads();
     uint32_t carry = base;
-    for (int start = 0; start < ntiles; start += kRtThreads) {
-        const int i = start + threadIdx.x;
-        const uint32_t c = i < ntiles ? row[i] : 0u;
-        uint32_t sum;
-        const uint32_t e = block_exclusive_scan_256<uint32_t>(c, ws, &sum);
-        if (i < ntiles) orow[i] = carry + e;
-        carry += sum;
+    for (int w = 0; w < warp; ++w) carry += s_wsum[w];
+#pragma unroll 4
+    for (int i0 = seg0; i0 < seg1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t c = i < seg1 ? row[i] : 0u;
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (i < seg1) orow[i] = carry + incl - c;
+        carry += __shfl_sync(kFull, incl, 31);
     }
 }
 
-template <typename K>
-__global__ void __launch_bounds__(kRtThreads)
+template <typename K, int kRtItems>
+__global__ void __launch_bounds__(kRtThreads, GSR_RT_MIN_BLOCKS)
 k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, const uint32_t *__restrict__ offsets)
 {
     grid_dependency_begin();
@@ -530,6 +635,7 @@ k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, co
     __shared__ uint32_t s_lstart[256];  // start of each digit's run in the staged tile
     __shared__ uint32_t s_goff[256];    // global start of each digit's run
     __shared__ uint32_t ws[8];
+    constexpr int kRtTile = kRtThreads * kRtItems;
     __shared__ K s_keys[kRtTile];
     __shared__ uint32_t s_vals[kRtTile];
 
@@ -611,15 +717,36 @@ __global__ void k_copy_if_unsorted(SortBuffers<K> bufs, uint32_t num, const unsi
 
 // --- ranges --------------------------------------------------------------------
 
-__global__ void k_extract_ranges(const uint64_t *__restrict__ keys, uint32_t num,
-                                 uint32_t *__restrict__ ranges)
+// Tile starts and ends where the tile field of the sorted keys changes; each
+// thread compares four consecutive keys (two 16-byte loads) and their
+// neighbours.
+__global__ void __launch_bounds__(256)
+k_extract_ranges(const uint64_t *__restrict__ keys, uint32_t num, uint32_t *__restrict__ ranges)
 {
     grid_dependency_begin();
-    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= num) return;
-    const uint32_t t = (uint32_t)(keys[i] >> 32);
-    if (i == 0 || (uint32_t)(keys[i - 1] >> 32) != t) ranges[2 * (size_t)t] = i;
-    if (i == num - 1 || (uint32_t)(keys[i + 1] >> 32) != t) ranges[2 * (size_t)t + 1] = i + 1;
+    const uint32_t i0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4u;
+    if (i0 >= num) return;
+    uint32_t t[6];  // tiles of keys i0 - 1 .. i0 + 4 (0xffffffff outside [0, num))
+    t[0] = i0 > 0 ? (uint32_t)(__ldg(keys + i0 - 1) >> 32) : 0xffffffffu;
+    if (i0 + 4 <= num) {
+        const ulonglong2 a = __ldg(reinterpret_cast<const ulonglong2 *>(keys + i0));
+        const ulonglong2 b = __ldg(reinterpret_cast<const ulonglong2 *>(keys + i0 + 2));
+        t[1] = (uint32_t)(a.x >> 32);
+        t[2] = (uint32_t)(a.y >> 32);
+        t[3] = (uint32_t)(b.x >> 32);
+        t[4] = (uint32_t)(b.y >> 32);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t[1 + k] = i0 + k < num ? (uint32_t)(__ldg(keys + i0 + k) >> 32) : 0xffffffffu;
+    }
+    t[5] = i0 + 4 < num ? (uint32_t)(__ldg(keys + i0 + 4) >> 32) : 0xffffffffu;
+#pragma unroll
+    for (int k = 1; k <= 4; ++k) {
+        const uint32_t i = i0 + k - 1;
+        if (i >= num) break;
+        if (t[k - 1] != t[k]) ranges[2 * (size_t)t[k]] = i;
+        if (t[k + 1] != t[k]) ranges[2 * (size_t)t[k] + 1] = i + 1;
+    }
 }
 
 int bits_for(uint64_t v)
@@ -694,11 +821,12 @@ int grow_sort_buffers(gsr_ctx *ctx, SortBuffers<K> &b, size_t *cap, size_t need,
 // [key_lo, key_hi).  and_or: the device AND / OR of the keys.  host_and_or:
 // the same two values already on the host, or null; with them only the passes
 // over varying digits are launched.
-template <typename K>
+template <typename K, int kRtItems>
 int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int key_hi,
                const unsigned long long *and_or, const unsigned long long *host_and_or, uint32_t *totals,
                cudaStream_t stream)
 {
+    constexpr int kRtTile = kRtThreads * kRtItems;
     const int ntiles = (int)((num + kRtTile - 1) / kRtTile);
     // [256][ntiles] counts, then [256][ntiles] offsets (sized by bin_splats).
     uint32_t *counts = ctx->radix_counts;
@@ -729,10 +857,10 @@ int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int 
         int sh, w;
         field_geom(key_lo, key_hi, nf, f, sh, w);
         uint32_t *tot = totals + 256 * f;
-        GSR_LAUNCH(ctx, k_radix_upsweep<K>, dim3(ntiles), dim3(kRtThreads), stream, bufs, num, ps, ntiles, counts,
+        GSR_LAUNCH(ctx, k_radix_upsweep<K, kRtItems>, dim3(ntiles), dim3(kRtThreads), stream, bufs, num, ps, ntiles, counts,
                    tot);
         GSR_LAUNCH(ctx, k_radix_scan, dim3(1 << w), dim3(kRtThreads), stream, ps, ntiles, counts, tot, offsets);
-        GSR_LAUNCH(ctx, k_radix_downsweep<K>, dim3(ntiles), dim3(kRtThreads), stream, bufs, num, ps, ntiles,
+        GSR_LAUNCH(ctx, k_radix_downsweep<K, kRtItems>, dim3(ntiles), dim3(kRtThreads), stream, bufs, num, ps, ntiles,
                    offsets);
     }
     if (!host_and_or)
@@ -768,8 +896,8 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     if (!ctx->depth.k[0] || (size_t)n > ctx->cap_splats) {
         size_t cap = 0;
         if ((rc = grow_sort_buffers(ctx, ctx->depth, &cap, (size_t)n, "depth sort buffers"))) return rc;
-        ctx->cap_splats = 0;  // regrow counts below to the same capacity
-        if ((rc = grow(ctx, &ctx->counts, &ctx->cap_splats, cap, 1, "counts"))) return rc;
+        ctx->cap_splats = 0;  // regrow the rectangles below to the same capacity
+        if ((rc = grow(ctx, &ctx->rects, &ctx->cap_splats, cap, 1, "tile rectangles"))) return rc;
     }
     // Three per-block arrays: [0, c) pair sums, [c, 2c) emitting counts then
     // offsets, [2c, 3c) pair sums in depth order then offsets.
@@ -784,7 +912,7 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     GSR_LAUNCH(ctx, k_init_scalars, dim3(1), dim3(32), stream, ctx->scalars);
     if (n > 0) {
         GSR_LAUNCH(ctx, k_count, dim3(nblk), dim3(kBinBlock), stream, splats, depths, n, tiles_x, tiles_y,
-                   ctx->counts, blk_pairs, blk_emit, ctx->scalars);
+                   ctx->rects, blk_pairs, blk_emit, ctx->scalars);
         GSR_LAUNCH(ctx, k_count_totals, dim3(1), dim3(1024), stream, blk_pairs, blk_emit, nblk, ctx->scalars);
         // Pair total, emitting count and the AND / OR of the emitting splats'
         // depth bits (scalar slots 0..3).
@@ -820,7 +948,8 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     // Radix counts and offsets for the larger of the two sorts, allocated before
     // any kernel that uses them is queued.
     {
-        const size_t rtiles = std::max<size_t>((m + kRtTile - 1) / kRtTile, (num + kRtTile - 1) / kRtTile);
+        constexpr size_t td = kRtThreads * kRtItemsDepth, tp = kRtThreads * kRtItemsPairs;
+        const size_t rtiles = std::max<size_t>((m + td - 1) / td, (num + tp - 1) / tp);
         if ((rc = grow(ctx, &ctx->radix_counts, &ctx->cap_radix_tiles, std::max<size_t>(rtiles, 1), 512,
                        "radix counts")))
             return rc;
@@ -836,21 +965,21 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
                              "cudaMemsetAsync")))
             return rc;
         // 3. depth sort of the emitting splats.
-        GSR_LAUNCH(ctx, k_compact, dim3(nblk), dim3(kBinBlock), stream, ctx->counts, depths, n, blk_emit,
+        GSR_LAUNCH(ctx, k_compact, dim3(nblk), dim3(kBinBlock), stream, ctx->rects, depths, n, blk_emit,
                    ctx->depth.k[0], ctx->depth.v[0]);
-        if ((rc = radix_sort<uint32_t>(ctx, ctx->depth, (uint32_t)m, 0, 32, ctx->scalars + kScalarDepthAnd,
+        if ((rc = radix_sort<uint32_t, kRtItemsDepth>(ctx, ctx->depth, (uint32_t)m, 0, 32, ctx->scalars + kScalarDepthAnd,
                                        ctx->host_total + 2, ctx->radix_totals, stream)))
             return rc;
         // 4. pair offsets in depth order, emission.
         const int mblk = (m + kBinBlock - 1) / kBinBlock;
-        GSR_LAUNCH(ctx, k_sorted_sums, dim3(mblk), dim3(kBinBlock), stream, ctx->depth.v[1], ctx->counts, m,
+        GSR_LAUNCH(ctx, k_sorted_sums, dim3(mblk), dim3(kBinBlock), stream, ctx->depth.v[1], ctx->rects, m,
                    blk_sorted);
         GSR_LAUNCH(ctx, k_scan_u64, dim3(1), dim3(1024), stream, blk_sorted, mblk);
-        GSR_LAUNCH(ctx, k_emit, dim3(mblk), dim3(kBinBlock), stream, splats, depths, ctx->depth.v[1], m, tiles_x,
-                   tiles_y, blk_sorted, ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars);
+        GSR_LAUNCH(ctx, k_emit, dim3(mblk), dim3(kBinBlock), stream, ctx->rects, depths, ctx->depth.v[1], m,
+                   tiles_x, blk_sorted, ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars);
         // 5. stable sort on the tile digits only.
         if (key_hi > 32) {
-            if ((rc = radix_sort<uint64_t>(ctx, ctx->pairs, num, 32, key_hi, ctx->scalars + kScalarKeyAnd,
+            if ((rc = radix_sort<uint64_t, kRtItemsPairs>(ctx, ctx->pairs, num, 32, key_hi, ctx->scalars + kScalarKeyAnd,
                                            nullptr, ctx->radix_totals + 4 * 256, stream)))
                 return rc;
         } else {
@@ -864,7 +993,7 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
                 return rc;
         }
         // 6. per-tile ranges.
-        GSR_LAUNCH(ctx, k_extract_ranges, dim3((num + 255) / 256), dim3(256), stream, ctx->pairs.k[1], num,
+        GSR_LAUNCH(ctx, k_extract_ranges, dim3((num + 1023) / 1024), dim3(256), stream, ctx->pairs.k[1], num,
                    ctx->ranges);
     }
 

@@ -40,7 +40,7 @@ struct gsr_ctx {
     size_t cap_pairs = 0;
     gsr::PairBuffers pairs = {};
     size_t cap_splats = 0;
-    uint32_t *counts = nullptr;                 // [cap_splats] tile count per splat
+    uint2 *rects = nullptr;                     // [cap_splats] packed tile rectangle per splat
     gsr::DepthBuffers depth = {};               // [cap_splats] x 3: depth sort of emitting splats
     size_t cap_blocks = 0;
     unsigned long long *blk_sums = nullptr;     // [3 * cap_blocks]: see bin.cu
