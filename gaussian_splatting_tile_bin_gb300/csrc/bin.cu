@@ -144,12 +144,14 @@ __device__ __forceinline__ void block_and_or_into(unsigned long long a, unsigned
     }
 }
 
-// Lanes in `members` whose `width`-bit digit equals this lane's, from one
+// Lanes in `members` whose kWidth-bit digit equals this lane's, from one
 // ballot per bit.  Every lane of the warp calls this together.
-__device__ __forceinline__ uint32_t digit_peers(uint32_t members, uint32_t digit, int width)
+template <int kWidth>
+__device__ __forceinline__ uint32_t digit_peers(uint32_t members, uint32_t digit)
 {
     uint32_t peers = members;
-    for (int b = 0; b < width; ++b) {
+#pragma unroll
+    for (int b = 0; b < kWidth; ++b) {
         const uint32_t bal = __ballot_sync(kFull, (digit >> b) & 1u);
         peers &= ((digit >> b) & 1u) ? bal : ~bal;
     }
@@ -488,7 +490,7 @@ k_emit(const uint2 *__restrict__ rects, const float *__restrict__ depths, const 
 #endif
 // Resident CTAs per SM the radix downsweep is compiled for (register budget).
 #ifndef GSR_RT_MIN_BLOCKS
-#define GSR_RT_MIN_BLOCKS 4
+#define GSR_RT_MIN_BLOCKS 3
 #endif
 constexpr int kRtThreads = 256;
 constexpr int kRtItemsDepth = GSR_RT_ITEMS_DEPTH;
@@ -558,12 +560,20 @@ k_radix_upsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, uint
     const uint32_t dmask = (1u << g.width) - 1u;
     __shared__ uint32_t h[256];
     h[threadIdx.x] = 0;
-    __syncthreads();
+    // All of the thread's keys are loaded before the first shared-memory
+    // atomic, so their latencies overlap.
     const uint32_t base = blockIdx.x * (kRtThreads * kRtItems);
+    K kk[kRtItems];
 #pragma unroll
     for (int k = 0; k < kRtItems; ++k) {
         const uint32_t i = base + k * kRtThreads + threadIdx.x;
-        if (i < num) atomicAdd(&h[(uint32_t)(keys[i] >> g.shift) & dmask], 1u);
+        kk[k] = i < num ? keys[i] : (K)0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kRtItems; ++k) {
+        const uint32_t i = base + k * kRtThreads + threadIdx.x;
+        if (i < num) atomicAdd(&h[(uint32_t)(kk[k] >> g.shift) & dmask], 1u);
     }
     __syncthreads();
     if (threadIdx.x <= (int)dmask) {
@@ -617,7 +627,7 @@ k_radix_scan(PassSpec ps, int ntiles, const uint32_t *__restrict__ counts, const
     }
 }
 
-template <typename K, int kRtItems>
+template <typename K, int kRtItems, int kWidth>
 __global__ void __launch_bounds__(kRtThreads, GSR_RT_MIN_BLOCKS)
 k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, const uint32_t *__restrict__ offsets)
 {
@@ -628,8 +638,8 @@ k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, co
     const uint32_t *__restrict__ vin = vals_of(bufs, g.src);
     K *__restrict__ kout = keys_of(bufs, g.dst);
     uint32_t *__restrict__ vout = vals_of(bufs, g.dst);
-    const int shift = g.shift, width = g.width;
-    const uint32_t radix = 1u << width, dmask = radix - 1u;
+    const int shift = g.shift;
+    constexpr uint32_t radix = 1u << kWidth, dmask = radix - 1u;
 
     __shared__ uint32_t wcnt[8][256];   // per-warp digit counts, then per-warp prefixes
     __shared__ uint32_t s_lstart[256];  // start of each digit's run in the staged tile
@@ -640,41 +650,53 @@ k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, co
     __shared__ uint32_t s_vals[kRtTile];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int k = tid; k < 8 * 256; k += kRtThreads) (&wcnt[0][0])[k] = 0;
-    s_goff[tid] = tid < (int)radix ? offsets[(size_t)tid * ntiles + blockIdx.x] : 0u;
-    __syncthreads();
     const uint32_t tbase = blockIdx.x * kRtTile;
     const uint32_t tcount = min((uint32_t)kRtTile, num - tbase);
 
-    // Warp w owns keys [w*256, w*256+256) of the tile and walks them in 8 rounds
-    // of 32; equal digits are ranked by lane within a round and by per-warp
-    // counters across rounds.
-    const uint32_t lanemask_lt = (1u << lane) - 1u;
+    // Warp w owns keys [w*256, w*256+256) of the tile.  They are all loaded
+    // first (their latencies overlap), then ranked in 8 rounds of 32: equal
+    // digits are ranked by lane within a round and by per-warp counters,
+    // updated by each digit's lowest lane, across rounds.
     const uint32_t wbase = warp * (32 * kRtItems);
     K key[kRtItems];
     uint32_t val[kRtItems], rank[kRtItems];
 #pragma unroll
     for (int k = 0; k < kRtItems; ++k) {
         const uint32_t i = wbase + k * 32 + lane;
-        const bool valid = i < tcount;
-        key[k] = valid ? kin[tbase + i] : (K)0;
-        val[k] = valid ? vin[tbase + i] : 0u;
+        key[k] = i < tcount ? kin[tbase + i] : (K)0;
+        val[k] = i < tcount ? vin[tbase + i] : 0u;
+    }
+    if (tid < (int)radix) {
+#pragma unroll
+        for (int w = 0; w < 8; ++w) wcnt[w][tid] = 0;
+        s_goff[tid] = offsets[(size_t)tid * ntiles + blockIdx.x];
+    }
+    __syncthreads();
+    const uint32_t lanemask_lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int k = 0; k < kRtItems; ++k) {
+        const bool valid = wbase + k * 32 + lane < tcount;
         const uint32_t digit = (uint32_t)(key[k] >> shift) & dmask;
-        const uint32_t peers = digit_peers(__ballot_sync(kFull, valid), digit, width);
-        const uint32_t prior = valid ? wcnt[warp][digit] : 0u;
-        __syncwarp();
+        const uint32_t peers = digit_peers<kWidth>(__ballot_sync(kFull, valid), digit);
         const uint32_t before = __popc(peers & lanemask_lt);
-        if (valid && before == 0) wcnt[warp][digit] = prior + __popc(peers);
+        uint32_t prior = 0;
+        if (valid && before == 0) {
+            prior = wcnt[warp][digit];
+            wcnt[warp][digit] = prior + __popc(peers);
+        }
+        prior = __shfl_sync(kFull, prior, valid ? __ffs(peers) - 1 : lane);
         __syncwarp();
         rank[k] = prior + before;
     }
     __syncthreads();
     uint32_t tot = 0;
+    if (tid < (int)radix) {
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        const uint32_t t = wcnt[w][tid];
-        wcnt[w][tid] = tot;
-        tot += t;
+        for (int w = 0; w < 8; ++w) {
+            const uint32_t t = wcnt[w][tid];
+            wcnt[w][tid] = tot;
+            tot += t;
+        }
     }
     uint32_t all;
     s_lstart[tid] = block_exclusive_scan_256<uint32_t>(tot, ws, &all);
@@ -690,6 +712,7 @@ k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, co
         }
     }
     __syncthreads();
+#pragma unroll 4
     for (uint32_t i = tid; i < tcount; i += kRtThreads) {
         const K kk = s_keys[i];
         const uint32_t digit = (uint32_t)(kk >> shift) & dmask;
@@ -817,6 +840,28 @@ int grow_sort_buffers(gsr_ctx *ctx, SortBuffers<K> &b, size_t *cap, size_t need,
         if (_rc) return _rc;                                                          \
     } while (0)
 
+// The downsweep compiled for digit width `width` (1..8 bits).
+template <typename K, int kRtItems>
+int launch_downsweep(gsr_ctx *ctx, int width, int ntiles, cudaStream_t stream, SortBuffers<K> bufs, uint32_t num,
+                     PassSpec ps, const uint32_t *offsets)
+{
+    auto go = [&](auto kernel) {
+        return cuda_check(ctx, launch_kernel(ctx, kernel, dim3(ntiles), dim3(kRtThreads), stream, bufs, num, ps,
+                                             ntiles, offsets),
+                          "kernel launch");
+    };
+    switch (width) {
+    case 1: return go(k_radix_downsweep<K, kRtItems, 1>);
+    case 2: return go(k_radix_downsweep<K, kRtItems, 2>);
+    case 3: return go(k_radix_downsweep<K, kRtItems, 3>);
+    case 4: return go(k_radix_downsweep<K, kRtItems, 4>);
+    case 5: return go(k_radix_downsweep<K, kRtItems, 5>);
+    case 6: return go(k_radix_downsweep<K, kRtItems, 6>);
+    case 7: return go(k_radix_downsweep<K, kRtItems, 7>);
+    default: return go(k_radix_downsweep<K, kRtItems, 8>);
+    }
+}
+
 // Stable LSD sort of bufs buffer 0 into buffer 1 over the key bits
 // [key_lo, key_hi).  and_or: the device AND / OR of the keys.  host_and_or:
 // the same two values already on the host, or null; with them only the passes
@@ -826,6 +871,7 @@ int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int 
                const unsigned long long *and_or, const unsigned long long *host_and_or, uint32_t *totals,
                cudaStream_t stream)
 {
+    int rc;
     constexpr int kRtTile = kRtThreads * kRtItems;
     const int ntiles = (int)((num + kRtTile - 1) / kRtTile);
     // [256][ntiles] counts, then [256][ntiles] offsets (sized by bin_splats).
@@ -837,7 +883,6 @@ int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int 
         field_pass(host_and_or[0] ^ host_and_or[1], key_lo, key_hi, -1, &executed);
         if (executed == 0) {
             // No digit varies: the input order is the sorted order.
-            int rc;
             if ((rc = cuda_check(ctx, cudaMemcpyAsync(bufs.k[1], bufs.k[0], (size_t)num * sizeof(K),
                                                       cudaMemcpyDeviceToDevice, stream), "cudaMemcpyAsync")) ||
                 (rc = cuda_check(ctx, cudaMemcpyAsync(bufs.v[1], bufs.v[0], (size_t)num * sizeof(uint32_t),
@@ -860,8 +905,7 @@ int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int 
         GSR_LAUNCH(ctx, k_radix_upsweep<K, kRtItems>, dim3(ntiles), dim3(kRtThreads), stream, bufs, num, ps, ntiles, counts,
                    tot);
         GSR_LAUNCH(ctx, k_radix_scan, dim3(1 << w), dim3(kRtThreads), stream, ps, ntiles, counts, tot, offsets);
-        GSR_LAUNCH(ctx, k_radix_downsweep<K, kRtItems>, dim3(ntiles), dim3(kRtThreads), stream, bufs, num, ps, ntiles,
-                   offsets);
+        if ((rc = launch_downsweep<K, kRtItems>(ctx, w, ntiles, stream, bufs, num, ps, offsets))) return rc;
     }
     if (!host_and_or)
         GSR_LAUNCH(ctx, k_copy_if_unsorted<K>, dim3(std::min(ntiles, 1024)), dim3(256), stream, bufs, num, and_or,
