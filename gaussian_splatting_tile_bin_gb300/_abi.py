@@ -63,6 +63,8 @@ def _load():
     lib.gsr_rasterize_backward.restype = ctypes.c_int
     lib.gsr_get_bin_stats.argtypes = [P, ctypes.POINTER(_BinStats)]
     lib.gsr_get_bin_stats.restype = ctypes.c_int
+    lib.gsr_exp_neg.argtypes = [P, P, P, i32, P]
+    lib.gsr_exp_neg.restype = ctypes.c_int
     return lib
 
 
@@ -146,6 +148,17 @@ class Bins:
     def tile_ranges(self) -> torch.Tensor:
         tx, ty = self.tiles
         return self._view(self.raw.tile_ranges, (tx * ty, 2), "<i4")
+
+
+def exp_neg(ctx: Context, s: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    """The raster kernels' exp(-s) on a device array (diagnostic)."""
+    _need(s, "s", torch.float32)
+    if out is None:
+        out = torch.empty_like(s)
+    _need(out, "out", torch.float32, tuple(s.shape))
+    ctx._check(lib.gsr_exp_neg(ctx._h, ctypes.c_void_p(s.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                               int(s.numel()), _stream_ptr(stream, s.device)))
+    return out
 
 
 def _stream_ptr(stream, device):

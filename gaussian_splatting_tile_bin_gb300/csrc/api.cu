@@ -230,6 +230,19 @@ int gsr_get_bin_stats(gsr_ctx *ctx, gsr_bin_stats *out)
     return GSR_OK;
 }
 
+int gsr_exp_neg(gsr_ctx *ctx, const float *s, float *out, int32_t n, void *stream)
+{
+    if (!ctx) return GSR_ERR_INVALID_ARG;
+    ctx->err.clear();
+    if (n < 0) return fail(ctx, GSR_ERR_INVALID_ARG, "n < 0");
+    if (n > 0 && (!s || !out)) return fail(ctx, GSR_ERR_INVALID_ARG, "s/out is NULL");
+    if (!aligned(s, 4) || !aligned(out, 4)) return fail(ctx, GSR_ERR_INVALID_ARG, "s/out must be 4-byte aligned");
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, GSR_ERR_CUDA, "cannot select the context's device");
+    if (n == 0) return GSR_OK;
+    return gsr::exp_neg_eval(ctx, s, out, n, (cudaStream_t)stream);
+}
+
 }  // extern "C"
 
 static_assert(sizeof(gsr_splat2d) == 36, "Splat2D is 9 floats");

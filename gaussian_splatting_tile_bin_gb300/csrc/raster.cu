@@ -161,14 +161,40 @@ __device__ __forceinline__ float splat_sigma(const float4 geo, const float c, fl
     return __fadd_rn(__fmul_rn(0.5f, q), __fmul_rn(__fmul_rn(geo.w, dx), dy));
 }
 
+// exp(-s) for 0 <= s <= 5.55 as 2^(-s log2 e), by Cody and Waite's argument
+// splitting: log2 e = L2E + L2E_LO with L2E the float nearest to it, the product
+// t = -s L2E rounded, and its rounding error plus -s L2E_LO (an FMA and a
+// product) kept as r, so t + r carries -s log2 e to well below an ulp.  2^t is
+// the hardware base-2 approximation, and 2^(t + r) = 2^t (1 + r ln 2) to first
+// order (|r| < 2^-21).  Over every float s in [0, 5.55] the result is within
+// 3 ulp (relative 2e-7) of the correctly rounded exp(-s).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float exp_neg(float s)
+{
+    constexpr float L2E = 1.44269502f;               // log2(e) rounded to float
+    constexpr float L2E_LO = 1.925963033500011e-08f;  // log2(e) - L2E
+    constexpr float LN2 = 0.693147182f;
+    const float t = __fmul_rn(-s, L2E);
+    const float r = __fadd_rn(__fmaf_rn(-s, L2E, -t), __fmul_rn(-s, L2E_LO));
+    const float e = ex2_approx(t);
+    return __fmaf_rn(e, __fmul_rn(r, LN2), e);
+}
+
 // alpha = min(0.999, color_a exp(-sigma)) ("A.9 f16 forward", snippet); also
-// returns exp(-sigma) and the unclamped product for the backward.  expf is the
-// accurate exponential (within 2 ulp): a deep pixel's colour error grows with the
-// sum of its alphas times the per-splat alpha error, and the 1e-5 forward
-// tolerance leaves no room for the approximate one.
+// returns exp(-sigma) and the unclamped product for the backward.  The
+// exponential must be accurate to a few ulp: a deep pixel's colour error grows
+// with the sum of its alphas times the per-splat alpha error, and the 1e-5
+// forward tolerance leaves no room for a plain hardware approximation, whose
+// error grows with the argument.
 __device__ __forceinline__ float splat_alpha(float sigma, float o, float &e, float &raw)
 {
-    e = expf(-sigma);
+    e = exp_neg(sigma);
     raw = __fmul_rn(o, e);
     return fminf(kAlphaMax, raw);
 }
@@ -506,6 +532,25 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
     }
     ctx->grad_acc_zero = true;
     return GSR_OK;
+}
+
+// --- the exponential on its own (diagnostic) --------------------------------------
+
+namespace {
+
+__global__ void k_exp_neg(const float *__restrict__ s, float *__restrict__ out, int n)
+{
+    grid_dependency_begin();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) out[i] = exp_neg(s[i]);
+}
+
+}  // namespace
+
+int exp_neg_eval(gsr_ctx *ctx, const float *s, float *out, int32_t n, cudaStream_t stream)
+{
+    const int blocks = (int)std::min<size_t>(((size_t)n + 255) / 256, (size_t)SM_BLOCKS_CAP);
+    return cuda_check(ctx, launch_kernel(ctx, k_exp_neg, dim3(blocks), dim3(256), stream, s, out, (int)n),
+                      "exp launch");
 }
 
 // --- backward without allocation ---------------------------------------------

@@ -210,6 +210,14 @@ typedef struct gsr_bin_stats {
 } gsr_bin_stats;
 int gsr_get_bin_stats(gsr_ctx *ctx, gsr_bin_stats *out);
 
+/* Diagnostic: out[i] = exp(-s[i]) computed by the exponential the raster
+ * kernels use for alpha = min(0.999, color_a exp(-sigma)) ("A.9 f16 forward",
+ * snippet), for 0 <= s[i] <= 5.55 (the only arguments the kernels pass it).
+ *   s, out  device, [n] float (4-byte aligned); n >= 0
+ * Enqueued on `stream`; nothing is allocated.  GSR_ERR_INVALID_ARG for a NULL
+ * or misaligned pointer or n < 0. */
+int gsr_exp_neg(gsr_ctx *ctx, const float *s, float *out, int32_t n, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
