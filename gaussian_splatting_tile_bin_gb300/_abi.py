@@ -27,7 +27,8 @@ class GsrError(RuntimeError):
 
 class _Bins(ctypes.Structure):
     _fields_ = [("keys", ctypes.c_void_p), ("sorted_idx", ctypes.c_void_p),
-                ("tile_ranges", ctypes.c_void_p), ("num_pairs", ctypes.c_uint32),
+                ("tile_ranges", ctypes.c_void_p), ("tile_order", ctypes.c_void_p),
+                ("num_pairs", ctypes.c_uint32),
                 ("n", ctypes.c_int32), ("width", ctypes.c_int32), ("height", ctypes.c_int32),
                 ("tiles_x", ctypes.c_int32), ("tiles_y", ctypes.c_int32)]
 
@@ -144,6 +145,11 @@ class Bins:
 
     def sorted_idx(self) -> torch.Tensor:
         return self._view(self.raw.sorted_idx, (self.num_pairs,), "<i4")
+
+    def tile_order(self) -> torch.Tensor:
+        """Launch order of the tiles (longest lists first)."""
+        tx, ty = self.tiles
+        return self._view(self.raw.tile_order, (tx * ty,), "<i4")
 
     def tile_ranges(self) -> torch.Tensor:
         tx, ty = self.tiles

@@ -102,6 +102,7 @@ void gsr_destroy(gsr_ctx *ctx)
         cudaFree(ctx->radix_totals);
         cudaFree(ctx->scalars);
         cudaFree(ctx->grad_acc);
+        cudaFree(ctx->bwd_tile_cost);
         if (ctx->host_total) cudaFreeHost(ctx->host_total);
     }
     delete ctx;

@@ -772,6 +772,56 @@ k_extract_ranges(const uint64_t *__restrict__ keys, uint32_t num, uint32_t *__re
     }
 }
 
+// --- launch order of the tiles -----------------------------------------------
+
+// 0 for no work, else 1 + floor(8 log2 c): 256 classes a factor 2^(1/8) apart
+// (the approximate log2 only moves a tile between neighbouring classes).
+__device__ __forceinline__ int cost_class(uint32_t c)
+{
+    return c == 0 ? 0 : min(255, 1 + (int)(8.0f * __log2f((float)c)));
+}
+
+// One block: a counting sort of the tiles by cost class, largest first.
+__global__ void __launch_bounds__(1024)
+k_tile_order(const uint2 *__restrict__ ranges, const uint32_t *__restrict__ costs, int num_tiles,
+             uint32_t *__restrict__ order)
+{
+    grid_dependency_begin();
+    __shared__ uint32_t s_hist[256];
+    __shared__ uint32_t s_cursor[256];
+    if (threadIdx.x < 256) s_hist[threadIdx.x] = 0;
+    __syncthreads();
+    auto cost_of = [&](int t) { return ranges ? ranges[t].y - ranges[t].x : costs[t]; };
+    for (int t = threadIdx.x; t < num_tiles; t += blockDim.x) atomicAdd(&s_hist[cost_class(cost_of(t))], 1u);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        // Exclusive scan over the classes from the largest down: lane l owns
+        // classes 255 - 8l down to 248 - 8l.
+        const int lane = threadIdx.x;
+        uint32_t local[8], sum = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            local[k] = s_hist[255 - (8 * lane + k)];
+            sum += local[k];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += t;
+        }
+        uint32_t run = incl - sum;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            s_cursor[255 - (8 * lane + k)] = run;
+            run += local[k];
+        }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < num_tiles; t += blockDim.x)
+        order[atomicAdd(&s_cursor[cost_class(cost_of(t))], 1u)] = (uint32_t)t;
+}
+
 int bits_for(uint64_t v)
 {
     int b = 0;
@@ -949,7 +999,9 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     unsigned long long *blk_pairs = ctx->blk_sums;
     unsigned long long *blk_emit = ctx->blk_sums + ctx->cap_blocks;
     unsigned long long *blk_sorted = ctx->blk_sums + 2 * ctx->cap_blocks;
-    if ((rc = grow(ctx, &ctx->ranges, &ctx->cap_tiles, num_tiles, 2, "tile ranges"))) return rc;
+    // Per tile: {start, end}, then the launch order after all tiles' ranges.
+    if ((rc = grow(ctx, &ctx->ranges, &ctx->cap_tiles, num_tiles, 3, "tile ranges"))) return rc;
+    ctx->tile_order = ctx->ranges + 2 * ctx->cap_tiles;
 
     // 1. counts, totals; read the pair total and the emitting count.
     uint64_t total = 0, emitting = 0;
@@ -1041,6 +1093,9 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
                    ctx->ranges);
     }
 
+    // 7. the forward's launch order: longest tile lists first.
+    if ((rc = launch_tile_order(ctx, ctx->ranges, nullptr, (int)num_tiles, ctx->tile_order, stream))) return rc;
+
     ctx->last_stream = stream;
     ctx->last_pairs = num;
     ctx->last_emitting = (uint32_t)m;
@@ -1048,6 +1103,7 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     out->keys = ctx->pairs.k[1];
     out->sorted_idx = ctx->pairs.v[1];
     out->tile_ranges = ctx->ranges;
+    out->tile_order = ctx->tile_order;
     out->num_pairs = num;
     out->n = n;
     out->width = width;
@@ -1080,6 +1136,15 @@ int bin_pass_masks(gsr_ctx *ctx, uint32_t *depth_mask, uint32_t *tile_mask, int 
         if (field_varies(sc[kScalarKeyAnd] ^ sc[kScalarKeyOr], sh, w)) *tile_mask |= 1u << f;
     }
     return GSR_OK;
+}
+
+int launch_tile_order(gsr_ctx *ctx, const uint32_t *ranges, const uint32_t *costs, int num_tiles, uint32_t *order,
+                      cudaStream_t stream)
+{
+    if (num_tiles <= 0) return GSR_OK;
+    return cuda_check(ctx, launch_kernel(ctx, k_tile_order, dim3(1), dim3(1024), stream,
+                                         reinterpret_cast<const uint2 *>(ranges), costs, num_tiles, order),
+                      "tile order launch");
 }
 
 }  // namespace gsr

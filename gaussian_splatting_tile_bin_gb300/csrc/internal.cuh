@@ -46,6 +46,10 @@ struct gsr_ctx {
     unsigned long long *blk_sums = nullptr;     // [3 * cap_blocks]: see bin.cu
     size_t cap_tiles = 0;
     uint32_t *ranges = nullptr;                 // [2 * cap_tiles]
+    uint32_t *tile_order = nullptr;             // [cap_tiles] forward launch order (pair count)
+    size_t cap_bwd_tiles = 0;
+    uint32_t *bwd_tile_cost = nullptr;          // [cap_bwd_tiles] largest last_contributor per tile
+    uint32_t *bwd_tile_order = nullptr;         // [cap_bwd_tiles] backward launch order
     size_t cap_radix_tiles = 0;
     uint32_t *radix_counts = nullptr;           // [512 * cap_radix_tiles] digit counts and offsets
     uint32_t *radix_totals = nullptr;           // [2 * 4 * 256] digit totals of both sorts
@@ -100,6 +104,13 @@ cudaError_t launch_kernel(gsr_ctx *ctx, void (*kernel)(Params...), dim3 grid, di
 // Records a CUDA error on the context; returns GSR_ERR_CUDA (or GSR_OK).
 int cuda_check(gsr_ctx *ctx, cudaError_t e, const char *what);
 int fail(gsr_ctx *ctx, int code, const std::string &msg);
+
+// Writes into order[0, num_tiles) every tile index once, tiles of larger cost
+// first.  cost: the tile's list length from ranges (uint2 per tile) when
+// ranges is set, else costs[tile].  Ties and near-ties (costs within one of 256
+// logarithmic classes) come in any order.
+int launch_tile_order(gsr_ctx *ctx, const uint32_t *ranges, const uint32_t *costs, int num_tiles, uint32_t *order,
+                      cudaStream_t stream);
 
 // Host sides of the three operations (validated arguments).
 int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n, int32_t width,

@@ -204,14 +204,14 @@ __device__ __forceinline__ float splat_alpha(float sigma, float o, float &e, flo
 template <bool kCull>
 __global__ void __launch_bounds__(kTilePixels, GSR_FWD_MIN_BLOCKS)
 k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
-          const uint2 *__restrict__ ranges, int width, int height, int tiles_x,
-          float4 *__restrict__ out_rgbw, float *__restrict__ final_T, uint32_t *__restrict__ last_out)
+          const uint2 *__restrict__ ranges, const uint32_t *__restrict__ order, int width, int height,
+          int tiles_x, float4 *__restrict__ out_rgbw, float *__restrict__ final_T, uint32_t *__restrict__ last_out)
 {
     grid_dependency_begin();
     __shared__ StagedBatch sb;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t wbit = 1u << warp;
-    const int tile = blockIdx.x;
+    const int tile = order ? (int)order[blockIdx.x] : (int)blockIdx.x;
     const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
     const int x = x0 + pixel_x(threadIdx.x);
     const int y = y0 + pixel_y(threadIdx.x);
@@ -311,8 +311,8 @@ __device__ __forceinline__ void warp_reduce_add9(float (&v)[9], double *__restri
 template <bool kWarpSkip, bool kLastContrib, bool kCull>
 __global__ void __launch_bounds__(kTilePixels, GSR_BWD_MIN_BLOCKS)
 k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
-           const uint2 *__restrict__ ranges, int width, int height, int tiles_x,
-           const float4 *__restrict__ dl_dout, const float *__restrict__ final_T,
+           const uint2 *__restrict__ ranges, const uint32_t *__restrict__ order, int width, int height,
+           int tiles_x, const float4 *__restrict__ dl_dout, const float *__restrict__ final_T,
            const uint32_t *__restrict__ last_in, double *__restrict__ grad_acc)
 {
     grid_dependency_begin();
@@ -320,7 +320,7 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
     __shared__ uint32_t s_wmax[kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t wbit = 1u << warp;
-    const int tile = blockIdx.x;
+    const int tile = order ? (int)order[blockIdx.x] : (int)blockIdx.x;
     const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
     const int x = x0 + pixel_x(threadIdx.x);
     const int y = y0 + pixel_y(threadIdx.x);
@@ -441,36 +441,58 @@ __global__ void k_grad_to_float(double *__restrict__ acc, float *__restrict__ gr
 
 template <bool kSkip, bool kLc>
 cudaError_t launch_backward_cull(gsr_ctx *ctx, bool cull, int grid, cudaStream_t stream, const float *splats,
-                                 const gsr_bins *bins, const float *dl_dout, const float *final_T,
-                                 const uint32_t *last_contrib, double *acc)
+                                 const gsr_bins *bins, const uint32_t *order, const float *dl_dout,
+                                 const float *final_T, const uint32_t *last_contrib, double *acc)
 {
     auto go = [&](auto kernel) {
         return launch_kernel(ctx, kernel, dim3(grid), dim3(kTilePixels), stream, splats, bins->sorted_idx,
-                             reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width, bins->height,
-                             bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T, last_contrib,
-                             acc);
+                             reinterpret_cast<const uint2 *>(bins->tile_ranges), order, bins->width,
+                             bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
+                             last_contrib, acc);
     };
     return cull ? go(k_backward<kSkip, kLc, true>) : go(k_backward<kSkip, kLc, false>);
 }
 
-// The backward kernel variant the context's options select, accumulating into acc.
+// The backward kernel variant the context's options select, launching tiles
+// in `order` (NULL: tile order) and accumulating into acc.
 cudaError_t launch_backward(gsr_ctx *ctx, cudaStream_t stream, const float *splats, const gsr_bins *bins,
-                            const float *dl_dout, const float *final_T, const uint32_t *last_contrib,
-                            double *acc)
+                            const uint32_t *order, const float *dl_dout, const float *final_T,
+                            const uint32_t *last_contrib, double *acc)
 {
     const int grid = bins->tiles_x * bins->tiles_y;
     const bool cull = ctx->opt_warp_cull != 0;
     if (ctx->opt_warp_skip && ctx->opt_last_contrib)
-        return launch_backward_cull<true, true>(ctx, cull, grid, stream, splats, bins, dl_dout, final_T,
+        return launch_backward_cull<true, true>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
                                                 last_contrib, acc);
     if (ctx->opt_warp_skip)
-        return launch_backward_cull<true, false>(ctx, cull, grid, stream, splats, bins, dl_dout, final_T,
+        return launch_backward_cull<true, false>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
                                                  last_contrib, acc);
     if (ctx->opt_last_contrib)
-        return launch_backward_cull<false, true>(ctx, cull, grid, stream, splats, bins, dl_dout, final_T,
+        return launch_backward_cull<false, true>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
                                                  last_contrib, acc);
-    return launch_backward_cull<false, false>(ctx, cull, grid, stream, splats, bins, dl_dout, final_T,
+    return launch_backward_cull<false, false>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
                                               last_contrib, acc);
+}
+
+// Per tile: the largest last_contributor of its pixels (one warp per tile), the
+// backward's work bound for the tile and the key of its launch order.
+__global__ void __launch_bounds__(256)
+k_tile_cost(const uint32_t *__restrict__ last, int width, int height, int tiles_x, int num_tiles,
+            uint32_t *__restrict__ cost)
+{
+    grid_dependency_begin();
+    const int tile = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (tile >= num_tiles) return;  // whole warps
+    const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
+    const int y = y0 + (lane >> 1), xs = x0 + (lane & 1) * 8;
+    uint32_t m = 0;
+    if (y < height) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (xs + k < width) m = max(m, last[(size_t)y * width + xs + k]);
+    }
+    m = __reduce_max_sync(kFull, m);
+    if (lane == 0) cost[tile] = m;
 }
 
 }  // namespace
@@ -481,8 +503,9 @@ int rasterize_forward(gsr_ctx *ctx, const float *splats, const gsr_bins *bins, f
     const int num_tiles = bins->tiles_x * bins->tiles_y;
     auto go = [&](auto kernel) {
         return launch_kernel(ctx, kernel, dim3(num_tiles), dim3(kTilePixels), stream, splats, bins->sorted_idx,
-                             reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->width, bins->height,
-                             bins->tiles_x, reinterpret_cast<float4 *>(out_rgbw), final_T, last_contrib);
+                             reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->tile_order, bins->width,
+                             bins->height, bins->tiles_x, reinterpret_cast<float4 *>(out_rgbw), final_T,
+                             last_contrib);
     };
     return cuda_check(ctx, ctx->opt_warp_cull ? go(k_forward<true>) : go(k_forward<false>), "forward launch");
 }
@@ -518,9 +541,34 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
             return rc;
         ctx->grad_acc_zero = true;
     }
+    // Launch order: tiles with the largest last_contributor (the most work)
+    // first, so that no long tile starts late and runs on alone.
+    const int num_tiles = bins->tiles_x * bins->tiles_y;
+    if ((size_t)num_tiles > ctx->cap_bwd_tiles || !ctx->bwd_tile_cost) {
+        if (ctx->bwd_tile_cost) {
+            if ((rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize"))) return rc;
+            cudaFree(ctx->bwd_tile_cost);
+        }
+        ctx->bwd_tile_cost = ctx->bwd_tile_order = nullptr;
+        ctx->cap_bwd_tiles = 0;
+        const size_t cap = std::max<size_t>((size_t)num_tiles, 1);
+        if (cudaMalloc(&ctx->bwd_tile_cost, 2 * cap * sizeof(uint32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            ctx->bwd_tile_cost = nullptr;
+            return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the backward tile order");
+        }
+        ctx->bwd_tile_order = ctx->bwd_tile_cost + cap;
+        ctx->cap_bwd_tiles = cap;
+    }
+    if ((rc = cuda_check(ctx, launch_kernel(ctx, k_tile_cost, dim3((num_tiles + 7) / 8), dim3(256), stream,
+                                            last_contrib, bins->width, bins->height, bins->tiles_x, num_tiles,
+                                            ctx->bwd_tile_cost),
+                         "tile cost launch")) ||
+        (rc = launch_tile_order(ctx, nullptr, ctx->bwd_tile_cost, num_tiles, ctx->bwd_tile_order, stream)))
+        return rc;
     ctx->grad_acc_zero = false;
-    if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins, dl_dout, final_T, last_contrib,
-                                              ctx->grad_acc),
+    if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins, ctx->bwd_tile_order, dl_dout, final_T,
+                                              last_contrib, ctx->grad_acc),
                          "backward launch")))
         return rc;
     if (count > 0) {
@@ -594,7 +642,9 @@ int rasterize_backward_noalloc(gsr_ctx *ctx, const float *splats, int32_t n, con
     // The array keeps the previous call's sums: clear the part this call uses.
     int rc = cuda_check(ctx, cudaMemsetAsync(acc, 0, count * sizeof(double), stream), "cudaMemsetAsync");
     if (rc) return rc;
-    if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins, dl_dout, final_T, last_contrib, acc),
+    // No allocation here: the forward's launch order (pair count) from the bins.
+    if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins, bins->tile_order, dl_dout, final_T,
+                                              last_contrib, acc),
                          "backward launch")))
         return rc;
     if (count == 0) return GSR_OK;

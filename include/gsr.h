@@ -90,6 +90,9 @@ typedef struct gsr_bins {
     const uint32_t *sorted_idx;  /* device, [num_pairs], splat index of each key */
     const uint32_t *tile_ranges; /* device, [2 * tiles_x * tiles_y]: {start, end} per tile,
                                     {0, 0} for an empty tile */
+    const uint32_t *tile_order;  /* device, [tiles_x * tiles_y]: every tile index once, longest
+                                    lists first (by classes of pair count); the forward
+                                    launches its CTAs in this order.  NULL: tile order. */
     uint32_t num_pairs;          /* host copy of the pair count */
     int32_t n;                   /* splat count the bins were built from */
     int32_t width, height;       /* image size in pixels */

@@ -243,6 +243,38 @@ def test_dependent_launch_changes_nothing(gsr, ctx):
     assert np.allclose(on["grad"], off["grad"], rtol=1e-6, atol=1e-9)
 
 
+@pytest.mark.parametrize("name", ["lego_final", "stress"])
+def test_tile_order_is_a_longest_first_permutation(gsr, ctx, name):
+    """bins.tile_order holds every tile once, longest lists first: a tile may
+    precede a longer one only within the 2^(1/8) width of a cost class."""
+    wl = gen.make(name)
+    sp, dp = to_dev(wl.splats), to_dev(wl.depths)
+    bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+    order = bins.tile_order().cpu().numpy().view(np.uint32).astype(np.int64)
+    r = bins.tile_ranges().cpu().numpy().view(np.uint32).astype(np.int64)
+    lengths = (r[:, 1] - r[:, 0])[order]
+    assert np.array_equal(np.sort(order), np.arange(len(r)))
+    later_max = np.maximum.accumulate(lengths[::-1])[::-1]   # longest list at or after each position
+    assert np.all(later_max <= np.maximum(lengths * 2 ** 0.25, lengths + 1)), "a much longer tile comes later"
+
+
+def test_results_do_not_depend_on_tile_order(gsr, ctx):
+    """Bins without a launch order (NULL, e.g. built by a caller) give the same
+    forward bit for bit and the same gradients up to the order of their sums."""
+    wl = gen.lego_early()
+    sp, dp, dl = to_dev(wl.splats), to_dev(wl.depths), to_dev(wl.dl_dout)
+    bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+    out_a, t_a, l_a = [x.clone() for x in gsr.rasterize_forward(ctx, sp, bins)]
+    g_a = gsr.rasterize_backward(ctx, sp, bins, dl, t_a, l_a).clone()
+    bins.raw.tile_order = None
+    out_b, t_b, l_b = gsr.rasterize_forward(ctx, sp, bins)
+    torch.cuda.synchronize()
+    for a, b in ((out_a, out_b), (t_a, t_b), (l_a, l_b)):
+        assert torch.equal(a, b)
+    g_b = gsr.rasterize_backward(ctx, sp, bins, dl, t_b, l_b)
+    assert np.allclose(g_a.cpu().numpy(), g_b.cpu().numpy(), rtol=1e-6, atol=1e-9)
+
+
 def test_self_noise(gsr, ctx):
     """Run-to-run spread of the atomically accumulated gradients (the pages'
     self-noise protocol: 20 repeats, "M3 per-splat backward", section 2)."""
