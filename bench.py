@@ -452,6 +452,7 @@ def gpu_arm(args):
                        "height": wl.height, "pairs": int(pairs),
                        "l2": "flushed between timed steps (256 MB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "ms_per_step_median": float(np.median(tot_ms)), "ms_per_step_std": float(np.std(tot_ms)),
             "stages_ms": {"bin": float(bin_ms.mean()), "forward": float(fwd_ms.mean()),
                           "backward": float(bwd_ms.mean()),
                           "bin_median": float(np.median(bin_ms)),

@@ -847,7 +847,7 @@ int grow(gsr_ctx *ctx, T **ptr, size_t *cap, size_t need, size_t elems_per, cons
         *ptr = nullptr;
     }
     *cap = 0;
-    cudaError_t e = cudaMalloc((void **)ptr, std::max<size_t>(need, 1) * elems_per * sizeof(T));
+    cudaError_t e = device_alloc(ctx, (void **)ptr, std::max<size_t>(need, 1) * elems_per * sizeof(T));
     if (e != cudaSuccess) {
         cudaGetLastError();
         *ptr = nullptr;
@@ -874,8 +874,8 @@ int grow_sort_buffers(gsr_ctx *ctx, SortBuffers<K> &b, size_t *cap, size_t need,
     *cap = 0;
     need = std::max<size_t>(need, 1);
     for (int j = 0; j < 3; ++j) {
-        if (cudaMalloc(&b.k[j], need * sizeof(K)) != cudaSuccess ||
-            cudaMalloc(&b.v[j], need * sizeof(uint32_t)) != cudaSuccess) {
+        if (device_alloc(ctx, (void **)&b.k[j], need * sizeof(K)) != cudaSuccess ||
+            device_alloc(ctx, (void **)&b.v[j], need * sizeof(uint32_t)) != cudaSuccess) {
             cudaGetLastError();
             return fail(ctx, GSR_ERR_OOM, std::string("cudaMalloc failed for ") + what);
         }
@@ -974,18 +974,25 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     const size_t num_tiles = (size_t)tiles_x * tiles_y;
     const int key_hi = 32 + bits_for(num_tiles - 1);  // keys occupy bits [0, key_hi)
 
-    // Fixed-size scratch, allocated once.
-    if (!ctx->scalars) {
-        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->scalars, kScalarCount * sizeof(unsigned long long)),
-                             "cudaMalloc")))
-            return rc;
-        if ((rc = cuda_check(ctx, cudaHostAlloc(&ctx->host_total, 4 * sizeof(unsigned long long),
-                                                cudaHostAllocDefault),
-                             "cudaHostAlloc")))
-            return rc;
-        if ((rc = cuda_check(ctx, cudaMalloc(&ctx->radix_totals, 2 * 4 * 256 * sizeof(uint32_t)), "cudaMalloc")))
-            return rc;
-    }
+    // Fixed-size scratch, allocated once (each piece again if an earlier
+    // allocation of it failed).
+    auto alloc_failed = [&](cudaError_t e, const char *what) -> int {
+        if (e == cudaSuccess) return GSR_OK;
+        cudaGetLastError();
+        return fail(ctx, GSR_ERR_OOM, std::string("cudaMalloc failed for ") + what);
+    };
+    if (!ctx->scalars &&
+        (rc = alloc_failed(device_alloc(ctx, (void **)&ctx->scalars, kScalarCount * sizeof(unsigned long long)),
+                           "binning scalars")))
+        return rc;
+    if (!ctx->host_total &&
+        (rc = alloc_failed(cudaHostAlloc(&ctx->host_total, 4 * sizeof(unsigned long long), cudaHostAllocDefault),
+                           "pinned pair count")))
+        return rc;
+    if (!ctx->radix_totals &&
+        (rc = alloc_failed(device_alloc(ctx, (void **)&ctx->radix_totals, 2 * 4 * 256 * sizeof(uint32_t)),
+                           "radix digit totals")))
+        return rc;
     const int nblk = (n + kBinBlock - 1) / kBinBlock;
     if (!ctx->depth.k[0] || (size_t)n > ctx->cap_splats) {
         size_t cap = 0;

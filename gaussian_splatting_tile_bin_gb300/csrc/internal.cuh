@@ -35,6 +35,7 @@ struct gsr_ctx {
     int opt_last_contrib = 1;
     int opt_warp_cull = 1;
     int opt_pdl = 1;
+    int fail_next_alloc = 0;                    // test hook: the next device allocation fails
 
     // Grow-only arena.
     size_t cap_pairs = 0;
@@ -99,6 +100,18 @@ cudaError_t launch_kernel(gsr_ctx *ctx, void (*kernel)(Params...), dim3 grid, di
     cfg.numAttrs = 1;
     ++ctx->launches;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// cudaMalloc for the context's arena and scratch.  With the context's test
+// hook armed (GSR_OPT_FAIL_NEXT_ALLOC) it fails once, as an out-of-memory would.
+inline cudaError_t device_alloc(gsr_ctx *ctx, void **ptr, size_t bytes)
+{
+    if (ctx->fail_next_alloc) {
+        ctx->fail_next_alloc = 0;
+        *ptr = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(ptr, bytes);
 }
 
 // Records a CUDA error on the context; returns GSR_ERR_CUDA (or GSR_OK).

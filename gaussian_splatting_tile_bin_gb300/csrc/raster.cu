@@ -525,7 +525,7 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
         ctx->grad_acc = nullptr;
         ctx->cap_grad_acc = 0;
         const size_t cap = std::max<size_t>(count, 1);
-        if (cudaMalloc(&ctx->grad_acc, cap * sizeof(double)) != cudaSuccess) {
+        if (device_alloc(ctx, (void **)&ctx->grad_acc, cap * sizeof(double)) != cudaSuccess) {
             cudaGetLastError();
             return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the gradient accumulator");
         }
@@ -552,7 +552,7 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
         ctx->bwd_tile_cost = ctx->bwd_tile_order = nullptr;
         ctx->cap_bwd_tiles = 0;
         const size_t cap = std::max<size_t>((size_t)num_tiles, 1);
-        if (cudaMalloc(&ctx->bwd_tile_cost, 2 * cap * sizeof(uint32_t)) != cudaSuccess) {
+        if (device_alloc(ctx, (void **)&ctx->bwd_tile_cost, 2 * cap * sizeof(uint32_t)) != cudaSuccess) {
             cudaGetLastError();
             ctx->bwd_tile_cost = nullptr;
             return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the backward tile order");

@@ -75,9 +75,12 @@ enum {
     GSR_OPT_BWD_LAST_CONTRIB = 2, /* stop each warp at its largest last_contributor */
     GSR_OPT_WARP_CULL = 3,        /* forward and backward: a warp skips splats whose alpha >= 1/255
                                      ellipse misses its 8x4 pixel block (same results) */
-    GSR_OPT_PDL = 4               /* launch kernels with programmatic dependent launch: a kernel may
+    GSR_OPT_PDL = 4,              /* launch kernels with programmatic dependent launch: a kernel may
                                      begin launching while the one before it in the stream drains,
                                      and waits for it before touching memory (same results) */
+    GSR_OPT_FAIL_NEXT_ALLOC = 5   /* test hook (default 0): the context's next device allocation
+                                     fails as if the GPU were out of memory; the call returns
+                                     GSR_ERR_OOM and later calls allocate normally */
 };
 
 typedef struct gsr_ctx gsr_ctx;
