@@ -241,27 +241,29 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
             while (m) {
                 const int j = c0 + __ffs(m) - 1;
                 m &= m - 1;
-                if (done) continue;
+                // Straight-line: every lane evaluates the splat and the predicates
+                // take the pixel's skip, stop and composite decisions.
                 const float4 geo = sb.geo[j];
                 const float4 aux = sb.aux[j];
+                const float4 c = sb.rgb[j];
                 float dx, dy;
                 const float sigma = splat_sigma(geo, aux.x, px, py, dx, dy);
-                if (!(sigma >= 0.0f) || !(sigma < aux.z)) continue;
+                const bool in_range = !done && sigma >= 0.0f && sigma < aux.z;
                 float e, raw;
-                const float alpha = splat_alpha(sigma, aux.y, e, raw);
-                if (alpha < kAlphaMin) continue;
+                const float alpha = splat_alpha(in_range ? sigma : 0.0f, aux.y, e, raw);
+                const bool ok = in_range && alpha >= kAlphaMin;
                 const float next_T = __fmul_rn(T, __fsub_rn(1.0f, alpha));
-                if (next_T < kTMin) {
-                    done = true;
-                    continue;
-                }
+                const bool stop = ok && next_T < kTMin;
+                const bool comp = ok && !stop;
                 const float w = __fmul_rn(alpha, T);
-                const float4 c = sb.rgb[j];
-                C.x = __fadd_rn(C.x, __fmul_rn(c.x, w));
-                C.y = __fadd_rn(C.y, __fmul_rn(c.y, w));
-                C.z = __fadd_rn(C.z, __fmul_rn(c.z, w));
-                T = next_T;
-                last = bstart - range.x + (uint32_t)j + 1u;
+                if (comp) {
+                    C.x = __fadd_rn(C.x, __fmul_rn(c.x, w));
+                    C.y = __fadd_rn(C.y, __fmul_rn(c.y, w));
+                    C.z = __fadd_rn(C.z, __fmul_rn(c.z, w));
+                    T = next_T;
+                    last = bstart - range.x + (uint32_t)j + 1u;
+                }
+                done = done || stop;
             }
             if (__all_sync(kFull, done)) break;
         }
@@ -372,52 +374,45 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                 m &= ~(1u << bit);
                 const int j = c0 + bit;
                 const uint32_t rel = (uint32_t)(bstart + j);
-                bool contrib = false;
+                // Straight-line: every lane evaluates the splat and the predicates
+                // select (no divergent branches in the warp's loop body).
+                const float4 geo = sb.geo[j];
+                const float4 aux = sb.aux[j];
+                const float4 c = sb.rgb[j];
+                float dx, dy;
+                const float sigma = splat_sigma(geo, aux.x, px, py, dx, dy);
+                const bool in_range = rel < L && sigma >= 0.0f && sigma < aux.z;
+                float e, raw;
+                const float alpha = splat_alpha(in_range ? sigma : 0.0f, aux.y, e, raw);
+                const bool contrib = in_range && alpha >= kAlphaMin;
+                const float one_m = __fsub_rn(1.0f, alpha);
+                const float inv = __fdividef(1.0f, one_m);
+                float Tj = T * inv;
+                Tj = __fmaf_rn(inv, __fmaf_rn(-one_m, Tj, T), Tj);
+                const float aT = alpha * Tj;
                 float v[9];
+                v[5] = g.x * aT;
+                v[6] = g.y * aT;
+                v[7] = g.z * aT;
+                float dA = g.x * (c.x * Tj - S.x * inv);
+                dA = __fmaf_rn(g.y, c.y * Tj - S.y * inv, dA);
+                dA = __fmaf_rn(g.z, c.z * Tj - S.z * inv, dA);
+                const float dRaw = raw < kAlphaMax ? dA : 0.0f;
+                v[8] = dRaw * e;
+                const float dSig = -dRaw * raw;
+                const float a = geo.z, bb = geo.w, cc = aux.x;
+                v[0] = -dSig * __fmaf_rn(a, dx, bb * dy);
+                v[1] = -dSig * __fmaf_rn(bb, dx, cc * dy);
+                v[2] = dSig * (0.5f * dx * dx);
+                v[3] = dSig * (dx * dy);
+                v[4] = dSig * (0.5f * dy * dy);
 #pragma unroll
-                for (int k = 0; k < 9; ++k) v[k] = 0.0f;
-                if (rel < L) {
-                    const float4 geo = sb.geo[j];
-                    const float4 aux = sb.aux[j];
-                    float dx, dy;
-                    const float sigma = splat_sigma(geo, aux.x, px, py, dx, dy);
-                    if (sigma >= 0.0f && sigma < aux.z) {
-                        float e, raw;
-                        const float alpha = splat_alpha(sigma, aux.y, e, raw);
-                        if (alpha >= kAlphaMin) {
-                            contrib = true;
-                            const float4 c = sb.rgb[j];
-                            const float one_m = __fsub_rn(1.0f, alpha);
-                            const float inv = __fdividef(1.0f, one_m);
-                            // Transmittance in front of this splat: the forward's
-                            // T_j (1 - alpha) undone by T / (1 - alpha), a reciprocal
-                            // refined by one Newton step on the exact residual (an
-                            // FMA), so a pixel replayed through hundreds of splats
-                            // drifts by about a rounding per splat.
-                            float Tj = T * inv;
-                            Tj = __fmaf_rn(inv, __fmaf_rn(-one_m, Tj, T), Tj);
-                            const float aT = alpha * Tj;
-                            v[5] = g.x * aT;
-                            v[6] = g.y * aT;
-                            v[7] = g.z * aT;
-                            float dA = g.x * (c.x * Tj - S.x * inv);
-                            dA = __fmaf_rn(g.y, c.y * Tj - S.y * inv, dA);
-                            dA = __fmaf_rn(g.z, c.z * Tj - S.z * inv, dA);
-                            S.x = __fmaf_rn(c.x, aT, S.x);
-                            S.y = __fmaf_rn(c.y, aT, S.y);
-                            S.z = __fmaf_rn(c.z, aT, S.z);
-                            const float dRaw = raw < kAlphaMax ? dA : 0.0f;
-                            v[8] = dRaw * e;
-                            const float dSig = -dRaw * raw;
-                            const float a = geo.z, b = geo.w, cc = aux.x;
-                            v[0] = -dSig * __fmaf_rn(a, dx, b * dy);
-                            v[1] = -dSig * __fmaf_rn(b, dx, cc * dy);
-                            v[2] = dSig * (0.5f * dx * dx);
-                            v[3] = dSig * (dx * dy);
-                            v[4] = dSig * (0.5f * dy * dy);
-                            T = Tj;
-                        }
-                    }
+                for (int k = 0; k < 9; ++k) v[k] = contrib ? v[k] : 0.0f;
+                if (contrib) {
+                    S.x = __fmaf_rn(c.x, aT, S.x);
+                    S.y = __fmaf_rn(c.y, aT, S.y);
+                    S.z = __fmaf_rn(c.z, aT, S.z);
+                    T = Tj;
                 }
                 // "W1 warp sparse skip": with no contributing lane every sum is +0.
                 if (kWarpSkip && !__any_sync(kFull, contrib)) continue;

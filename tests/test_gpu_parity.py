@@ -96,6 +96,26 @@ def test_ragged_images(gsr, ctx, w, h):
     _full(gsr, ctx, _random(600, w, h, w * 1000 + h))
 
 
+def test_maximum_image_side(gsr, ctx):
+    """The widest image the API takes (2^19 px, 32768 tiles in a row): tile
+    coordinates at the top of their 16-bit packing, 15-bit tile ids, splats
+    over both ends of the strip."""
+    w, h, n = 1 << 19, 16, 64
+    rng = np.random.Generator(np.random.PCG64(11))
+    s = np.zeros((n, 9), dtype=np.float32)
+    s[:, 0] = np.concatenate([rng.uniform(-20, 60, 16), rng.uniform(w - 60, w + 20, 16), rng.uniform(0, w, 32)])
+    s[:, 1] = rng.uniform(-4, h + 4, n)
+    std = rng.uniform(0.5, 6.0, n)
+    s[:, 2] = 1.0 / std ** 2
+    s[:, 3] = rng.uniform(-0.3, 0.3, n) / std ** 2
+    s[:, 4] = 1.0 / std ** 2
+    s[:, 5:8] = rng.uniform(0, 1, (n, 3))
+    s[:, 8] = rng.uniform(0.05, 1.0, n)
+    d = rng.uniform(0.5, 20.0, n).astype(np.float32)
+    g, o, fs, bs = _full(gsr, ctx, gen.from_arrays("max_side", w, h, s, d, seed=12))
+    assert int(o["keys"].max() >> 32) == (w // 16) - 1  # a splat reaches the last tile
+
+
 def test_huge_splats_long_lists(gsr, ctx):
     # A few splats cover every tile; every tile list holds thousands of entries.
     _full(gsr, ctx, _random(3000, 160, 144, 5, big=40))
