@@ -390,14 +390,18 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                 float Tj = T * inv;
                 Tj = __fmaf_rn(inv, __fmaf_rn(-one_m, Tj, T), Tj);
                 const float aT = alpha * Tj;
+                // A lane that does not composite the splat adds zeros: its aT and
+                // dRaw are forced to 0 and every term below is a product with one
+                // of them (all factors are finite here).
+                const float aT_c = contrib ? aT : 0.0f;
                 float v[9];
-                v[5] = g.x * aT;
-                v[6] = g.y * aT;
-                v[7] = g.z * aT;
+                v[5] = g.x * aT_c;
+                v[6] = g.y * aT_c;
+                v[7] = g.z * aT_c;
                 float dA = g.x * (c.x * Tj - S.x * inv);
                 dA = __fmaf_rn(g.y, c.y * Tj - S.y * inv, dA);
                 dA = __fmaf_rn(g.z, c.z * Tj - S.z * inv, dA);
-                const float dRaw = raw < kAlphaMax ? dA : 0.0f;
+                const float dRaw = contrib && raw < kAlphaMax ? dA : 0.0f;
                 v[8] = dRaw * e;
                 const float dSig = -dRaw * raw;
                 const float a = geo.z, bb = geo.w, cc = aux.x;
@@ -406,8 +410,6 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                 v[2] = dSig * (0.5f * dx * dx);
                 v[3] = dSig * (dx * dy);
                 v[4] = dSig * (0.5f * dy * dy);
-#pragma unroll
-                for (int k = 0; k < 9; ++k) v[k] = contrib ? v[k] : 0.0f;
                 if (contrib) {
                     S.x = __fmaf_rn(c.x, aT, S.x);
                     S.y = __fmaf_rn(c.y, aT, S.y);
