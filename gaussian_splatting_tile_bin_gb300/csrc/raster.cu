@@ -418,8 +418,7 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                 }
                 // "W1 warp sparse skip": with no contributing lane every sum is +0.
                 if (kWarpSkip && !__any_sync(kFull, contrib)) continue;
-                const uint32_t idx = __float_as_uint(sb.aux[j].w);
-                warp_reduce_add9(v, grad_acc + 9 * (size_t)idx, lane);
+                warp_reduce_add9(v, grad_acc + 9 * (size_t)__float_as_uint(aux.w), lane);
             }
         }
     }
