@@ -18,7 +18,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = [os.path.join(_HERE, "oracle.c"), os.path.join(_HERE, "raster.inc"),
-        os.path.join(_HERE, "oracle.h")]
+        os.path.join(_HERE, "project.c"), os.path.join(_HERE, "oracle.h")]
 _LIB = os.path.join(_HERE, "_build", "liboracle.so")
 
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-Wall", "-Wextra",
@@ -33,7 +33,8 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         os.makedirs(os.path.dirname(_LIB), exist_ok=True)
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, os.path.join(_HERE, "oracle.c"), "-lm"])
+        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, os.path.join(_HERE, "oracle.c"),
+                               os.path.join(_HERE, "project.c"), "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -64,6 +65,10 @@ def _load():
         fn = getattr(lib, name)
         fn.argtypes = [P, P, i32, i32, i32, P, P, P]
         fn.restype = None
+    lib.orc_project_forward.argtypes = [P, i32, P, P, P, P]
+    lib.orc_project_forward.restype = None
+    lib.orc_project_backward.argtypes = [P, i32, P, P, P]
+    lib.orc_project_backward.restype = None
     _lib = lib
     return lib
 
@@ -166,3 +171,38 @@ def backward(splats, idx, ranges, width, height, dl_dout, *, f64=False, eps_alph
        float(eps_alpha), float(sigma_ulps), _ptr(cnt))
     return {"grad": grad, "gabs": gabs, "knife": knife.astype(bool),
             "counters": {"n_eval": int(cnt[0]), "n_exp": int(cnt[1]), "n_contrib": int(cnt[2])}}
+
+
+# --- projection (project.c) -------------------------------------------------
+
+GAUSSIAN_FIELDS = 14   # mean xyz, log_scale xyz, quat wxyz, logit_opacity, rgb
+CAMERA_FIELDS = 18     # W row-major (9), t (3), fx, fy, cx, cy, z_near, eps
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def project_forward(gaussians, camera):
+    """Returns (splats float64 [n,9], depths float64 [n], visible bool [n])."""
+    lib = _load()
+    g = _f64(gaussians).reshape(-1, GAUSSIAN_FIELDS)
+    cam = _f64(camera).reshape(CAMERA_FIELDS)
+    n = g.shape[0]
+    splats = np.zeros((n, 9), dtype=np.float64)
+    depths = np.zeros(n, dtype=np.float64)
+    vis = np.zeros(n, dtype=np.uint8)
+    lib.orc_project_forward(_ptr(g), n, _ptr(cam), _ptr(splats), _ptr(depths), _ptr(vis))
+    return splats, depths, vis.astype(bool)
+
+
+def project_backward(gaussians, camera, dl_dsplat):
+    """Returns dL/dgaussians float64 [n,14] for dL/dsplat [n,9]."""
+    lib = _load()
+    g = _f64(gaussians).reshape(-1, GAUSSIAN_FIELDS)
+    cam = _f64(camera).reshape(CAMERA_FIELDS)
+    d = _f64(dl_dsplat).reshape(-1, 9)
+    out = np.zeros_like(g)
+    lib.orc_project_backward(_ptr(g), g.shape[0], _ptr(cam), _ptr(d), _ptr(out))
+    return out
+

@@ -19,6 +19,8 @@
  *   orc_tile_rect / orc_count_pairs / orc_bin      pinned
  *   orc_forward_f32 / orc_forward_untiled_f32      pinned
  *   orc_backward_f32 / orc_backward_f64            pinned (finite differences)
+ *   orc_project_forward / orc_project_backward     pinned (closed forms, invariances,
+ *                                                  finite differences); project.c
  */
 #ifndef GSR_ORACLE_H
 #define GSR_ORACLE_H
@@ -96,5 +98,14 @@ void orc_backward_f64(const double *splats, int32_t n, const uint32_t *idx,
                       const uint32_t *ranges, int32_t width, int32_t height,
                       const double *dl_dout, double *grad, double *gabs, uint8_t *knife,
                       double eps_alpha, double sigma_ulps, int64_t *counters);
+
+/* Projection of 3-D Gaussians to Splat2D records and depths, and its backward
+ * (project.c).  Doubles.  g: [n][14] (mean xyz, log_scale xyz, quat wxyz,
+ * logit_opacity, rgb); cam: [18] (W row-major, t, fx, fy, cx, cy, z_near,
+ * eps); splats: [n][9]; dl_dsplat: [n][9]; dl_dg: [n][14]. */
+void orc_project_forward(const double *g, int32_t n, const double *cam, double *splats, double *depths,
+                         uint8_t *visible);
+void orc_project_backward(const double *g, int32_t n, const double *cam, const double *dl_dsplat,
+                          double *dl_dg);
 
 #endif
