@@ -87,6 +87,8 @@ def parse_args(argv=None):
     p.add_argument("--config", default="lego_final", choices=sorted(gen.CONFIGS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-projection", action="store_true",
+                   help="skip the separate timing of the projection kernels")
     p.add_argument("--min-warm-s", type=float, default=1.5,
                    help="keep warming up until this many seconds passed (clock sampling)")
     return p.parse_args(argv)
@@ -303,6 +305,48 @@ def roofline_for(kind, counters, pairs, wl, ms, peaks, sm_mhz):
             if (sm_mhz and bound != "hbm") else None}
 
 
+# Algorithmic bytes per Gaussian of the projection kernels: the forward reads a
+# 56-byte Gaussian and writes a 36-byte Splat2D and a 4-byte depth; the
+# backward reads the Gaussian and its 36-byte Splat2D gradient and writes a
+# 56-byte gradient.
+PROJ_BYTES = {"project_forward": 56 + 36 + 4, "project_backward": 56 + 36 + 56}
+
+
+def time_projection(gsr, ctx, dev, stream, flush, steps, warmup, peaks):
+    """Times the projection forward and backward on the Lego-shaped 3-D scene
+    (409,660 Gaussians, one 800x800 view), each launch alone between L2 flushes."""
+    import torch
+
+    sc = gen.lego_scene()
+    g = torch.from_numpy(sc.gaussians).to(dev)
+    G = torch.from_numpy(sc.dl_dsplat).to(dev)
+    sp = torch.empty((sc.n, 9), dtype=torch.float32, device=dev)
+    d = torch.empty((sc.n,), dtype=torch.float32, device=dev)
+    dg = torch.empty((sc.n, 14), dtype=torch.float32, device=dev)
+    calls = {"project_forward": lambda: gsr.project_forward(ctx, g, sc.camera, sp, d),
+             "project_backward": lambda: gsr.project_backward(ctx, g, sc.camera, G, dg)}
+    out = {"workload": f"lego_scene: {sc.n:,} Gaussians, 800x800 view, seed 3", "gaussians": sc.n}
+    for name, call in calls.items():
+        for i in range(warmup):
+            flush.fill_(float(i))
+            call()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            call()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        ms = np.array([a.elapsed_time(b) for a, b in evs])
+        gbs = PROJ_BYTES[name] * sc.n / (float(ms.mean()) * 1e-3) / 1e9
+        out[name] = {"ms": float(ms.mean()), "ms_median": float(np.median(ms)),
+                     "bytes_per_gaussian": PROJ_BYTES[name],
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}}
+    return out
+
+
 def gpu_arm(args):
     import torch
 
@@ -438,11 +482,16 @@ def gpu_arm(args):
                "d2h_bytes_per_step": int(d2h),
                "pipelining": "two contexts on two streams; a step's copies overlap the other's kernels"}
 
+    peaks = measured_peaks()
+    projection = None
+    if not args.no_projection:
+        projection = time_projection(gsr, ctx, dev, stream, flush, max(args.steps, 20), max(args.warmup, 3),
+                                     peaks)
+
     rows = sampler.stop()
     clocks = ClockSampler.summarize(rows)
 
     value = job_ms_per_iter(float(tot_ms.sum()), args.steps, world, dev)
-    peaks = measured_peaks()
 
     line = {"metric": METRIC, "value": value, "unit": "ms/iter", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(tot_ms.mean()),
@@ -461,6 +510,8 @@ def gpu_arm(args):
             "wall_s": wall, "gpu_launches": int(launches), "clocks": clocks}
     if e2e:
         line["e2e"] = e2e
+    if projection:
+        line["projection"] = projection
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(wl)

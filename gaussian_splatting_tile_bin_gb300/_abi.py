@@ -33,6 +33,14 @@ class _Bins(ctypes.Structure):
                 ("tiles_x", ctypes.c_int32), ("tiles_y", ctypes.c_int32)]
 
 
+GAUSSIAN_FIELDS = 14   # mean xyz, log_scale xyz, quat wxyz, logit_opacity, rgb
+CAMERA_FIELDS = 18     # W row-major (9), t (3), fx, fy, cx, cy, z_near, eps
+
+
+class _Camera(ctypes.Structure):
+    _fields_ = [("v", ctypes.c_float * CAMERA_FIELDS)]
+
+
 class _BinStats(ctypes.Structure):
     _fields_ = [("num_pairs", ctypes.c_uint32), ("emitting", ctypes.c_uint32),
                 ("radix_passes", ctypes.c_int32), ("depth_pass_mask", ctypes.c_uint32),
@@ -64,6 +72,10 @@ def _load():
     lib.gsr_rasterize_backward.restype = ctypes.c_int
     lib.gsr_get_bin_stats.argtypes = [P, ctypes.POINTER(_BinStats)]
     lib.gsr_get_bin_stats.restype = ctypes.c_int
+    lib.gsr_project_forward.argtypes = [P, P, i32, ctypes.POINTER(_Camera), P, P, P]
+    lib.gsr_project_forward.restype = ctypes.c_int
+    lib.gsr_project_backward.argtypes = [P, P, i32, ctypes.POINTER(_Camera), P, P, P]
+    lib.gsr_project_backward.restype = ctypes.c_int
     lib.gsr_exp_neg.argtypes = [P, P, P, i32, P]
     lib.gsr_exp_neg.restype = ctypes.c_int
     return lib
@@ -238,3 +250,49 @@ def rasterize_backward(ctx: Context, splats: torch.Tensor, bins: Bins, dl_dout: 
         ctypes.c_void_p(last_contrib.data_ptr()), ctypes.c_void_p(grad.data_ptr()),
         _stream_ptr(stream, dev)))
     return grad
+
+
+def _camera(camera) -> _Camera:
+    vals = [float(v) for v in (camera.tolist() if hasattr(camera, "tolist") else camera)]
+    if len(vals) != CAMERA_FIELDS:
+        raise ValueError(f"camera must hold {CAMERA_FIELDS} numbers (W row-major, t, fx, fy, cx, cy, "
+                         "z_near, eps)")
+    cam = _Camera()
+    cam.v[:] = vals
+    return cam
+
+
+def project_forward(ctx: Context, gauss: torch.Tensor, camera, splats=None, depths=None, stream=None):
+    """Projects 3-D Gaussians [n, 14] f32 through `camera` (18 numbers).
+    Returns (splats [n, 9] f32, depths [n] f32)."""
+    n = gauss.shape[0] if gauss.dim() == 2 else -1
+    _need(gauss, "gauss", torch.float32, (n, GAUSSIAN_FIELDS))
+    dev = gauss.device
+    if splats is None:
+        splats = torch.empty((n, 9), dtype=torch.float32, device=dev)
+    if depths is None:
+        depths = torch.empty((n,), dtype=torch.float32, device=dev)
+    _need(splats, "splats", torch.float32, (n, 9))
+    _need(depths, "depths", torch.float32, (n,))
+    cam = _camera(camera)
+    ctx._check(lib.gsr_project_forward(ctx._h, ctypes.c_void_p(gauss.data_ptr()), n, ctypes.byref(cam),
+                                       ctypes.c_void_p(splats.data_ptr()), ctypes.c_void_p(depths.data_ptr()),
+                                       _stream_ptr(stream, dev)))
+    return splats, depths
+
+
+def project_backward(ctx: Context, gauss: torch.Tensor, camera, dl_dsplat: torch.Tensor, dl_dgauss=None,
+                     stream=None) -> torch.Tensor:
+    """Returns dL/dgauss [n, 14] f32 for dL/dsplat [n, 9] f32."""
+    n = gauss.shape[0] if gauss.dim() == 2 else -1
+    _need(gauss, "gauss", torch.float32, (n, GAUSSIAN_FIELDS))
+    _need(dl_dsplat, "dl_dsplat", torch.float32, (n, 9))
+    dev = gauss.device
+    if dl_dgauss is None:
+        dl_dgauss = torch.empty((n, GAUSSIAN_FIELDS), dtype=torch.float32, device=dev)
+    _need(dl_dgauss, "dl_dgauss", torch.float32, (n, GAUSSIAN_FIELDS))
+    cam = _camera(camera)
+    ctx._check(lib.gsr_project_backward(ctx._h, ctypes.c_void_p(gauss.data_ptr()), n, ctypes.byref(cam),
+                                        ctypes.c_void_p(dl_dsplat.data_ptr()),
+                                        ctypes.c_void_p(dl_dgauss.data_ptr()), _stream_ptr(stream, dev)))
+    return dl_dgauss

@@ -3,6 +3,7 @@
 // themselves live in bin.cu and raster.cu.
 #include <nvtx3/nvToolsExt.h>
 
+#include <cmath>
 #include <new>
 #include <string>
 
@@ -261,4 +262,58 @@ int gsr_exp_neg(gsr_ctx *ctx, const float *s, float *out, int32_t n, void *strea
 
 }  // extern "C"
 
+namespace {
+
+int check_projection(gsr_ctx *ctx, const void *gauss, int32_t n, const gsr_camera *cam, const void *a,
+                     const void *b)
+{
+    if (!cam) return fail(ctx, GSR_ERR_INVALID_ARG, "camera is NULL");
+    if (n < 0 || n > GSR_MAX_SPLATS) return fail(ctx, GSR_ERR_INVALID_ARG, "n out of range");
+    if (n > 0 && (!gauss || !a || !b)) return fail(ctx, GSR_ERR_INVALID_ARG, "an array is NULL");
+    if (!aligned(gauss, 4) || !aligned(a, 4) || !aligned(b, 4))
+        return fail(ctx, GSR_ERR_INVALID_ARG, "arrays must be 4-byte aligned");
+    const float *f = reinterpret_cast<const float *>(cam);
+    for (size_t k = 0; k < sizeof(gsr_camera) / sizeof(float); ++k)
+        if (!std::isfinite(f[k])) return fail(ctx, GSR_ERR_INVALID_ARG, "camera field not finite");
+    if (!(cam->z_near > 0.0f)) return fail(ctx, GSR_ERR_INVALID_ARG, "camera z_near must be > 0");
+    if (!(cam->eps >= 0.0f)) return fail(ctx, GSR_ERR_INVALID_ARG, "camera eps must be >= 0");
+    return GSR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gsr_project_forward(gsr_ctx *ctx, const gsr_gaussian3d *gauss, int32_t n, const gsr_camera *camera,
+                        gsr_splat2d *splats, float *depths, void *stream)
+{
+    gsr::Range range("gsr_project_forward");
+    if (!ctx) return GSR_ERR_INVALID_ARG;
+    ctx->err.clear();
+    if (int rc = check_projection(ctx, gauss, n, camera, splats, depths)) return rc;
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, GSR_ERR_CUDA, "cannot select the context's device");
+    if (n == 0) return GSR_OK;
+    return gsr::project_forward(ctx, reinterpret_cast<const float *>(gauss), n, *camera,
+                                reinterpret_cast<float *>(splats), depths, (cudaStream_t)stream);
+}
+
+int gsr_project_backward(gsr_ctx *ctx, const gsr_gaussian3d *gauss, int32_t n, const gsr_camera *camera,
+                         const float *dl_dsplat, float *dl_dgauss, void *stream)
+{
+    gsr::Range range("gsr_project_backward");
+    if (!ctx) return GSR_ERR_INVALID_ARG;
+    ctx->err.clear();
+    if (int rc = check_projection(ctx, gauss, n, camera, dl_dsplat, dl_dgauss)) return rc;
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, GSR_ERR_CUDA, "cannot select the context's device");
+    if (n == 0) return GSR_OK;
+    return gsr::project_backward(ctx, reinterpret_cast<const float *>(gauss), n, *camera, dl_dsplat, dl_dgauss,
+                                 (cudaStream_t)stream);
+}
+
+}  // extern "C"
+
 static_assert(sizeof(gsr_splat2d) == 36, "Splat2D is 9 floats");
+static_assert(sizeof(gsr_gaussian3d) == GSR_GAUSSIAN_FLOATS * 4, "a Gaussian is 14 floats");
+static_assert(sizeof(gsr_camera) == 18 * 4, "a camera is 18 floats");

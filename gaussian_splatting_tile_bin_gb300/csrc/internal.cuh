@@ -138,6 +138,10 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
 int rasterize_backward_noalloc(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_bins *bins,
                                const float *dl_dout, const float *final_T,
                                const uint32_t *last_contrib, float *grad, cudaStream_t stream);
+int project_forward(gsr_ctx *ctx, const float *gauss, int32_t n, const gsr_camera &camera, float *splats,
+                    float *depths, cudaStream_t stream);
+int project_backward(gsr_ctx *ctx, const float *gauss, int32_t n, const gsr_camera &camera,
+                     const float *dl_dsplat, float *dl_dg, cudaStream_t stream);
 // out[i] = the raster kernels' exp(-s[i]).
 int exp_neg_eval(gsr_ctx *ctx, const float *s, float *out, int32_t n, cudaStream_t stream);
 

@@ -56,6 +56,30 @@ typedef struct gsr_splat2d {
     float color_a;
 } gsr_splat2d;
 
+/* One 3-D Gaussian, the input of gsr_project_forward: 14 floats, 56 bytes.
+ * quat is (w, x, y, z) and need not be normalised; the scales are exp(log_scale)
+ * along the rotated axes; color_a = 1 / (1 + exp(-logit_opacity)). */
+#define GSR_GAUSSIAN_FLOATS 14
+typedef struct gsr_gaussian3d {
+    float mean[3];
+    float log_scale[3];
+    float quat[4];
+    float logit_opacity;
+    float rgb[3];
+} gsr_gaussian3d;
+
+/* A pinhole camera: camera-space point p = W x + t (W row-major, usually a
+ * rotation), pixel = (fx p.x / p.z + cx, fy p.y / p.z + cy).  Points with
+ * p.z <= z_near are not projected.  eps is added to both diagonal entries of
+ * every projected 2-D covariance (a low-pass dilation; 0 disables it). */
+typedef struct gsr_camera {
+    float W[9];
+    float t[3];
+    float fx, fy, cx, cy;
+    float z_near;
+    float eps;
+} gsr_camera;
+
 #define GSR_TILE 16
 #define GSR_MAX_IMAGE_SIDE (1 << 19)   /* width and height limit */
 #define GSR_MAX_SPLATS (1 << 28)       /* n limit */
@@ -215,6 +239,47 @@ typedef struct gsr_bin_stats {
     uint64_t capacity;
 } gsr_bin_stats;
 int gsr_get_bin_stats(gsr_ctx *ctx, gsr_bin_stats *out);
+
+/* Projection of n 3-D Gaussians to Splat2D records and depths, the step that
+ * makes the rasterizer's input in the trainer the pages profile ("M3 per-splat
+ * backward", section 3; "W1 warp sparse skip + exp-skip": color_a is the
+ * sigmoid of the opacity logit).  The pages give no formula; this is the
+ * standard perspective (EWA) projection:
+ *
+ *   p = W mean + t,  depth = p.z,  mean2 = (fx p.x / p.z + cx, fy p.y / p.z + cy)
+ *   J = [[fx / p.z, 0, -fx p.x / p.z^2], [0, fy / p.z, -fy p.y / p.z^2]]
+ *   Sigma2 = (J W R S)(J W R S)^T + eps I,  R = rotation of quat / |quat|,
+ *            S = diag(exp(log_scale))
+ *   conic (a, b, c): [[a, b], [b, c]] = Sigma2^-1,  rgb copied,
+ *   color_a = 1 / (1 + exp(-logit_opacity))
+ *
+ * A Gaussian with a non-finite field, p.z <= z_near, quat = 0 or a singular
+ * Sigma2 is not visible: its Splat2D has mean, conic and color_a 0 (rgb is
+ * still copied) and its depth is 0, so gsr_bin_splats emits no pair for it.
+ *
+ *   gauss   device, [n] gsr_gaussian3d (4-byte aligned)
+ *   camera  host; read during the call only
+ *   splats  device, [n] gsr_splat2d, overwritten
+ *   depths  device, [n] float, overwritten
+ * Arrays 16-byte aligned take a vectorised path (same results).  Nothing is
+ * allocated.  Errors: GSR_ERR_INVALID_ARG (null ctx or camera; n < 0 or
+ * > GSR_MAX_SPLATS; null or misaligned arrays with n > 0; a camera field not
+ * finite, z_near <= 0 or eps < 0), GSR_ERR_CUDA. */
+int gsr_project_forward(gsr_ctx *ctx, const gsr_gaussian3d *gauss, int32_t n, const gsr_camera *camera,
+                        gsr_splat2d *splats, float *depths, void *stream);
+
+/* Backward of gsr_project_forward: the gradient of L with respect to every
+ * field of every Gaussian, given dl_dsplat = dL/d(each Splat2D field), for
+ * example the grad of gsr_rasterize_backward.  Depth carries no gradient (it
+ * only orders the splats).  Gaussians that are not visible get 0 in every
+ * field, rgb included.
+ *
+ *   gauss      device, [n] gsr_gaussian3d, as passed to the forward
+ *   dl_dsplat  device, [n * 9] float, in gsr_splat2d field order
+ *   dl_dgauss  device, [n * 14] float, overwritten, in gsr_gaussian3d field order
+ * Errors: as gsr_project_forward. */
+int gsr_project_backward(gsr_ctx *ctx, const gsr_gaussian3d *gauss, int32_t n, const gsr_camera *camera,
+                         const float *dl_dsplat, float *dl_dgauss, void *stream);
 
 /* Diagnostic: out[i] = exp(-s[i]) computed by the exponential the raster
  * kernels use for alpha = min(0.999, color_a exp(-sigma)) ("A.9 f16 forward",

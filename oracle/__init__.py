@@ -67,7 +67,7 @@ def _load():
         fn.restype = None
     lib.orc_project_forward.argtypes = [P, i32, P, P, P, P]
     lib.orc_project_forward.restype = None
-    lib.orc_project_backward.argtypes = [P, i32, P, P, P]
+    lib.orc_project_backward.argtypes = [P, i32, P, P, P, P]
     lib.orc_project_backward.restype = None
     _lib = lib
     return lib
@@ -196,13 +196,16 @@ def project_forward(gaussians, camera):
     return splats, depths, vis.astype(bool)
 
 
-def project_backward(gaussians, camera, dl_dsplat):
-    """Returns dL/dgaussians float64 [n,14] for dL/dsplat [n,9]."""
+def project_backward(gaussians, camera, dl_dsplat, with_abs=False):
+    """Returns dL/dgaussians float64 [n,14] for dL/dsplat [n,9]; with_abs: also
+    the sum of |terms| of each output's last sum, [n,14]."""
     lib = _load()
     g = _f64(gaussians).reshape(-1, GAUSSIAN_FIELDS)
     cam = _f64(camera).reshape(CAMERA_FIELDS)
     d = _f64(dl_dsplat).reshape(-1, 9)
     out = np.zeros_like(g)
-    lib.orc_project_backward(_ptr(g), g.shape[0], _ptr(cam), _ptr(d), _ptr(out))
-    return out
+    gabs = np.zeros_like(g) if with_abs else None
+    lib.orc_project_backward(_ptr(g), g.shape[0], _ptr(cam), _ptr(d), _ptr(out),
+                             _ptr(gabs) if with_abs else None)
+    return (out, gabs) if with_abs else out
 

@@ -102,10 +102,11 @@ void orc_backward_f64(const double *splats, int32_t n, const uint32_t *idx,
 /* Projection of 3-D Gaussians to Splat2D records and depths, and its backward
  * (project.c).  Doubles.  g: [n][14] (mean xyz, log_scale xyz, quat wxyz,
  * logit_opacity, rgb); cam: [18] (W row-major, t, fx, fy, cx, cy, z_near,
- * eps); splats: [n][9]; dl_dsplat: [n][9]; dl_dg: [n][14]. */
+ * eps); splats: [n][9]; dl_dsplat: [n][9]; dl_dg: [n][14]; gabs: NULL or
+ * [n][14], the sum of |terms| of each output's last sum. */
 void orc_project_forward(const double *g, int32_t n, const double *cam, double *splats, double *depths,
                          uint8_t *visible);
 void orc_project_backward(const double *g, int32_t n, const double *cam, const double *dl_dsplat,
-                          double *dl_dg);
+                          double *dl_dg, double *gabs);
 
 #endif

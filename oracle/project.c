@@ -163,8 +163,12 @@ void orc_project_forward(const double *g, int32_t n, const double *cam, double *
     }
 }
 
+/* gabs (optional): for each output, the sum of the absolute values of the
+ * terms its last sum adds up (the rounding scale of that sum: an exact zero
+ * such as the rotation gradient of an isotropic Gaussian is a sum of terms
+ * that cancel, and a float evaluation leaves about u times this much). */
 void orc_project_backward(const double *g, int32_t n, const double *cam, const double *dl_dsplat,
-                          double *dl_dg)
+                          double *dl_dg, double *gabs)
 {
     const double *W = cam;
     const double fx = cam[12], fy = cam[13];
@@ -172,7 +176,10 @@ void orc_project_backward(const double *g, int32_t n, const double *cam, const d
         const double *gi = g + 14 * (int64_t)i;
         const double *G = dl_dsplat + 9 * (int64_t)i;
         double *out = dl_dg + 14 * (int64_t)i;
+        double ab[14];
         memset(out, 0, 14 * sizeof(double));
+        memset(ab, 0, sizeof ab);
+        if (gabs) memset(gabs + 14 * (int64_t)i, 0, 14 * sizeof(double));
         proj_state st;
         project_one(gi, cam, &st);
         if (!st.visible) continue;
@@ -181,6 +188,7 @@ void orc_project_backward(const double *g, int32_t n, const double *cam, const d
         out[12] = G[6];
         out[13] = G[7];
         out[10] = G[8] * st.alpha * (1.0 - st.alpha);
+        for (int k = 10; k < 14; ++k) ab[k] = fabs(out[k]);
         /* conic -> Sigma2: the entries of [[a, b], [b, c]] = Sigma2^-1 as
          * functions of s00, s01 (both off-diagonal entries), s11 */
         const double a = st.a, b = st.b, c = st.c;
@@ -221,8 +229,17 @@ void orc_project_backward(const double *g, int32_t n, const double *cam, const d
         gp[1] = GJ[5] * (-fy / (z * z)) + G[1] * fy / z;
         gp[2] = GJ[0] * (-fx / (z * z)) + GJ[2] * (2.0 * fx * x / (z * z * z)) + GJ[4] * (-fy / (z * z)) +
                 GJ[5] * (2.0 * fy * y / (z * z * z)) - G[0] * fx * x / (z * z) - G[1] * fy * y / (z * z);
+        double gpa[3];
+        gpa[0] = fabs(GJ[2] * fx / (z * z)) + fabs(G[0] * fx / z);
+        gpa[1] = fabs(GJ[5] * fy / (z * z)) + fabs(G[1] * fy / z);
+        gpa[2] = fabs(GJ[0] * fx / (z * z)) + fabs(GJ[2] * 2.0 * fx * x / (z * z * z)) + fabs(GJ[4] * fy / (z * z)) +
+                 fabs(GJ[5] * 2.0 * fy * y / (z * z * z)) + fabs(G[0] * fx * x / (z * z)) +
+                 fabs(G[1] * fy * y / (z * z));
         /* p = W mu + t: dmu = W^T dp */
-        for (int k = 0; k < 3; ++k) out[k] = W[k] * gp[0] + W[3 + k] * gp[1] + W[6 + k] * gp[2];
+        for (int k = 0; k < 3; ++k) {
+            out[k] = W[k] * gp[0] + W[3 + k] * gp[1] + W[6 + k] * gp[2];
+            ab[k] = fabs(W[k]) * gpa[0] + fabs(W[3 + k]) * gpa[1] + fabs(W[6 + k]) * gpa[2];
+        }
         /* Sigma3 = M M^T: dM = 2 G3 M */
         double GM[9];
         for (int r = 0; r < 3; ++r)
@@ -234,12 +251,14 @@ void orc_project_backward(const double *g, int32_t n, const double *cam, const d
         /* M = R diag(s): ds_j = column j of R . column j of dM; dR = dM diag(s) */
         double GR[9];
         for (int j = 0; j < 3; ++j) {
-            double v = 0.0;
+            double v = 0.0, va = 0.0;
             for (int r = 0; r < 3; ++r) {
                 v += st.R[3 * r + j] * GM[3 * r + j];
+                va += fabs(st.R[3 * r + j] * GM[3 * r + j]);
                 GR[3 * r + j] = GM[3 * r + j] * st.s[j];
             }
             out[3 + j] = v * st.s[j]; /* d log_scale = ds * s */
+            ab[3 + j] = va * st.s[j];
         }
         /* R of the unit quaternion (w, x, y, z): dqn from the entries' partials */
         const double w = st.qn[0], qx = st.qn[1], qy = st.qn[2], qz = st.qn[3];
@@ -251,8 +270,23 @@ void orc_project_backward(const double *g, int32_t n, const double *cam, const d
                 4.0 * qy * (GR[0] + GR[8]);
         gq[3] = 2.0 * (-w * GR[1] + qx * GR[2] + w * GR[3] + qy * GR[5] + qx * GR[6] + qy * GR[7]) -
                 4.0 * qz * (GR[0] + GR[4]);
+        double gqa[4];
+        gqa[0] = 2.0 * (fabs(qz * GR[1]) + fabs(qy * GR[2]) + fabs(qz * GR[3]) + fabs(qx * GR[5]) +
+                        fabs(qy * GR[6]) + fabs(qx * GR[7]));
+        gqa[1] = 2.0 * (fabs(qy * GR[1]) + fabs(qz * GR[2]) + fabs(qy * GR[3]) + fabs(w * GR[5]) +
+                        fabs(qz * GR[6]) + fabs(w * GR[7])) + 4.0 * fabs(qx) * (fabs(GR[4]) + fabs(GR[8]));
+        gqa[2] = 2.0 * (fabs(qx * GR[1]) + fabs(w * GR[2]) + fabs(qx * GR[3]) + fabs(qz * GR[5]) +
+                        fabs(w * GR[6]) + fabs(qz * GR[7])) + 4.0 * fabs(qy) * (fabs(GR[0]) + fabs(GR[8]));
+        gqa[3] = 2.0 * (fabs(w * GR[1]) + fabs(qx * GR[2]) + fabs(w * GR[3]) + fabs(qy * GR[5]) +
+                        fabs(qx * GR[6]) + fabs(qy * GR[7])) + 4.0 * fabs(qz) * (fabs(GR[0]) + fabs(GR[4]));
         /* qn = q / |q|: dq = (dqn - qn (qn . dqn)) / |q| */
         const double dot = w * gq[0] + qx * gq[1] + qy * gq[2] + qz * gq[3];
-        for (int k = 0; k < 4; ++k) out[6 + k] = (gq[k] - st.qn[k] * dot) / st.qlen;
+        double dota = 0.0;
+        for (int k = 0; k < 4; ++k) dota += fabs(st.qn[k]) * gqa[k];
+        for (int k = 0; k < 4; ++k) {
+            out[6 + k] = (gq[k] - st.qn[k] * dot) / st.qlen;
+            ab[6 + k] = (gqa[k] + fabs(st.qn[k]) * dota) / st.qlen;
+        }
+        if (gabs) memcpy(gabs + 14 * (int64_t)i, ab, sizeof ab);
     }
 }

@@ -141,3 +141,16 @@ def test_backward_matches_central_differences():
             gm[i, k] -= h
             fd = (loss(gp) - loss(gm)) / (2 * h)
             assert grad[i, k] == pytest.approx(fd, rel=2e-5, abs=2e-5 * (1 + abs(fd))), (i, k)
+
+
+def test_isotropic_gaussian_has_no_rotation_gradient():
+    """An isotropic Gaussian looks the same under any rotation: the quaternion
+    gradient vanishes (up to rounding of its terms, whose size gabs reports),
+    and every |gradient| is at most its gabs."""
+    rng = np.random.default_rng(6)
+    g = np.stack([gaussian(mean=(0.3, -0.1, 3.0), log_scale=(np.log(0.07),) * 3, quat=rng.normal(size=4))
+                  for _ in range(4)])
+    grad, gabs = oracle.project_backward(g, camera(), rng.normal(size=(4, 9)), with_abs=True)
+    assert np.all(gabs[:, 6:10] > 0)
+    assert np.all(np.abs(grad[:, 6:10]) <= 1e-12 * gabs[:, 6:10])
+    assert np.all(np.abs(grad) <= gabs * (1 + 1e-12))
