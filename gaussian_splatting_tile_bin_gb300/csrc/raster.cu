@@ -278,11 +278,26 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
 
 // --- backward --------------------------------------------------------------
 
+// float -> double with integer operations (the FP64 pipe is narrow): exact for
+// normal floats and infinities, subnormals flush to a signed zero.
+__device__ __forceinline__ double widen(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    const uint32_t mag = u & 0x7fffffffu;
+    uint32_t hi = (mag >> 3) + (896u << 20);
+    uint32_t lo = mag << 29;
+    const bool small = mag < 0x00800000u;
+    hi = small ? 0u : hi;
+    lo = small ? 0u : lo;
+    hi = mag >= 0x7f800000u ? (0x7ff00000u | ((mag >> 3) & 0xfffffu)) : hi;
+    return __hiloint2double((int)(hi | (u & 0x80000000u)), (int)lo);
+}
+
 // Sums the 9 per-lane values over the warp and adds the totals to acc[0..8] in
 // one atomic instruction: a transposed butterfly leaves component k (k < 8) in
 // lanes 4k..4k+3 after 7 shuffles, component 8 takes a plain butterfly, and
-// lanes 4k and lane 1 widen their sums to double and issue the adds (9 lanes
-// share one conversion instruction on the narrow FP64 pipe).
+// lanes 4k and lane 1 widen their sums to double (with integer operations, off
+// the narrow FP64 pipe) and issue the adds.
 __device__ __forceinline__ void warp_reduce_add9(float (&v)[9], double *__restrict__ acc, int lane)
 {
     const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
@@ -306,8 +321,8 @@ __device__ __forceinline__ void warp_reduce_add9(float (&v)[9], double *__restri
     float z = v[8];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
-    if ((lane & 3) == 0) atomicAdd(acc + (lane >> 2), (double)y);
-    else if (lane == 1) atomicAdd(acc + 8, (double)z);
+    const float mine = (lane & 3) == 0 ? y : z;
+    if ((lane & 3) == 0 || lane == 1) atomicAdd(acc + ((lane & 3) == 0 ? (lane >> 2) : 8), widen(mine));
 }
 
 template <bool kWarpSkip, bool kLastContrib, bool kCull>
@@ -385,6 +400,8 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                 float e, raw;
                 const float alpha = splat_alpha(in_range ? sigma : 0.0f, aux.y, e, raw);
                 const bool contrib = in_range && alpha >= kAlphaMin;
+                // "W1 warp sparse skip": with no contributing lane nothing changes.
+                if (kWarpSkip && !__any_sync(kFull, contrib)) continue;
                 const float one_m = __fsub_rn(1.0f, alpha);
                 const float inv = __fdividef(1.0f, one_m);
                 float Tj = T * inv;
@@ -416,8 +433,6 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                     S.z = __fmaf_rn(c.z, aT, S.z);
                     T = Tj;
                 }
-                // "W1 warp sparse skip": with no contributing lane every sum is +0.
-                if (kWarpSkip && !__any_sync(kFull, contrib)) continue;
                 warp_reduce_add9(v, grad_acc + 9 * (size_t)__float_as_uint(aux.w), lane);
             }
         }

@@ -95,7 +95,8 @@ enum {
 
 /* Per-call variant switches (A/B and equivalence tests; defaults are 1). */
 enum {
-    GSR_OPT_BWD_WARP_SKIP = 1,   /* skip the reduction when no lane contributes */
+    GSR_OPT_BWD_WARP_SKIP = 1,   /* a warp skips the gradient arithmetic and reduction of a splat
+                                    no lane composites */
     GSR_OPT_BWD_LAST_CONTRIB = 2, /* stop each warp at its largest last_contributor */
     GSR_OPT_WARP_CULL = 3,        /* forward and backward: a warp skips splats whose alpha >= 1/255
                                      ellipse misses its 8x4 pixel block (same results) */
