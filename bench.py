@@ -49,23 +49,32 @@ SFU_LANES_PER_SM = 16
 FWD_OPS = {"n_eval": 9, "n_exp": 4, "n_contrib": 7}
 BWD_OPS = {"n_eval": 9, "n_exp": 4, "n_contrib": 44}
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch on the
-# 800x800, 409,660-splat workload, from one ncu capture (profiles/k_*_lego_final.md),
-# with the SHA-256 of the kernel sources it was taken on.  Once the sources
-# change, the figure no longer describes the kernel and is reported as null.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from one
+# ncu capture (profiles/k_*.md), with the SHA-256 of the kernel sources it was
+# taken on.  Once the sources change, the figure no longer describes the kernel
+# and is reported as null.
+RASTER_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/raster.cu",
+                  "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
+PROJECT_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/project.cu",
+                   "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
+RASTER_SHA256 = "57454195c7c6063d3fa6761712abd223fb0e3395839f25a5c5da40765f671ee3"
+PROJECT_SHA256 = "af03230ed0e75024a78e2ac01240d844d06f339899c263eb0fb9c1518003ed96"
 NCU_TRAFFIC = {
-    "forward": {"bytes": 22_279_680 + 1_792, "workload": "lego_final"},
-    "backward": {"bytes": 50_584_832 + 74_240, "workload": "lego_final"},
+    "forward": {"bytes": 22_277_376 + 2_048, "workload": "lego_final", "sources": RASTER_SOURCES,
+                "sha256": RASTER_SHA256},
+    "backward": {"bytes": 50_601_472 + 74_752, "workload": "lego_final", "sources": RASTER_SOURCES,
+                 "sha256": RASTER_SHA256},
+    "project_forward": {"bytes": 22_957_056 + 0, "workload": "lego_scene", "sources": PROJECT_SOURCES,
+                        "sha256": PROJECT_SHA256},
+    "project_backward": {"bytes": 37_710_848 + 235_264, "workload": "lego_scene", "sources": PROJECT_SOURCES,
+                         "sha256": PROJECT_SHA256},
 }
-NCU_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/raster.cu",
-               "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
-NCU_SOURCES_SHA256 = "26d6ef4ad5e86c3a83452337a2e4bbb4e21dca892f3fc099b8ee2122f58efb42"
 
 
-def raster_sources_digest() -> str:
+def sources_digest(sources) -> str:
     import hashlib
     h = hashlib.sha256()
-    for rel in NCU_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(hashlib.sha256(f.read()).digest())
     return h.hexdigest()
@@ -73,7 +82,7 @@ def raster_sources_digest() -> str:
 
 def ncu_traffic(kind: str, workload: str):
     entry = NCU_TRAFFIC.get(kind)
-    if entry is None or entry["workload"] != workload or raster_sources_digest() != NCU_SOURCES_SHA256:
+    if entry is None or entry["workload"] != workload or sources_digest(entry["sources"]) != entry["sha256"]:
         return None
     return entry["bytes"]
 
@@ -343,7 +352,8 @@ def time_projection(gsr, ctx, dev, stream, flush, steps, warmup, peaks):
         out[name] = {"ms": float(ms.mean()), "ms_median": float(np.median(ms)),
                      "bytes_per_gaussian": PROJ_BYTES[name],
                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}}
+                                  "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                                  "traffic": ncu_traffic(name, "lego_scene")}}
     return out
 
 
