@@ -96,6 +96,8 @@ def parse_args(argv=None):
     p.add_argument("--config", default="lego_final", choices=sorted(gen.CONFIGS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--deterministic", action="store_true",
+                   help="time the backward's deterministic mode (fixed-point accumulation)")
     p.add_argument("--no-projection", action="store_true",
                    help="skip the separate timing of the projection kernels")
     p.add_argument("--min-warm-s", type=float, default=1.5,
@@ -370,6 +372,8 @@ def gpu_arm(args):
     dev = torch.device("cuda", local)
     wl = gen.make(args.config)
     ctx = gsr.Context(local)
+    if args.deterministic:
+        ctx.set_option("deterministic", True)
     stream = torch.cuda.current_stream(dev)
 
     sp = torch.from_numpy(wl.splats).to(dev)
@@ -442,8 +446,11 @@ def gpu_arm(args):
         h_dl = torch.from_numpy(wl.dl_dout).pin_memory()
         slots = []
         for k in range(2):
+            c2 = ctx if k == 0 else gsr.Context(local)
+            if args.deterministic:
+                c2.set_option("deterministic", True)
             slots.append({
-                "ctx": ctx if k == 0 else gsr.Context(local), "stream": torch.cuda.Stream(dev),
+                "ctx": c2, "stream": torch.cuda.Stream(dev),
                 "sp": torch.empty_like(sp), "dp": torch.empty_like(dp), "dl": torch.empty_like(dl),
                 "out": torch.empty_like(out), "fT": torch.empty_like(fT), "last": torch.empty_like(last),
                 "grad": torch.empty_like(grad),
@@ -510,7 +517,9 @@ def gpu_arm(args):
             "config": {"workload": workload_label(wl), "splats": wl.n, "width": wl.width,
                        "height": wl.height, "pairs": int(pairs),
                        "l2": "flushed between timed steps (256 MB write)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "backward_accumulation": "fixed point (deterministic)" if args.deterministic
+                       else "double atomics"},
             "ms_per_step_median": float(np.median(tot_ms)), "ms_per_step_std": float(np.std(tot_ms)),
             "stages_ms": {"bin": float(bin_ms.mean()), "forward": float(fwd_ms.mean()),
                           "backward": float(bwd_ms.mean()),

@@ -16,7 +16,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("GSR_LIBRARY") or os.path.join(_PKG, "lib", "libgsr.so")
 
 GSR_OK, GSR_ERR_INVALID_ARG, GSR_ERR_CUDA, GSR_ERR_OOM, GSR_ERR_TOO_MANY_PAIRS = range(5)
-OPTIONS = {"bwd_warp_skip": 1, "bwd_last_contrib": 2, "warp_cull": 3, "pdl": 4, "fail_next_alloc": 5}
+OPTIONS = {"bwd_warp_skip": 1, "bwd_last_contrib": 2, "warp_cull": 3, "pdl": 4, "fail_next_alloc": 5,
+           "deterministic": 6}
 
 
 class GsrError(RuntimeError):

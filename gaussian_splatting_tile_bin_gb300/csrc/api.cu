@@ -113,6 +113,7 @@ void gsr_destroy(gsr_ctx *ctx)
         cudaFree(ctx->scalars);
         cudaFree(ctx->grad_acc);
         cudaFree(ctx->bwd_tile_cost);
+        cudaFree(ctx->det_escale);
         if (ctx->host_total) cudaFreeHost(ctx->host_total);
     }
     delete ctx;
@@ -130,6 +131,7 @@ int gsr_set_option(gsr_ctx *ctx, int option, int value)
     case GSR_OPT_WARP_CULL: ctx->opt_warp_cull = value; return GSR_OK;
     case GSR_OPT_PDL: ctx->opt_pdl = value; return GSR_OK;
     case GSR_OPT_FAIL_NEXT_ALLOC: ctx->fail_next_alloc = value; return GSR_OK;
+    case GSR_OPT_DETERMINISTIC: ctx->opt_deterministic = value; return GSR_OK;
     default: return fail(ctx, GSR_ERR_INVALID_ARG, "unknown option " + std::to_string(option));
     }
 }

@@ -35,6 +35,7 @@ struct gsr_ctx {
     int opt_last_contrib = 1;
     int opt_warp_cull = 1;
     int opt_pdl = 1;
+    int opt_deterministic = 0;
     int fail_next_alloc = 0;                    // test hook: the next device allocation fails
     int num_sms = 0;                            // multiprocessors of the device (0: not queried yet)
 
@@ -60,6 +61,9 @@ struct gsr_ctx {
     size_t cap_grad_acc = 0;
     double *grad_acc = nullptr;                 // [9 * cap] backward accumulator
     bool grad_acc_zero = false;                 // grad_acc holds zeros when no call is in flight
+    size_t cap_det = 0;
+    uint2 *det_escale = nullptr;                // [cap_det] fixed-point exponents (deterministic backward)
+    uint32_t *det_maxima = nullptr;             // after det_escale: per-block maxima of the bounds (raster.cu)
 
     // Last binning, for gsr_get_bin_stats.
     cudaStream_t last_stream = nullptr;

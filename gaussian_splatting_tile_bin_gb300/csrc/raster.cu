@@ -33,6 +33,9 @@
 #ifndef GSR_STAGE_PER_THREAD
 #define GSR_STAGE_PER_THREAD 2
 #endif
+#ifndef GSR_BWD_STAGE_PER_THREAD
+#define GSR_BWD_STAGE_PER_THREAD 2
+#endif
 
 namespace gsr {
 namespace {
@@ -41,6 +44,7 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int SM_BLOCKS_CAP = 152 * 16;     // grid-stride cap for elementwise passes
 constexpr int kWarps = kTilePixels / 32;
 constexpr int kBatch = kTilePixels * GSR_STAGE_PER_THREAD;  // splats per staged batch
+constexpr int kBwdBatch = kTilePixels * GSR_BWD_STAGE_PER_THREAD;
 constexpr float kAlphaMin = 1.0f / 255.0f;  // "W1 warp sparse skip + exp-skip", body
 constexpr float kAlphaMax = 0.999f;         // "A.9 f16 forward", snippet
 constexpr float kSigmaSkip = 5.55f;         // "W1 warp sparse skip + exp-skip", section 1, W1b
@@ -57,12 +61,14 @@ constexpr float kLn255Margin = 5.5412636f + 1e-3f;
 // with sigma at or above it is skipped without computing an exponential.  At
 // 5.55 the bound is the pages' exact skip; below it only lanes whose exact alpha
 // test would fail are dropped, so the decisions are those of the exact test.
-struct StagedBatch {
-    float4 geo[kBatch];
-    float4 aux[kBatch];
-    float4 rgb[kBatch];
-    uint32_t mask[kBatch];  // bit w: warp w's 8x4 block may see sigma < bound
+template <int kSize>
+struct StagedBatchT {
+    float4 geo[kSize];
+    float4 aux[kSize];
+    float4 rgb[kSize];
+    uint32_t mask[kSize];  // bit w: warp w's 8x4 block may see sigma < bound
 };
+using StagedBatch = StagedBatchT<kBatch>;
 
 // Warp w covers the 8x4 block (w & 1, w >> 1) of the tile; lane l the pixel
 // (l & 7, l >> 3) inside it.
@@ -133,8 +139,8 @@ __device__ __forceinline__ uint32_t block_mask(float mx, float my, float a, floa
     return m;
 }
 
-template <bool kCull>
-__device__ __forceinline__ void stage_splat(StagedBatch &sb, int slot, const float *__restrict__ splats,
+template <bool kCull, int kSize>
+__device__ __forceinline__ void stage_splat(StagedBatchT<kSize> &sb, int slot, const float *__restrict__ splats,
                                             uint32_t idx, int x0, int y0)
 {
     const float *s = splats + 9 * (size_t)idx;
@@ -293,12 +299,47 @@ __device__ __forceinline__ double widen(float f)
     return __hiloint2double((int)(hi | (u & 0x80000000u)), (int)lo);
 }
 
+// Deterministic accumulation (GSR_OPT_DETERMINISTIC).  Each warp's partial sum
+// x of a gradient component is added to a 64-bit integer accumulator as
+// round(x * 2^-E), with E chosen per splat and component group so that the sum
+// of every partial the launch can add stays below 2^62 in magnitude (the bounds
+// are in k_det_scales).  Integer addition is associative, so the result does not
+// depend on the order in which warps add their partials.
+//
+// round(|x| 2^-E) from the float's bits (ties away from zero); zero and
+// subnormal floats give 0.  |x| 2^-E < 2^62 by the choice of E.
+__device__ __forceinline__ long long to_fixed(float x, int E)
+{
+    const uint32_t u = __float_as_uint(x);
+    const int ex = (int)((u >> 23) & 0xffu);
+    const unsigned long long m = (unsigned long long)((u & 0x7fffffu) | 0x800000u);
+    const int sh = ex - 150 - E;  // |x| 2^-E = m 2^sh
+    unsigned long long r;
+    if (sh >= 0) r = m << min(sh, 39);
+    else if (sh > -63) r = (m + (1ull << (-sh - 1))) >> (-sh);
+    else r = 0;
+    r = ex == 0 ? 0ull : r;
+    return (u >> 31) ? -(long long)r : (long long)r;
+}
+
+// Group of each gradient component for its fixed-point exponent: 0 the mean
+// (components 0, 1), 1 the conic (2..4), 2 the colour (5..7), 3 color_a (8).
+__device__ __forceinline__ int det_group(int k) { return k < 2 ? 0 : (k < 5 ? 1 : (k < 8 ? 2 : 3)); }
+
+// Exponent of group grp from a splat's packed exponents (four int16).
+__device__ __forceinline__ int det_exponent(uint2 esc, int grp)
+{
+    const uint32_t w = grp < 2 ? esc.x : esc.y;
+    return (int)(int16_t)((grp & 1) ? (w >> 16) : (w & 0xffffu));
+}
+
 // Sums the 9 per-lane values over the warp and adds the totals to acc[0..8] in
 // one atomic instruction: a transposed butterfly leaves component k (k < 8) in
 // lanes 4k..4k+3 after 7 shuffles, component 8 takes a plain butterfly, and
 // lanes 4k and lane 1 widen their sums to double (with integer operations, off
 // the narrow FP64 pipe) and issue the adds.
-__device__ __forceinline__ void warp_reduce_add9(float (&v)[9], double *__restrict__ acc, int lane)
+template <bool kDet>
+__device__ __forceinline__ void warp_reduce_add9(float (&v)[9], double *__restrict__ acc, int lane, uint2 esc)
 {
     const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
     float w[4];
@@ -322,18 +363,26 @@ __device__ __forceinline__ void warp_reduce_add9(float (&v)[9], double *__restri
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
     const float mine = (lane & 3) == 0 ? y : z;
-    if ((lane & 3) == 0 || lane == 1) atomicAdd(acc + ((lane & 3) == 0 ? (lane >> 2) : 8), widen(mine));
+    const int k = (lane & 3) == 0 ? (lane >> 2) : 8;
+    if ((lane & 3) == 0 || lane == 1) {
+        if (kDet)
+            atomicAdd(reinterpret_cast<unsigned long long *>(acc) + k,
+                      (unsigned long long)to_fixed(mine, det_exponent(esc, det_group(k))));
+        else
+            atomicAdd(acc + k, widen(mine));
+    }
 }
 
-template <bool kWarpSkip, bool kLastContrib, bool kCull>
+template <bool kWarpSkip, bool kLastContrib, bool kCull, bool kDet>
 __global__ void __launch_bounds__(kTilePixels, GSR_BWD_MIN_BLOCKS)
 k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
            const uint2 *__restrict__ ranges, const uint32_t *__restrict__ order, int width, int height,
            int tiles_x, const float4 *__restrict__ dl_dout, const float *__restrict__ final_T,
-           const uint32_t *__restrict__ last_in, double *__restrict__ grad_acc)
+           const uint32_t *__restrict__ last_in, double *__restrict__ grad_acc, const uint2 *__restrict__ escale)
 {
     grid_dependency_begin();
-    __shared__ StagedBatch sb;
+    __shared__ StagedBatchT<kBwdBatch> sb;
+    __shared__ uint2 s_esc[kDet ? kBwdBatch : 1];   // fixed-point exponents (deterministic mode)
     __shared__ uint32_t s_wmax[kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t wbit = 1u << warp;
@@ -370,15 +419,18 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
     }
     float3 S = make_float3(0.0f, 0.0f, 0.0f);
 
-    for (int bend = (int)cta_end; bend > 0; bend -= kBatch) {
-        const int bstart = max(0, bend - kBatch);
+    for (int bend = (int)cta_end; bend > 0; bend -= kBwdBatch) {
+        const int bstart = max(0, bend - kBwdBatch);
         const int cnt = bend - bstart;
         __syncthreads();
 #pragma unroll
-        for (int q = 0; q < GSR_STAGE_PER_THREAD; ++q) {
+        for (int q = 0; q < GSR_BWD_STAGE_PER_THREAD; ++q) {
             const int slot = q * kTilePixels + threadIdx.x;
-            if (slot < cnt)
-                stage_splat<kCull>(sb, slot, splats, __ldg(sorted_idx + range.x + bstart + slot), x0, y0);
+            if (slot < cnt) {
+                const uint32_t idx = __ldg(sorted_idx + range.x + bstart + slot);
+                stage_splat<kCull>(sb, slot, splats, idx, x0, y0);
+                if (kDet) s_esc[slot] = escale[idx];
+            }
         }
         __syncthreads();
         const int jlim = min(cnt, (int)warp_end - bstart);  // this warp's positions: j < jlim
@@ -433,7 +485,8 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                     S.z = __fmaf_rn(c.z, aT, S.z);
                     T = Tj;
                 }
-                warp_reduce_add9(v, grad_acc + 9 * (size_t)__float_as_uint(aux.w), lane);
+                warp_reduce_add9<kDet>(v, grad_acc + 9 * (size_t)__float_as_uint(aux.w), lane,
+                                       kDet ? s_esc[j] : make_uint2(0u, 0u));
             }
         }
     }
@@ -450,39 +503,209 @@ __global__ void k_grad_to_float(double *__restrict__ acc, float *__restrict__ gr
     }
 }
 
+// Deterministic mode: the maxima the fixed-point bounds need, one triple per
+// block (no atomics): part[3 b], part[3 b + 1] hold the bits of the block's
+// largest |dL/dout rgb| and largest |rgb| of a splat whose fields are all
+// finite (non-negative floats order like their bits); part[3 b + 2] is set when
+// the block saw a non-finite dL/dout.
+constexpr int kDetMaxBlocks = 1024;
+
+__global__ void __launch_bounds__(256) k_det_maxima(const float *__restrict__ splats, int n,
+                                                    const float4 *__restrict__ dl_dout, size_t npx,
+                                                    uint32_t *__restrict__ part)
+{
+    grid_dependency_begin();
+    __shared__ uint32_t s_m[3][8];
+    float gm = 0.0f, cm = 0.0f;
+    uint32_t nonfinite = 0;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < npx; i += stride) {
+        const float4 d = dl_dout[i];
+        nonfinite |= !(isfinite(d.x) && isfinite(d.y) && isfinite(d.z));
+        gm = fmaxf(gm, fmaxf(fabsf(d.x), fmaxf(fabsf(d.y), fabsf(d.z))));
+    }
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < (size_t)n; i += stride) {
+        const float *sp = splats + 9 * i;
+        bool finite = true;
+#pragma unroll
+        for (int k = 0; k < 9; ++k) finite &= isfinite(sp[k]);
+        if (finite) cm = fmaxf(cm, fmaxf(fabsf(sp[5]), fmaxf(fabsf(sp[6]), fabsf(sp[7]))));
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t gb = __reduce_max_sync(kFull, __float_as_uint(gm));
+    const uint32_t cb = __reduce_max_sync(kFull, __float_as_uint(cm));
+    const uint32_t nf = __reduce_or_sync(kFull, nonfinite);
+    if (lane == 0) {
+        s_m[0][warp] = gb;
+        s_m[1][warp] = cb;
+        s_m[2][warp] = nf;
+    }
+    __syncthreads();
+    if (threadIdx.x < 3) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) m = threadIdx.x == 2 ? (m | s_m[2][w]) : max(m, s_m[threadIdx.x][w]);
+        part[3 * blockIdx.x + threadIdx.x] = m;
+    }
+}
+
+// The global maxima from the per-block triples (every thread gets them).
+__device__ __forceinline__ void det_global_maxima(const uint32_t *__restrict__ part, int nparts, float &G, float &C,
+                                                  bool &nonfinite)
+{
+    __shared__ uint32_t s_g[3];
+    if (threadIdx.x < 32) {
+        uint32_t g = 0, c = 0, f = 0;
+        for (int b = threadIdx.x; b < nparts; b += 32) {
+            g = max(g, part[3 * b]);
+            c = max(c, part[3 * b + 1]);
+            f |= part[3 * b + 2];
+        }
+        g = __reduce_max_sync(kFull, g);
+        c = __reduce_max_sync(kFull, c);
+        f = __reduce_or_sync(kFull, f);
+        if (threadIdx.x == 0) {
+            s_g[0] = g;
+            s_g[1] = c;
+            s_g[2] = f;
+        }
+    }
+    __syncthreads();
+    G = __uint_as_float(s_g[0]);
+    C = __uint_as_float(s_g[1]);
+    nonfinite = s_g[2] != 0;
+}
+
+// Deterministic mode: per splat, the exponents E of its four gradient groups
+// (mean, conic, colour, color_a), packed as int16.  E makes the total of every
+// partial the launch can add for the group below 2^62 in magnitude:
+//
+// One pixel's terms.  With G = max |dL/dout rgb|, C = max |rgb|, and
+// alpha <= o' = min(0.999, color_a), the transmittances at most 1 and the
+// colour S of the splats behind at most C, |dL/dalpha| <= 3 G C (1 + 1/(1 - o'))
+// = A.  A term reaches the conic and mean through dL/dsigma = -dL/dalpha raw,
+// raw = color_a e^-sigma < 0.999, and sigma bounds the offsets: 1/2 dx^2 <=
+// sigma c / det, 1/2 dy^2 <= sigma a / det, |a dx + b dy| <= sqrt(2 sigma a),
+// |b dx + c dy| <= sqrt(2 sigma c); with sigma e^-sigma <= 1/e and
+// sqrt(sigma) e^-sigma <= 1 / sqrt(2e) (or raw < 0.999, sigma < 5.55):
+//   colour G o';  color_a A;  mean A color_a sqrt(max(a, c) / e);
+//   conic A color_a max(c, 2 sqrt(a c), a) / (e det).
+// A conic too ill-conditioned for its sigma to carry those bounds through
+// float rounding (lambda_max / lambda_min > 1e4) uses the box instead:
+// |dx|, |dy| <= hx, hy, the 3-sigma box radius plus a tile and a pixel.
+//
+// Partials.  A warp adds 32 pixels' terms, and each of the 8 warps of a tile
+// the splat's box reaches adds at most one partial; the total is below
+// 2 (margin) x 32 x 8 x tiles x the bound.
+__global__ void __launch_bounds__(256) k_det_scales(const float *__restrict__ splats, int n,
+                                                    const uint32_t *__restrict__ part, int nparts, int num_tiles,
+                                                    uint2 *__restrict__ escale)
+{
+    // Float arithmetic in the log2 domain (GB300's FP64 pipe is narrow, and
+    // nothing overflows there); every bound carries a factor 2 of margin, far
+    // above the rounding of these few operations.
+    grid_dependency_begin();
+    float G, C;
+    bool nonfinite;
+    det_global_maxima(part, nparts, G, C, nonfinite);
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float *sp = splats + 9 * (size_t)i;
+    const float a = sp[2], b = sp[3], c = sp[4];
+    const float op = fmaxf(0.0f, sp[8]);    // raw = color_a e^-sigma <= op
+    const float o = fminf(0.999f, op);       // alpha <= o
+    const float l2A = log2f(3.0f * G) + log2f(C) + log2f(1.0f + 1.0f / (1.0f - o));
+    const float detf = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, b));
+    const float neg_inf = -INFINITY;
+    float l2[4] = {neg_inf, neg_inf, log2f(G) + log2f(o), l2A};
+    float l2tiles = 0.0f;
+    if (detf > 0.0f && a > 0.0f && isfinite(detf) && isfinite(op)) {
+        const float rx = 3.0f * sqrtf(c / detf) * 1.0001f, ry = 3.0f * sqrtf(a / detf) * 1.0001f;
+        l2tiles = fminf(log2f((float)num_tiles),
+                        log2f(floorf(2.0f * rx / 16.0f) + 2.0f) + log2f(floorf(2.0f * ry / 16.0f) + 2.0f));
+        const float half_tr = 0.5f * (a + c), rad = sqrtf(0.25f * (a - c) * (a - c) + b * b);
+        const float lmax = half_tr + rad, lmin = detf / lmax;
+        const float inv_e = 0.36787944f, amax = fmaxf(a, c);
+        if (lmin > 0.0f && lmax <= 1e4f * lmin) {
+            // raw < 0.999 and sigma < 5.55 also cap raw sqrt(sigma) and raw sigma
+            l2[0] = l2A + log2f(fminf(op * sqrtf(amax * inv_e), 0.999f * sqrtf(2.0f * 5.55f * amax)));
+            l2[1] = l2A + log2f(fminf(op * inv_e, 0.999f * 5.55f)) +
+                    log2f(fmaxf(fmaxf(c, 2.0f * sqrtf(a) * sqrtf(c)), a)) - log2f(detf);
+        } else {
+            const float hx = rx + 17.0f, hy = ry + 17.0f;
+            l2[0] = l2A + log2f(fmaxf(fabsf(a) * hx + fabsf(b) * hy, fabsf(b) * hx + fabsf(c) * hy));
+            l2[1] = l2A + fmaxf(fmaxf(2.0f * log2f(hx) - 1.0f, log2f(hx) + log2f(hy)), 2.0f * log2f(hy) - 1.0f);
+        }
+    }
+    // 2 (margin) x 32 lanes x 8 warps per tile x tiles
+    const float l2total = 9.0f + l2tiles;
+    int E[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float t = l2[k] + l2total + 0.01f;   // log2 of the bound on the total
+        E[k] = isfinite(t) ? max(-1100, min(1100, (int)floorf(t) + 1 - 62)) : (t > 0.0f ? 1100 : -200);
+    }
+    escale[i] = make_uint2(((uint32_t)E[0] & 0xffffu) | ((uint32_t)E[1] << 16),
+                           ((uint32_t)E[2] & 0xffffu) | ((uint32_t)E[3] << 16));
+}
+
+// Deterministic mode: grad = acc 2^E, and acc back to zero.  A non-finite
+// dL/dout makes every gradient NaN.
+__global__ void __launch_bounds__(256) k_grad_to_float_det(long long *__restrict__ acc,
+                                                           const uint2 *__restrict__ escale,
+                                                           const uint32_t *__restrict__ part, int nparts,
+                                                           float *__restrict__ grad, size_t count)
+{
+    grid_dependency_begin();
+    float G, C;
+    bool nonfinite;
+    det_global_maxima(part, nparts, G, C, nonfinite);
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t splat = i / 9;
+        const int k = (int)(i - splat * 9);
+        const int E = det_exponent(escale[splat], det_group(k));
+        const float f = ldexpf(__ll2float_rn(acc[i]), E);
+        grad[i] = nonfinite ? __int_as_float(0x7fc00000) : f;
+        acc[i] = 0;
+    }
+}
+
 template <bool kSkip, bool kLc>
 cudaError_t launch_backward_cull(gsr_ctx *ctx, bool cull, int grid, cudaStream_t stream, const float *splats,
                                  const gsr_bins *bins, const uint32_t *order, const float *dl_dout,
-                                 const float *final_T, const uint32_t *last_contrib, double *acc)
+                                 const float *final_T, const uint32_t *last_contrib, double *acc,
+                                 const uint2 *escale)
 {
     auto go = [&](auto kernel) {
         return launch_kernel(ctx, kernel, dim3(grid), dim3(kTilePixels), stream, splats, bins->sorted_idx,
                              reinterpret_cast<const uint2 *>(bins->tile_ranges), order, bins->width,
                              bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
-                             last_contrib, acc);
+                             last_contrib, acc, escale);
     };
-    return cull ? go(k_backward<kSkip, kLc, true>) : go(k_backward<kSkip, kLc, false>);
+    if (escale) return cull ? go(k_backward<kSkip, kLc, true, true>) : go(k_backward<kSkip, kLc, false, true>);
+    return cull ? go(k_backward<kSkip, kLc, true, false>) : go(k_backward<kSkip, kLc, false, false>);
 }
 
 // The backward kernel variant the context's options select, launching tiles
 // in `order` (NULL: tile order) and accumulating into acc.
 cudaError_t launch_backward(gsr_ctx *ctx, cudaStream_t stream, const float *splats, const gsr_bins *bins,
                             const uint32_t *order, const float *dl_dout, const float *final_T,
-                            const uint32_t *last_contrib, double *acc)
+                            const uint32_t *last_contrib, double *acc, const uint2 *escale)
 {
     const int grid = bins->tiles_x * bins->tiles_y;
     const bool cull = ctx->opt_warp_cull != 0;
     if (ctx->opt_warp_skip && ctx->opt_last_contrib)
         return launch_backward_cull<true, true>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                                last_contrib, acc);
+                                                last_contrib, acc, escale);
     if (ctx->opt_warp_skip)
         return launch_backward_cull<true, false>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                                 last_contrib, acc);
+                                                 last_contrib, acc, escale);
     if (ctx->opt_last_contrib)
         return launch_backward_cull<false, true>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                                 last_contrib, acc);
+                                                 last_contrib, acc, escale);
     return launch_backward_cull<false, false>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                              last_contrib, acc);
+                                              last_contrib, acc, escale);
 }
 
 // Per tile: the largest last_contributor of its pixels (one warp per tile), the
@@ -577,17 +800,53 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
                          "tile cost launch")) ||
         (rc = launch_tile_order(ctx, nullptr, ctx->bwd_tile_cost, num_tiles, ctx->bwd_tile_order, stream)))
         return rc;
+    // Deterministic mode: the maxima and the per-splat fixed-point exponents.
+    const uint2 *escale = nullptr;
+    if (ctx->opt_deterministic) {
+        if ((size_t)std::max(n, 1) > ctx->cap_det || !ctx->det_escale) {
+            if (ctx->det_escale) {
+                if ((rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize"))) return rc;
+                cudaFree(ctx->det_escale);
+            }
+            ctx->det_escale = nullptr;
+            ctx->det_maxima = nullptr;
+            ctx->cap_det = 0;
+            const size_t cap = std::max<size_t>((size_t)n, 1);
+            if (device_alloc(ctx, (void **)&ctx->det_escale, cap * sizeof(uint2) + 3 * kDetMaxBlocks * sizeof(uint32_t)) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                ctx->det_escale = nullptr;
+                return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the deterministic scales");
+            }
+            ctx->det_maxima = reinterpret_cast<uint32_t *>(ctx->det_escale + cap);
+            ctx->cap_det = cap;
+        }
+        const size_t npx = (size_t)bins->width * bins->height;
+        if ((rc = cuda_check(ctx, launch_kernel(ctx, k_det_maxima, dim3(kDetMaxBlocks), dim3(256), stream, splats,
+                                                (int)n, reinterpret_cast<const float4 *>(dl_dout), npx,
+                                                ctx->det_maxima),
+                             "deterministic maxima launch")))
+            return rc;
+        if (n > 0 && (rc = cuda_check(ctx, launch_kernel(ctx, k_det_scales, dim3((n + 255) / 256), dim3(256), stream,
+                                                         splats, (int)n, (const uint32_t *)ctx->det_maxima,
+                                                         kDetMaxBlocks, num_tiles, ctx->det_escale),
+                                      "deterministic scales launch")))
+            return rc;
+        escale = ctx->det_escale;
+    }
     ctx->grad_acc_zero = false;
     if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins, ctx->bwd_tile_order, dl_dout, final_T,
-                                              last_contrib, ctx->grad_acc),
+                                              last_contrib, ctx->grad_acc, escale),
                          "backward launch")))
         return rc;
     if (count > 0) {
         const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)SM_BLOCKS_CAP);
-        if ((rc = cuda_check(ctx, launch_kernel(ctx, k_grad_to_float, dim3(blocks), dim3(256), stream,
-                                                ctx->grad_acc, grad, count),
-                             "gradient conversion launch")))
-            return rc;
+        const cudaError_t e =
+            escale ? launch_kernel(ctx, k_grad_to_float_det, dim3(blocks), dim3(256), stream,
+                                   reinterpret_cast<long long *>(ctx->grad_acc), escale,
+                                   (const uint32_t *)ctx->det_maxima, kDetMaxBlocks, grad, count)
+                   : launch_kernel(ctx, k_grad_to_float, dim3(blocks), dim3(256), stream, ctx->grad_acc, grad, count);
+        if ((rc = cuda_check(ctx, e, "gradient conversion launch"))) return rc;
     }
     ctx->grad_acc_zero = true;
     return GSR_OK;
@@ -639,6 +898,8 @@ int rasterize_backward_noalloc(gsr_ctx *ctx, const float *splats, int32_t n, con
                         std::to_string(GSR_NOALLOC_MAX_SPLATS) + ")");
     if (ctx->device < 0 || ctx->device >= 64)
         return fail(ctx, GSR_ERR_INVALID_ARG, "device ordinal out of range for the fixed scratch table");
+    if (ctx->opt_deterministic)
+        return fail(ctx, GSR_ERR_INVALID_ARG, "the deterministic backward needs the context's arena");
     double *acc = g_noalloc_ptr[ctx->device];
     if (!acc) {
         // First call on this device (the device is current here): find the
@@ -655,7 +916,7 @@ int rasterize_backward_noalloc(gsr_ctx *ctx, const float *splats, int32_t n, con
     if (rc) return rc;
     // No allocation here: the forward's launch order (pair count) from the bins.
     if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins, bins->tile_order, dl_dout, final_T,
-                                              last_contrib, acc),
+                                              last_contrib, acc, nullptr),
                          "backward launch")))
         return rc;
     if (count == 0) return GSR_OK;

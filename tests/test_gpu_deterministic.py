@@ -1,0 +1,102 @@
+"""The deterministic backward (GSR_OPT_DETERMINISTIC): 64-bit fixed-point
+accumulation gives the same gradient bits on every run and under every launch
+variant, and the gradients keep the oracle parity of the default backward."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+from gpu_helpers import check_backward, run_gpu, run_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gsr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gaussian_splatting_tile_bin_gb300 as g
+    return g
+
+
+@pytest.fixture()
+def ctx(gsr):
+    c = gsr.Context(0)
+    c.set_option("deterministic", True)
+    yield c
+    c.close()
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "lego_early", "stress"])
+def test_deterministic_parity(gsr, ctx, name):
+    wl = gen.make(name)
+    g = run_gpu(gsr, ctx, wl)
+    o = run_oracle(wl)
+    print(name, check_backward(g, o))
+
+
+def test_deterministic_parity_elongated_and_overlap(gsr, ctx):
+    for wl in (gen.elongated_fixture(), gen.overlap_fixture(32), gen.overlap_fixture(24)):
+        check_backward(run_gpu(gsr, ctx, wl), run_oracle(wl))
+
+
+def _grads(gsr, ctx, wl, runs):
+    sp, dp, dl = to_dev(wl.splats), to_dev(wl.depths), to_dev(wl.dl_dout)
+    bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+    _, t, last = gsr.rasterize_forward(ctx, sp, bins)
+    out = [gsr.rasterize_backward(ctx, sp, bins, dl, t, last).cpu().numpy() for _ in range(runs)]
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("name", ["lego_early", "stress"])
+def test_same_bits_on_every_run(gsr, ctx, name):
+    runs = _grads(gsr, ctx, gen.make(name), 10)
+    for r in runs[1:]:
+        assert np.array_equal(r.view(np.uint32), runs[0].view(np.uint32))
+
+
+def test_same_bits_under_every_launch_variant(gsr, ctx):
+    """Culling, the last-contributor bound, the warp skip and dependent launch
+    change which warps add which partials and when; the sums stay exact."""
+    wl = gen.lego_early()
+    ref = _grads(gsr, ctx, wl, 1)[0]
+    for opt in ("warp_cull", "bwd_last_contrib", "bwd_warp_skip", "pdl"):
+        ctx.set_option(opt, False)
+        got = _grads(gsr, ctx, wl, 1)[0]
+        ctx.set_option(opt, True)
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), opt
+
+
+def test_close_to_the_default_backward(gsr, ctx):
+    wl = gen.lego_final()
+    det = _grads(gsr, ctx, wl, 1)[0].astype(np.float64)
+    ctx.set_option("deterministic", False)
+    dbl = _grads(gsr, ctx, wl, 1)[0].astype(np.float64)
+    diff = np.abs(det - dbl) / (1e-4 + 1e-4 * np.abs(dbl))
+    print("deterministic vs default: max |d| / tolerance", float(diff.max()))
+    assert diff.max() < 0.05
+
+
+def test_non_finite_dl_dout_gives_nan(gsr, ctx):
+    wl = gen.tiny()
+    wl.dl_dout[5, 1] = np.nan
+    g = run_gpu(gsr, ctx, wl)
+    assert np.all(np.isnan(g["grad"]))
+
+
+def test_noalloc_rejects_deterministic(gsr, ctx):
+    import ctypes
+    from gaussian_splatting_tile_bin_gb300 import _abi
+    fn = _abi.lib.gsr_rasterize_backward_noalloc
+    P = ctypes.c_void_p
+    fn.argtypes = [P, P, ctypes.c_int32, ctypes.POINTER(_abi._Bins), P, P, P, P, P]
+    fn.restype = ctypes.c_int
+    wl = gen.tiny()
+    sp, dp, dl = to_dev(wl.splats), to_dev(wl.depths), to_dev(wl.dl_dout)
+    bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+    _, t, last = gsr.rasterize_forward(ctx, sp, bins)
+    grad = torch.empty((wl.n, 9), dtype=torch.float32, device="cuda:0")
+    rc = fn(ctx._h, P(sp.data_ptr()), wl.n, ctypes.byref(bins.raw), P(dl.data_ptr()), P(t.data_ptr()),
+            P(last.data_ptr()), P(grad.data_ptr()), P(torch.cuda.current_stream().cuda_stream))
+    assert rc == 1
