@@ -98,6 +98,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--deterministic", action="store_true",
                    help="time the backward's deterministic mode (fixed-point accumulation)")
+    p.add_argument("--bwd-per-splat", action="store_true",
+                   help="time the backward's transposed (per-splat) loop nest instead of the per-pixel one")
     p.add_argument("--no-projection", action="store_true",
                    help="skip the separate timing of the projection kernels")
     p.add_argument("--min-warm-s", type=float, default=1.5,
@@ -374,6 +376,8 @@ def gpu_arm(args):
     ctx = gsr.Context(local)
     if args.deterministic:
         ctx.set_option("deterministic", True)
+    if args.bwd_per_splat:
+        ctx.set_option("bwd_per_splat", True)
     stream = torch.cuda.current_stream(dev)
 
     sp = torch.from_numpy(wl.splats).to(dev)
@@ -449,6 +453,8 @@ def gpu_arm(args):
             c2 = ctx if k == 0 else gsr.Context(local)
             if args.deterministic:
                 c2.set_option("deterministic", True)
+            if args.bwd_per_splat:
+                c2.set_option("bwd_per_splat", True)
             slots.append({
                 "ctx": c2, "stream": torch.cuda.Stream(dev),
                 "sp": torch.empty_like(sp), "dp": torch.empty_like(dp), "dl": torch.empty_like(dl),
@@ -519,7 +525,8 @@ def gpu_arm(args):
                        "l2": "flushed between timed steps (256 MB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "backward_accumulation": "fixed point (deterministic)" if args.deterministic
-                       else "double atomics"},
+                       else "double atomics",
+                       "backward_loop_nest": "per splat (diagonal)" if args.bwd_per_splat else "per pixel"},
             "ms_per_step_median": float(np.median(tot_ms)), "ms_per_step_std": float(np.std(tot_ms)),
             "stages_ms": {"bin": float(bin_ms.mean()), "forward": float(fwd_ms.mean()),
                           "backward": float(bwd_ms.mean()),

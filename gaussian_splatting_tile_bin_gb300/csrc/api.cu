@@ -132,6 +132,7 @@ int gsr_set_option(gsr_ctx *ctx, int option, int value)
     case GSR_OPT_PDL: ctx->opt_pdl = value; return GSR_OK;
     case GSR_OPT_FAIL_NEXT_ALLOC: ctx->fail_next_alloc = value; return GSR_OK;
     case GSR_OPT_DETERMINISTIC: ctx->opt_deterministic = value; return GSR_OK;
+    case GSR_OPT_BWD_PER_SPLAT: ctx->opt_bwd_per_splat = value; return GSR_OK;
     default: return fail(ctx, GSR_ERR_INVALID_ARG, "unknown option " + std::to_string(option));
     }
 }

@@ -36,6 +36,7 @@ struct gsr_ctx {
     int opt_warp_cull = 1;
     int opt_pdl = 1;
     int opt_deterministic = 0;
+    int opt_bwd_per_splat = 0;
     int fail_next_alloc = 0;                    // test hook: the next device allocation fails
     int num_sms = 0;                            // multiprocessors of the device (0: not queried yet)
 

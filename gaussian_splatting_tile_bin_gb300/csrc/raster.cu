@@ -492,6 +492,129 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
     }
 }
 
+// --- per-splat backward ("M3 per-splat backward", section 1) ---------------
+//
+// The transposed loop nest: one warp per tile, one lane per splat.  The tile's
+// composited range is taken back to front in groups of 32 splats; lane l holds
+// the splat at position end - 1 - l of the group and meets pixel p at step
+// p + l (diagonal scheduling), right after lane l - 1 (the splat behind it) has
+// left that pixel's state (T, S) in shared memory.  A lane sums its splat's 9
+// gradient components over the tile's 256 pixels in registers, in a fixed
+// order, and adds them once per (tile, splat): no reduction across lanes, and
+// no atomics within a tile.  Each (pixel, splat) evaluation is the per-pixel
+// kernel's: the same skips, the same un-blend of T, the same formulas.
+template <bool kDet>
+__global__ void __launch_bounds__(32)
+k_backward_per_splat(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
+                     const uint2 *__restrict__ ranges, const uint32_t *__restrict__ order, int width, int height,
+                     int tiles_x, const float4 *__restrict__ dl_dout, const float *__restrict__ final_T,
+                     const uint32_t *__restrict__ last_in, double *__restrict__ grad_acc,
+                     const uint2 *__restrict__ escale)
+{
+    grid_dependency_begin();
+    __shared__ float sT[kTilePixels];       // transmittance in front of the next splat to meet the pixel
+    __shared__ float sS[3][kTilePixels];    // colour of the splats behind it
+    __shared__ float sG[3][kTilePixels];    // dL/dout rgb
+    __shared__ uint32_t sL[kTilePixels];    // last_contributor (0 outside the image)
+    const int lane = threadIdx.x;
+    const int tile = order ? (int)order[blockIdx.x] : (int)blockIdx.x;
+    const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
+    const uint2 range = ranges[tile];
+    const uint32_t len = range.y - range.x;
+    uint32_t lmax = 0;
+    for (int p = lane; p < kTilePixels; p += 32) {
+        const int x = x0 + (p & 15), y = y0 + (p >> 4);
+        float T = 1.0f;
+        uint32_t L = 0;
+        float4 d = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (x < width && y < height) {
+            const size_t pix = (size_t)y * width + x;
+            T = final_T[pix];
+            L = min(last_in[pix], len);
+            d = dl_dout[pix];
+        }
+        sT[p] = T;
+        sS[0][p] = sS[1][p] = sS[2][p] = 0.0f;
+        sG[0][p] = d.x;
+        sG[1][p] = d.y;
+        sG[2][p] = d.z;
+        sL[p] = L;
+        lmax = max(lmax, L);
+    }
+    lmax = __reduce_max_sync(kFull, lmax);
+    __syncwarp();
+    for (int gend = (int)lmax; gend > 0; gend -= 32) {
+        const int pos = gend - 1 - lane;           // this lane's position in the tile's range
+        const bool valid = pos >= 0;
+        float4 geo = make_float4(0.0f, 0.0f, 0.0f, 0.0f), aux = geo, col = geo;
+        uint32_t idx = 0;
+        if (valid) {
+            idx = __ldg(sorted_idx + range.x + pos);
+            const float *sp = splats + 9 * (size_t)idx;
+            geo = make_float4(__ldg(sp + 0), __ldg(sp + 1), __ldg(sp + 2), __ldg(sp + 3));
+            const float o = __ldg(sp + 8);
+            aux = make_float4(__ldg(sp + 4), o, fminf(kSigmaSkip, __logf(o) + kLn255Margin), 0.0f);
+            col = make_float4(__ldg(sp + 5), __ldg(sp + 6), __ldg(sp + 7), 0.0f);
+        }
+        float v[9];
+#pragma unroll
+        for (int k = 0; k < 9; ++k) v[k] = 0.0f;
+        for (int step = 0; step < kTilePixels + 31; ++step) {
+            const int p = step - lane;
+            if (valid && p >= 0 && p < kTilePixels && (uint32_t)pos < sL[p]) {
+                const float px = (float)(x0 + (p & 15)), py = (float)(y0 + (p >> 4));
+                float dx, dy;
+                const float sigma = splat_sigma(geo, aux.x, px, py, dx, dy);
+                if (sigma >= 0.0f && sigma < aux.z) {
+                    float e, raw;
+                    const float alpha = splat_alpha(sigma, aux.y, e, raw);
+                    if (alpha >= kAlphaMin) {
+                        const float T = sT[p];
+                        const float one_m = __fsub_rn(1.0f, alpha);
+                        const float inv = __fdividef(1.0f, one_m);
+                        float Tj = T * inv;
+                        Tj = __fmaf_rn(inv, __fmaf_rn(-one_m, Tj, T), Tj);
+                        const float aT = alpha * Tj;
+                        const float gx = sG[0][p], gy = sG[1][p], gz = sG[2][p];
+                        const float Sx = sS[0][p], Sy = sS[1][p], Sz = sS[2][p];
+                        v[5] += gx * aT;
+                        v[6] += gy * aT;
+                        v[7] += gz * aT;
+                        float dA = gx * (col.x * Tj - Sx * inv);
+                        dA = __fmaf_rn(gy, col.y * Tj - Sy * inv, dA);
+                        dA = __fmaf_rn(gz, col.z * Tj - Sz * inv, dA);
+                        const float dRaw = raw < kAlphaMax ? dA : 0.0f;
+                        v[8] += dRaw * e;
+                        const float dSig = -dRaw * raw;
+                        v[0] += -dSig * __fmaf_rn(geo.z, dx, geo.w * dy);
+                        v[1] += -dSig * __fmaf_rn(geo.w, dx, aux.x * dy);
+                        v[2] += dSig * (0.5f * dx * dx);
+                        v[3] += dSig * (dx * dy);
+                        v[4] += dSig * (0.5f * dy * dy);
+                        sS[0][p] = __fmaf_rn(col.x, aT, Sx);
+                        sS[1][p] = __fmaf_rn(col.y, aT, Sy);
+                        sS[2][p] = __fmaf_rn(col.z, aT, Sz);
+                        sT[p] = Tj;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        if (valid) {
+            double *acc = grad_acc + 9 * (size_t)idx;
+            const uint2 esc = kDet ? escale[idx] : make_uint2(0u, 0u);
+#pragma unroll
+            for (int k = 0; k < 9; ++k) {
+                if (kDet)
+                    atomicAdd(reinterpret_cast<unsigned long long *>(acc) + k,
+                              (unsigned long long)to_fixed(v[k], det_exponent(esc, det_group(k))));
+                else
+                    atomicAdd(acc + k, widen(v[k]));
+            }
+        }
+    }
+}
+
 // grad = (float)acc, and acc back to zero for the next backward.
 __global__ void k_grad_to_float(double *__restrict__ acc, float *__restrict__ grad, size_t count)
 {
@@ -694,6 +817,15 @@ cudaError_t launch_backward(gsr_ctx *ctx, cudaStream_t stream, const float *spla
                             const uint32_t *last_contrib, double *acc, const uint2 *escale)
 {
     const int grid = bins->tiles_x * bins->tiles_y;
+    if (ctx->opt_bwd_per_splat) {
+        auto go = [&](auto kernel) {
+            return launch_kernel(ctx, kernel, dim3(grid), dim3(32), stream, splats, bins->sorted_idx,
+                                 reinterpret_cast<const uint2 *>(bins->tile_ranges), order, bins->width,
+                                 bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
+                                 last_contrib, acc, escale);
+        };
+        return escale ? go(k_backward_per_splat<true>) : go(k_backward_per_splat<false>);
+    }
     const bool cull = ctx->opt_warp_cull != 0;
     if (ctx->opt_warp_skip && ctx->opt_last_contrib)
         return launch_backward_cull<true, true>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,

@@ -106,12 +106,17 @@ enum {
     GSR_OPT_FAIL_NEXT_ALLOC = 5,  /* test hook (default 0): the context's next device allocation
                                      fails as if the GPU were out of memory; the call returns
                                      GSR_ERR_OOM and later calls allocate normally */
-    GSR_OPT_DETERMINISTIC = 6     /* default 0.  1: gsr_rasterize_backward accumulates in 64-bit fixed
+    GSR_OPT_DETERMINISTIC = 6,    /* default 0.  1: gsr_rasterize_backward accumulates in 64-bit fixed
                                      point (exponents chosen per splat from bounds on its terms), so
                                      its gradients are the same bits on every run, whatever order the
                                      warps add in ("M3 per-splat backward", sections 2 and 4: run-to-run
                                      self-noise).  A non-finite dL/dout makes every gradient NaN.  Not
                                      available to gsr_rasterize_backward_noalloc (GSR_ERR_INVALID_ARG). */
+    GSR_OPT_BWD_PER_SPLAT = 7     /* default 0.  1: the backward runs the transposed loop nest ("M3
+                                     per-splat backward", section 1): one warp per tile, one lane per
+                                     splat, the tile's pixels met in diagonal order, each lane's sums
+                                     kept in registers and added once per (tile, splat).  Same
+                                     gradients within float rounding; slower on this workload. */
 };
 
 typedef struct gsr_ctx gsr_ctx;

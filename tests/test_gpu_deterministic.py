@@ -100,3 +100,35 @@ def test_noalloc_rejects_deterministic(gsr, ctx):
     rc = fn(ctx._h, P(sp.data_ptr()), wl.n, ctypes.byref(bins.raw), P(dl.data_ptr()), P(t.data_ptr()),
             P(last.data_ptr()), P(grad.data_ptr()), P(torch.cuda.current_stream().cuda_stream))
     assert rc == 1
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "lego_early"])
+def test_per_splat_backward_parity(gsr, name):
+    """The transposed loop nest ("M3 per-splat backward", section 1) keeps the
+    oracle parity, with double accumulation across tiles."""
+    c = gsr.Context(0)
+    try:
+        c.set_option("bwd_per_splat", True)
+        wl = gen.make(name)
+        print(name, check_backward(run_gpu(gsr, c, wl), run_oracle(wl)))
+    finally:
+        c.close()
+
+
+def test_per_splat_backward_fixtures(gsr):
+    c = gsr.Context(0)
+    try:
+        c.set_option("bwd_per_splat", True)
+        for wl in (gen.elongated_fixture(), gen.overlap_fixture(32), gen.overlap_fixture(24)):
+            check_backward(run_gpu(gsr, c, wl), run_oracle(wl))
+    finally:
+        c.close()
+
+
+def test_per_splat_deterministic_same_bits(gsr, ctx):
+    ctx.set_option("bwd_per_splat", True)
+    wl = gen.lego_early()
+    runs = _grads(gsr, ctx, wl, 5)
+    for r in runs[1:]:
+        assert np.array_equal(r.view(np.uint32), runs[0].view(np.uint32))
+    check_backward(run_gpu(gsr, ctx, wl), run_oracle(wl))
