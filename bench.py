@@ -57,16 +57,16 @@ RASTER_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/raster.cu",
                   "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
 PROJECT_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/project.cu",
                    "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
-RASTER_SHA256 = "57454195c7c6063d3fa6761712abd223fb0e3395839f25a5c5da40765f671ee3"
-PROJECT_SHA256 = "af03230ed0e75024a78e2ac01240d844d06f339899c263eb0fb9c1518003ed96"
+RASTER_SHA256 = "bc52cb210818c1f78b4049a0778320c4cdef1d84b95be4bdcbe3e6f81664ce62"
+PROJECT_SHA256 = "569472d5cc6cac5dc5435ef69c278d328b198bcd1696a2d913b007b6986e2c3e"
 NCU_TRAFFIC = {
-    "forward": {"bytes": 22_277_376 + 2_048, "workload": "lego_final", "sources": RASTER_SOURCES,
+    "forward": {"bytes": 22_277_376 + 512, "workload": "lego_final", "sources": RASTER_SOURCES,
                 "sha256": RASTER_SHA256},
-    "backward": {"bytes": 50_601_472 + 74_752, "workload": "lego_final", "sources": RASTER_SOURCES,
+    "backward": {"bytes": 50_563_584 + 109_824, "workload": "lego_final", "sources": RASTER_SOURCES,
                  "sha256": RASTER_SHA256},
-    "project_forward": {"bytes": 22_957_056 + 0, "workload": "lego_scene", "sources": PROJECT_SOURCES,
+    "project_forward": {"bytes": 22_960_640 + 0, "workload": "lego_scene", "sources": PROJECT_SOURCES,
                         "sha256": PROJECT_SHA256},
-    "project_backward": {"bytes": 37_710_848 + 235_264, "workload": "lego_scene", "sources": PROJECT_SOURCES,
+    "project_backward": {"bytes": 37_724_416 + 367_360, "workload": "lego_scene", "sources": PROJECT_SOURCES,
                          "sha256": PROJECT_SHA256},
 }
 

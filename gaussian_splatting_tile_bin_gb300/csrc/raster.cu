@@ -255,6 +255,7 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
                 float dx, dy;
                 const float sigma = splat_sigma(geo, aux.x, px, py, dx, dy);
                 const bool in_range = !done && sigma >= 0.0f && sigma < aux.z;
+                if (!__any_sync(kFull, in_range)) continue;   // no lane can composite: skip the exponential
                 float e, raw;
                 const float alpha = splat_alpha(in_range ? sigma : 0.0f, aux.y, e, raw);
                 const bool ok = in_range && alpha >= kAlphaMin;
