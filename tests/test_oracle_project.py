@@ -154,3 +154,45 @@ def test_isotropic_gaussian_has_no_rotation_gradient():
     assert np.all(gabs[:, 6:10] > 0)
     assert np.all(np.abs(grad[:, 6:10]) <= 1e-12 * gabs[:, 6:10])
     assert np.all(np.abs(grad) <= gabs * (1 + 1e-12))
+
+
+def test_chain_rule_through_the_rasterizer():
+    """d/dtheta of sum(dL/dout . render(project(theta))) by central differences
+    of the double oracle (bins held fixed: they are piecewise constant) against
+    the oracle's projection backward of its double rasterizer backward."""
+    rng = np.random.default_rng(12)
+    n, size = 30, 48
+    g = np.zeros((n, 14))
+    g[:, 0:2] = rng.uniform(-1.2, 1.2, (n, 2))
+    g[:, 2] = rng.uniform(-0.5, 0.5, n)
+    g[:, 3:6] = rng.uniform(np.log(0.15), np.log(0.5), (n, 3))
+    g[:, 6:10] = rng.normal(size=(n, 4))
+    g[:, 10] = rng.normal(0.0, 1.0, n)
+    g[:, 11:14] = rng.uniform(0, 1, (n, 3))
+    cam = camera(t=(0.0, 0.0, 4.0), fx=60.0, fy=60.0, cx=23.5, cy=23.5)
+    dl = np.zeros((size * size, 4))
+    dl[:, 0:3] = rng.normal(size=(size * size, 3))
+    sp, d, vis = oracle.project_forward(g, cam)
+    assert vis.all()
+    _, idx, ranges = oracle.bin_splats(sp.astype(np.float32), d.astype(np.float32), size, size)
+    b = oracle.backward(sp, idx, ranges, size, size, dl, f64=True)
+    grad = oracle.project_backward(g, cam, b["grad"])
+
+    def loss(gg):
+        s2, _, _ = oracle.project_forward(gg, cam)
+        out = oracle.forward(s2, idx, ranges, size, size, f64=True)["out"]
+        return float(np.sum(out[:, 0:3] * dl[:, 0:3]))
+
+    checked = 0
+    for i in range(n):
+        if b["knife"][i]:
+            continue
+        for k in (0, 1, 2, 3, 5, 6, 8, 10, 12):
+            h = 1e-6 * max(1.0, abs(g[i, k]))
+            gp, gm = g.copy(), g.copy()
+            gp[i, k] += h
+            gm[i, k] -= h
+            fd = (loss(gp) - loss(gm)) / (2 * h)
+            assert grad[i, k] == pytest.approx(fd, rel=1e-3, abs=1e-4 * (1 + abs(fd))), (i, k, grad[i, k], fd)
+            checked += 1
+    assert checked >= 100
