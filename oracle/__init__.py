@@ -61,7 +61,7 @@ def _load():
         bw = getattr(lib, f"orc_backward_{sfx}")
         bw.argtypes = [P, i32, P, P, i32, i32, P, P, P, P, f64, f64, P]
         bw.restype = None
-    for name in ("orc_forward_untiled_f32", "orc_forward_untiled_noskip_f32"):
+    for name in ("orc_forward_untiled_f32", "orc_forward_untiled_noskip_f32", "orc_forward_untiled_nobox_f32"):
         fn = getattr(lib, name)
         fn.argtypes = [P, P, i32, i32, i32, P, P, P]
         fn.restype = None
@@ -139,14 +139,19 @@ def forward(splats, idx, ranges, width, height, *, f64=False, eps_alpha=0.0, sig
             "counters": {"n_eval": int(cnt[0]), "n_exp": int(cnt[1]), "n_contrib": int(cnt[2])}}
 
 
-def forward_untiled(splats, depths, width, height, *, sigma_skip=True):
+def forward_untiled(splats, depths, width, height, *, sigma_skip=True, box=True):
+    """Brute force over all splats per pixel.  box=False drops the 3-sigma box
+    predicate (a diagnostic of the colour the box truncates)."""
     lib = _load()
     s, d = _f32(splats).reshape(-1, 9), _f32(depths).reshape(-1)
     npx = width * height
     out = np.zeros((npx, 4), dtype=np.float32)
     final_t = np.zeros(npx, dtype=np.float32)
     last = np.zeros(npx, dtype=np.uint32)
-    fn = lib.orc_forward_untiled_f32 if sigma_skip else lib.orc_forward_untiled_noskip_f32
+    if not box:
+        fn = lib.orc_forward_untiled_nobox_f32
+    else:
+        fn = lib.orc_forward_untiled_f32 if sigma_skip else lib.orc_forward_untiled_noskip_f32
     fn(_ptr(s), _ptr(d), s.shape[0], width, height, _ptr(out), _ptr(final_t), _ptr(last))
     return {"out": out, "final_T": final_t, "last": last}
 

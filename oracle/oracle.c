@@ -205,9 +205,20 @@ static int cmp_depth(const void *pa, const void *pb)
     return 0;
 }
 
+/* The culling rule without the box: every field finite, depth > 0, a > 0 and
+ * det > 0 (the binning's own tests, before its tile rectangle). */
+static int splat_valid(const float *s, float depth)
+{
+    for (int k = 0; k < 9; ++k)
+        if (!isfinite(s[k])) return 0;
+    if (!isfinite(depth) || !(depth > 0.0f)) return 0;
+    float det = s[2] * s[4] - s[3] * s[3];
+    return s[2] > 0.0f && det > 0.0f;
+}
+
 static void forward_untiled(const float *splats, const float *depths, int32_t n, int32_t width,
                             int32_t height, float *out_rgbw, float *final_T, uint32_t *last,
-                            int skip_sigma)
+                            int skip_sigma, int box)
 {
     int32_t tiles_x = (width + ORC_TILE - 1) / ORC_TILE;
     int32_t tiles_y = (height + ORC_TILE - 1) / ORC_TILE;
@@ -219,6 +230,12 @@ static void forward_untiled(const float *splats, const float *depths, int32_t n,
         order[i].idx = (uint32_t)i;
         alive[i] = (uint8_t)orc_tile_rect(splats + 9 * (int64_t)i, depths[i], tiles_x, tiles_y,
                                          rects + 4 * (int64_t)i);
+        if (!box) {
+            /* every pixel of the image admits every valid splat */
+            alive[i] = (uint8_t)splat_valid(splats + 9 * (int64_t)i, depths[i]);
+            int32_t *r = rects + 4 * (int64_t)i;
+            r[0] = 0; r[1] = 0; r[2] = tiles_x - 1; r[3] = tiles_y - 1;
+        }
     }
     qsort(order, (size_t)n, sizeof *order, cmp_depth);
     int64_t cnt[3] = {0, 0, 0};
@@ -252,12 +269,18 @@ static void forward_untiled(const float *splats, const float *depths, int32_t n,
 void orc_forward_untiled_f32(const float *splats, const float *depths, int32_t n, int32_t width,
                              int32_t height, float *out_rgbw, float *final_T, uint32_t *last)
 {
-    forward_untiled(splats, depths, n, width, height, out_rgbw, final_T, last, 1);
+    forward_untiled(splats, depths, n, width, height, out_rgbw, final_T, last, 1, 1);
 }
 
 void orc_forward_untiled_noskip_f32(const float *splats, const float *depths, int32_t n,
                                     int32_t width, int32_t height, float *out_rgbw,
                                     float *final_T, uint32_t *last)
 {
-    forward_untiled(splats, depths, n, width, height, out_rgbw, final_T, last, 0);
+    forward_untiled(splats, depths, n, width, height, out_rgbw, final_T, last, 0, 1);
+}
+
+void orc_forward_untiled_nobox_f32(const float *splats, const float *depths, int32_t n, int32_t width,
+                                   int32_t height, float *out_rgbw, float *final_T, uint32_t *last)
+{
+    forward_untiled(splats, depths, n, width, height, out_rgbw, final_T, last, 1, 0);
 }

@@ -84,6 +84,13 @@ void orc_forward_untiled_noskip_f32(const float *splats, const float *depths, in
                                     int32_t width, int32_t height, float *out_rgbw,
                                     float *final_T, uint32_t *last);
 
+/* Diagnostic: the brute force without the 3-sigma box predicate (every valid
+ * splat may reach every pixel); its difference from orc_forward_untiled_f32 is
+ * the colour the box truncates (sigma in [4.5, 5.55) lies outside the box). */
+void orc_forward_untiled_nobox_f32(const float *splats, const float *depths, int32_t n,
+                                   int32_t width, int32_t height, float *out_rgbw,
+                                   float *final_T, uint32_t *last);
+
 /* Backward: gradient of L = sum_p sum_ch dl_dout[p][ch] * out[p][ch] (ch = rgb;
  * w carries no gradient) with respect to the 9 Splat2D fields, accumulated in
  * double into grad[n*9] (overwritten).  gabs (nullable, n*9): the sums of the

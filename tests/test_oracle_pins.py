@@ -399,3 +399,16 @@ def test_f32_backward_agrees_with_f64_instantiation():
     assert ok.mean() > 0.75
     d = np.abs(a["grad"][ok] - b["grad"][ok])
     assert np.all(d <= 1e-4 + 1e-4 * np.abs(b["grad"][ok]))
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_box_truncation_diagnostic(name):
+    """Reported, not gated: the colour the 3-sigma box leaves out (sigma in
+    [4.5, 5.55) lies outside the box but inside the 5.55 skip)."""
+    w = gen.make(name)
+    a = oracle.forward_untiled(w.splats, w.depths, w.width, w.height)
+    b = oracle.forward_untiled(w.splats, w.depths, w.width, w.height, box=False)
+    d = np.abs(b["out"][:, :3] - a["out"][:, :3]).max(axis=1)
+    print(name, "box truncation: max |dC|", float(d.max()), "mean", float(d.mean()),
+          "pixels changed", int((d > 0).sum()), "of", d.size)
+    assert np.isfinite(d).all()
