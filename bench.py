@@ -95,6 +95,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", default="gsr", choices=["gsr", "reference"])
     p.add_argument("--config", default="lego_final", choices=sorted(gen.CONFIGS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-cpu-all-cores", action="store_true",
+                   help="skip the oracle's run on all host cores (tile-row bands in parallel processes)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--deterministic", action="store_true",
                    help="time the backward's deterministic mode (fixed-point accumulation)")
@@ -226,6 +228,34 @@ def cpu_baseline(wl):
     return {"ms": (t3 - t0) * 1e3, "bin_ms": (t1 - t0) * 1e3, "fwd_ms": (t2 - t1) * 1e3,
             "bwd_ms": (t3 - t2) * 1e3, "pairs": int(len(keys)),
             "fwd_counters": f["counters"], "bwd_counters": b["counters"]}
+
+
+def _oracle_band(job):
+    """One tile-row band of a workload through the oracle (bin, forward,
+    backward); runs in a spawned worker process."""
+    name, band, bands = job
+    import oracle
+    sub, _ = band_workload(gen.make(name), band, bands)
+    keys, idx, ranges = oracle.bin_splats(sub.splats, sub.depths, sub.width, sub.height)
+    oracle.forward(sub.splats, idx, ranges, sub.width, sub.height)
+    oracle.backward(sub.splats, idx, ranges, sub.width, sub.height, sub.dl_dout)
+    return len(keys)
+
+
+def cpu_baseline_all_cores(name):
+    """The oracle, as it stands, over the whole frame split into one tile-row
+    band per host core, the bands in parallel worker processes (spawned: this
+    process has used the GPU).  Returns (ms, cores)."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+    cores = len(os.sched_getaffinity(0))
+    # A worker that dies raises BrokenProcessPool here instead of hanging.
+    with ProcessPoolExecutor(cores, mp_context=mp.get_context("spawn")) as pool:
+        list(pool.map(_oracle_band, [(name, 0, cores)] * cores))   # workers up, oracle loaded
+        t0 = time.perf_counter()
+        list(pool.map(_oracle_band, [(name, k, cores) for k in range(cores)]))
+        ms = (time.perf_counter() - t0) * 1e3
+    return ms, cores
 
 
 def band_workload(wl, band, bands):
@@ -546,6 +576,12 @@ def gpu_arm(args):
                                           "single thread",
                                 "stages_ms": {"bin": cb["bin_ms"], "forward": cb["fwd_ms"],
                                               "backward": cb["bwd_ms"]}}
+        if not args.no_cpu_all_cores:
+            ms_all, cores = cpu_baseline_all_cores(args.config)
+            line["cpu_baseline_all_cores"] = {
+                "value": ms_all, "unit": "ms/iter", "cores": cores, "kind": "oracle",
+                "sample": f"the whole frame as {cores} tile-row bands (each bins every splat against "
+                          "its rows, then forward and backward), one worker process per band, wall time"}
         rf = roofline_for("forward", cb["fwd_counters"], cb["pairs"], wl, float(fwd_ms.mean()), peaks,
                           clocks.get("sm_mhz"))
         rb = roofline_for("backward", cb["bwd_counters"], cb["pairs"], wl, float(bwd_ms.mean()),
