@@ -536,6 +536,21 @@ def gpu_arm(args):
                "pipelining": "two contexts on two streams; a step's copies overlap the other's kernels"}
 
     peaks = measured_peaks()
+    # Binning against HBM: N·40 B of splats and depths read, each pair's 12-byte
+    # key and index written once and read and written by every executed pair
+    # pass, 8 B per pair for the range extraction, 8 B per tile of ranges.  The
+    # pair arrays (12 B x pairs) stay in L2 at this size, so the kernels run
+    # against L2 rather than HBM bandwidth.
+    st = ctx.bin_stats()
+    k_pass = bin(st["tile_pass_mask"]).count("1")
+    bin_bytes = wl.n * 40 + pairs * 12 * (1 + 2 * k_pass) + pairs * 8 + \
+        ((wl.width + 15) // 16) * ((wl.height + 15) // 16) * 8
+    bin_gbs = bin_bytes / (float(bin_ms.mean()) * 1e-3) / 1e9
+    roofline_bin = {"kernel": "bin (all binning launches)", "bound": "hbm", "achieved": bin_gbs,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": bin_gbs / peaks["hbm_gbs"],
+                    "algorithmic_bytes": int(bin_bytes), "pair_passes": k_pass,
+                    "radix_passes": st["radix_passes"],
+                    "note": "pair arrays are L2-resident at this size"}
     projection = None
     if not args.no_projection:
         projection = time_projection(gsr, ctx, dev, stream, flush, max(args.steps, 20), max(args.warmup, 3),
@@ -568,6 +583,7 @@ def gpu_arm(args):
         line["e2e"] = e2e
     if projection:
         line["projection"] = projection
+    line["roofline_bin"] = roofline_bin
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(wl)
