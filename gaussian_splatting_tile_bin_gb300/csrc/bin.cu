@@ -486,7 +486,7 @@ k_emit(const uint2 *__restrict__ rects, const float *__restrict__ depths, const 
 #define GSR_RT_ITEMS_DEPTH 8
 #endif
 #ifndef GSR_RT_ITEMS_PAIRS
-#define GSR_RT_ITEMS_PAIRS 8
+#define GSR_RT_ITEMS_PAIRS 12
 #endif
 // Resident CTAs per SM the radix downsweep is compiled for (register budget).
 #ifndef GSR_RT_MIN_BLOCKS
