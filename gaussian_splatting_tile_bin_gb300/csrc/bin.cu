@@ -472,7 +472,7 @@ k_emit(const uint2 *__restrict__ rects, const float *__restrict__ depths, const 
 //
 // A stable LSD sort over the key bits [key_lo, key_hi), one pass per varying
 // digit, each pass three kernels with no waits between CTAs:
-//   upsweep  : per 2048-key radix tile, the count of each digit value, written
+//   upsweep  : per radix tile (256 threads x 8 or 12 keys), the count of each digit value, written
 //              digit-major, counts[digit][tile], and added to totals[digit];
 //   scan     : one CTA per digit value: the digit's global start (the totals of
 //              all smaller digits) plus the exclusive scan of its row, written
