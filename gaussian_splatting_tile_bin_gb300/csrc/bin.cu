@@ -671,6 +671,7 @@ k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, co
         for (int w = 0; w < 8; ++w) wcnt[w][tid] = 0;
         s_goff[tid] = offsets[(size_t)tid * ntiles + blockIdx.x];
     }
+    GSR_CANARY(11);
     __syncthreads();
     const uint32_t lanemask_lt = (1u << lane) - 1u;
 #pragma unroll
@@ -688,6 +689,7 @@ k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, co
         __syncwarp();
         rank[k] = prior + before;
     }
+    GSR_CANARY(12);
     __syncthreads();
     uint32_t tot = 0;
     if (tid < (int)radix) {

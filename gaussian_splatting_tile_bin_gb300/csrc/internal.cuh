@@ -88,6 +88,25 @@ __device__ __forceinline__ void grid_dependency_begin()
 #endif
 }
 
+// Race canary (a build with -DGSR_RACE_CANARY, for tests): at the call sites a
+// warp sleeps a pseudo-random time that depends on its CTA, its warp and the
+// site, so warps interleave differently from an unperturbed build.  A kernel
+// whose results change under it depends on an ordering that no barrier or
+// atomic guarantees.  In the normal build the sites compile to nothing.
+#ifdef GSR_RACE_CANARY
+__device__ __forceinline__ void race_canary(uint32_t site)
+{
+    uint32_t h = (blockIdx.x * 0x9E3779B1u) ^ ((threadIdx.x >> 5) * 0x85EBCA77u) ^ (site * 0xC2B2AE3Du);
+    h ^= h >> 15;
+    h *= 0x2C1B3C6Du;
+    h ^= h >> 12;
+    __nanosleep(h & 511u);
+}
+#define GSR_CANARY(site) ::gsr::race_canary(site)
+#else
+#define GSR_CANARY(site) ((void)0)
+#endif
+
 // Launches `kernel` on `stream`, with programmatic stream serialisation when the
 // context allows it (GSR_OPT_PDL), and counts the launch.
 template <typename... Params, typename... Args>

@@ -233,16 +233,19 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
     for (uint32_t bstart = range.x; bstart < range.y; bstart += kBatch) {
         // Every pixel of the tile has stopped: no later splat can change it.
         if (__syncthreads_count(done) == kTilePixels) break;
+        GSR_CANARY(1);
 #pragma unroll
         for (int q = 0; q < GSR_STAGE_PER_THREAD; ++q) {
             const int slot = q * kTilePixels + threadIdx.x;
             const uint32_t pos = bstart + slot;
             if (pos < range.y) stage_splat<kCull>(sb, slot, splats, __ldg(sorted_idx + pos), x0, y0);
         }
+        GSR_CANARY(2);
         __syncthreads();
         const int cnt = (int)min(range.y - bstart, (uint32_t)kBatch);
         if (__all_sync(kFull, done)) continue;
         for (int c0 = 0; c0 < cnt; c0 += 32) {
+            GSR_CANARY(3);
             uint32_t m = __ballot_sync(kFull, c0 + lane < cnt && (sb.mask[c0 + lane] & wbit));
             while (m) {
                 const int j = c0 + __ffs(m) - 1;
@@ -423,6 +426,7 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
     for (int bend = (int)cta_end; bend > 0; bend -= kBwdBatch) {
         const int bstart = max(0, bend - kBwdBatch);
         const int cnt = bend - bstart;
+        GSR_CANARY(4);
         __syncthreads();
 #pragma unroll
         for (int q = 0; q < GSR_BWD_STAGE_PER_THREAD; ++q) {
@@ -433,9 +437,11 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                 if (kDet) s_esc[slot] = escale[idx];
             }
         }
+        GSR_CANARY(5);
         __syncthreads();
         const int jlim = min(cnt, (int)warp_end - bstart);  // this warp's positions: j < jlim
         for (int c0 = ((jlim - 1) >> 5) << 5; c0 >= 0 && jlim > 0; c0 -= 32) {
+            GSR_CANARY(6);
             uint32_t m = __ballot_sync(kFull, c0 + lane < jlim && (sb.mask[c0 + lane] & wbit));
             while (m) {
                 const int bit = 31 - __clz(m);
