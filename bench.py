@@ -57,16 +57,16 @@ RASTER_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/raster.cu",
                   "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
 PROJECT_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/project.cu",
                    "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
-RASTER_SHA256 = "bc52cb210818c1f78b4049a0778320c4cdef1d84b95be4bdcbe3e6f81664ce62"
-PROJECT_SHA256 = "569472d5cc6cac5dc5435ef69c278d328b198bcd1696a2d913b007b6986e2c3e"
+RASTER_SHA256 = "96f5d03825e91b33d3aec524a50b4723ea85f069582391702b5df1d1f61abcf2"
+PROJECT_SHA256 = "5f49acc944f050d6510d0e9b291b1aa2b607e9cecd5cd46094bc8b7b3000ab42"
 NCU_TRAFFIC = {
-    "forward": {"bytes": 22_277_376 + 512, "workload": "lego_final", "sources": RASTER_SOURCES,
+    "forward": {"bytes": 22_277_120 + 4_096, "workload": "lego_final", "sources": RASTER_SOURCES,
                 "sha256": RASTER_SHA256},
-    "backward": {"bytes": 50_563_584 + 109_824, "workload": "lego_final", "sources": RASTER_SOURCES,
+    "backward": {"bytes": 50_601_216 + 122_112, "workload": "lego_final", "sources": RASTER_SOURCES,
                  "sha256": RASTER_SHA256},
-    "project_forward": {"bytes": 22_960_640 + 0, "workload": "lego_scene", "sources": PROJECT_SOURCES,
+    "project_forward": {"bytes": 22_959_872 + 0, "workload": "lego_scene", "sources": PROJECT_SOURCES,
                         "sha256": PROJECT_SHA256},
-    "project_backward": {"bytes": 37_724_416 + 367_360, "workload": "lego_scene", "sources": PROJECT_SOURCES,
+    "project_backward": {"bytes": 37_718_528 + 231_168, "workload": "lego_scene", "sources": PROJECT_SOURCES,
                          "sha256": PROJECT_SHA256},
 }
 

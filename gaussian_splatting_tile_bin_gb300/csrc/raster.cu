@@ -720,8 +720,9 @@ __device__ __forceinline__ void det_global_maxima(const uint32_t *__restrict__ p
 // sqrt(sigma) e^-sigma <= 1 / sqrt(2e) (or raw < 0.999, sigma < 5.55):
 //   colour G o';  color_a A;  mean A color_a sqrt(max(a, c) / e);
 //   conic A color_a max(c, 2 sqrt(a c), a) / (e det).
-// A conic too ill-conditioned for its sigma to carry those bounds through
-// float rounding (lambda_max / lambda_min > 1e4) uses the box instead:
+// The float sigma is within about 3u lambda_max / lambda_min of the exact one
+// (its terms can cancel), far inside the margin while lambda_max / lambda_min
+// <= 1e6; a conic worse conditioned than that uses the box instead:
 // |dx|, |dy| <= hx, hy, the 3-sigma box radius plus a tile and a pixel.
 //
 // Partials.  A warp adds 32 pixels' terms, and each of the 8 warps of a tile
@@ -756,7 +757,7 @@ __global__ void __launch_bounds__(256) k_det_scales(const float *__restrict__ sp
         const float half_tr = 0.5f * (a + c), rad = sqrtf(0.25f * (a - c) * (a - c) + b * b);
         const float lmax = half_tr + rad, lmin = detf / lmax;
         const float inv_e = 0.36787944f, amax = fmaxf(a, c);
-        if (lmin > 0.0f && lmax <= 1e4f * lmin) {
+        if (lmin > 0.0f && lmax <= 1e6f * lmin) {
             // raw < 0.999 and sigma < 5.55 also cap raw sqrt(sigma) and raw sigma
             l2[0] = l2A + log2f(fminf(op * sqrtf(amax * inv_e), 0.999f * sqrtf(2.0f * 5.55f * amax)));
             l2[1] = l2A + log2f(fminf(op * inv_e, 0.999f * 5.55f)) +
