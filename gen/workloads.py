@@ -230,3 +230,39 @@ def elongated_fixture(seed: int = 8, n: int = 3000, size: int = 512) -> Workload
     return _assemble("elongated", rng, size, size, means, depths, s_long, s_short, theta, rgb, opac,
                      {"seed": seed, "aspect": "logU(1,400)", "long_std": "logU(2,150)"})
 
+
+
+def random_case(seed: int) -> Workload:
+    """A randomised small case for fuzzing: image sides 1..300 (rarely a
+    multiple of 16), 0..3,000 splats centred anywhere from 50 px outside the
+    image to inside it, stds log-uniform in [0.2, 80] px with aspect ratios to
+    100, color_a in (0, 1) (the rasterizer's domain), depths U(0.5, 20) with a few exact ties; 2% of the
+    splats get a culled value (depth <= 0 or NaN, a NaN field, a negative
+    determinant)."""
+    rng = np.random.Generator(np.random.PCG64(1_000_003 + seed))
+    w = int(rng.integers(1, 301))
+    h = int(rng.integers(1, 301))
+    n = int(rng.integers(0, 3001)) if seed % 7 else 0
+    means = np.column_stack([rng.uniform(-50.0, w + 50.0, n), rng.uniform(-50.0, h + 50.0, n)])
+    depths = rng.uniform(0.5, 20.0, n)
+    ties = rng.random(n) < 0.1
+    depths[ties] = np.round(depths[ties])
+    s1 = np.exp(rng.uniform(np.log(0.2), np.log(80.0), n))
+    s2 = s1 / np.exp(rng.uniform(0.0, np.log(100.0), n))
+    theta = rng.uniform(0.0, np.pi, n)
+    rgb = rng.uniform(0.0, 1.0, (n, 3))
+    opac = rng.uniform(0.0, 1.0, n)
+    wl = _assemble(f"random{seed}", rng, w, h, means, depths, np.maximum(s2, 0.05), s1, theta, rgb, opac,
+                   {"seed": seed})
+    bad = np.nonzero(rng.random(n) < 0.02)[0]
+    for j, i in enumerate(bad):
+        kind = j % 4
+        if kind == 0:
+            wl.depths[i] = -1.0 if j % 8 == 0 else 0.0
+        elif kind == 1:
+            wl.depths[i] = np.nan
+        elif kind == 2:
+            wl.splats[i, int(rng.integers(0, 9))] = np.nan
+        else:
+            wl.splats[i, 3] = np.sqrt(abs(wl.splats[i, 2] * wl.splats[i, 4])) * 1.5   # b^2 > a c
+    return wl
