@@ -131,3 +131,29 @@ def edge_scene(seed: int = 11) -> Scene:
     g = np.concatenate([front, behind, near, zero_q, nan, inf, needle, large, off]).astype(np.float32)
     dl = rng.standard_normal((g.shape[0], 9)).astype(np.float32)
     return Scene("edge_scene", 512, 512, g, cam, dl, {"seed": seed, "block": m})
+
+
+def random_scene(seed: int) -> Scene:
+    """A randomised projection case: 1..5,000 Gaussians in a box of side 4
+    around the origin, log-scales N(ln 0.05, 1.2) per axis, any rotation and
+    logit; a look-at camera at distance U(0.5, 8) (so some Gaussians fall behind
+    it or inside its near plane), focal lengths U(100, 2000) and a principal
+    point anywhere in a 64..1024-pixel image, dilation 0.3 or 0."""
+    rng = np.random.Generator(np.random.PCG64(2_000_003 + seed))
+    n = int(rng.integers(1, 5001))
+    means = rng.uniform(-2.0, 2.0, (n, 3))
+    log_scale = rng.normal(np.log(0.05), 1.2, (n, 3))
+    quat = rng.standard_normal((n, 4))
+    logit = rng.normal(0.0, 2.0, n)
+    rgb = rng.uniform(0.0, 1.0, (n, 3))
+    g = np.concatenate([means, log_scale, quat, logit[:, None], rgb], axis=1).astype(np.float32)
+    w, h = (int(v) for v in rng.integers(64, 1025, 2))
+    d = rng.uniform(0.5, 8.0)
+    direction = rng.standard_normal(3)
+    direction /= np.linalg.norm(direction)
+    up = np.array([0.0, 0.0, 1.0]) if abs(direction[2]) < 0.9 else np.array([1.0, 0.0, 0.0])
+    f = rng.uniform(100.0, 2000.0, 2)
+    cam = look_at_camera(d * direction, (0.0, 0.0, 0.0), up, f[0], f[1], rng.uniform(0, w), rng.uniform(0, h),
+                         eps=0.3 if seed % 3 else 0.0)
+    dl = rng.standard_normal((n, 9)).astype(np.float32)
+    return Scene(f"random_scene{seed}", w, h, g, cam, dl, {"seed": seed})

@@ -135,3 +135,11 @@ def test_projection_chain_matches_oracle_chain(gsr, ctx):
     keep = ~knife
     proj_checks.check_backward(sc.gaussians[keep], sc.camera, G_ref[keep].astype(np.float32), dg[keep],
                                extra_G=G_tol[keep])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_projection_random_cameras(gsr, ctx, seed):
+    sc = gen.random_scene(seed)
+    sp, d, grad = _project(gsr, ctx, sc.gaussians, sc.camera, sc.dl_dsplat)
+    proj_checks.check_forward(sc.gaussians, sc.camera, sp, d)
+    proj_checks.check_backward(sc.gaussians, sc.camera, sc.dl_dsplat, grad)

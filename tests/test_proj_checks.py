@@ -64,3 +64,13 @@ def test_dropped_conic_term_is_caught(scene):
     grad = oracle.project_backward(g64, scene.camera, G)
     with pytest.raises(AssertionError):
         proj_checks.check_backward(scene.gaussians, scene.camera, scene.dl_dsplat, grad.astype(np.float32))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_rounded_oracle_passes_random_scenes(seed):
+    sc = gen.random_scene(seed)
+    g64 = sc.gaussians.astype(np.float64)
+    sp, d, _ = oracle.project_forward(g64, sc.camera)
+    proj_checks.check_forward(sc.gaussians, sc.camera, sp.astype(np.float32), d.astype(np.float32))
+    g = oracle.project_backward(g64, sc.camera, sc.dl_dsplat)
+    proj_checks.check_backward(sc.gaussians, sc.camera, sc.dl_dsplat, g.astype(np.float32))
