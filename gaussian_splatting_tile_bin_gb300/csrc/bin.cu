@@ -41,6 +41,8 @@ enum {
     kScalarDepthOr = 3,
     kScalarKeyAnd = 4,     // AND / OR of the emitted keys
     kScalarKeyOr = 5,
+    kScalarTicketCount = 6,  // blocks of k_count / k_sorted_sums done (the last one scans)
+    kScalarTicketSums = 7,
     kScalarCount = 8
 };
 
@@ -201,13 +203,52 @@ __host__ __device__ __forceinline__ int field_pass(unsigned long long diff, int 
     return j;
 }
 
-__global__ void k_init_scalars(unsigned long long *__restrict__ scalars)
+// Clears the binning's scalars and the radix digit totals of both sorts.
+__global__ void k_init_scalars(unsigned long long *__restrict__ scalars, uint32_t *__restrict__ radix_totals,
+                               int ntotals)
 {
     grid_dependency_begin();
+    for (int i = threadIdx.x; i < ntotals; i += blockDim.x) radix_totals[i] = 0u;
     if (threadIdx.x != 0) return;
     for (int k = 0; k < kScalarCount; ++k) scalars[k] = 0ull;
     scalars[kScalarDepthAnd] = ~0ull;
     scalars[kScalarKeyAnd] = ~0ull;
+}
+
+// True in the one block that finishes last: every block calls this after it has
+// written its per-block results, and the last block then reads all of them
+// (the fences order each block's writes before its ticket).
+__device__ __forceinline__ bool last_block_done(unsigned long long *ticket)
+{
+    __shared__ bool s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(ticket, 1ull) == (unsigned long long)(gridDim.x - 1);
+    }
+    __syncthreads();
+    if (s_last) __threadfence();
+    return s_last;
+}
+
+// Exclusive scan in place of vals[0, num) by one 256-thread block (reads that
+// bypass L1: other blocks wrote the values); returns the total.  Each thread
+// takes a contiguous run of the values: one block-wide scan of the runs' sums.
+__device__ unsigned long long block_scan_inplace_256(unsigned long long *__restrict__ vals, int num,
+                                                     unsigned long long *ws)
+{
+    const int per = (num + kBinBlock - 1) / kBinBlock;
+    const int b0 = min(num, (int)threadIdx.x * per), b1 = min(num, b0 + per);
+    unsigned long long sum = 0;
+    for (int i = b0; i < b1; ++i) sum += __ldcg(vals + i);
+    unsigned long long total;
+    unsigned long long run = block_exclusive_scan_256<unsigned long long>(sum, ws, &total);
+    for (int i = b0; i < b1; ++i) {
+        const unsigned long long v = __ldcg(vals + i);
+        vals[i] = run;
+        run += v;
+    }
+    return total;
 }
 
 // --- count -----------------------------------------------------------------
@@ -257,66 +298,19 @@ k_count(const float *__restrict__ splats, const float *__restrict__ depths, int 
     }
     block_and_or_into(c > 0 ? (unsigned long long)db : ~0ull, c > 0 ? (unsigned long long)db : 0ull,
                       s_and, s_or, scalars + kScalarDepthAnd);
-}
-
-// Exclusive scan in place of vals[0, num) by one 1024-thread block; returns the total.
-__device__ unsigned long long block_scan_inplace_1024(unsigned long long *__restrict__ vals, int num,
-                                                      unsigned long long *ws)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    unsigned long long carry = 0;
-    for (int base = 0; base < num; base += 1024) {
-        const int i = base + threadIdx.x;
-        unsigned long long v = i < num ? vals[i] : 0ull;
-        unsigned long long incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            unsigned long long x = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += x;
-        }
-        if (lane == 31) ws[warp] = incl;
+    // The last block: the pair total (a plain sum) and the exclusive scan of the
+    // per-block emitting counts with their total.
+    if (last_block_done(scalars + kScalarTicketCount)) {
+        unsigned long long s = 0;
+        for (int b = threadIdx.x; b < (int)gridDim.x; b += kBinBlock) s += __ldcg(blk_pairs + b);
+        unsigned long long t;
+        block_exclusive_scan_256<unsigned long long>(s, ws, &t);
         __syncthreads();
-        unsigned long long off = 0, sum = 0;
-        for (int w = 0; w < 32; ++w) {
-            if (w < warp) off += ws[w];
-            sum += ws[w];
+        const unsigned long long m = block_scan_inplace_256(blk_emitting, (int)gridDim.x, ws);
+        if (threadIdx.x == 0) {
+            scalars[kScalarPairs] = t;
+            scalars[kScalarEmitting] = m;
         }
-        __syncthreads();
-        if (i < num) vals[i] = carry + off + incl - v;
-        carry += sum;
-    }
-    return carry;
-}
-
-__global__ void __launch_bounds__(1024)
-k_scan_u64(unsigned long long *__restrict__ vals, int num)
-{
-    grid_dependency_begin();
-    __shared__ unsigned long long ws[32];
-    block_scan_inplace_1024(vals, num, ws);
-}
-
-// One block: the pair total (a plain sum) and the exclusive scan of the
-// per-block emitting counts with their total.
-__global__ void __launch_bounds__(1024)
-k_count_totals(const unsigned long long *__restrict__ blk_pairs, unsigned long long *__restrict__ blk_emitting,
-               int nblk, unsigned long long *__restrict__ scalars)
-{
-    grid_dependency_begin();
-    __shared__ unsigned long long ws[32];
-    unsigned long long s = 0;
-    for (int i = threadIdx.x; i < nblk; i += 1024) s += blk_pairs[i];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-    if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = s;
-    __syncthreads();
-    unsigned long long t = 0;
-    for (int w = 0; w < 32; ++w) t += ws[w];
-    __syncthreads();
-    const unsigned long long m = block_scan_inplace_1024(blk_emitting, nblk, ws);
-    if (threadIdx.x == 0) {
-        scalars[kScalarPairs] = t;
-        scalars[kScalarEmitting] = m;
     }
 }
 
@@ -342,7 +336,7 @@ k_compact(const uint2 *__restrict__ rects, const float *__restrict__ depths, int
 // Per block of 256 depth-sorted splats: their pair total.
 __global__ void __launch_bounds__(kBinBlock)
 k_sorted_sums(const uint32_t *__restrict__ sorted_idx, const uint2 *__restrict__ rects, int m,
-              unsigned long long *__restrict__ blk_sorted)
+              unsigned long long *__restrict__ blk_sorted, unsigned long long *__restrict__ scalars)
 {
     grid_dependency_begin();
     __shared__ unsigned long long ws[8];
@@ -351,6 +345,8 @@ k_sorted_sums(const uint32_t *__restrict__ sorted_idx, const uint2 *__restrict__
     unsigned long long total;
     block_exclusive_scan_256<unsigned long long>(c, ws, &total);
     if (threadIdx.x == 0) blk_sorted[blockIdx.x] = total;
+    // The last block turns the per-block sums into offsets.
+    if (last_block_done(scalars + kScalarTicketSums)) block_scan_inplace_256(blk_sorted, (int)gridDim.x, ws);
 }
 
 // --- emit ------------------------------------------------------------------
@@ -746,11 +742,26 @@ __global__ void k_copy_if_unsorted(SortBuffers<K> bufs, uint32_t num, const unsi
 // thread compares four consecutive keys (two 16-byte loads) and their
 // neighbours.
 __global__ void __launch_bounds__(256)
-k_extract_ranges(const uint64_t *__restrict__ keys, uint32_t num, uint32_t *__restrict__ ranges)
+k_extract_ranges(PairBuffers bufs, uint32_t num, uint32_t *__restrict__ ranges,
+                 const unsigned long long *__restrict__ and_or, int key_lo, int key_hi)
 {
     grid_dependency_begin();
     const uint32_t i0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4u;
     if (i0 >= num) return;
+    // A tile sort that ran no pass (every key shares its tile bits) left the
+    // emitted order, already sorted, in buffer 0: copy it to the result.
+    const uint64_t *__restrict__ keys = bufs.k[1];
+    if (and_or) {
+        int executed;
+        field_pass(and_or[0] ^ and_or[1], key_lo, key_hi, -1, &executed);
+        if (executed == 0) {
+            keys = bufs.k[0];
+            for (uint32_t i = i0; i < min(i0 + 4u, num); ++i) {
+                bufs.k[1][i] = bufs.k[0][i];
+                bufs.v[1][i] = bufs.v[0][i];
+            }
+        }
+    }
     uint32_t t[6];  // tiles of keys i0 - 1 .. i0 + 4 (0xffffffff outside [0, num))
     t[0] = i0 > 0 ? (uint32_t)(__ldg(keys + i0 - 1) >> 32) : 0xffffffffu;
     if (i0 + 4 <= num) {
@@ -921,7 +932,7 @@ int launch_downsweep(gsr_ctx *ctx, int width, int ntiles, cudaStream_t stream, S
 template <typename K, int kRtItems>
 int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int key_hi,
                const unsigned long long *and_or, const unsigned long long *host_and_or, uint32_t *totals,
-               cudaStream_t stream)
+               cudaStream_t stream, bool copy_unsorted = true)
 {
     int rc;
     constexpr int kRtTile = kRtThreads * kRtItems;
@@ -959,7 +970,7 @@ int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int 
         GSR_LAUNCH(ctx, k_radix_scan, dim3(1 << w), dim3(kRtThreads), stream, ps, ntiles, counts, tot, offsets);
         if ((rc = launch_downsweep<K, kRtItems>(ctx, w, ntiles, stream, bufs, num, ps, offsets))) return rc;
     }
-    if (!host_and_or)
+    if (!host_and_or && copy_unsorted)
         GSR_LAUNCH(ctx, k_copy_if_unsorted<K>, dim3(std::min(ntiles, 1024)), dim3(256), stream, bufs, num, and_or,
                    key_lo, key_hi);
     return GSR_OK;
@@ -1014,11 +1025,10 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
 
     // 1. counts, totals; read the pair total and the emitting count.
     uint64_t total = 0, emitting = 0;
-    GSR_LAUNCH(ctx, k_init_scalars, dim3(1), dim3(32), stream, ctx->scalars);
+    GSR_LAUNCH(ctx, k_init_scalars, dim3(1), dim3(256), stream, ctx->scalars, ctx->radix_totals, 2 * 4 * 256);
     if (n > 0) {
         GSR_LAUNCH(ctx, k_count, dim3(nblk), dim3(kBinBlock), stream, splats, depths, n, tiles_x, tiles_y,
                    ctx->rects, blk_pairs, blk_emit, ctx->scalars);
-        GSR_LAUNCH(ctx, k_count_totals, dim3(1), dim3(1024), stream, blk_pairs, blk_emit, nblk, ctx->scalars);
         // Pair total, emitting count and the AND / OR of the emitting splats'
         // depth bits (scalar slots 0..3).
         if ((rc = cuda_check(ctx, cudaMemcpyAsync(ctx->host_total, ctx->scalars,
@@ -1065,10 +1075,6 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         return rc;
 
     if (num > 0) {
-        // Digit totals: 4 digits x 256 values for each of the two sorts.
-        if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->radix_totals, 0, 2 * 4 * 256 * sizeof(uint32_t), stream),
-                             "cudaMemsetAsync")))
-            return rc;
         // 3. depth sort of the emitting splats.
         GSR_LAUNCH(ctx, k_compact, dim3(nblk), dim3(kBinBlock), stream, ctx->rects, depths, n, blk_emit,
                    ctx->depth.k[0], ctx->depth.v[0]);
@@ -1078,14 +1084,14 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         // 4. pair offsets in depth order, emission.
         const int mblk = (m + kBinBlock - 1) / kBinBlock;
         GSR_LAUNCH(ctx, k_sorted_sums, dim3(mblk), dim3(kBinBlock), stream, ctx->depth.v[1], ctx->rects, m,
-                   blk_sorted);
-        GSR_LAUNCH(ctx, k_scan_u64, dim3(1), dim3(1024), stream, blk_sorted, mblk);
+                   blk_sorted, ctx->scalars);
         GSR_LAUNCH(ctx, k_emit, dim3(mblk), dim3(kBinBlock), stream, ctx->rects, depths, ctx->depth.v[1], m,
                    tiles_x, blk_sorted, ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars);
         // 5. stable sort on the tile digits only.
         if (key_hi > 32) {
+            // (a sort that runs no pass is completed by the range extraction)
             if ((rc = radix_sort<uint64_t, kRtItemsPairs>(ctx, ctx->pairs, num, 32, key_hi, ctx->scalars + kScalarKeyAnd,
-                                           nullptr, ctx->radix_totals + 4 * 256, stream)))
+                                           nullptr, ctx->radix_totals + 4 * 256, stream, false)))
                 return rc;
         } else {
             // One tile: the emitted order is already sorted.
@@ -1098,8 +1104,9 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
                 return rc;
         }
         // 6. per-tile ranges.
-        GSR_LAUNCH(ctx, k_extract_ranges, dim3((num + 1023) / 1024), dim3(256), stream, ctx->pairs.k[1], num,
-                   ctx->ranges);
+        GSR_LAUNCH(ctx, k_extract_ranges, dim3((num + 1023) / 1024), dim3(256), stream, ctx->pairs, num,
+                   ctx->ranges, key_hi > 32 ? (const unsigned long long *)(ctx->scalars + kScalarKeyAnd) : nullptr,
+                   32, key_hi);
     }
 
     // 7. the forward's launch order: longest tile lists first.
