@@ -338,10 +338,13 @@ __device__ __forceinline__ int det_exponent(uint2 esc, int grp)
 }
 
 // Sums the 9 per-lane values over the warp and adds the totals to acc[0..8] in
-// one atomic instruction: a transposed butterfly leaves component k (k < 8) in
-// lanes 4k..4k+3 after 7 shuffles, component 8 takes a plain butterfly, and
-// lanes 4k and lane 1 widen their sums to double (with integer operations, off
-// the narrow FP64 pipe) and issue the adds.
+// one atomic instruction, with 12 shuffles: a transposed butterfly over the
+// 16-, 8- and 4-lane exchanges leaves component k (k < 8) summed over those in
+// lane group 4k..4k+3 while component 8 rides along as a plain butterfly; at the
+// 2-lane exchange the two pair up (lanes with bit 1 clear keep component k,
+// the others component 8), and the 1-lane exchange finishes both.  Lanes 4k
+// and lane 2 widen their sums to double (with integer operations, off the
+// narrow FP64 pipe) and issue the adds.
 template <bool kDet>
 __device__ __forceinline__ void warp_reduce_add9(float (&v)[9], double *__restrict__ acc, int lane, uint2 esc)
 {
@@ -361,14 +364,17 @@ __device__ __forceinline__ void warp_reduce_add9(float (&v)[9], double *__restri
         x2[i] = keep + __shfl_xor_sync(kFull, send, 8);
     }
     float y = (h4 ? x2[1] : x2[0]) + __shfl_xor_sync(kFull, h4 ? x2[0] : x2[1], 4);
-    y += __shfl_xor_sync(kFull, y, 2);
-    y += __shfl_xor_sync(kFull, y, 1);
+    // component 8 rides along the first three levels, then pairs with y
     float z = v[8];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
-    const float mine = (lane & 3) == 0 ? y : z;
-    const int k = (lane & 3) == 0 ? (lane >> 2) : 8;
-    if ((lane & 3) == 0 || lane == 1) {
+    z += __shfl_xor_sync(kFull, z, 16);
+    z += __shfl_xor_sync(kFull, z, 8);
+    z += __shfl_xor_sync(kFull, z, 4);
+    const bool h2 = lane & 2;
+    float t = (h2 ? z : y) + __shfl_xor_sync(kFull, h2 ? y : z, 2);
+    t += __shfl_xor_sync(kFull, t, 1);
+    const float mine = t;
+    const int k = h2 ? 8 : (lane >> 2);
+    if ((lane & 3) == 0 || lane == 2) {
         if (kDet)
             atomicAdd(reinterpret_cast<unsigned long long *>(acc) + k,
                       (unsigned long long)to_fixed(mine, det_exponent(esc, det_group(k))));
@@ -452,7 +458,6 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                 // select (no divergent branches in the warp's loop body).
                 const float4 geo = sb.geo[j];
                 const float4 aux = sb.aux[j];
-                const float4 c = sb.rgb[j];
                 float dx, dy;
                 const float sigma = splat_sigma(geo, aux.x, px, py, dx, dy);
                 const bool in_range = rel < L && sigma >= 0.0f && sigma < aux.z;
@@ -461,6 +466,7 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                 const bool contrib = in_range && alpha >= kAlphaMin;
                 // "W1 warp sparse skip": with no contributing lane nothing changes.
                 if (kWarpSkip && !__any_sync(kFull, contrib)) continue;
+                const float4 c = sb.rgb[j];
                 const float one_m = __fsub_rn(1.0f, alpha);
                 const float inv = __fdividef(1.0f, one_m);
                 float Tj = T * inv;
