@@ -57,16 +57,16 @@ RASTER_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/raster.cu",
                   "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
 PROJECT_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/project.cu",
                    "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
-RASTER_SHA256 = "96f5d03825e91b33d3aec524a50b4723ea85f069582391702b5df1d1f61abcf2"
+RASTER_SHA256 = "a3f1a5eca56b101f6534dd8df3a16432326d3a51b635af0190f52b5ceaa1ebaf"
 PROJECT_SHA256 = "5f49acc944f050d6510d0e9b291b1aa2b607e9cecd5cd46094bc8b7b3000ab42"
 NCU_TRAFFIC = {
-    "forward": {"bytes": 22_277_120 + 4_096, "workload": "lego_final", "sources": RASTER_SOURCES,
+    "forward": {"bytes": 22_276_864 + 5_376, "workload": "lego_final", "sources": RASTER_SOURCES,
                 "sha256": RASTER_SHA256},
-    "backward": {"bytes": 50_601_216 + 122_112, "workload": "lego_final", "sources": RASTER_SOURCES,
+    "backward": {"bytes": 50_592_000 + 114_432, "workload": "lego_final", "sources": RASTER_SOURCES,
                  "sha256": RASTER_SHA256},
-    "project_forward": {"bytes": 22_959_872 + 0, "workload": "lego_scene", "sources": PROJECT_SOURCES,
+    "project_forward": {"bytes": 22_961_152 + 0, "workload": "lego_scene", "sources": PROJECT_SOURCES,
                         "sha256": PROJECT_SHA256},
-    "project_backward": {"bytes": 37_718_528 + 231_168, "workload": "lego_scene", "sources": PROJECT_SOURCES,
+    "project_backward": {"bytes": 37_724_416 + 272_384, "workload": "lego_scene", "sources": PROJECT_SOURCES,
                          "sha256": PROJECT_SHA256},
 }
 
