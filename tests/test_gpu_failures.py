@@ -78,3 +78,24 @@ def test_backward_reports_an_allocation_failure_and_recovers(gsr):
         assert np.all(np.isfinite(grad))
     finally:
         ctx.close()
+
+
+def test_deterministic_backward_reports_an_allocation_failure_and_recovers(gsr):
+    """The deterministic mode allocates its exponent table on first use: a
+    failure there is reported and the next call recovers."""
+    wl = gen.small()
+    sp, dp, dl = to_dev(wl.splats), to_dev(wl.depths), to_dev(wl.dl_dout)
+    ctx = gsr.Context(0)
+    try:
+        bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+        out, final_t, last = gsr.rasterize_forward(ctx, sp, bins)
+        gsr.rasterize_backward(ctx, sp, bins, dl, final_t, last)   # accumulator and tile order allocated
+        ctx.set_option("deterministic", True)
+        ctx.set_option("fail_next_alloc", 1)                       # the exponent table
+        with pytest.raises(gsr.GsrError) as err:
+            gsr.rasterize_backward(ctx, sp, bins, dl, final_t, last)
+        assert err.value.code == GSR_ERR_OOM and "deterministic" in str(err.value)
+        grad = gsr.rasterize_backward(ctx, sp, bins, dl, final_t, last).cpu().numpy()
+        check_backward({"grad": grad}, run_oracle(wl))
+    finally:
+        ctx.close()
