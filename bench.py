@@ -102,6 +102,8 @@ def parse_args(argv=None):
                    help="time the backward's deterministic mode (fixed-point accumulation)")
     p.add_argument("--bwd-per-splat", action="store_true",
                    help="time the backward's transposed (per-splat) loop nest instead of the per-pixel one")
+    p.add_argument("--graph", action="store_true",
+                   help="also time the step with forward and backward replayed as one captured CUDA graph")
     p.add_argument("--no-projection", action="store_true",
                    help="skip the separate timing of the projection kernels")
     p.add_argument("--min-warm-s", type=float, default=1.5,
@@ -391,6 +393,46 @@ def time_projection(gsr, ctx, dev, stream, flush, steps, warmup, peaks):
     return out
 
 
+def time_graph(gsr, ctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush, steps):
+    """The step with binning as usual and forward + backward replayed from one
+    captured CUDA graph (the binning's host synchronisation keeps it outside),
+    against the same step with direct calls, alternating, between L2 flushes."""
+    import torch
+    bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            gsr.rasterize_forward(ctx, sp, bins, out, fT, last)
+            gsr.rasterize_backward(ctx, sp, bins, dl, fT, last, grad)
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+
+    def run(graph):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            b = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+            if graph:
+                g.replay()
+            else:
+                gsr.rasterize_forward(ctx, sp, b, out, fT, last)
+                gsr.rasterize_backward(ctx, sp, b, dl, fT, last, grad)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return float(np.median([a.elapsed_time(b) for a, b in evs]))
+
+    res = {"direct_ms": [], "graph_ms": []}
+    for _ in range(3):
+        res["direct_ms"].append(run(False))
+        res["graph_ms"].append(run(True))
+    return {"direct_ms": float(np.median(res["direct_ms"])), "graph_ms": float(np.median(res["graph_ms"])),
+            "note": "binning direct (its host sync), forward + backward one graph replay; medians"}
+
+
 def gpu_arm(args):
     import torch
 
@@ -535,6 +577,9 @@ def gpu_arm(args):
                "d2h_bytes_per_step": int(d2h),
                "pipelining": "two contexts on two streams; a step's copies overlap the other's kernels"}
 
+    graph = None
+    if args.graph:
+        graph = time_graph(gsr, ctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush, max(args.steps, 20))
     peaks = measured_peaks()
     # Binning against HBM: N·40 B of splats and depths read, each pair's 12-byte
     # key and index written once and read and written by every executed pair
@@ -584,6 +629,8 @@ def gpu_arm(args):
     if projection:
         line["projection"] = projection
     line["roofline_bin"] = roofline_bin
+    if graph:
+        line["graph"] = graph
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(wl)
