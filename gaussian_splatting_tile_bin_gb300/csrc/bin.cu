@@ -720,22 +720,6 @@ k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, co
     }
 }
 
-// When no digit varied no pass ran and the input order is already sorted;
-// copy it to the result buffer.
-template <typename K>
-__global__ void k_copy_if_unsorted(SortBuffers<K> bufs, uint32_t num, const unsigned long long *__restrict__ and_or,
-                                   int key_lo, int key_hi)
-{
-    grid_dependency_begin();
-    int executed;
-    field_pass(and_or[0] ^ and_or[1], key_lo, key_hi, -1, &executed);
-    if (executed != 0) return;
-    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < num; i += gridDim.x * blockDim.x) {
-        bufs.k[1][i] = bufs.k[0][i];
-        bufs.v[1][i] = bufs.v[0][i];
-    }
-}
-
 // --- ranges --------------------------------------------------------------------
 
 // Tile starts and ends where the tile field of the sorted keys changes; each
@@ -932,7 +916,7 @@ int launch_downsweep(gsr_ctx *ctx, int width, int ntiles, cudaStream_t stream, S
 template <typename K, int kRtItems>
 int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int key_hi,
                const unsigned long long *and_or, const unsigned long long *host_and_or, uint32_t *totals,
-               cudaStream_t stream, bool copy_unsorted = true)
+               cudaStream_t stream)
 {
     int rc;
     constexpr int kRtTile = kRtThreads * kRtItems;
@@ -970,9 +954,8 @@ int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int 
         GSR_LAUNCH(ctx, k_radix_scan, dim3(1 << w), dim3(kRtThreads), stream, ps, ntiles, counts, tot, offsets);
         if ((rc = launch_downsweep<K, kRtItems>(ctx, w, ntiles, stream, bufs, num, ps, offsets))) return rc;
     }
-    if (!host_and_or && copy_unsorted)
-        GSR_LAUNCH(ctx, k_copy_if_unsorted<K>, dim3(std::min(ntiles, 1024)), dim3(256), stream, bufs, num, and_or,
-                   key_lo, key_hi);
+    // A device-planned sort that runs no pass leaves the sorted order in buffer
+    // 0; the caller completes it (the range extraction copies it to buffer 1).
     return GSR_OK;
 }
 
@@ -1091,7 +1074,7 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         if (key_hi > 32) {
             // (a sort that runs no pass is completed by the range extraction)
             if ((rc = radix_sort<uint64_t, kRtItemsPairs>(ctx, ctx->pairs, num, 32, key_hi, ctx->scalars + kScalarKeyAnd,
-                                           nullptr, ctx->radix_totals + 4 * 256, stream, false)))
+                                           nullptr, ctx->radix_totals + 4 * 256, stream)))
                 return rc;
         } else {
             // One tile: the emitted order is already sorted.
