@@ -116,7 +116,9 @@ enum {
                                      per-splat backward", section 1): one warp per tile, one lane per
                                      splat, the tile's pixels met in diagonal order, each lane's sums
                                      kept in registers and added once per (tile, splat).  Same
-                                     gradients within float rounding; slower on this workload. */
+                                     gradients within float rounding; it evaluates every pixel of a
+                                     tile for every splat, and ran 24 times slower than the default
+                                     backward on an 800x800 image of 409,660 splats. */
 };
 
 typedef struct gsr_ctx gsr_ctx;
