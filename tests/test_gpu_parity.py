@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import gen
+import oracle
 from gpu_helpers import (check_backward, check_bins, check_forward, run_gpu, run_oracle, to_dev,
                          varying_digit_mask)
 
@@ -171,6 +172,37 @@ def test_stress_tile_digits(gsr, ctx):
     st = ctx.bin_stats()
     # 120 x 68 = 8160 tiles: 13 tile bits as a 7-bit and a 6-bit digit.
     assert (st["tile_digits"], st["tile_digit_bits"]) == (2, 7)
+
+
+def test_radix_sort_40000_tiles(gsr, ctx):
+    """The pages' sort check at 40,000 tiles ("C0 resident arena + C1 pass
+    skip", section 2, C1): about 200k keys against a plain stable sort (the
+    oracle's), 16 tile bits sorted as two 8-bit digits, depths over several
+    binades so that all four depth digits vary.  Binning only: a 3200x3200
+    frame."""
+    rng = np.random.Generator(np.random.PCG64(40_000))
+    w = h = 3200
+    n = 50_000
+    s = np.zeros((n, 9), dtype=np.float32)
+    s[:, 0] = rng.uniform(-10, w + 10, n)
+    s[:, 1] = rng.uniform(-10, h + 10, n)
+    std = rng.uniform(0.4, 5.0, n)
+    s[:, 2] = 1.0 / std ** 2
+    s[:, 3] = rng.uniform(-0.3, 0.3, n) / std ** 2
+    s[:, 4] = 1.0 / std ** 2
+    s[:, 5:9] = rng.uniform(0, 1, (n, 4))
+    d = rng.uniform(0.5, 30.0, n).astype(np.float32)
+    sp, dp = to_dev(s), to_dev(d)
+    bins = gsr.bin_splats(ctx, sp, dp, w, h)
+    g = {"keys": bins.keys().cpu().numpy().view(np.uint64), "idx": bins.sorted_idx().cpu().numpy().view(np.uint32),
+         "ranges": bins.tile_ranges().cpu().numpy().view(np.uint32), "num_pairs": bins.num_pairs}
+    st = ctx.bin_stats()
+    keys, idx, ranges = oracle.bin_splats(s, d, w, h)
+    check_bins(g, {"keys": keys, "idx": idx, "ranges": ranges})
+    assert 150_000 < len(keys) < 400_000
+    assert (st["tile_digits"], st["tile_digit_bits"]) == (2, 8)
+    assert st["tile_pass_mask"] == varying_digit_mask(keys, 32, 48, 2) == 0b11
+    assert st["depth_pass_mask"] == varying_digit_mask(keys, 0, 32, 4) == 0b1111
 
 
 def test_no_pass_needed(gsr, ctx):
