@@ -51,6 +51,43 @@ def test_struct_layouts_match_binding(tmp_path, lib):
     assert got == want
 
 
+def test_plain_c_client_links_and_runs(tmp_path, lib):
+    """A C program links libgsr.so by name and calls the ABI: argument errors
+    come back as codes, and creating a context without a usable device gives
+    GSR_ERR_CUDA (with a device: GSR_OK)."""
+    src = tmp_path / "client.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "gsr.h"
+int main(void) {
+    gsr_ctx *ctx = (gsr_ctx *)1;
+    if (gsr_create(NULL, 0) != GSR_ERR_INVALID_ARG) return 10;
+    if (gsr_set_option(NULL, GSR_OPT_PDL, 1) != GSR_ERR_INVALID_ARG) return 11;
+    if (strcmp(gsr_last_error(NULL), "NULL context") != 0) return 12;
+    if (gsr_bin_splats(NULL, NULL, NULL, 0, 16, 16, NULL, NULL) != GSR_ERR_INVALID_ARG) return 13;
+    int rc = gsr_create(&ctx, 0);
+    printf("%d\n", rc);
+    if (rc == GSR_OK) {
+        if (gsr_set_option(ctx, GSR_OPT_PDL, 2) != GSR_ERR_INVALID_ARG) return 14;
+        if (gsr_bin_splats(ctx, NULL, NULL, -1, 16, 16, NULL, NULL) != GSR_ERR_INVALID_ARG) return 15;
+        gsr_destroy(ctx);
+    } else if (ctx != NULL) {
+        return 16;
+    }
+    return 0;
+}
+''')
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(lib._name)
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                           "-L", libdir, "-lgsr", f"-Wl,-rpath,{libdir}", "-o", str(exe)])
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    import torch
+    assert int(r.stdout.split()[-1]) == (0 if torch.cuda.is_available() else 2)
+
+
 def test_null_and_invalid_arguments(lib):
     P = ctypes.c_void_p
     lib.gsr_create.argtypes = [ctypes.POINTER(P), ctypes.c_int]
