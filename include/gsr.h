@@ -212,7 +212,7 @@ int gsr_rasterize_backward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n,
                            const gsr_bins *bins, const float *dl_dout, const float *final_T,
                            const uint32_t *last_contrib, float *grad, void *stream);
 
-/* Backward rasterization that allocates nothing.  The paper has no counterpart
+/* Backward rasterization that allocates nothing.  The pages have no counterpart
  * to this entry point; it exists for callers that cannot call cudaMalloc, for
  * example code whose device memory is all reserved up front by another
  * allocator, or loops that must not stall: cudaMalloc may synchronise the
