@@ -103,6 +103,9 @@ class Context:
             raise GsrError(rc, "gsr_create failed")
         self._h = h
         self.device = int(device)
+        # Bumped by every bin_splats: bins from an earlier call may point into
+        # arena buffers that call freed or overwrote.
+        self._bin_generation = 0
 
     def _check(self, rc):
         if rc != GSR_OK:
@@ -133,10 +136,17 @@ class Context:
 
 class Bins:
     """Result of bin_splats: device views into the context's arena (valid until
-    the next bin_splats on the same context)."""
+    the next bin_splats on the same context, which may free or overwrite the
+    buffers; later use raises ValueError)."""
 
-    def __init__(self, ctx: Context, raw: _Bins, device):
-        self.ctx, self.raw, self._device = ctx, raw, device
+    def __init__(self, ctx: Context, raw: _Bins, device, generation: int):
+        self.ctx, self.raw, self._device, self.generation = ctx, raw, device, generation
+
+    def _check_current(self):
+        if getattr(self.ctx, "_h", None) is None:
+            raise ValueError("the context these bins belong to is closed")
+        if self.generation != self.ctx._bin_generation:
+            raise ValueError("these bins were replaced by a later bin_splats on the same context")
 
     @property
     def num_pairs(self) -> int:
@@ -147,6 +157,7 @@ class Bins:
         return int(self.raw.tiles_x), int(self.raw.tiles_y)
 
     def _view(self, ptr, shape, typestr):
+        self._check_current()
         if shape[0] == 0:
             return torch.empty(shape, dtype={"<i8": torch.int64, "<i4": torch.int32}[typestr],
                                device=self._device)
@@ -203,15 +214,17 @@ def bin_splats(ctx: Context, splats: torch.Tensor, depths: torch.Tensor, width: 
     _need(splats, "splats", torch.float32, (n, 9))
     _need(depths, "depths", torch.float32, (n,))
     raw = _Bins()
+    ctx._bin_generation += 1   # even a failed call may have regrown the arena
     ctx._check(lib.gsr_bin_splats(ctx._h, ctypes.c_void_p(splats.data_ptr()),
                                   ctypes.c_void_p(depths.data_ptr()), n, int(width), int(height),
                                   _stream_ptr(stream, splats.device), ctypes.byref(raw)))
-    return Bins(ctx, raw, splats.device)
+    return Bins(ctx, raw, splats.device, ctx._bin_generation)
 
 
 def rasterize_forward(ctx: Context, splats: torch.Tensor, bins: Bins, out_rgbw=None, final_T=None,
                       last_contrib=None, stream=None):
     """Returns (out_rgbw [H*W, 4] f32, final_T [H*W] f32, last_contrib [H*W] int32)."""
+    bins._check_current()
     n = splats.shape[0]
     _need(splats, "splats", torch.float32, (n, 9))
     npx = int(bins.raw.width) * int(bins.raw.height)
@@ -235,6 +248,7 @@ def rasterize_forward(ctx: Context, splats: torch.Tensor, bins: Bins, out_rgbw=N
 def rasterize_backward(ctx: Context, splats: torch.Tensor, bins: Bins, dl_dout: torch.Tensor,
                        final_T: torch.Tensor, last_contrib: torch.Tensor, grad=None, stream=None):
     """Returns grad [N, 9] f32 (d/d of each Splat2D field)."""
+    bins._check_current()
     n = splats.shape[0]
     _need(splats, "splats", torch.float32, (n, 9))
     npx = int(bins.raw.width) * int(bins.raw.height)

@@ -130,3 +130,26 @@ def test_package_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def test_stale_bins_are_refused(lib):
+    """Bins from an earlier bin_splats may point into arena buffers a later
+    call freed: the binding refuses them before any device access, as it does
+    bins of a closed context."""
+    from gaussian_splatting_tile_bin_gb300 import _abi
+
+    class FakeContext:
+        _h = ctypes.c_void_p(1)
+        _bin_generation = 2
+
+    stale = _abi.Bins(FakeContext, _abi._Bins(), "cpu", 1)
+    for call in (stale.keys, stale.sorted_idx, stale.tile_ranges, stale.tile_order,
+                 lambda: _abi.rasterize_forward(FakeContext, None, stale),
+                 lambda: _abi.rasterize_backward(FakeContext, None, stale, None, None, None)):
+        with pytest.raises(ValueError, match="later bin_splats"):
+            call()
+    current = _abi.Bins(FakeContext, _abi._Bins(), "cpu", 2)
+    current._check_current()
+    FakeContext._h = None
+    with pytest.raises(ValueError, match="closed"):
+        current.keys()
