@@ -167,12 +167,29 @@ def stress(seed: int = 4) -> Workload:
                       "large_scale": STRESS_LARGE_SCALE})
 
 
+def lego_far(seed: int = 3, distance: float = 4.0) -> Workload:
+    """lego_final seen from `distance` times farther away: a pinhole camera
+    maps a Gaussian's footprint linearly in 1/depth, so the means move toward
+    the image centre, every std shrinks by that factor (the conic grows by its
+    square) and depths grow by it.  The whole object lands in a few dozen tiles
+    with very long lists, the crowded-tile case the frame's other sets lack."""
+    base = lego_final(seed)
+    sp = base.splats.astype(np.float64)
+    c = (base.width - 1) / 2.0
+    sp[:, 0:2] = c + (sp[:, 0:2] - c) / distance
+    sp[:, 2:5] *= distance ** 2
+    recipe = dict(base.recipe, name_of_base="lego_final", distance=distance)
+    return Workload("lego_far", base.width, base.height, sp.astype(np.float32),
+                    (base.depths.astype(np.float64) * distance).astype(np.float32), base.dl_dout, recipe)
+
+
 CONFIGS = {
     "tiny": tiny,
     "small": small,
     "lego_early": lego_early,
     "lego_final": lego_final,
     "stress": stress,
+    "lego_far": lego_far,
 }
 
 

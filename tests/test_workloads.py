@@ -43,3 +43,22 @@ def test_lego_final_shape():
     c = oracle.forward(wl.splats, idx, ranges, wl.width, wl.height)["counters"]
     frac = 1.0 - c["n_contrib"] / c["n_eval"]
     assert 0.90 <= frac <= 0.97, frac
+
+
+def test_lego_far_crowds_a_few_tiles():
+    """lego_final from four times the distance: the same splats, footprints a
+    quarter the size, depth order kept.  Its heaviest tile carries more than ten
+    times a balanced share of 608 CTA slots (152 SMs x 4) of the per-pixel work
+    (the sum of last_contributor over the tile), the case a split of long
+    lists is for."""
+    near, far = gen.lego_final(), gen.lego_far()
+    assert far.n == near.n
+    assert np.array_equal(np.argsort(far.depths, kind="stable"), np.argsort(near.depths, kind="stable"))
+    s = far.splats.astype(np.float64)
+    assert np.all(np.isfinite(s)) and np.all(s[:, 2] * s[:, 4] - s[:, 3] ** 2 > 0)
+    keys, idx, ranges = oracle.bin_splats(far.splats, far.depths, far.width, far.height)
+    last = oracle.forward(far.splats, idx, ranges, far.width, far.height)["last"].astype(np.int64)
+    cost = last.reshape(50, 16, 50, 16).transpose(0, 2, 1, 3).reshape(2500, 256).sum(axis=1)
+    share = cost.sum() / 608.0
+    assert cost.max() > 10.0 * share
+    assert len(keys) < len(oracle.bin_splats(near.splats, near.depths, 800, 800)[0])
