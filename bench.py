@@ -11,9 +11,10 @@ inside the timed region.  N > 1 (torchrun): independent replicas, one per
 GPU, the slowest rank's time counts.
 
 Reference arm (--impl reference): the CPU oracle, unchanged, on the host
-cores, on the same workload; each step bins the splats of one band of tile
-rows and runs the forward and backward there, and the step time is scaled to
-the full frame by pixel count; successive steps walk the bands.
+cores, on the same workload; each step is the whole frame cut into one band of
+tile rows per core (each band bins every splat against its rows, then runs the
+forward and backward), the bands in parallel worker processes, timed by the
+wall clock.
 """
 from __future__ import annotations
 
@@ -33,9 +34,11 @@ import gen  # noqa: E402
 
 METRIC = "rasterize bin+fwd+bwd ms/iter @800×800, 409,660 splats; % of roofline"
 FLUSH_BYTES = 256 << 20
-SM_COUNT = 152
+# Lanes per SM per clock of the FP32 (FFMA) pipe and of the SFU's ex2: the
+# formula the measured rates (peak_kernel) are shown beside.  GB300's SFU runs
+# ex2 at 32 lanes per SM per clock (measured with gsr_peak_kernel).
 FP32_LANES_PER_SM = 128
-SFU_LANES_PER_SM = 16
+SFU_LANES_PER_SM = 32
 
 # Algorithmic FP32 operations per unit (the counts come from the oracle's counters).
 #   forward, per examined (pixel, splat): dx, dy, 5 for sigma, 2 range compares   = 9
@@ -272,41 +275,49 @@ def band_workload(wl, band, bands):
     return gen.from_arrays(f"{wl.name}[rows {y0}:{y1}]", wl.width, y1 - y0, s, wl.depths, dl), y1 - y0
 
 
+def bench_config(wl, args, pairs, world):
+    """The `config` object of the JSON line; both arms print the same one."""
+    return {"workload": workload_label(wl), "splats": wl.n, "width": wl.width, "height": wl.height,
+            "pairs": int(pairs), "l2": "flushed between timed steps (256 MB write)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "backward_accumulation": "fixed point (deterministic)" if args.deterministic else "double atomics",
+            "backward_loop_nest": "per splat (diagonal)" if args.bwd_per_splat else "per pixel"}
+
+
 def reference_arm(args):
+    """The oracle, as it stands, on the host cores: every step is one whole
+    frame (binning, forward, backward) cut into one tile-row band per core,
+    the bands in parallel worker processes; the step time is the wall time."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+
+    import oracle
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    import oracle
     wl = gen.make(args.config)
-    bands = 8
+    pairs = oracle.count_pairs(wl.splats, wl.depths, wl.width, wl.height)
+    cores = len(os.sched_getaffinity(0))
     steps_ms = []
-
-    def one(k):
-        sub, rows = band_workload(wl, k % bands, bands)
-        t0 = time.perf_counter()
-        keys, idx, ranges = oracle.bin_splats(sub.splats, sub.depths, sub.width, sub.height)
-        f = oracle.forward(sub.splats, idx, ranges, sub.width, sub.height)
-        oracle.backward(sub.splats, idx, ranges, sub.width, sub.height, sub.dl_dout)
-        dt = time.perf_counter() - t0
-        del f
-        return dt * 1e3 * wl.height / max(rows, 1)
-
-    for k in range(args.warmup):
-        one(k)
-    for k in range(args.steps):
-        steps_ms.append(one(args.warmup + k))
+    with ProcessPoolExecutor(cores, mp_context=mp.get_context("spawn")) as pool:
+        def one():
+            t0 = time.perf_counter()
+            list(pool.map(_oracle_band, [(args.config, k, cores) for k in range(cores)]))
+            return (time.perf_counter() - t0) * 1e3
+        for _ in range(args.warmup):
+            one()
+        for _ in range(args.steps):
+            steps_ms.append(one())
     value = float(np.mean(steps_ms))
-    cores = 1
     line = {"metric": METRIC, "value": value, "unit": "ms/iter", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": value,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": workload_label(wl), "splats": wl.n, "width": wl.width,
-                       "height": wl.height, "parallelism": "single process, host cores"},
+            "config": bench_config(wl, args, pairs, 1),
             "cpu_baseline": {"value": value, "unit": "ms/iter", "cores": cores, "kind": "oracle",
-                             "sample": f"per step one of {bands} tile-row bands (binning of the "
-                                       "band's splats, forward, backward), scaled to the full "
-                                       "frame by rows; steps walk the bands"},
+                             "sample": f"every step the whole frame as {cores} tile-row bands (each bins "
+                                       "every splat against its rows, then forward and backward), one "
+                                       "worker process per band, wall time"},
             "e2e": {"value": value, "unit": "ms/iter", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -317,8 +328,8 @@ def reference_arm(args):
 # GPU arm
 # --------------------------------------------------------------------------
 
-def roofline_for(kind, counters, pairs, wl, ms, peaks, sm_mhz):
-    """Algorithmic work of one launch against the FP32 / SFU / HBM peaks."""
+def roofline_for(kind, counters, pairs, wl, ms, peaks, alu):
+    """Algorithmic work of one launch against the measured FP32 / SFU / HBM peaks."""
     ops = FWD_OPS if kind == "forward" else BWD_OPS
     fp32 = sum(ops[k] * counters[k] for k in ops)
     sfu = counters["n_exp"] + (counters["n_contrib"] if kind == "backward" else 0)
@@ -327,9 +338,8 @@ def roofline_for(kind, counters, pairs, wl, ms, peaks, sm_mhz):
         bytes_ = pairs * (36 + 4) + px * 24
     else:
         bytes_ = pairs * (36 + 4) + px * (16 + 4 + 4) + wl.n * 36 * 2
-    clk = peaks["sm_max_mhz"] * 1e6
-    fp32_peak = SM_COUNT * FP32_LANES_PER_SM * clk
-    sfu_peak = SM_COUNT * SFU_LANES_PER_SM * clk
+    fp32_peak = alu["fp32_lane_ops_per_s"]
+    sfu_peak = alu["sfu_lane_ops_per_s"]
     hbm_peak = peaks["hbm_gbs"] * 1e9
     t = {"alu": fp32 / fp32_peak, "sfu": sfu / sfu_peak, "hbm": bytes_ / hbm_peak}
     bound = max(t, key=t.get)
@@ -340,14 +350,42 @@ def roofline_for(kind, counters, pairs, wl, ms, peaks, sm_mhz):
         achieved, peak, unit = fp32 / sec / 1e9, fp32_peak / 1e9, "Gop/s (fp32 lane ops)"
     else:
         achieved, peak, unit = sfu / sec / 1e9, sfu_peak / 1e9, "Gop/s (sfu lane ops)"
+    formula = alu["formula_fp32_lane_ops_per_s"] if bound == "alu" else alu["formula_sfu_lane_ops_per_s"]
     return {"kernel": kind, "bound": "alu" if bound in ("alu", "sfu") else "hbm",
             "pipe": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "traffic": ncu_traffic(kind, wl.name),
-            "peak_source": f"{peaks['source']} HBM; FP32/SFU = {SM_COUNT} SMs x "
-                           f"{FP32_LANES_PER_SM}/{SFU_LANES_PER_SM} lanes x {peaks['sm_max_mhz']:.0f} MHz",
-            "algorithmic": {"fp32_ops": fp32, "sfu_ops": sfu, "bytes": bytes_},
-            "frac_at_sampled_clock": (achieved / peak) * (peaks["sm_max_mhz"] / sm_mhz)
-            if (sm_mhz and bound != "hbm") else None}
+            "peak_source": ("measured HBM copy (MEASURED_PEAKS.json)" if bound == "hbm" else
+                            f"measured: the {'FFMA' if bound == 'alu' else 'ex2'} rate kernel (gsr_peak_kernel) "
+                            f"timed in this run, {alu['sms']} SMs"),
+            "peak_formula": None if bound == "hbm" else formula / 1e9,
+            "algorithmic": {"fp32_ops": fp32, "sfu_ops": sfu, "bytes": bytes_}}
+
+
+def measure_alu_peaks(gsr, ctx, dev, stream, reps=5):
+    """FP32 (FFMA) and SFU (ex2) lane-operation rates of this GPU, from the
+    library's rate kernels timed with CUDA events (best of `reps` launches of
+    about 2 ms each after warm-up), beside the formula SMs x lanes x max clock."""
+    import torch
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    sms = int(props.multi_processor_count)
+    out = {"sms": sms}
+    for kind, iters in (("ffma", 16384), ("ex2", 2048)):
+        rates = []
+        for r in range(3 + reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ops = gsr.peak_kernel(ctx, kind, iters, sink, stream=stream)
+            b.record(stream)
+            b.synchronize()
+            if r >= 3:
+                rates.append(ops / (a.elapsed_time(b) * 1e-3))
+        out["fp32_lane_ops_per_s" if kind == "ffma" else "sfu_lane_ops_per_s"] = float(max(rates))
+    mhz = measured_peaks()["sm_max_mhz"]
+    out["formula_fp32_lane_ops_per_s"] = sms * FP32_LANES_PER_SM * mhz * 1e6
+    out["formula_sfu_lane_ops_per_s"] = sms * SFU_LANES_PER_SM * mhz * 1e6
+    out["formula"] = f"{sms} SMs x {FP32_LANES_PER_SM} FP32 / {SFU_LANES_PER_SM} SFU lanes x {mhz:.0f} MHz"
+    return out
 
 
 # Algorithmic bytes per Gaussian of the projection kernels: the forward reads a
@@ -641,6 +679,7 @@ def gpu_arm(args):
         projection = time_projection(gsr, ctx, dev, stream, flush, max(args.steps, 20), max(args.warmup, 3),
                                      peaks)
 
+    alu = measure_alu_peaks(gsr, ctx, dev, stream)
     rows = sampler.stop()
     clocks = ClockSampler.summarize(rows)
 
@@ -650,13 +689,7 @@ def gpu_arm(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(tot_ms.mean()),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": workload_label(wl), "splats": wl.n, "width": wl.width,
-                       "height": wl.height, "pairs": int(pairs),
-                       "l2": "flushed between timed steps (256 MB write)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "backward_accumulation": "fixed point (deterministic)" if args.deterministic
-                       else "double atomics",
-                       "backward_loop_nest": "per splat (diagonal)" if args.bwd_per_splat else "per pixel"},
+            "config": bench_config(wl, args, pairs, world),
             "ms_per_step_median": float(np.median(tot_ms)), "ms_per_step_std": float(np.std(tot_ms)),
             "stages_ms": {"bin": float(bin_ms.mean()), "forward": float(fwd_ms.mean()),
                           "backward": float(bwd_ms.mean()),
@@ -669,6 +702,7 @@ def gpu_arm(args):
     if projection:
         line["projection"] = projection
     line["roofline_bin"] = roofline_bin
+    line["alu_peaks"] = alu
     if graph:
         line["graph"] = graph
 
@@ -685,10 +719,8 @@ def gpu_arm(args):
                 "value": ms_all, "unit": "ms/iter", "cores": cores, "kind": "oracle",
                 "sample": f"the whole frame as {cores} tile-row bands (each bins every splat against "
                           "its rows, then forward and backward), one worker process per band, wall time"}
-        rf = roofline_for("forward", cb["fwd_counters"], cb["pairs"], wl, float(fwd_ms.mean()), peaks,
-                          clocks.get("sm_mhz"))
-        rb = roofline_for("backward", cb["bwd_counters"], cb["pairs"], wl, float(bwd_ms.mean()),
-                          peaks, clocks.get("sm_mhz"))
+        rf = roofline_for("forward", cb["fwd_counters"], cb["pairs"], wl, float(fwd_ms.mean()), peaks, alu)
+        rb = roofline_for("backward", cb["bwd_counters"], cb["pairs"], wl, float(bwd_ms.mean()), peaks, alu)
         dom = rb if bwd_ms.mean() >= fwd_ms.mean() else rf
         line["roofline"] = dom
         line["roofline_other"] = rf if dom is rb else rb

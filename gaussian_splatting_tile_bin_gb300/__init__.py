@@ -13,8 +13,8 @@ and on either side the projection of 3-D Gaussians and its backward:
     splats, depths = project_forward(ctx, gaussians, camera)
     dl_dgaussians = project_backward(ctx, gaussians, camera, grad)
 """
-from ._abi import (LIB_PATH, Bins, Context, GsrError, bin_splats, project_backward, project_forward,
-                   rasterize_backward, rasterize_forward)
+from ._abi import (LIB_PATH, Bins, Context, GsrError, bin_splats, peak_kernel, project_backward,
+                   project_forward, rasterize_backward, rasterize_forward)
 
 __all__ = ["LIB_PATH", "Bins", "Context", "GsrError", "bin_splats", "rasterize_forward",
-           "rasterize_backward", "project_forward", "project_backward"]
+           "rasterize_backward", "project_forward", "project_backward", "peak_kernel"]

@@ -79,6 +79,8 @@ def _load():
     lib.gsr_project_backward.restype = ctypes.c_int
     lib.gsr_exp_neg.argtypes = [P, P, P, i32, P]
     lib.gsr_exp_neg.restype = ctypes.c_int
+    lib.gsr_peak_kernel.argtypes = [P, ctypes.c_int, i32, P, ctypes.POINTER(ctypes.c_uint64), P]
+    lib.gsr_peak_kernel.restype = ctypes.c_int
     return lib
 
 
@@ -189,6 +191,19 @@ def exp_neg(ctx: Context, s: torch.Tensor, out=None, stream=None) -> torch.Tenso
     ctx._check(lib.gsr_exp_neg(ctx._h, ctypes.c_void_p(s.data_ptr()), ctypes.c_void_p(out.data_ptr()),
                                int(s.numel()), _stream_ptr(stream, s.device)))
     return out
+
+
+PEAK_KINDS = {"ffma": 0, "ex2": 1}
+
+
+def peak_kernel(ctx: Context, kind: str, iters: int, sink: torch.Tensor, stream=None) -> int:
+    """Enqueues one launch of the FP32 ("ffma") or SFU ("ex2") rate kernel;
+    returns the number of lane operations it performs (time it with events)."""
+    _need(sink, "sink", torch.float32)
+    ops = ctypes.c_uint64()
+    ctx._check(lib.gsr_peak_kernel(ctx._h, PEAK_KINDS[kind], int(iters), ctypes.c_void_p(sink.data_ptr()),
+                                   ctypes.byref(ops), _stream_ptr(stream, sink.device)))
+    return int(ops.value)
 
 
 def _stream_ptr(stream, device):

@@ -85,9 +85,16 @@ int gsr_create(gsr_ctx **out, int device)
         return GSR_ERR_CUDA;
     }
     if (device < 0 || device >= count) return GSR_ERR_INVALID_ARG;
+    // Grid sizes of the grid-stride kernels are multiples of the SM count.
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0) {
+        cudaGetLastError();
+        return GSR_ERR_CUDA;
+    }
     gsr_ctx *ctx = new (std::nothrow) gsr_ctx();
     if (!ctx) return GSR_ERR_OOM;
     ctx->device = device;
+    ctx->num_sms = sms;
     *out = ctx;
     return GSR_OK;
 }
@@ -261,6 +268,19 @@ int gsr_exp_neg(gsr_ctx *ctx, const float *s, float *out, int32_t n, void *strea
     if (!g.ok) return fail(ctx, GSR_ERR_CUDA, "cannot select the context's device");
     if (n == 0) return GSR_OK;
     return gsr::exp_neg_eval(ctx, s, out, n, (cudaStream_t)stream);
+}
+
+int gsr_peak_kernel(gsr_ctx *ctx, int kind, int32_t iters, float *sink, uint64_t *lane_ops, void *stream)
+{
+    gsr::Range range("gsr_peak_kernel");
+    if (!ctx) return GSR_ERR_INVALID_ARG;
+    ctx->err.clear();
+    if (kind != GSR_PEAK_FFMA && kind != GSR_PEAK_EX2) return fail(ctx, GSR_ERR_INVALID_ARG, "unknown peak kind");
+    if (iters < 1 || iters > (1 << 24)) return fail(ctx, GSR_ERR_INVALID_ARG, "iters outside [1, 2^24]");
+    if (!sink || !lane_ops) return fail(ctx, GSR_ERR_INVALID_ARG, "sink/lane_ops is NULL");
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, GSR_ERR_CUDA, "cannot select the context's device");
+    return gsr::peak_kernel(ctx, kind, iters, sink, lane_ops, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -38,7 +38,7 @@ struct gsr_ctx {
     int opt_deterministic = 0;
     int opt_bwd_per_splat = 0;
     int fail_next_alloc = 0;                    // test hook: the next device allocation fails
-    int num_sms = 0;                            // multiprocessors of the device (0: not queried yet)
+    int num_sms = 0;                            // multiprocessors of the device (read by gsr_create)
 
     // Grow-only arena.
     size_t cap_pairs = 0;
@@ -169,5 +169,7 @@ int project_backward(gsr_ctx *ctx, const float *gauss, int32_t n, const gsr_came
                      const float *dl_dsplat, float *dl_dg, cudaStream_t stream);
 // out[i] = the raster kernels' exp(-s[i]).
 int exp_neg_eval(gsr_ctx *ctx, const float *s, float *out, int32_t n, cudaStream_t stream);
+// One launch of the FP32 / SFU rate kernel (peak.cu); *lane_ops = its lane operations.
+int peak_kernel(gsr_ctx *ctx, int kind, int32_t iters, float *sink, uint64_t *lane_ops, cudaStream_t stream);
 
 }  // namespace gsr

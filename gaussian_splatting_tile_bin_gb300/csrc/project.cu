@@ -408,14 +408,6 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
 int projection_grid(gsr_ctx *ctx, int32_t n, int blocks_per_sm)
 {
-    if (ctx->num_sms <= 0) {
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess || sms <= 0) {
-            cudaGetLastError();
-            sms = 152;
-        }
-        ctx->num_sms = sms;
-    }
     const int64_t chunks = ((int64_t)n + kProjBlock - 1) / kProjBlock;
     return (int)std::min<int64_t>(chunks, (int64_t)ctx->num_sms * blocks_per_sm);
 }

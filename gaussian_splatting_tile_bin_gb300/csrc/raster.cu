@@ -18,6 +18,7 @@
 // (splat_sigma, splat_alpha), so the backward takes exactly the forward's skip
 // and stop decisions.
 #include <algorithm>
+#include <atomic>
 #include <string>
 
 #include "internal.cuh"
@@ -41,7 +42,6 @@ namespace gsr {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int SM_BLOCKS_CAP = 152 * 16;     // grid-stride cap for elementwise passes
 constexpr int kWarps = kTilePixels / 32;
 constexpr int kBatch = kTilePixels * GSR_STAGE_PER_THREAD;  // splats per staged batch
 constexpr int kBwdBatch = kTilePixels * GSR_BWD_STAGE_PER_THREAD;
@@ -986,7 +986,7 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
                          "backward launch")))
         return rc;
     if (count > 0) {
-        const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)SM_BLOCKS_CAP);
+        const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)ctx->num_sms * 16);
         const cudaError_t e =
             escale ? launch_kernel(ctx, k_grad_to_float_det, dim3(blocks), dim3(256), stream,
                                    reinterpret_cast<long long *>(ctx->grad_acc), escale,
@@ -1012,7 +1012,7 @@ __global__ void k_exp_neg(const float *__restrict__ s, float *__restrict__ out, 
 
 int exp_neg_eval(gsr_ctx *ctx, const float *s, float *out, int32_t n, cudaStream_t stream)
 {
-    const int blocks = (int)std::min<size_t>(((size_t)n + 255) / 256, (size_t)SM_BLOCKS_CAP);
+    const int blocks = (int)std::min<size_t>(((size_t)n + 255) / 256, (size_t)ctx->num_sms * 16);
     return cuda_check(ctx, launch_kernel(ctx, k_exp_neg, dim3(blocks), dim3(256), stream, s, out, (int)n),
                       "exp launch");
 }
@@ -1029,8 +1029,10 @@ namespace {
 __device__ __align__(256) double g_noalloc_grad_acc[(size_t)GSR_NOALLOC_MAX_SPLATS * 9];
 
 // Device address of g_noalloc_grad_acc, looked up once per device (the array's
-// name in host code is only a stand-in, not a device pointer).
-double *g_noalloc_ptr[64] = {};
+// name in host code is only a stand-in, not a device pointer).  Atomic: two
+// host threads may make their first call on a device at the same time (both
+// store the same address).  A device reset invalidates the address.
+std::atomic<double *> g_noalloc_ptr[64] = {};
 
 }  // namespace
 
@@ -1046,7 +1048,7 @@ int rasterize_backward_noalloc(gsr_ctx *ctx, const float *splats, int32_t n, con
         return fail(ctx, GSR_ERR_INVALID_ARG, "device ordinal out of range for the fixed scratch table");
     if (ctx->opt_deterministic)
         return fail(ctx, GSR_ERR_INVALID_ARG, "the deterministic backward needs the context's arena");
-    double *acc = g_noalloc_ptr[ctx->device];
+    double *acc = g_noalloc_ptr[ctx->device].load(std::memory_order_acquire);
     if (!acc) {
         // First call on this device (the device is current here): find the
         // array's device address.
@@ -1054,7 +1056,7 @@ int rasterize_backward_noalloc(gsr_ctx *ctx, const float *splats, int32_t n, con
         int rc = cuda_check(ctx, cudaGetSymbolAddress(&p, g_noalloc_grad_acc), "cudaGetSymbolAddress");
         if (rc) return rc;
         acc = static_cast<double *>(p);
-        g_noalloc_ptr[ctx->device] = acc;
+        g_noalloc_ptr[ctx->device].store(acc, std::memory_order_release);
     }
     const size_t count = (size_t)n * 9;
     // The array keeps the previous call's sums: clear the part this call uses.
@@ -1066,7 +1068,7 @@ int rasterize_backward_noalloc(gsr_ctx *ctx, const float *splats, int32_t n, con
                          "backward launch")))
         return rc;
     if (count == 0) return GSR_OK;
-    const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)SM_BLOCKS_CAP);
+    const int blocks = (int)std::min<size_t>((count + 255) / 256, (size_t)ctx->num_sms * 16);
     return cuda_check(ctx, launch_kernel(ctx, k_grad_to_float, dim3(blocks), dim3(256), stream, acc, grad, count),
                       "gradient conversion launch");
 }

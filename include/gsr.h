@@ -206,8 +206,10 @@ int gsr_rasterize_forward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n,
  *   final_T, last_contrib   the forward's outputs for the same bins
  *   grad          device, [n * 9] float, overwritten; row i holds d/d of splat i's
  *                 fields in gsr_splat2d order
- * Gradients are accumulated with float atomics, so the last bits may differ
- * between runs.  Errors: as gsr_rasterize_forward. */
+ * Each warp's float partial sums are added with double-precision atomics and
+ * converted to float at the end; the order of the adds may vary between runs,
+ * so the last bits may too (GSR_OPT_DETERMINISTIC makes them fixed).
+ * Errors: as gsr_rasterize_forward. */
 int gsr_rasterize_backward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n,
                            const gsr_bins *bins, const float *dl_dout, const float *final_T,
                            const uint32_t *last_contrib, float *grad, void *stream);
@@ -226,7 +228,8 @@ int gsr_rasterize_backward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n,
  * usual (which does use the context's arena).
  *   - n > GSR_NOALLOC_MAX_SPLATS is rejected with GSR_ERR_INVALID_ARG.
  *   - The first call on a device looks up the array's device address (with that
- *     device current); make that first call before any stream capture.
+ *     device current); make that first call before any stream capture.  A
+ *     device reset (cudaDeviceReset) invalidates the address it keeps.
  *   - All calls on a device share the one array, and each call clears the part
  *     it uses before accumulating.  Calls whose work overlaps on the GPU (other
  *     streams, other contexts, other threads) race on it: order them. */
@@ -302,6 +305,23 @@ int gsr_project_backward(gsr_ctx *ctx, const gsr_gaussian3d *gauss, int32_t n, c
  * Enqueued on `stream`; nothing is allocated.  GSR_ERR_INVALID_ARG for a NULL
  * or misaligned pointer or n < 0. */
 int gsr_exp_neg(gsr_ctx *ctx, const float *s, float *out, int32_t n, void *stream);
+
+/* Diagnostic: one launch of a kernel of known arithmetic, for measuring the
+ * device's FP32 and SFU lane-operation rates (the peaks the raster kernels'
+ * roofline is taken against; they are ALU-bound).  The grid is 8 CTAs of 256
+ * threads per SM.  Each thread runs iters (rounded up to a multiple of 8)
+ * rounds of 16 independent operations:
+ *   kind GSR_PEAK_FFMA  fused multiply-adds (x = x a + b), 1 lane operation each;
+ *   kind GSR_PEAK_EX2   base-2 exponentials on the SFU (ex2.approx, the
+ *                       instruction under the kernels' exp(-sigma)).
+ *   sink      device, [1] float; written only in a case that never occurs, so
+ *             the compiler keeps the work
+ *   lane_ops  host; receives the number of lane operations of the launch
+ * Time the launch with events on `stream`; rate = lane_ops / time.  Nothing is
+ * allocated.  GSR_ERR_INVALID_ARG for an unknown kind, iters outside
+ * [1, 2^24], or a NULL pointer. */
+enum { GSR_PEAK_FFMA = 0, GSR_PEAK_EX2 = 1 };
+int gsr_peak_kernel(gsr_ctx *ctx, int kind, int32_t iters, float *sink, uint64_t *lane_ops, void *stream);
 
 #ifdef __cplusplus
 }

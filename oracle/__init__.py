@@ -65,6 +65,20 @@ def _load():
         fn = getattr(lib, name)
         fn.argtypes = [P, P, i32, i32, i32, P, P, P]
         fn.restype = None
+    lib.orc_forward_forced_f32.argtypes = [P, P, P, i32, i32, P, i64, P, P, P, f64, f64, P]
+    lib.orc_forward_forced_f32.restype = None
+    lib.orc_pixel_forced_f32.argtypes = [P, P, P, i32, i32, i32, i32, P, i64, f64, f64, P, P, P, i32, P, P]
+    lib.orc_pixel_forced_f32.restype = None
+    lib.orc_backward_forced_f32.argtypes = [P, i32, P, P, i32, i32, P, P, i64, P, P, f64, f64, P]
+    lib.orc_backward_forced_f32.restype = None
+    lib.orc_backward_targets_f32.argtypes = [P, i32, P, P, i32, i32, P, P, i64, P, i32, P, P, f64, f64, P]
+    lib.orc_backward_targets_f32.restype = None
+    lib.orc_splat_decisions_f32.argtypes = [P, i32, P, P, i32, i32, P, i64, ctypes.c_uint32, f64, f64, P, P,
+                                            i32, P]
+    lib.orc_splat_decisions_f32.restype = None
+    lib.orc_pixel_backward_forced_f32.argtypes = [P, P, P, i32, i32, P, i32, i32, P, i64, ctypes.c_uint32, P,
+                                                  f64, f64, P]
+    lib.orc_pixel_backward_forced_f32.restype = None
     lib.orc_project_forward.argtypes = [P, i32, P, P, P, P]
     lib.orc_project_forward.restype = None
     lib.orc_project_backward.argtypes = [P, i32, P, P, P, P]
@@ -176,6 +190,145 @@ def backward(splats, idx, ranges, width, height, dl_dout, *, f64=False, eps_alph
        float(eps_alpha), float(sigma_ulps), _ptr(cnt))
     return {"grad": grad, "gabs": gabs, "knife": knife.astype(bool),
             "counters": {"n_eval": int(cnt[0]), "n_exp": int(cnt[1]), "n_contrib": int(cnt[2])}}
+
+
+# --- forced replays ---------------------------------------------------------
+
+# Decisions a forced replay may take the other way (oracle.h): alpha against
+# 1/255, next_T against 1e-4 (the stop), raw against 0.999 (the clamp).
+DEC_ALPHA, DEC_STOP, DEC_CLAMP = 1, 2, 4
+FLIP_DTYPE = np.dtype([("pixel", "<i8"), ("pos", "<u4"), ("type", "<u4")])
+DECISION_DTYPE = np.dtype([("pos", "<u4"), ("type", "<u4"), ("splat", "<u4"), ("margin", "<f4")])
+
+
+def flip_table(entries=()):
+    """A flip table sorted by (pixel, pos) from (pixel, pos, type) triples;
+    entries of the same (pixel, pos) are merged."""
+    merged = {}
+    for pixel, pos, typ in entries:
+        key = (int(pixel), int(pos))
+        merged[key] = merged.get(key, 0) | int(typ)
+    t = np.zeros(len(merged), dtype=FLIP_DTYPE)
+    for k, ((pixel, pos), typ) in enumerate(sorted(merged.items())):
+        t[k] = (pixel, pos, typ)
+    return t
+
+
+def _flips(table):
+    t = np.ascontiguousarray(table if table is not None else np.zeros(0, FLIP_DTYPE), dtype=FLIP_DTYPE)
+    return t, len(t)
+
+
+def forward_forced(splats, idx, ranges, width, height, flips, *, eps_alpha, sigma_ulps=0.0):
+    """The f32 forward with the decisions of `flips` taken the other way.
+    Returns dict(out, final_T, last, refused)."""
+    lib = _load()
+    s = _f32(splats).reshape(-1, 9)
+    ix = np.ascontiguousarray(idx, dtype=np.uint32)
+    rg = np.ascontiguousarray(ranges, dtype=np.uint32)
+    t, nt = _flips(flips)
+    npx = width * height
+    out = np.zeros((npx, 4), dtype=np.float32)
+    final_t = np.zeros(npx, dtype=np.float32)
+    last = np.zeros(npx, dtype=np.uint32)
+    refused = np.zeros(1, dtype=np.int64)
+    lib.orc_forward_forced_f32(_ptr(s), _ptr(ix), _ptr(rg), width, height, _ptr(t), nt, _ptr(out),
+                               _ptr(final_t), _ptr(last), float(eps_alpha), float(sigma_ulps), _ptr(refused))
+    return {"out": out, "final_T": final_t, "last": last, "refused": int(refused[0])}
+
+
+def pixel_forced(splats, idx, ranges, width, height, px, py, flips, *, eps_alpha, sigma_ulps=0.0,
+                 max_decisions=256):
+    """One pixel's forced forward: (out5 = rgb, w, final_T; last; the decisions
+    within their uncertainty along it; refused flips)."""
+    lib = _load()
+    s = _f32(splats).reshape(-1, 9)
+    ix = np.ascontiguousarray(idx, dtype=np.uint32)
+    rg = np.ascontiguousarray(ranges, dtype=np.uint32)
+    t, nt = _flips(flips)
+    out5 = np.zeros(5, dtype=np.float32)
+    last = np.zeros(1, dtype=np.uint32)
+    dec = np.zeros(max_decisions, dtype=DECISION_DTYPE)
+    ndec = np.zeros(1, dtype=np.int32)
+    refused = np.zeros(1, dtype=np.int64)
+    lib.orc_pixel_forced_f32(_ptr(s), _ptr(ix), _ptr(rg), width, height, int(px), int(py), _ptr(t), nt,
+                             float(eps_alpha), float(sigma_ulps), _ptr(out5), _ptr(last), _ptr(dec),
+                             max_decisions, _ptr(ndec), _ptr(refused))
+    return out5, int(last[0]), dec[:ndec[0]].copy(), int(refused[0])
+
+
+def backward_forced(splats, idx, ranges, width, height, dl_dout, flips, *, eps_alpha, sigma_ulps=0.0):
+    """The f32 backward (double sums) with the decisions of `flips` taken the
+    other way.  Returns dict(grad [N,9], gabs [N,9], refused)."""
+    lib = _load()
+    s = _f32(splats).reshape(-1, 9)
+    ix = np.ascontiguousarray(idx, dtype=np.uint32)
+    rg = np.ascontiguousarray(ranges, dtype=np.uint32)
+    g = _f32(dl_dout).reshape(-1, 4)
+    t, nt = _flips(flips)
+    n = s.shape[0]
+    grad = np.zeros((n, 9), dtype=np.float64)
+    gabs = np.zeros((n, 9), dtype=np.float64)
+    refused = np.zeros(1, dtype=np.int64)
+    lib.orc_backward_forced_f32(_ptr(s), n, _ptr(ix), _ptr(rg), width, height, _ptr(g), _ptr(t), nt,
+                                _ptr(grad), _ptr(gabs), float(eps_alpha), float(sigma_ulps), _ptr(refused))
+    return {"grad": grad, "gabs": gabs, "refused": int(refused[0])}
+
+
+def backward_targets(splats, idx, ranges, width, height, dl_dout, flips, targets, *, eps_alpha,
+                     sigma_ulps=0.0):
+    """The forced backward's gradients of the splats `targets` only.
+    Returns (grad [k,9], gabs [k,9], refused)."""
+    lib = _load()
+    s = _f32(splats).reshape(-1, 9)
+    ix = np.ascontiguousarray(idx, dtype=np.uint32)
+    rg = np.ascontiguousarray(ranges, dtype=np.uint32)
+    g = _f32(dl_dout).reshape(-1, 4)
+    t, nt = _flips(flips)
+    tg = np.ascontiguousarray(targets, dtype=np.uint32).reshape(-1)
+    grad = np.zeros((len(tg), 9), dtype=np.float64)
+    gabs = np.zeros((len(tg), 9), dtype=np.float64)
+    refused = np.zeros(1, dtype=np.int64)
+    lib.orc_backward_targets_f32(_ptr(s), s.shape[0], _ptr(ix), _ptr(rg), width, height, _ptr(g), _ptr(t), nt,
+                                 _ptr(tg), len(tg), _ptr(grad), _ptr(gabs), float(eps_alpha), float(sigma_ulps),
+                                 _ptr(refused))
+    return grad, gabs, int(refused[0])
+
+
+def pixel_backward_forced(splats, idx, ranges, width, height, dl_dout, px, py, flips, target, *, eps_alpha,
+                          sigma_ulps=0.0):
+    """Splat `target`'s gradient terms at pixel (px, py) under the flips:
+    (terms float64 [9], refused)."""
+    lib = _load()
+    s = _f32(splats).reshape(-1, 9)
+    ix = np.ascontiguousarray(idx, dtype=np.uint32)
+    rg = np.ascontiguousarray(ranges, dtype=np.uint32)
+    g = _f32(dl_dout).reshape(-1, 4)
+    t, nt = _flips(flips)
+    out = np.zeros(9, dtype=np.float64)
+    refused = np.zeros(1, dtype=np.int64)
+    lib.orc_pixel_backward_forced_f32(_ptr(s), _ptr(ix), _ptr(rg), width, height, _ptr(g), int(px), int(py),
+                                      _ptr(t), nt, int(target), _ptr(out), float(eps_alpha), float(sigma_ulps),
+                                      _ptr(refused))
+    return out, int(refused[0])
+
+
+def splat_decisions(splats, idx, ranges, width, height, flips, target, *, eps_alpha, sigma_ulps=0.0,
+                    max_decisions=4096):
+    """Splat `target`'s own decisions within their uncertainty at every pixel it
+    is evaluated at: (flip-table entries, margins)."""
+    lib = _load()
+    s = _f32(splats).reshape(-1, 9)
+    ix = np.ascontiguousarray(idx, dtype=np.uint32)
+    rg = np.ascontiguousarray(ranges, dtype=np.uint32)
+    t, nt = _flips(flips)
+    out = np.zeros(max_decisions, dtype=FLIP_DTYPE)
+    margins = np.zeros(max_decisions, dtype=np.float32)
+    count = np.zeros(1, dtype=np.int32)
+    lib.orc_splat_decisions_f32(_ptr(s), s.shape[0], _ptr(ix), _ptr(rg), width, height, _ptr(t), nt,
+                                int(target), float(eps_alpha), float(sigma_ulps), _ptr(out), _ptr(margins),
+                                max_decisions, _ptr(count))
+    return out[:count[0]].copy(), margins[:count[0]].copy()
 
 
 # --- projection (project.c) -------------------------------------------------

@@ -149,6 +149,15 @@ int32_t orc_radix_passes_4bit(uint64_t num_tiles)
 /* Forward and backward, once per precision                                  */
 /* ------------------------------------------------------------------------ */
 
+/* Decisions within their uncertainty met during a replay (dec nullable, at
+ * most max kept), and the flips a replay refused because the decision they
+ * name was not within its uncertainty. */
+typedef struct {
+    orc_decision *dec;
+    int32_t max, n;
+    int64_t refused;
+} orc_trace;
+
 static float orc_exp_f32(float x) { return (float)exp((double)x); }
 static double orc_exp_f64(double x) { return exp(x); }
 
@@ -249,8 +258,8 @@ static void forward_untiled(const float *splats, const float *depths, int32_t n,
                 uint32_t i = order[k].idx;
                 const int32_t *r = rects + 4 * (int64_t)i;
                 if (!alive[i] || tx < r[0] || tx > r[2] || ty < r[1] || ty > r[3]) continue;
-                composite_f32(&st, splats + 9 * (int64_t)i, (float)px, (float)py, pos, 0.0, 0.0,
-                              cnt, skip_sigma, NULL);
+                composite_f32(&st, splats + 9 * (int64_t)i, i, (float)px, (float)py, pos, 0.0, 0.0,
+                              cnt, skip_sigma, 0u, NULL, NULL);
                 ++pos;
             }
             int64_t p = (int64_t)py * width + px;

@@ -34,6 +34,31 @@
  * last_contributor) in counters[0..2]. */
 enum { ORC_N_EVAL = 0, ORC_N_EXP = 1, ORC_N_CONTRIB = 2 };
 
+/* Threshold decisions of one evaluation that another correct float
+ * implementation may take the other way when the tested value lies within its
+ * rounding uncertainty of the threshold: alpha against 1/255, next_T against
+ * 1e-4 (the stop), raw = color_a exp(-sigma) against 0.999 (the clamp, which
+ * only the gradient sees). */
+enum { ORC_DEC_ALPHA = 1, ORC_DEC_STOP = 2, ORC_DEC_CLAMP = 4 };
+
+/* One entry of a flip table: at pixel (py * width + px), the evaluation at
+ * position pos of the tile's list takes the decisions in `type` the other way.
+ * Tables are sorted by (pixel, pos). */
+typedef struct {
+    int64_t pixel;
+    uint32_t pos;
+    uint32_t type;
+} orc_flip;
+
+/* A decision met within its uncertainty: margin = distance to the threshold
+ * over the uncertainty of the tested value (below 1). */
+typedef struct {
+    uint32_t pos;
+    uint32_t type;
+    uint32_t splat;
+    float margin;
+} orc_decision;
+
 /* Tile rectangle of one splat's 3-sigma box, inclusive [tx0,tx1]x[ty0,ty1].
  * Returns 0 when the splat is culled (non-finite field, depth <= 0,
  * non-positive-definite conic, box off the image). */
@@ -105,6 +130,46 @@ void orc_backward_f64(const double *splats, int32_t n, const uint32_t *idx,
                       const uint32_t *ranges, int32_t width, int32_t height,
                       const double *dl_dout, double *grad, double *gabs, uint8_t *knife,
                       double eps_alpha, double sigma_ulps, int64_t *counters);
+
+/* Forced replays.  The same forward and backward with the decisions a flip
+ * table names taken the other way, where each lies within its uncertainty
+ * (margin < 1 under eps_alpha and sigma_ulps as above); *refused receives the
+ * number of flips that named a decision outside it (those are not taken).
+ * They show that a difference between another implementation and the oracle
+ * is the other outcome of decisions within rounding, and nothing else. */
+void orc_forward_forced_f32(const float *splats, const uint32_t *idx, const uint32_t *ranges,
+                            int32_t width, int32_t height, const orc_flip *flips, int64_t nflips,
+                            float *out_rgbw, float *final_T, uint32_t *last, double eps_alpha,
+                            double sigma_ulps, int64_t *refused);
+/* One pixel (px, py): out5 = (r, g, b, 1 - final_T, final_T), *last; the
+ * decisions within their uncertainty along its (forced) replay in dec[0, *ndec)
+ * (at most max_dec). */
+void orc_pixel_forced_f32(const float *splats, const uint32_t *idx, const uint32_t *ranges, int32_t width,
+                          int32_t height, int32_t px, int32_t py, const orc_flip *flips, int64_t nflips,
+                          double eps_alpha, double sigma_ulps, float *out5, uint32_t *last,
+                          orc_decision *dec, int32_t max_dec, int32_t *ndec, int64_t *refused);
+void orc_backward_forced_f32(const float *splats, int32_t n, const uint32_t *idx, const uint32_t *ranges,
+                             int32_t width, int32_t height, const float *dl_dout, const orc_flip *flips,
+                             int64_t nflips, double *grad, double *gabs, double eps_alpha, double sigma_ulps,
+                             int64_t *refused);
+/* The forced backward's gradients (and sums of |terms|) of the splats
+ * targets[0, nt) only, row k for targets[k]; it replays only the tiles whose
+ * lists hold a target. */
+void orc_backward_targets_f32(const float *splats, int32_t n, const uint32_t *idx, const uint32_t *ranges,
+                              int32_t width, int32_t height, const float *dl_dout, const orc_flip *flips,
+                              int64_t nflips, const uint32_t *targets, int32_t nt, double *grad_t,
+                              double *gabs_t, double eps_alpha, double sigma_ulps, int64_t *refused);
+/* Splat `target`'s gradient terms at pixel (px, py) under the flips, out9[9]. */
+void orc_pixel_backward_forced_f32(const float *splats, const uint32_t *idx, const uint32_t *ranges,
+                                   int32_t width, int32_t height, const float *dl_dout, int32_t px, int32_t py,
+                                   const orc_flip *flips, int64_t nflips, uint32_t target, double *out9,
+                                   double eps_alpha, double sigma_ulps, int64_t *refused);
+/* Splat `target`'s own decisions within their uncertainty at every pixel it is
+ * evaluated at (flips applied): out[0, *count) as flip entries, with margins. */
+void orc_splat_decisions_f32(const float *splats, int32_t n, const uint32_t *idx, const uint32_t *ranges,
+                             int32_t width, int32_t height, const orc_flip *flips, int64_t nflips,
+                             uint32_t target, double eps_alpha, double sigma_ulps, orc_flip *out,
+                             float *margins, int32_t max, int32_t *count);
 
 /* Projection of 3-D Gaussians to Splat2D records and depths, and its backward
  * (project.c).  Doubles.  g: [n][14] (mean xyz, log_scale xyz, quat wxyz,

@@ -24,7 +24,10 @@ def _run(args, timeout=300):
 
 
 def test_reference_arm_prints_one_contract_line():
+    import time
+    t0 = time.perf_counter()
     r = _run(["--impl", "reference", "--config", "tiny", "--steps", "3", "--warmup", "3"])
+    wall = time.perf_counter() - t0
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
     assert len(lines) == 1, r.stdout
@@ -41,6 +44,17 @@ def test_reference_arm_prints_one_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "ms/iter", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+    # every timed step is real work: the steps fit in the process's own run time
+    assert d["ms_per_step"] * d["steps"] / 1e3 <= wall
+    # the same config object as the GPU arm's (pairs from the oracle's binning)
+    sys.path.insert(0, ROOT)
+    import bench
+    import gen
+    import oracle
+    wl = gen.make("tiny")
+    args = bench.parse_args(["--config", "tiny"])
+    pairs = oracle.count_pairs(wl.splats, wl.depths, wl.width, wl.height)
+    assert d["config"] == bench.bench_config(wl, args, pairs, 1)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a CUDA device")

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import gen
-from gpu_helpers import check_backward, check_bins, check_forward, run_gpu, run_oracle, to_dev
+from gpu_helpers import as_result, check_backward, check_bins, check_forward, run_gpu, run_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -74,7 +74,7 @@ def test_backward_reports_an_allocation_failure_and_recovers(gsr):
         assert err.value.code == GSR_ERR_OOM
         grad = gsr.rasterize_backward(ctx, sp, bins, dl, final_t, last).cpu().numpy()
         o = run_oracle(wl)
-        check_backward({"grad": grad}, o)
+        check_backward(as_result(out, final_t, last, grad), o)
         assert np.all(np.isfinite(grad))
     finally:
         ctx.close()
@@ -96,6 +96,6 @@ def test_deterministic_backward_reports_an_allocation_failure_and_recovers(gsr):
             gsr.rasterize_backward(ctx, sp, bins, dl, final_t, last)
         assert err.value.code == GSR_ERR_OOM and "deterministic" in str(err.value)
         grad = gsr.rasterize_backward(ctx, sp, bins, dl, final_t, last).cpu().numpy()
-        check_backward({"grad": grad}, run_oracle(wl))
+        check_backward(as_result(out, final_t, last, grad), run_oracle(wl))
     finally:
         ctx.close()

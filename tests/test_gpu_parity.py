@@ -1,10 +1,13 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle.
 
 Binning must match bit for bit (sorted keys, sorted indices, tile ranges);
-forward pixels within 1e-5 absolute; gradients within 1e-4 + 1e-4 |ref|.
-A pixel or splat may differ beyond that only where the oracle flags a
-threshold decision (alpha vs 1/255, T vs 1e-4, the 0.999 clamp, the sign of
-sigma) within the rounding uncertainty of the two implementations.
+forward pixels within 1e-5 absolute with last_contrib equal; gradients within
+1e-4 + 1e-4 |ref| (+ 8u sum|t| for sums whose terms cancel, on at most a stated
+number of components per config).  A threshold decision (alpha vs 1/255, T vs
+1e-4, the 0.999 clamp) whose tested value lies within the two sides' rounding
+uncertainty may go either way; a pixel or splat passes then only if the oracle,
+re-run with such decisions taken the other way, reproduces the GPU within the
+same tolerances.
 """
 import numpy as np
 import pytest
@@ -12,7 +15,7 @@ import torch
 
 import gen
 import oracle
-from gpu_helpers import (check_backward, check_bins, check_forward, run_gpu, run_oracle, to_dev,
+from gpu_helpers import (check_backward, check_bins, check_forward, record_stats, run_gpu, run_oracle, to_dev,
                          varying_digit_mask)
 
 pytestmark = pytest.mark.gpu
@@ -33,24 +36,30 @@ def ctx(gsr):
     c.close()
 
 
-def _full(gsr, ctx, wl, backward=True):
+# The most gradient components per config allowed to need the 8u sum|t| term
+# (sums whose terms cancel; measured counts with the forced replays applied).
+COND_CAPS = {"tiny": 0, "small": 0, "lego_early": 4, "lego_final": 4, "stress": 100}
+
+
+def _full(gsr, ctx, wl, backward=True, cond_cap=None):
     g = run_gpu(gsr, ctx, wl, backward)
     o = run_oracle(wl, backward)
     check_bins(g, o)
     fs = check_forward(g, o)
-    bs = check_backward(g, o) if backward else None
+    bs = check_backward(g, o, cond_cap=cond_cap) if backward else None
+    record_stats(wl.name, pairs=int(g["num_pairs"]), forward=fs, backward=bs)
     return g, o, fs, bs
 
 
 @pytest.mark.parametrize("name", ["tiny", "small", "lego_early", "lego_final"])
 def test_config_parity(gsr, ctx, name):
-    g, o, fs, bs = _full(gsr, ctx, gen.make(name))
+    g, o, fs, bs = _full(gsr, ctx, gen.make(name), cond_cap=COND_CAPS[name])
     print(name, "pairs", g["num_pairs"], "forward", fs, "backward", bs)
 
 
 def test_stress_parity(gsr, ctx):
     wl = gen.stress()
-    g, o, fs, bs = _full(gsr, ctx, wl)
+    g, o, fs, bs = _full(gsr, ctx, wl, cond_cap=COND_CAPS["stress"])
     print("stress pairs", g["num_pairs"], "forward", fs, "backward", bs)
 
 
@@ -241,13 +250,13 @@ def test_backward_variants_single_pixel_bit_equal(gsr, ctx):
         for lc in (1, 0):
             ctx.set_option("bwd_warp_skip", skip)
             ctx.set_option("bwd_last_contrib", lc)
-            results.append(run_gpu(gsr, ctx, wl)["grad"])
+            results.append(run_gpu(gsr, ctx, wl))
     ctx.set_option("bwd_warp_skip", 1)
     ctx.set_option("bwd_last_contrib", 1)
     for r in results[1:]:
-        assert np.array_equal(r.view(np.uint32), results[0].view(np.uint32))
-    assert np.any(results[0] != 0)
-    check_backward({"grad": results[0]}, run_oracle(wl))
+        assert np.array_equal(r["grad"].view(np.uint32), results[0]["grad"].view(np.uint32))
+    assert np.any(results[0]["grad"] != 0)
+    check_backward(results[0], run_oracle(wl))
 
 
 def test_backward_variants_agree(gsr, ctx):

@@ -6,7 +6,8 @@ by another allocator, or they run a loop that must not stall or fail halfway
 them with a fixed device array as its accumulator.  This test calls it through
 the C ABI, twice in a row with different splat counts, and checks each result
 against gsr_rasterize_backward within the gradient tolerance of the other GPU
-tests.  It also checks that a splat count above the array's limit is refused.
+tests, and the first (the small set) against the CPU oracle as well.  It also
+checks that a splat count above the array's limit is refused.
 
 This file is named to be collected last, and it builds everything it needs, so
 it runs the same alone in a fresh process as after the other tests.
@@ -18,7 +19,7 @@ import pytest
 import torch
 
 import gen
-from gpu_helpers import GRAD_ATOL, GRAD_RTOL, to_dev
+from gpu_helpers import GRAD_ATOL, GRAD_RTOL, as_result, check_backward, run_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +45,7 @@ def _prepare(gsr, ctx, wl):
     sp, dp, dl = to_dev(wl.splats), to_dev(wl.depths), to_dev(wl.dl_dout)
     bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
     out, final_t, last = gsr.rasterize_forward(ctx, sp, bins)
-    return sp, dl, bins, final_t, last
+    return sp, dl, bins, out, final_t, last
 
 
 def _call_noalloc(fn, ctx, sp, bins, dl, final_t, last, grad):
@@ -61,7 +62,7 @@ def test_noalloc_backward_matches_backward_on_two_calls(gsr):
         # Two calls in a row; the second is larger, so it must clear and reuse
         # more of the shared array than the first left behind.
         for wl in (gen.small(), gen.lego_early()):
-            sp, dl, bins, final_t, last = _prepare(gsr, ctx, wl)
+            sp, dl, bins, out, final_t, last = _prepare(gsr, ctx, wl)
             ref = gsr.rasterize_backward(ctx, sp, bins, dl, final_t, last).cpu().numpy()
             grad = torch.full((wl.n, 9), float("nan"), dtype=torch.float32, device="cuda:0")
             rc = _call_noalloc(fn, ctx, sp, bins, dl, final_t, last, grad)
@@ -69,6 +70,8 @@ def test_noalloc_backward_matches_backward_on_two_calls(gsr):
             got = grad.cpu().numpy()
             assert np.all(np.isfinite(got))
             assert np.all(np.abs(got - ref) <= GRAD_ATOL + GRAD_RTOL * np.abs(ref)), wl.name
+            if wl.name == "small":
+                check_backward(as_result(out, final_t, last, got), run_oracle(wl))
     finally:
         ctx.close()
 
@@ -79,7 +82,7 @@ def test_noalloc_backward_refuses_too_many_splats(gsr):
     ctx = gsr.Context(0)
     try:
         wl = gen.lego_final()   # 409,660 splats: above the fixed array's 131,072
-        sp, dl, bins, final_t, last = _prepare(gsr, ctx, wl)
+        sp, dl, bins, out, final_t, last = _prepare(gsr, ctx, wl)
         grad = torch.zeros((wl.n, 9), dtype=torch.float32, device="cuda:0")
         rc = _call_noalloc(fn, ctx, sp, bins, dl, final_t, last, grad)
         assert rc == 1
