@@ -106,7 +106,12 @@ def parse_args(argv=None):
     p.add_argument("--bwd-per-splat", action="store_true",
                    help="time the backward's transposed (per-splat) loop nest instead of the per-pixel one")
     p.add_argument("--graph", action="store_true",
-                   help="also time the step with forward and backward replayed as one captured CUDA graph")
+                   help="also time the whole step (binning, forward, backward) replayed as one captured CUDA graph")
+    p.add_argument("--no-split", action="store_true",
+                   help="run the backward as one CTA per tile (no segments of long lists)")
+    p.add_argument("--read-back", action="store_true",
+                   help="bin in the default mode, which reads the pair count back to the host every call, "
+                        "instead of with a reserved arena")
     p.add_argument("--no-projection", action="store_true",
                    help="skip the separate timing of the projection kernels")
     p.add_argument("--min-warm-s", type=float, default=1.5,
@@ -281,7 +286,10 @@ def bench_config(wl, args, pairs, world):
             "pairs": int(pairs), "l2": "flushed between timed steps (256 MB write)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "backward_accumulation": "fixed point (deterministic)" if args.deterministic else "double atomics",
-            "backward_loop_nest": "per splat (diagonal)" if args.bwd_per_splat else "per pixel"}
+            "backward_loop_nest": "per splat (diagonal)" if args.bwd_per_splat else "per pixel",
+            "long_lists": "one CTA per tile" if args.no_split else "backward segments of 2,048 positions",
+            "binning": "pair count read back every call" if args.read_back
+            else "reserved arena (1.5 x the pair count), no host read-back"}
 
 
 def reference_arm(args):
@@ -432,18 +440,24 @@ def time_projection(gsr, ctx, dev, stream, flush, steps, warmup, peaks):
 
 
 def time_graph(gsr, ctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush, steps):
-    """The step with binning as usual and forward + backward replayed from one
-    captured CUDA graph (the binning's host synchronisation keeps it outside),
-    against the same step with direct calls, alternating, between L2 flushes."""
+    """The whole step (binning with the context's reservation, forward,
+    backward) replayed from one captured CUDA graph, against the same step
+    with direct calls, alternating, between L2 flushes; medians."""
     import torch
-    bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+
+    def direct():
+        b = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+        gsr.rasterize_forward(ctx, sp, b, out, fT, last)
+        gsr.rasterize_backward(ctx, sp, b, dl, fT, last, grad)
+
+    direct()
+    torch.cuda.synchronize(dev)
     g = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
         with torch.cuda.graph(g, stream=side):
-            gsr.rasterize_forward(ctx, sp, bins, out, fT, last)
-            gsr.rasterize_backward(ctx, sp, bins, dl, fT, last, grad)
+            direct()
     stream.wait_stream(side)
     torch.cuda.synchronize(dev)
 
@@ -453,12 +467,10 @@ def time_graph(gsr, ctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush
         for i in range(steps):
             flush.fill_(float(i))
             evs[i][0].record(stream)
-            b = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
             if graph:
                 g.replay()
             else:
-                gsr.rasterize_forward(ctx, sp, b, out, fT, last)
-                gsr.rasterize_backward(ctx, sp, b, dl, fT, last, grad)
+                direct()
             evs[i][1].record(stream)
         torch.cuda.synchronize(dev)
         return float(np.median([a.elapsed_time(b) for a, b in evs]))
@@ -468,7 +480,8 @@ def time_graph(gsr, ctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush
         res["direct_ms"].append(run(False))
         res["graph_ms"].append(run(True))
     return {"direct_ms": float(np.median(res["direct_ms"])), "graph_ms": float(np.median(res["graph_ms"])),
-            "note": "binning direct (its host sync), forward + backward one graph replay; medians"}
+            "note": "binning, forward and backward as one graph replay against direct calls; medians of 3 x "
+                    f"{steps} steps"}
 
 
 def gpu_arm(args):
@@ -488,7 +501,10 @@ def gpu_arm(args):
         ctx.set_option("deterministic", True)
     if args.bwd_per_splat:
         ctx.set_option("bwd_per_splat", True)
+    if args.no_split:
+        ctx.set_option("split", False)
     stream = torch.cuda.current_stream(dev)
+    reserve = 0
 
     sp = torch.from_numpy(wl.splats).to(dev)
     dp = torch.from_numpy(wl.depths).to(dev)
@@ -499,6 +515,11 @@ def gpu_arm(args):
     last = torch.empty((npx,), dtype=torch.int32, device=dev)
     grad = torch.empty((wl.n, 9), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if not args.read_back:
+        # One binning that reads its count back sizes the reservation (setup,
+        # outside any timing); the timed steps then read nothing back.
+        reserve = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height).num_pairs * 3 // 2
+        ctx.reserve_pairs(reserve)
 
     def step(evs):
         evs[0].record(stream)
@@ -535,10 +556,11 @@ def gpu_arm(args):
     pairs = 0
     for i in range(args.steps):
         flush.fill_(float(i))      # L2 flush between timed steps (outside the events)
-        pairs = step(evs[i]).num_pairs
+        step(evs[i])
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     launches = ctx.launch_count() - launches0
+    pairs = ctx.num_pairs()          # raises if a step exceeded the reservation
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -561,10 +583,14 @@ def gpu_arm(args):
         slots = []
         for k in range(2):
             c2 = ctx if k == 0 else gsr.Context(local)
+            if reserve:
+                c2.reserve_pairs(reserve)
             if args.deterministic:
                 c2.set_option("deterministic", True)
             if args.bwd_per_splat:
                 c2.set_option("bwd_per_splat", True)
+            if args.no_split:
+                c2.set_option("split", False)
             slots.append({
                 "ctx": c2, "stream": torch.cuda.Stream(dev),
                 "sp": torch.empty_like(sp), "dp": torch.empty_like(dp), "dl": torch.empty_like(dl),
@@ -656,7 +682,7 @@ def gpu_arm(args):
                "two_threads_ms_per_iter": e2e_two_ms / args.steps}
 
     graph = None
-    if args.graph:
+    if args.graph and not args.read_back:
         graph = time_graph(gsr, ctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush, max(args.steps, 20))
     peaks = measured_peaks()
     # Binning against HBM: N·40 B of splats and depths read, each pair's 12-byte

@@ -16,8 +16,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("GSR_LIBRARY") or os.path.join(_PKG, "lib", "libgsr.so")
 
 GSR_OK, GSR_ERR_INVALID_ARG, GSR_ERR_CUDA, GSR_ERR_OOM, GSR_ERR_TOO_MANY_PAIRS = range(5)
+GSR_PAIRS_ON_DEVICE = 0xFFFFFFFF
 OPTIONS = {"bwd_warp_skip": 1, "bwd_last_contrib": 2, "warp_cull": 3, "pdl": 4, "fail_next_alloc": 5,
-           "deterministic": 6, "bwd_per_splat": 7}
+           "deterministic": 6, "bwd_per_splat": 7, "split": 8}
 
 
 class GsrError(RuntimeError):
@@ -29,7 +30,7 @@ class GsrError(RuntimeError):
 class _Bins(ctypes.Structure):
     _fields_ = [("keys", ctypes.c_void_p), ("sorted_idx", ctypes.c_void_p),
                 ("tile_ranges", ctypes.c_void_p), ("tile_order", ctypes.c_void_p),
-                ("num_pairs", ctypes.c_uint32),
+                ("num_pairs_dev", ctypes.c_void_p), ("num_pairs", ctypes.c_uint32),
                 ("n", ctypes.c_int32), ("width", ctypes.c_int32), ("height", ctypes.c_int32),
                 ("tiles_x", ctypes.c_int32), ("tiles_y", ctypes.c_int32)]
 
@@ -71,6 +72,10 @@ def _load():
     lib.gsr_rasterize_forward.restype = ctypes.c_int
     lib.gsr_rasterize_backward.argtypes = [P, P, i32, ctypes.POINTER(_Bins), P, P, P, P, P]
     lib.gsr_rasterize_backward.restype = ctypes.c_int
+    lib.gsr_reserve_pairs.argtypes = [P, ctypes.c_uint64]
+    lib.gsr_reserve_pairs.restype = ctypes.c_int
+    lib.gsr_num_pairs.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.gsr_num_pairs.restype = ctypes.c_int
     lib.gsr_get_bin_stats.argtypes = [P, ctypes.POINTER(_BinStats)]
     lib.gsr_get_bin_stats.restype = ctypes.c_int
     lib.gsr_project_forward.argtypes = [P, P, i32, ctypes.POINTER(_Camera), P, P, P]
@@ -119,6 +124,18 @@ class Context:
     def launch_count(self) -> int:
         return int(lib.gsr_launch_count(self._h))
 
+    def reserve_pairs(self, max_pairs: int):
+        """Sizes the arena for max_pairs tile pairs; later bin_splats calls
+        read nothing back to the host (0: back to reading the count)."""
+        self._check(lib.gsr_reserve_pairs(self._h, int(max_pairs)))
+
+    def num_pairs(self) -> int:
+        """The last binning's pair count (waits for it); GsrError with code
+        GSR_ERR_TOO_MANY_PAIRS when it exceeded the reservation."""
+        out = ctypes.c_uint32()
+        self._check(lib.gsr_num_pairs(self._h, ctypes.byref(out)))
+        return int(out.value)
+
     def bin_stats(self) -> dict:
         st = _BinStats()
         self._check(lib.gsr_get_bin_stats(self._h, ctypes.byref(st)))
@@ -152,6 +169,11 @@ class Bins:
 
     @property
     def num_pairs(self) -> int:
+        """The pair count; for bins whose count stayed on the device this waits
+        for the binning and reads it."""
+        if int(self.raw.num_pairs) == GSR_PAIRS_ON_DEVICE:
+            self._check_current()
+            return self.ctx.num_pairs()
         return int(self.raw.num_pairs)
 
     @property

@@ -63,7 +63,7 @@ int check_bins(gsr_ctx *ctx, const gsr_bins *bins, int32_t n)
     if (bins->tiles_x != (bins->width + GSR_TILE - 1) / GSR_TILE ||
         bins->tiles_y != (bins->height + GSR_TILE - 1) / GSR_TILE)
         return fail(ctx, GSR_ERR_INVALID_ARG, "bins carry an inconsistent tile grid");
-    if (!bins->tile_ranges || (bins->num_pairs > 0 && !bins->sorted_idx))
+    if (!bins->tile_ranges || (n > 0 && bins->num_pairs > 0 && !bins->sorted_idx))
         return fail(ctx, GSR_ERR_INVALID_ARG, "bins hold NULL arrays");
     return GSR_OK;
 }
@@ -121,6 +121,8 @@ void gsr_destroy(gsr_ctx *ctx)
         cudaFree(ctx->grad_acc);
         cudaFree(ctx->bwd_tile_cost);
         cudaFree(ctx->det_escale);
+        cudaFree(ctx->bnd);
+        cudaFree(ctx->bwd_items);
         if (ctx->host_total) cudaFreeHost(ctx->host_total);
     }
     delete ctx;
@@ -140,6 +142,7 @@ int gsr_set_option(gsr_ctx *ctx, int option, int value)
     case GSR_OPT_FAIL_NEXT_ALLOC: ctx->fail_next_alloc = value; return GSR_OK;
     case GSR_OPT_DETERMINISTIC: ctx->opt_deterministic = value; return GSR_OK;
     case GSR_OPT_BWD_PER_SPLAT: ctx->opt_bwd_per_splat = value; return GSR_OK;
+    case GSR_OPT_SPLIT: ctx->opt_split = value; return GSR_OK;
     default: return fail(ctx, GSR_ERR_INVALID_ARG, "unknown option " + std::to_string(option));
     }
 }
@@ -175,7 +178,7 @@ int gsr_rasterize_forward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n, co
     if (rc) return rc;
     if (!out_rgbw || !final_T || !last_contrib)
         return fail(ctx, GSR_ERR_INVALID_ARG, "an output pointer is NULL");
-    if (bins->num_pairs > 0 && !splats) return fail(ctx, GSR_ERR_INVALID_ARG, "splats is NULL");
+    if (n > 0 && bins->num_pairs > 0 && !splats) return fail(ctx, GSR_ERR_INVALID_ARG, "splats is NULL");
     if (!aligned(out_rgbw, 16) || !aligned(final_T, 4) || !aligned(last_contrib, 4) ||
         !aligned(splats, 4))
         return fail(ctx, GSR_ERR_INVALID_ARG, "misaligned buffer (out_rgbw needs 16 bytes)");
@@ -196,7 +199,7 @@ int gsr_rasterize_backward(gsr_ctx *ctx, const gsr_splat2d *splats, int32_t n, c
     if (rc) return rc;
     if (!dl_dout || !final_T || !last_contrib || (n > 0 && !grad))
         return fail(ctx, GSR_ERR_INVALID_ARG, "an input/output pointer is NULL");
-    if (bins->num_pairs > 0 && !splats) return fail(ctx, GSR_ERR_INVALID_ARG, "splats is NULL");
+    if (n > 0 && bins->num_pairs > 0 && !splats) return fail(ctx, GSR_ERR_INVALID_ARG, "splats is NULL");
     if (!aligned(dl_dout, 16) || !aligned(final_T, 4) || !aligned(last_contrib, 4) ||
         !aligned(grad, 4) || !aligned(splats, 4))
         return fail(ctx, GSR_ERR_INVALID_ARG, "misaligned buffer (dl_dout needs 16 bytes)");
@@ -222,7 +225,7 @@ int gsr_rasterize_backward_noalloc(gsr_ctx *ctx, const gsr_splat2d *splats, int3
     if (rc) return rc;
     if (!dl_dout || !final_T || !last_contrib || (n > 0 && !grad))
         return fail(ctx, GSR_ERR_INVALID_ARG, "an input/output pointer is NULL");
-    if (bins->num_pairs > 0 && !splats) return fail(ctx, GSR_ERR_INVALID_ARG, "splats is NULL");
+    if (n > 0 && bins->num_pairs > 0 && !splats) return fail(ctx, GSR_ERR_INVALID_ARG, "splats is NULL");
     if (!aligned(dl_dout, 16) || !aligned(final_T, 4) || !aligned(last_contrib, 4) ||
         !aligned(grad, 4) || !aligned(splats, 4))
         return fail(ctx, GSR_ERR_INVALID_ARG, "misaligned buffer (dl_dout needs 16 bytes)");
@@ -240,19 +243,42 @@ int gsr_get_bin_stats(gsr_ctx *ctx, gsr_bin_stats *out)
     ctx->err.clear();
     DeviceGuard g(ctx->device);
     *out = gsr_bin_stats{};
-    out->num_pairs = ctx->last_pairs;
-    out->emitting = ctx->last_emitting;
     out->capacity = ctx->cap_pairs;
-    if (ctx->last_stream || ctx->scalars) {
-        int rc = cuda_check(ctx, cudaStreamSynchronize(ctx->last_stream), "cudaStreamSynchronize");
-        if (rc) return rc;
-    }
+    uint32_t status = GSR_OK;
+    int rc = gsr::bin_result(ctx, &out->num_pairs, &status, &out->emitting);
+    if (rc) return rc;
     int tile_bits = 0, tile_digits = 0;
-    int rc = gsr::bin_pass_masks(ctx, &out->depth_pass_mask, &out->tile_pass_mask, &tile_bits, &tile_digits);
+    rc = gsr::bin_pass_masks(ctx, &out->depth_pass_mask, &out->tile_pass_mask, &tile_bits, &tile_digits);
     if (rc) return rc;
     out->tile_digit_bits = tile_bits;
     out->tile_digits = tile_digits;
     out->radix_passes = __builtin_popcount(out->depth_pass_mask) + __builtin_popcount(out->tile_pass_mask);
+    return GSR_OK;
+}
+
+int gsr_reserve_pairs(gsr_ctx *ctx, uint64_t max_pairs)
+{
+    if (!ctx) return GSR_ERR_INVALID_ARG;
+    ctx->err.clear();
+    if (max_pairs > (uint64_t)GSR_MAX_PAIRS)
+        return fail(ctx, GSR_ERR_INVALID_ARG, "max_pairs exceeds GSR_MAX_PAIRS");
+    ctx->reserved_pairs = max_pairs;
+    return GSR_OK;
+}
+
+int gsr_num_pairs(gsr_ctx *ctx, uint32_t *out)
+{
+    if (!ctx || !out) return GSR_ERR_INVALID_ARG;
+    ctx->err.clear();
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return fail(ctx, GSR_ERR_CUDA, "cannot select the context's device");
+    uint32_t status = GSR_OK;
+    int rc = gsr::bin_result(ctx, out, &status, nullptr);
+    if (rc) return rc;
+    if (status != GSR_OK)
+        return fail(ctx, GSR_ERR_TOO_MANY_PAIRS,
+                    "the last binning needed " + std::to_string(*out) + " tile pairs, more than the arena's " +
+                        std::to_string(ctx->cap_pairs) + ": its bins are empty");
     return GSR_OK;
 }
 

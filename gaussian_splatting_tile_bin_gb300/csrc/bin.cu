@@ -43,7 +43,10 @@ enum {
     kScalarKeyOr = 5,
     kScalarTicketCount = 6,  // blocks of k_count / k_sorted_sums done (the last one scans)
     kScalarTicketSums = 7,
-    kScalarCount = 8
+    kScalarNum = 8,        // pairs the sort and the ranges take: the total, or 0 when it exceeds the capacity
+    kScalarResult = 9,     // two uint32: the pair count (saturated) and the status (GSR_OK or
+                           // GSR_ERR_TOO_MANY_PAIRS); gsr_bins.num_pairs_dev points here
+    kScalarCount = 10
 };
 
 // The 3-sigma box of a splat (its 9 fields v and its depth) as an inclusive
@@ -260,7 +263,8 @@ __device__ unsigned long long block_scan_inplace_256(unsigned long long *__restr
 __global__ void __launch_bounds__(kBinBlock)
 k_count(const float *__restrict__ splats, const float *__restrict__ depths, int n, int tiles_x,
         int tiles_y, uint2 *__restrict__ rects, unsigned long long *__restrict__ blk_pairs,
-        unsigned long long *__restrict__ blk_emitting, unsigned long long *__restrict__ scalars)
+        unsigned long long *__restrict__ blk_emitting, unsigned long long *__restrict__ scalars,
+        unsigned long long capacity)
 {
     grid_dependency_begin();
     __shared__ float s_rec[kBinBlock * 9];
@@ -308,8 +312,15 @@ k_count(const float *__restrict__ splats, const float *__restrict__ depths, int 
         __syncthreads();
         const unsigned long long m = block_scan_inplace_256(blk_emitting, (int)gridDim.x, ws);
         if (threadIdx.x == 0) {
+            // More pairs than the arena holds (or than 32-bit indices reach):
+            // nothing is emitted, sorted or ranged, and every tile stays empty.
+            const bool fits = t <= capacity && t <= (unsigned long long)GSR_MAX_PAIRS;
             scalars[kScalarPairs] = t;
-            scalars[kScalarEmitting] = m;
+            scalars[kScalarEmitting] = fits ? m : 0ull;
+            scalars[kScalarNum] = fits ? t : 0ull;
+            uint32_t *res = reinterpret_cast<uint32_t *>(scalars + kScalarResult);
+            res[0] = t < 0xffffffffull ? (uint32_t)t : 0xffffffffu;
+            res[1] = fits ? (uint32_t)GSR_OK : (uint32_t)GSR_ERR_TOO_MANY_PAIRS;
         }
     }
 }
@@ -333,13 +344,27 @@ k_compact(const uint2 *__restrict__ rects, const float *__restrict__ depths, int
     }
 }
 
+// The depth-sorted splat indices: buffer 1, or buffer 0 when a device-planned
+// sort (depth_and_or set) found no varying digit and ran no pass.
+__device__ __forceinline__ const uint32_t *depth_sorted(const DepthBuffers &b, const unsigned long long *depth_and_or)
+{
+    if (!depth_and_or) return b.v[1];
+    int executed;
+    field_pass(__ldcg(depth_and_or) ^ __ldcg(depth_and_or + 1), 0, 32, -1, &executed);
+    return executed ? b.v[1] : b.v[0];
+}
+
 // Per block of 256 depth-sorted splats: their pair total.
 __global__ void __launch_bounds__(kBinBlock)
-k_sorted_sums(const uint32_t *__restrict__ sorted_idx, const uint2 *__restrict__ rects, int m,
-              unsigned long long *__restrict__ blk_sorted, unsigned long long *__restrict__ scalars)
+k_sorted_sums(DepthBuffers dbufs, const uint2 *__restrict__ rects, int n, int m_host,
+              unsigned long long *__restrict__ blk_sorted, unsigned long long *__restrict__ scalars,
+              const unsigned long long *__restrict__ depth_and_or)
 {
     grid_dependency_begin();
     __shared__ unsigned long long ws[8];
+    // the emitting count: m_host when the host knows it, else the device's
+    const int m = m_host >= 0 ? m_host : (int)min(__ldcg(scalars + kScalarEmitting), (unsigned long long)n);
+    const uint32_t *__restrict__ sorted_idx = depth_sorted(dbufs, depth_and_or);
     const int k = blockIdx.x * kBinBlock + threadIdx.x;
     const uint32_t c = k < m ? rect_count(rects[sorted_idx[k]]) : 0u;
     unsigned long long total;
@@ -363,11 +388,18 @@ constexpr int kEmitIndexPairs = 16384;
 // marks the starts; every splat here has at least one pair).  Also folds the
 // AND / OR of the keys for the tile sort's plan.
 __global__ void __launch_bounds__(kBinBlock)
-k_emit(const uint2 *__restrict__ rects, const float *__restrict__ depths, const uint32_t *__restrict__ sorted_idx,
-       int m, int tiles_x, const unsigned long long *__restrict__ blk_offs, uint64_t *__restrict__ keys,
-       uint32_t *__restrict__ vals, unsigned long long *__restrict__ scalars)
+k_emit(const uint2 *__restrict__ rects, const float *__restrict__ depths, DepthBuffers dbufs, int n, int m_host,
+       int tiles_x, const unsigned long long *__restrict__ blk_offs, uint64_t *__restrict__ keys,
+       uint32_t *__restrict__ vals, unsigned long long *__restrict__ scalars,
+       const unsigned long long *__restrict__ depth_and_or)
 {
     grid_dependency_begin();
+    const int m = m_host >= 0 ? m_host : (int)min(__ldcg(scalars + kScalarEmitting), (unsigned long long)n);
+    const uint32_t *__restrict__ sorted_idx = depth_sorted(dbufs, depth_and_or);
+    if ((int)(blockIdx.x * kBinBlock) >= m) {
+        // no splat of this block emits; its part of the keys' AND / OR is empty
+        return;
+    }
     __shared__ uint32_t s_off[kBinBlock];
     __shared__ uint32_t s_x0y0[kBinBlock];
     __shared__ uint32_t s_w[kBinBlock];
@@ -517,7 +549,15 @@ struct PassSpec {
     const unsigned long long *and_or;
     int key_lo, key_hi, field;
     PassGeom host;
+    const unsigned long long *num;  // device: the number of keys (min'd with num_max); null: num_max
+    uint32_t num_max;                // the number of keys, or their bound (the buffers' capacity)
+    int stride;                      // radix tiles per digit row of counts / offsets
 };
+
+__device__ __forceinline__ uint32_t pass_num(const PassSpec &p)
+{
+    return p.num ? (uint32_t)min(__ldcg(p.num), (unsigned long long)p.num_max) : p.num_max;
+}
 
 // Geometry of pass `field` of `executed` varying digits, whose position among
 // them is j.
@@ -546,46 +586,57 @@ __device__ __forceinline__ bool pass_geom(const PassSpec &p, PassGeom &g)
 
 template <typename K, int kRtItems>
 __global__ void __launch_bounds__(kRtThreads)
-k_radix_upsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, uint32_t *__restrict__ counts,
-                uint32_t *__restrict__ totals)
+k_radix_upsweep(SortBuffers<K> bufs, PassSpec ps, uint32_t *__restrict__ counts, uint32_t *__restrict__ totals)
 {
     grid_dependency_begin();
     PassGeom g;
     if (!pass_geom(ps, g)) return;
+    const uint32_t num = pass_num(ps);
+    constexpr uint32_t kRtTile = kRtThreads * kRtItems;
+    const uint32_t ntiles = (num + kRtTile - 1) / kRtTile;
     const K *__restrict__ keys = keys_of(bufs, g.src);
     const uint32_t dmask = (1u << g.width) - 1u;
     __shared__ uint32_t h[256];
-    h[threadIdx.x] = 0;
-    // All of the thread's keys are loaded before the first shared-memory
-    // atomic, so their latencies overlap.
-    const uint32_t base = blockIdx.x * (kRtThreads * kRtItems);
-    K kk[kRtItems];
+    uint32_t total = 0;   // this block's count of digit threadIdx.x over its tiles
+    // The grid strides over the radix tiles (one tile per block when the grid
+    // covers them all).
+    for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        h[threadIdx.x] = 0;
+        // All of the thread's keys are loaded before the first shared-memory
+        // atomic, so their latencies overlap.
+        const uint32_t base = tile * kRtTile;
+        K kk[kRtItems];
 #pragma unroll
-    for (int k = 0; k < kRtItems; ++k) {
-        const uint32_t i = base + k * kRtThreads + threadIdx.x;
-        kk[k] = i < num ? keys[i] : (K)0;
-    }
-    __syncthreads();
+        for (int k = 0; k < kRtItems; ++k) {
+            const uint32_t i = base + k * kRtThreads + threadIdx.x;
+            kk[k] = i < num ? keys[i] : (K)0;
+        }
+        __syncthreads();
 #pragma unroll
-    for (int k = 0; k < kRtItems; ++k) {
-        const uint32_t i = base + k * kRtThreads + threadIdx.x;
-        if (i < num) atomicAdd(&h[(uint32_t)(kk[k] >> g.shift) & dmask], 1u);
+        for (int k = 0; k < kRtItems; ++k) {
+            const uint32_t i = base + k * kRtThreads + threadIdx.x;
+            if (i < num) atomicAdd(&h[(uint32_t)(kk[k] >> g.shift) & dmask], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x <= (int)dmask) {
+            const uint32_t c = h[threadIdx.x];
+            counts[(size_t)threadIdx.x * ps.stride + tile] = c;
+            total += c;
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    if (threadIdx.x <= (int)dmask) {
-        const uint32_t c = h[threadIdx.x];
-        counts[(size_t)threadIdx.x * ntiles + blockIdx.x] = c;
-        if (c) atomicAdd(&totals[threadIdx.x], c);
-    }
+    if (threadIdx.x <= (int)dmask && total) atomicAdd(&totals[threadIdx.x], total);
 }
 
 __global__ void __launch_bounds__(kRtThreads)
-k_radix_scan(PassSpec ps, int ntiles, const uint32_t *__restrict__ counts, const uint32_t *__restrict__ totals,
+k_radix_scan(PassSpec ps, int rt_tile, const uint32_t *__restrict__ counts, const uint32_t *__restrict__ totals,
              uint32_t *__restrict__ offsets)
 {
     grid_dependency_begin();
     PassGeom g;
     if (!pass_geom(ps, g)) return;
+    // the radix tiles that hold keys; rows are ps.stride long
+    const int ntiles = (int)((pass_num(ps) + (uint32_t)rt_tile - 1) / (uint32_t)rt_tile);
     const uint32_t digit = blockIdx.x;
     if (digit >= (1u << g.width)) return;
     __shared__ uint32_t ws[8];
@@ -594,8 +645,8 @@ k_radix_scan(PassSpec ps, int ntiles, const uint32_t *__restrict__ counts, const
     // Global start of this digit: the totals of all smaller digits.
     uint32_t base;
     block_exclusive_scan_256<uint32_t>(threadIdx.x < digit ? totals[threadIdx.x] : 0u, ws, &base);
-    const uint32_t *row = counts + (size_t)digit * ntiles;
-    uint32_t *orow = offsets + (size_t)digit * ntiles;
+    const uint32_t *row = counts + (size_t)digit * ps.stride;
+    uint32_t *orow = offsets + (size_t)digit * ps.stride;
     // Warp w scans the segment [seg0, seg1) of the row: first its sum (all loads
     // independent), then, after the warps' sums are exchanged, the segment in
     // runs of 32 with a carried prefix.
@@ -625,11 +676,12 @@ k_radix_scan(PassSpec ps, int ntiles, const uint32_t *__restrict__ counts, const
 
 template <typename K, int kRtItems, int kWidth>
 __global__ void __launch_bounds__(kRtThreads, GSR_RT_MIN_BLOCKS)
-k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, const uint32_t *__restrict__ offsets)
+k_radix_downsweep(SortBuffers<K> bufs, PassSpec ps, const uint32_t *__restrict__ offsets)
 {
     grid_dependency_begin();
     PassGeom g;
     if (!pass_geom(ps, g)) return;
+    const uint32_t num = pass_num(ps);
     const K *__restrict__ kin = keys_of(bufs, g.src);
     const uint32_t *__restrict__ vin = vals_of(bufs, g.src);
     K *__restrict__ kout = keys_of(bufs, g.dst);
@@ -646,7 +698,11 @@ k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, co
     __shared__ uint32_t s_vals[kRtTile];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t tbase = blockIdx.x * kRtTile;
+    const uint32_t ntiles = (num + kRtTile - 1) / kRtTile;
+    // The grid strides over the radix tiles (one tile per block when the grid
+    // covers them all).
+    for (uint32_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const uint32_t tbase = tile * kRtTile;
     const uint32_t tcount = min((uint32_t)kRtTile, num - tbase);
 
     // Warp w owns keys [w*256, w*256+256) of the tile.  They are all loaded
@@ -665,7 +721,7 @@ k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, co
     if (tid < (int)radix) {
 #pragma unroll
         for (int w = 0; w < 8; ++w) wcnt[w][tid] = 0;
-        s_goff[tid] = offsets[(size_t)tid * ntiles + blockIdx.x];
+        s_goff[tid] = offsets[(size_t)tid * ps.stride + tile];
     }
     GSR_CANARY(11);
     __syncthreads();
@@ -718,6 +774,8 @@ k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, co
         kout[gpos] = kk;
         vout[gpos] = s_vals[i];
     }
+    __syncthreads();   // the staged tile is read before the next one is staged
+    }
 }
 
 // --- ranges --------------------------------------------------------------------
@@ -726,46 +784,50 @@ k_radix_downsweep(SortBuffers<K> bufs, uint32_t num, PassSpec ps, int ntiles, co
 // thread compares four consecutive keys (two 16-byte loads) and their
 // neighbours.
 __global__ void __launch_bounds__(256)
-k_extract_ranges(PairBuffers bufs, uint32_t num, uint32_t *__restrict__ ranges,
-                 const unsigned long long *__restrict__ and_or, int key_lo, int key_hi)
+k_extract_ranges(PairBuffers bufs, const unsigned long long *__restrict__ num_dev, uint32_t num_max,
+                 uint32_t *__restrict__ ranges, const unsigned long long *__restrict__ and_or, int key_lo, int key_hi)
 {
     grid_dependency_begin();
-    const uint32_t i0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4u;
-    if (i0 >= num) return;
+    const uint32_t num = num_dev ? (uint32_t)min(__ldcg(num_dev), (unsigned long long)num_max) : num_max;
     // A tile sort that ran no pass (every key shares its tile bits) left the
     // emitted order, already sorted, in buffer 0: copy it to the result.
     const uint64_t *__restrict__ keys = bufs.k[1];
+    bool copy = false;
     if (and_or) {
         int executed;
         field_pass(and_or[0] ^ and_or[1], key_lo, key_hi, -1, &executed);
-        if (executed == 0) {
-            keys = bufs.k[0];
+        copy = executed == 0;
+        if (copy) keys = bufs.k[0];
+    }
+    const uint32_t step = gridDim.x * blockDim.x * 4u;
+    for (uint32_t i0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4u; i0 < num; i0 += step) {
+        if (copy)
             for (uint32_t i = i0; i < min(i0 + 4u, num); ++i) {
                 bufs.k[1][i] = bufs.k[0][i];
                 bufs.v[1][i] = bufs.v[0][i];
             }
+        uint32_t t[6];  // tiles of keys i0 - 1 .. i0 + 4 (0xffffffff outside [0, num))
+        t[0] = i0 > 0 ? (uint32_t)(__ldg(keys + i0 - 1) >> 32) : 0xffffffffu;
+        if (i0 + 4 <= num) {
+            const ulonglong2 a = __ldg(reinterpret_cast<const ulonglong2 *>(keys + i0));
+            const ulonglong2 b = __ldg(reinterpret_cast<const ulonglong2 *>(keys + i0 + 2));
+            t[1] = (uint32_t)(a.x >> 32);
+            t[2] = (uint32_t)(a.y >> 32);
+            t[3] = (uint32_t)(b.x >> 32);
+            t[4] = (uint32_t)(b.y >> 32);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                t[1 + k] = i0 + k < num ? (uint32_t)(__ldg(keys + i0 + k) >> 32) : 0xffffffffu;
         }
-    }
-    uint32_t t[6];  // tiles of keys i0 - 1 .. i0 + 4 (0xffffffff outside [0, num))
-    t[0] = i0 > 0 ? (uint32_t)(__ldg(keys + i0 - 1) >> 32) : 0xffffffffu;
-    if (i0 + 4 <= num) {
-        const ulonglong2 a = __ldg(reinterpret_cast<const ulonglong2 *>(keys + i0));
-        const ulonglong2 b = __ldg(reinterpret_cast<const ulonglong2 *>(keys + i0 + 2));
-        t[1] = (uint32_t)(a.x >> 32);
-        t[2] = (uint32_t)(a.y >> 32);
-        t[3] = (uint32_t)(b.x >> 32);
-        t[4] = (uint32_t)(b.y >> 32);
-    } else {
+        t[5] = i0 + 4 < num ? (uint32_t)(__ldg(keys + i0 + 4) >> 32) : 0xffffffffu;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) t[1 + k] = i0 + k < num ? (uint32_t)(__ldg(keys + i0 + k) >> 32) : 0xffffffffu;
-    }
-    t[5] = i0 + 4 < num ? (uint32_t)(__ldg(keys + i0 + 4) >> 32) : 0xffffffffu;
-#pragma unroll
-    for (int k = 1; k <= 4; ++k) {
-        const uint32_t i = i0 + k - 1;
-        if (i >= num) break;
-        if (t[k - 1] != t[k]) ranges[2 * (size_t)t[k]] = i;
-        if (t[k + 1] != t[k]) ranges[2 * (size_t)t[k] + 1] = i + 1;
+        for (int k = 1; k <= 4; ++k) {
+            const uint32_t i = i0 + k - 1;
+            if (i >= num) break;
+            if (t[k - 1] != t[k]) ranges[2 * (size_t)t[k]] = i;
+            if (t[k + 1] != t[k]) ranges[2 * (size_t)t[k] + 1] = i + 1;
+        }
     }
 }
 
@@ -889,12 +951,11 @@ int grow_sort_buffers(gsr_ctx *ctx, SortBuffers<K> &b, size_t *cap, size_t need,
 
 // The downsweep compiled for digit width `width` (1..8 bits).
 template <typename K, int kRtItems>
-int launch_downsweep(gsr_ctx *ctx, int width, int ntiles, cudaStream_t stream, SortBuffers<K> bufs, uint32_t num,
-                     PassSpec ps, const uint32_t *offsets)
+int launch_downsweep(gsr_ctx *ctx, int width, int ntiles, cudaStream_t stream, SortBuffers<K> bufs, PassSpec ps,
+                     const uint32_t *offsets)
 {
     auto go = [&](auto kernel) {
-        return cuda_check(ctx, launch_kernel(ctx, kernel, dim3(ntiles), dim3(kRtThreads), stream, bufs, num, ps,
-                                             ntiles, offsets),
+        return cuda_check(ctx, launch_kernel(ctx, kernel, dim3(ntiles), dim3(kRtThreads), stream, bufs, ps, offsets),
                           "kernel launch");
     };
     switch (width) {
@@ -910,17 +971,21 @@ int launch_downsweep(gsr_ctx *ctx, int width, int ntiles, cudaStream_t stream, S
 }
 
 // Stable LSD sort of bufs buffer 0 into buffer 1 over the key bits
-// [key_lo, key_hi).  and_or: the device AND / OR of the keys.  host_and_or:
-// the same two values already on the host, or null; with them only the passes
-// over varying digits are launched.
+// [key_lo, key_hi).  num_dev: the number of keys on the device, num_max its
+// bound (the buffers' capacity): the grids then hold as many blocks as the
+// SMs keep resident and stride over the radix tiles; null: num_max is the
+// count, and every radix tile gets its block.  and_or: the device
+// AND / OR of the keys.  host_and_or: the same two values already on the host,
+// or null; with them only the passes over varying digits are launched.
 template <typename K, int kRtItems>
-int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int key_hi,
-               const unsigned long long *and_or, const unsigned long long *host_and_or, uint32_t *totals,
-               cudaStream_t stream)
+int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, const unsigned long long *num_dev, uint32_t num_max, int key_lo,
+               int key_hi, const unsigned long long *and_or, const unsigned long long *host_and_or,
+               uint32_t *totals, cudaStream_t stream)
 {
     int rc;
     constexpr int kRtTile = kRtThreads * kRtItems;
-    const int ntiles = (int)((num + kRtTile - 1) / kRtTile);
+    const int ntiles = (int)((num_max + kRtTile - 1) / kRtTile);
+    if (ntiles == 0) return GSR_OK;
     // [256][ntiles] counts, then [256][ntiles] offsets (sized by bin_splats).
     uint32_t *counts = ctx->radix_counts;
     uint32_t *offsets = ctx->radix_counts + (size_t)256 * ntiles;
@@ -929,17 +994,19 @@ int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int 
     if (host_and_or) {
         field_pass(host_and_or[0] ^ host_and_or[1], key_lo, key_hi, -1, &executed);
         if (executed == 0) {
-            // No digit varies: the input order is the sorted order.
-            if ((rc = cuda_check(ctx, cudaMemcpyAsync(bufs.k[1], bufs.k[0], (size_t)num * sizeof(K),
+            // No digit varies: the input order is the sorted order (num_max
+            // keys exactly when the host planned the sort).
+            if ((rc = cuda_check(ctx, cudaMemcpyAsync(bufs.k[1], bufs.k[0], (size_t)num_max * sizeof(K),
                                                       cudaMemcpyDeviceToDevice, stream), "cudaMemcpyAsync")) ||
-                (rc = cuda_check(ctx, cudaMemcpyAsync(bufs.v[1], bufs.v[0], (size_t)num * sizeof(uint32_t),
+                (rc = cuda_check(ctx, cudaMemcpyAsync(bufs.v[1], bufs.v[0], (size_t)num_max * sizeof(uint32_t),
                                                       cudaMemcpyDeviceToDevice, stream), "cudaMemcpyAsync")))
                 return rc;
             return GSR_OK;
         }
     }
+    const int grid = num_dev ? std::min(ntiles, ctx->num_sms * GSR_RT_MIN_BLOCKS) : ntiles;
     for (int f = 0; f < nf; ++f) {
-        PassSpec ps = {and_or, key_lo, key_hi, f, {}};
+        PassSpec ps = {and_or, key_lo, key_hi, f, {}, num_dev, num_max, ntiles};
         if (host_and_or) {
             const int j = field_pass(host_and_or[0] ^ host_and_or[1], key_lo, key_hi, f, &executed);
             if (j < 0) continue;
@@ -949,10 +1016,9 @@ int radix_sort(gsr_ctx *ctx, SortBuffers<K> bufs, uint32_t num, int key_lo, int 
         int sh, w;
         field_geom(key_lo, key_hi, nf, f, sh, w);
         uint32_t *tot = totals + 256 * f;
-        GSR_LAUNCH(ctx, k_radix_upsweep<K, kRtItems>, dim3(ntiles), dim3(kRtThreads), stream, bufs, num, ps, ntiles, counts,
-                   tot);
-        GSR_LAUNCH(ctx, k_radix_scan, dim3(1 << w), dim3(kRtThreads), stream, ps, ntiles, counts, tot, offsets);
-        if ((rc = launch_downsweep<K, kRtItems>(ctx, w, ntiles, stream, bufs, num, ps, offsets))) return rc;
+        GSR_LAUNCH(ctx, k_radix_upsweep<K, kRtItems>, dim3(grid), dim3(kRtThreads), stream, bufs, ps, counts, tot);
+        GSR_LAUNCH(ctx, k_radix_scan, dim3(1 << w), dim3(kRtThreads), stream, ps, kRtTile, counts, tot, offsets);
+        if ((rc = launch_downsweep<K, kRtItems>(ctx, w, grid, stream, bufs, ps, offsets))) return rc;
     }
     // A device-planned sort that runs no pass leaves the sorted order in buffer
     // 0; the caller completes it (the range extraction copies it to buffer 1).
@@ -969,6 +1035,10 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     const int tiles_y = (height + kTile - 1) / kTile;
     const size_t num_tiles = (size_t)tiles_x * tiles_y;
     const int key_hi = 32 + bits_for(num_tiles - 1);  // keys occupy bits [0, key_hi)
+    // With a reservation (gsr_reserve_pairs) the call reads nothing back: the
+    // arena holds the reserved pairs, the count is checked on the device, and
+    // every kernel takes its key counts from the device.
+    const bool sync_free = ctx->reserved_pairs > 0;
 
     // Fixed-size scratch, allocated once (each piece again if an earlier
     // allocation of it failed).
@@ -1006,48 +1076,59 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     if ((rc = grow(ctx, &ctx->ranges, &ctx->cap_tiles, num_tiles, 3, "tile ranges"))) return rc;
     ctx->tile_order = ctx->ranges + 2 * ctx->cap_tiles;
 
-    // 1. counts, totals; read the pair total and the emitting count.
+    // The pair buffers: max(65536, 16 n, 1.5 x pairs) ("C0 resident arena": grow,
+    // never shrink).  Without a reservation the count is read first.
+    auto grow_pairs = [&](uint64_t need, bool headroom) -> int {
+        if (need <= ctx->cap_pairs && ctx->pairs.k[0]) return GSR_OK;
+        size_t cap = std::max<size_t>(65536, (size_t)16 * (size_t)n);
+        cap = std::max<size_t>(cap, (size_t)need + (headroom ? need / 2 : 0));
+        cap = std::min<size_t>(cap, (size_t)GSR_MAX_PAIRS);
+        cap = std::max<size_t>(cap, (size_t)need);
+        size_t have = 0;
+        if (int r = grow_sort_buffers(ctx, ctx->pairs, &have, cap, "tile pairs")) {
+            ctx->cap_pairs = 0;
+            return r;
+        }
+        ctx->cap_pairs = cap;
+        return GSR_OK;
+    };
+    if (sync_free && (rc = grow_pairs(ctx->reserved_pairs, false))) return rc;
+
+    // 1. counts, totals; without a reservation, read the pair total, the
+    //    emitting count and the depth bits' AND / OR (the one host sync).
     uint64_t total = 0, emitting = 0;
     GSR_LAUNCH(ctx, k_init_scalars, dim3(1), dim3(256), stream, ctx->scalars, ctx->radix_totals, 2 * 4 * 256);
     if (n > 0) {
         GSR_LAUNCH(ctx, k_count, dim3(nblk), dim3(kBinBlock), stream, splats, depths, n, tiles_x, tiles_y,
-                   ctx->rects, blk_pairs, blk_emit, ctx->scalars);
-        // Pair total, emitting count and the AND / OR of the emitting splats'
-        // depth bits (scalar slots 0..3).
-        if ((rc = cuda_check(ctx, cudaMemcpyAsync(ctx->host_total, ctx->scalars,
-                                                  4 * sizeof(unsigned long long),
-                                                  cudaMemcpyDeviceToHost, stream),
-                             "cudaMemcpyAsync")))
-            return rc;
-        if ((rc = cuda_check(ctx, cudaStreamSynchronize(stream), "cudaStreamSynchronize"))) return rc;
-        total = ctx->host_total[0];
-        emitting = ctx->host_total[1];
-    }
-    if (total > (uint64_t)GSR_MAX_PAIRS)
-        return fail(ctx, GSR_ERR_TOO_MANY_PAIRS,
-                    "tile-pair count " + std::to_string(total) + " exceeds GSR_MAX_PAIRS");
-    const uint32_t num = (uint32_t)total;
-    const int m = (int)emitting;
-
-    // 2. grow the pair buffers: max(65536, 16 n, 1.5 x pairs).
-    if (num > ctx->cap_pairs || !ctx->pairs.k[0]) {
-        size_t cap = std::max<size_t>(65536, (size_t)16 * (size_t)n);
-        cap = std::max<size_t>(cap, (size_t)num + num / 2);
-        cap = std::min<size_t>(cap, (size_t)GSR_MAX_PAIRS);
-        cap = std::max<size_t>(cap, num);
-        size_t have = 0;
-        if ((rc = grow_sort_buffers(ctx, ctx->pairs, &have, cap, "tile pairs"))) {
-            ctx->cap_pairs = 0;
-            return rc;
+                   ctx->rects, blk_pairs, blk_emit, ctx->scalars,
+                   sync_free ? (unsigned long long)ctx->cap_pairs : (unsigned long long)GSR_MAX_PAIRS);
+        if (!sync_free) {
+            // Pair total, emitting count and the AND / OR of the emitting
+            // splats' depth bits (scalar slots 0..3).
+            if ((rc = cuda_check(ctx, cudaMemcpyAsync(ctx->host_total, ctx->scalars, 4 * sizeof(unsigned long long),
+                                                      cudaMemcpyDeviceToHost, stream),
+                                 "cudaMemcpyAsync")))
+                return rc;
+            if ((rc = cuda_check(ctx, cudaStreamSynchronize(stream), "cudaStreamSynchronize"))) return rc;
+            total = ctx->host_total[0];
+            emitting = ctx->host_total[1];
         }
-        ctx->cap_pairs = cap;
     }
+    if (!sync_free) {
+        if (total > (uint64_t)GSR_MAX_PAIRS)
+            return fail(ctx, GSR_ERR_TOO_MANY_PAIRS,
+                        "tile-pair count " + std::to_string(total) + " exceeds GSR_MAX_PAIRS");
+        if ((rc = grow_pairs(total, true))) return rc;
+    }
+    // Bounds of the key counts (exact when they were read back).
+    const uint32_t num_max = sync_free ? (uint32_t)ctx->cap_pairs : (uint32_t)total;
+    const uint32_t m_max = sync_free ? (uint32_t)n : (uint32_t)emitting;
 
     // Radix counts and offsets for the larger of the two sorts, allocated before
     // any kernel that uses them is queued.
     {
         constexpr size_t td = kRtThreads * kRtItemsDepth, tp = kRtThreads * kRtItemsPairs;
-        const size_t rtiles = std::max<size_t>((m + td - 1) / td, (num + tp - 1) / tp);
+        const size_t rtiles = std::max<size_t>((m_max + td - 1) / td, (num_max + tp - 1) / tp);
         if ((rc = grow(ctx, &ctx->radix_counts, &ctx->cap_radix_tiles, std::max<size_t>(rtiles, 1), 512,
                        "radix counts")))
             return rc;
@@ -1057,58 +1138,76 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
                          "cudaMemsetAsync")))
         return rc;
 
-    if (num > 0) {
+    if (num_max > 0 && m_max > 0) {
         // 3. depth sort of the emitting splats.
         GSR_LAUNCH(ctx, k_compact, dim3(nblk), dim3(kBinBlock), stream, ctx->rects, depths, n, blk_emit,
                    ctx->depth.k[0], ctx->depth.v[0]);
-        if ((rc = radix_sort<uint32_t, kRtItemsDepth>(ctx, ctx->depth, (uint32_t)m, 0, 32, ctx->scalars + kScalarDepthAnd,
-                                       ctx->host_total + 2, ctx->radix_totals, stream)))
+        if ((rc = radix_sort<uint32_t, kRtItemsDepth>(ctx, ctx->depth,
+                                                      sync_free ? ctx->scalars + kScalarEmitting : nullptr, m_max, 0, 32,
+                                                      ctx->scalars + kScalarDepthAnd,
+                                                      sync_free ? nullptr : ctx->host_total + 2, ctx->radix_totals,
+                                                      stream)))
             return rc;
         // 4. pair offsets in depth order, emission.
-        const int mblk = (m + kBinBlock - 1) / kBinBlock;
-        GSR_LAUNCH(ctx, k_sorted_sums, dim3(mblk), dim3(kBinBlock), stream, ctx->depth.v[1], ctx->rects, m,
-                   blk_sorted, ctx->scalars);
-        GSR_LAUNCH(ctx, k_emit, dim3(mblk), dim3(kBinBlock), stream, ctx->rects, depths, ctx->depth.v[1], m,
-                   tiles_x, blk_sorted, ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars);
-        // 5. stable sort on the tile digits only.
-        if (key_hi > 32) {
-            // (a sort that runs no pass is completed by the range extraction)
-            if ((rc = radix_sort<uint64_t, kRtItemsPairs>(ctx, ctx->pairs, num, 32, key_hi, ctx->scalars + kScalarKeyAnd,
-                                           nullptr, ctx->radix_totals + 4 * 256, stream)))
-                return rc;
-        } else {
-            // One tile: the emitted order is already sorted.
-            if ((rc = cuda_check(ctx, cudaMemcpyAsync(ctx->pairs.k[1], ctx->pairs.k[0], (size_t)num * 8,
-                                                      cudaMemcpyDeviceToDevice, stream),
-                                 "cudaMemcpyAsync")) ||
-                (rc = cuda_check(ctx, cudaMemcpyAsync(ctx->pairs.v[1], ctx->pairs.v[0], (size_t)num * 4,
-                                                      cudaMemcpyDeviceToDevice, stream),
-                                 "cudaMemcpyAsync")))
-                return rc;
-        }
+        const int mblk = (int)((m_max + kBinBlock - 1) / kBinBlock);
+        const unsigned long long *depth_plan = sync_free ? ctx->scalars + kScalarDepthAnd : nullptr;
+        const int m_host = sync_free ? -1 : (int)m_max;
+        GSR_LAUNCH(ctx, k_sorted_sums, dim3(mblk), dim3(kBinBlock), stream, ctx->depth, ctx->rects, n, m_host,
+                   blk_sorted, ctx->scalars, depth_plan);
+        GSR_LAUNCH(ctx, k_emit, dim3(mblk), dim3(kBinBlock), stream, ctx->rects, depths, ctx->depth, n, m_host,
+                   tiles_x, blk_sorted, ctx->pairs.k[0], ctx->pairs.v[0], ctx->scalars, depth_plan);
+        // 5. stable sort on the tile digits only (a sort that runs no pass,
+        //    one tile included, is completed by the range extraction).
+        const unsigned long long *num_dev = sync_free ? ctx->scalars + kScalarNum : nullptr;
+        if ((rc = radix_sort<uint64_t, kRtItemsPairs>(ctx, ctx->pairs, num_dev, num_max, 32,
+                                                      key_hi, ctx->scalars + kScalarKeyAnd, nullptr,
+                                                      ctx->radix_totals + 4 * 256, stream)))
+            return rc;
         // 6. per-tile ranges.
-        GSR_LAUNCH(ctx, k_extract_ranges, dim3((num + 1023) / 1024), dim3(256), stream, ctx->pairs, num,
-                   ctx->ranges, key_hi > 32 ? (const unsigned long long *)(ctx->scalars + kScalarKeyAnd) : nullptr,
-                   32, key_hi);
+        const int xgrid = (int)((num_max + 1023) / 1024);
+        GSR_LAUNCH(ctx, k_extract_ranges, dim3(sync_free ? std::min(xgrid, ctx->num_sms * 8) : xgrid), dim3(256),
+                   stream, ctx->pairs, num_dev, num_max, ctx->ranges,
+                   (const unsigned long long *)(ctx->scalars + kScalarKeyAnd), 32, key_hi);
     }
 
     // 7. the forward's launch order: longest tile lists first.
     if ((rc = launch_tile_order(ctx, ctx->ranges, nullptr, (int)num_tiles, ctx->tile_order, stream))) return rc;
 
     ctx->last_stream = stream;
-    ctx->last_pairs = num;
-    ctx->last_emitting = (uint32_t)m;
+    ctx->last_sync_free = sync_free;
+    ++ctx->bin_calls;
     ctx->last_key_hi = key_hi;
     out->keys = ctx->pairs.k[1];
     out->sorted_idx = ctx->pairs.v[1];
     out->tile_ranges = ctx->ranges;
     out->tile_order = ctx->tile_order;
-    out->num_pairs = num;
+    out->num_pairs_dev = reinterpret_cast<const uint32_t *>(ctx->scalars + kScalarResult);
+    out->num_pairs = sync_free ? GSR_PAIRS_ON_DEVICE : (uint32_t)total;
     out->n = n;
     out->width = width;
     out->height = height;
     out->tiles_x = tiles_x;
     out->tiles_y = tiles_y;
+    return GSR_OK;
+}
+
+// The last binning's pair count and status from the device (waits for its
+// stream).
+int bin_result(gsr_ctx *ctx, uint32_t *count, uint32_t *status, uint32_t *emitting)
+{
+    *count = 0;
+    *status = GSR_OK;
+    if (emitting) *emitting = 0;
+    if (!ctx->scalars) return GSR_OK;
+    int rc = cuda_check(ctx, cudaStreamSynchronize(ctx->last_stream), "cudaStreamSynchronize");
+    if (rc) return rc;
+    unsigned long long sc[kScalarCount];
+    if ((rc = cuda_check(ctx, cudaMemcpy(sc, ctx->scalars, sizeof sc, cudaMemcpyDeviceToHost), "cudaMemcpy")))
+        return rc;
+    const uint32_t *res = reinterpret_cast<const uint32_t *>(sc + kScalarResult);
+    *count = res[0];
+    *status = res[1];
+    if (emitting) *emitting = (uint32_t)sc[kScalarEmitting];
     return GSR_OK;
 }
 
@@ -1120,10 +1219,11 @@ int bin_pass_masks(gsr_ctx *ctx, uint32_t *depth_mask, uint32_t *tile_mask, int 
     *depth_mask = *tile_mask = 0;
     *tile_digits = num_fields(32, ctx->last_key_hi);
     *tile_digit_bits = *tile_digits ? (ctx->last_key_hi - 32 + *tile_digits - 1) / *tile_digits : 0;
-    if (!ctx->scalars || ctx->last_pairs == 0) return GSR_OK;
+    if (!ctx->scalars) return GSR_OK;
     unsigned long long sc[kScalarCount];
     int rc = cuda_check(ctx, cudaMemcpy(sc, ctx->scalars, sizeof sc, cudaMemcpyDeviceToHost), "cudaMemcpy");
     if (rc) return rc;
+    if (sc[kScalarNum] == 0) return GSR_OK;   // nothing was sorted
     for (int f = 0; f < 4; ++f) {
         int sh, w;
         field_geom(0, 32, 4, f, sh, w);

@@ -37,6 +37,7 @@ struct gsr_ctx {
     int opt_pdl = 1;
     int opt_deterministic = 0;
     int opt_bwd_per_splat = 0;
+    int opt_split = 1;
     int fail_next_alloc = 0;                    // test hook: the next device allocation fails
     int num_sms = 0;                            // multiprocessors of the device (read by gsr_create)
 
@@ -66,10 +67,31 @@ struct gsr_ctx {
     uint2 *det_escale = nullptr;                // [cap_det] fixed-point exponents (deterministic backward)
     uint32_t *det_maxima = nullptr;             // after det_escale: per-block maxima of the bounds (raster.cu)
 
-    // Last binning, for gsr_get_bin_stats.
+    // Pairs reserved by gsr_reserve_pairs (0: none; the binning reads its
+    // count back and sizes the arena to it).
+    uint64_t reserved_pairs = 0;
+
+    // Split backward (raster.cu): the forward records every pixel's state at
+    // each segment boundary of long lists; the backward runs each segment of a
+    // long list as its own CTA from that state.
+    size_t cap_bnd = 0;
+    float4 *bnd = nullptr;                      // [cap_bnd * 256] boundary states (S, T)
+    size_t cap_items = 0;
+    uint2 *bwd_items = nullptr;                 // [cap_items] (tile, segment) work items
+    uint32_t *bwd_item_cost = nullptr;          // after bwd_items: [cap_items] positions per item
+    uint32_t *bwd_item_order = nullptr;         // then [cap_items] launch order, then the item count
+    // The forward whose boundary states bnd holds (the backward splits only
+    // over the same bins and the same forward outputs).
+    bool fwd_bnd_valid = false;
+    uint64_t fwd_bin_call = 0;
+    const float *fwd_final_T = nullptr;
+    const uint32_t *fwd_last = nullptr;
+    uint64_t fwd_pairs_bound = 0;
+    uint64_t bin_calls = 0;                     // gsr_bin_splats calls made
+
+    // Last binning, for gsr_get_bin_stats and gsr_num_pairs.
     cudaStream_t last_stream = nullptr;
-    uint32_t last_pairs = 0;
-    uint32_t last_emitting = 0;                 // splats with at least one pair
+    bool last_sync_free = false;                // its counts stayed on the device
     int last_key_hi = 32;                       // keys occupied bits [0, last_key_hi)
 };
 
@@ -155,6 +177,9 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
                int32_t height, cudaStream_t stream, gsr_bins *out);
 int bin_pass_masks(gsr_ctx *ctx, uint32_t *depth_mask, uint32_t *tile_mask, int *tile_digit_bits,
                    int *tile_digits);
+// The last binning's pair count, status (GSR_OK or GSR_ERR_TOO_MANY_PAIRS) and
+// emitting splats, read from the device after waiting for its stream.
+int bin_result(gsr_ctx *ctx, uint32_t *count, uint32_t *status, uint32_t *emitting);
 int rasterize_forward(gsr_ctx *ctx, const float *splats, const gsr_bins *bins, float *out_rgbw,
                       float *final_T, uint32_t *last_contrib, cudaStream_t stream);
 int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_bins *bins,

@@ -37,6 +37,9 @@
 #ifndef GSR_BWD_STAGE_PER_THREAD
 #define GSR_BWD_STAGE_PER_THREAD 2
 #endif
+#ifndef GSR_SPLIT_POSITIONS
+#define GSR_SPLIT_POSITIONS 512
+#endif
 
 namespace gsr {
 namespace {
@@ -49,6 +52,23 @@ constexpr float kAlphaMin = 1.0f / 255.0f;  // "W1 warp sparse skip + exp-skip",
 constexpr float kAlphaMax = 0.999f;         // "A.9 f16 forward", snippet
 constexpr float kSigmaSkip = 5.55f;         // "W1 warp sparse skip + exp-skip", section 1, W1b
 constexpr float kTMin = 1e-4f;              // stop once the transmittance would fall below this
+// Granularity of the backward's segments of long lists: the forward records
+// each pixel's state at every multiple of this many positions of a list, and
+// the backward runs segments of a multiple of it, each from the state
+// recorded at its end (a multiple of both batch sizes).
+constexpr uint32_t kSplit = GSR_SPLIT_POSITIONS;
+static_assert(kSplit % kBatch == 0 && kSplit % kBwdBatch == 0, "segments hold whole batches");
+// The backward's segments are sized so that the frame's work (the sum over
+// tiles of their largest last_contributor) spreads over this many items per
+// CTA slot.
+#ifndef GSR_SPLIT_ITEMS_PER_SLOT
+#define GSR_SPLIT_ITEMS_PER_SLOT 4
+#endif
+#ifndef GSR_SPLIT_MIN_SEGMENT
+#define GSR_SPLIT_MIN_SEGMENT 512
+#endif
+constexpr int kSplitItemsPerSlot = GSR_SPLIT_ITEMS_PER_SLOT;
+constexpr unsigned long long kSplitMinSegment = GSR_SPLIT_MIN_SEGMENT;   // a multiple of kSplit
 // ln(255) plus a margin far above the rounding of the exponent path: a lane whose
 // sigma exceeds ln(color_a) + this cannot reach alpha >= 1/255.
 constexpr float kLn255Margin = 5.5412636f + 1e-3f;
@@ -211,7 +231,8 @@ template <bool kCull>
 __global__ void __launch_bounds__(kTilePixels, GSR_FWD_MIN_BLOCKS)
 k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
           const uint2 *__restrict__ ranges, const uint32_t *__restrict__ order, int width, int height,
-          int tiles_x, float4 *__restrict__ out_rgbw, float *__restrict__ final_T, uint32_t *__restrict__ last_out)
+          int tiles_x, float4 *__restrict__ out_rgbw, float *__restrict__ final_T, uint32_t *__restrict__ last_out,
+          float4 *__restrict__ bnd)
 {
     grid_dependency_begin();
     __shared__ StagedBatch sb;
@@ -224,15 +245,30 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
     const bool inside = x < width && y < height;
     const float px = (float)x, py = (float)y;
     const uint2 range = ranges[tile];
+    // A list longer than one backward segment records each pixel's state at
+    // every segment boundary.  C then holds the colour of the current segment
+    // only: it is stored and restarted at each boundary, and the pixel's
+    // colour is the sum of its segments' colours, formed at the end.
+    const bool record = bnd && range.y - range.x > kSplit;
 
     float T = 1.0f;
     float3 C = make_float3(0.0f, 0.0f, 0.0f);
     uint32_t last = 0;
     bool done = !inside;
+    uint32_t bounds = 0;   // segment boundaries whose state this CTA recorded
 
     for (uint32_t bstart = range.x; bstart < range.y; bstart += kBatch) {
         // Every pixel of the tile has stopped: no later splat can change it.
         if (__syncthreads_count(done) == kTilePixels) break;
+        // At every multiple of kSplit positions inside the list: the pixel's
+        // transmittance and the colour of the segment that ends there (slot
+        // (list start + position) / kSplit: boundaries of different tiles are
+        // more than kSplit apart).
+        if (record && bstart > range.x && (bstart - range.x) % kSplit == 0) {
+            bnd[(size_t)(bstart / kSplit) * kTilePixels + threadIdx.x] = make_float4(C.x, C.y, C.z, T);
+            C = make_float3(0.0f, 0.0f, 0.0f);
+            ++bounds;
+        }
         GSR_CANARY(1);
 #pragma unroll
         for (int q = 0; q < GSR_STAGE_PER_THREAD; ++q) {
@@ -277,6 +313,17 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
             }
             if (__all_sync(kFull, done)) break;
         }
+    }
+    // The backward of a segment needs the colour of the splats behind its
+    // end: S at a boundary is the sum of the colours of the segments after
+    // it, added from the back (as the backward itself accumulates S; a
+    // difference of running sums would lose S's digits deep in a long list).
+    // The sum over all segments is the pixel's colour.
+    for (uint32_t k = bounds; k >= 1; --k) {
+        float4 &b = bnd[(size_t)((range.x + k * kSplit) / kSplit) * kTilePixels + threadIdx.x];
+        const float4 c = b;   // the colour of the segment before boundary k
+        b = make_float4(C.x, C.y, C.z, c.w);
+        C = make_float3(__fadd_rn(C.x, c.x), __fadd_rn(C.y, c.y), __fadd_rn(C.z, c.z));
     }
     if (inside) {
         const size_t p = (size_t)y * width + x;
@@ -388,15 +435,27 @@ __global__ void __launch_bounds__(kTilePixels, GSR_BWD_MIN_BLOCKS)
 k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
            const uint2 *__restrict__ ranges, const uint32_t *__restrict__ order, int width, int height,
            int tiles_x, const float4 *__restrict__ dl_dout, const float *__restrict__ final_T,
-           const uint32_t *__restrict__ last_in, double *__restrict__ grad_acc, const uint2 *__restrict__ escale)
+           const uint32_t *__restrict__ last_in, double *__restrict__ grad_acc, const uint2 *__restrict__ escale,
+           const uint2 *__restrict__ items, const uint32_t *__restrict__ nitems, const float4 *__restrict__ bnd)
 {
     grid_dependency_begin();
+    // Split mode (items set): CTA i takes work item items[order[i]] = (tile,
+    // segment), the positions [segment G, (segment + 1) G) of the tile's list,
+    // G = nitems[1] (a multiple of kSplit); otherwise CTA i takes tile
+    // order[i] (or i), all of it.
+    uint2 item = make_uint2(0u, 0u);
+    uint32_t seg_len = 0;
+    if (items) {
+        if (blockIdx.x >= __ldg(nitems)) return;
+        item = items[order[blockIdx.x]];
+        seg_len = __ldg(nitems + 1);
+    }
     __shared__ StagedBatchT<kBwdBatch> sb;
     __shared__ uint2 s_esc[kDet ? kBwdBatch : 1];   // fixed-point exponents (deterministic mode)
     __shared__ uint32_t s_wmax[kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t wbit = 1u << warp;
-    const int tile = order ? (int)order[blockIdx.x] : (int)blockIdx.x;
+    const int tile = items ? (int)item.x : (order ? (int)order[blockIdx.x] : (int)blockIdx.x);
     const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
     const int x = x0 + pixel_x(threadIdx.x);
     const int y = y0 + pixel_y(threadIdx.x);
@@ -404,21 +463,32 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
     const float px = (float)x, py = (float)y;
     const uint2 range = ranges[tile];
     const uint32_t len = range.y - range.x;
+    const uint32_t s0 = items ? item.y * seg_len : 0u;
+    const uint32_t s1 = items ? min(len, s0 + seg_len) : len;
 
     float T = 1.0f;
     uint32_t L = 0;
     float3 g = make_float3(0.0f, 0.0f, 0.0f);
+    float3 S = make_float3(0.0f, 0.0f, 0.0f);
     if (inside) {
         const size_t p = (size_t)y * width + x;
         T = final_T[p];
         L = min(last_in[p], len);  // a caller's stale last_contrib cannot reach past the range
+        if (L > s1) {
+            // The pixel composites splats past this segment: start from the
+            // state the forward recorded at the segment's end.
+            const float4 b = bnd[(size_t)((range.x + s1) / kSplit) * kTilePixels + threadIdx.x];
+            S = make_float3(b.x, b.y, b.z);
+            T = b.w;
+            L = s1;
+        }
         const float4 d = dl_dout[p];
         g = make_float3(d.x, d.y, d.z);
     }
     // Positions at or beyond a pixel's last_contributor were never composited
     // there; a warp stops at its largest, the CTA at the largest of its warps.
-    uint32_t warp_end = len;
-    uint32_t cta_end = len;
+    uint32_t warp_end = s1;
+    uint32_t cta_end = s1;
     if (kLastContrib) {
         warp_end = __reduce_max_sync(kFull, L);
         if (lane == 0) s_wmax[warp] = warp_end;
@@ -427,10 +497,8 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) cta_end = max(cta_end, s_wmax[w]);
     }
-    float3 S = make_float3(0.0f, 0.0f, 0.0f);
-
-    for (int bend = (int)cta_end; bend > 0; bend -= kBwdBatch) {
-        const int bstart = max(0, bend - kBwdBatch);
+    for (int bend = (int)cta_end; bend > (int)s0; bend -= kBwdBatch) {
+        const int bstart = max((int)s0, bend - kBwdBatch);
         const int cnt = bend - bstart;
         GSR_CANARY(4);
         __syncthreads();
@@ -808,17 +876,24 @@ __global__ void __launch_bounds__(256) k_grad_to_float_det(long long *__restrict
     }
 }
 
+// Work items of the split backward (all null: one CTA per tile).
+struct SplitItems {
+    const uint2 *items;
+    const uint32_t *nitems;
+    const float4 *bnd;
+};
+
 template <bool kSkip, bool kLc>
 cudaError_t launch_backward_cull(gsr_ctx *ctx, bool cull, int grid, cudaStream_t stream, const float *splats,
                                  const gsr_bins *bins, const uint32_t *order, const float *dl_dout,
                                  const float *final_T, const uint32_t *last_contrib, double *acc,
-                                 const uint2 *escale)
+                                 const uint2 *escale, SplitItems sp)
 {
     auto go = [&](auto kernel) {
         return launch_kernel(ctx, kernel, dim3(grid), dim3(kTilePixels), stream, splats, bins->sorted_idx,
                              reinterpret_cast<const uint2 *>(bins->tile_ranges), order, bins->width,
                              bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
-                             last_contrib, acc, escale);
+                             last_contrib, acc, escale, sp.items, sp.nitems, sp.bnd);
     };
     if (escale) return cull ? go(k_backward<kSkip, kLc, true, true>) : go(k_backward<kSkip, kLc, false, true>);
     return cull ? go(k_backward<kSkip, kLc, true, false>) : go(k_backward<kSkip, kLc, false, false>);
@@ -828,9 +903,10 @@ cudaError_t launch_backward_cull(gsr_ctx *ctx, bool cull, int grid, cudaStream_t
 // in `order` (NULL: tile order) and accumulating into acc.
 cudaError_t launch_backward(gsr_ctx *ctx, cudaStream_t stream, const float *splats, const gsr_bins *bins,
                             const uint32_t *order, const float *dl_dout, const float *final_T,
-                            const uint32_t *last_contrib, double *acc, const uint2 *escale)
+                            const uint32_t *last_contrib, double *acc, const uint2 *escale,
+                            SplitItems sp = {nullptr, nullptr, nullptr}, int split_grid = 0)
 {
-    const int grid = bins->tiles_x * bins->tiles_y;
+    const int grid = sp.items ? split_grid : bins->tiles_x * bins->tiles_y;
     if (ctx->opt_bwd_per_splat) {
         auto go = [&](auto kernel) {
             return launch_kernel(ctx, kernel, dim3(grid), dim3(32), stream, splats, bins->sorted_idx,
@@ -843,15 +919,15 @@ cudaError_t launch_backward(gsr_ctx *ctx, cudaStream_t stream, const float *spla
     const bool cull = ctx->opt_warp_cull != 0;
     if (ctx->opt_warp_skip && ctx->opt_last_contrib)
         return launch_backward_cull<true, true>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                                last_contrib, acc, escale);
+                                                last_contrib, acc, escale, sp);
     if (ctx->opt_warp_skip)
         return launch_backward_cull<true, false>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                                 last_contrib, acc, escale);
+                                                 last_contrib, acc, escale, sp);
     if (ctx->opt_last_contrib)
         return launch_backward_cull<false, true>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                                 last_contrib, acc, escale);
+                                                 last_contrib, acc, escale, sp);
     return launch_backward_cull<false, false>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                              last_contrib, acc, escale);
+                                              last_contrib, acc, escale, sp);
 }
 
 // Per tile: the largest last_contributor of its pixels (one warp per tile), the
@@ -875,19 +951,156 @@ k_tile_cost(const uint32_t *__restrict__ last, int width, int height, int tiles_
     if (lane == 0) cost[tile] = m;
 }
 
+// 0 for no work, else 1 + floor(8 log2 c): 256 classes a factor 2^(1/8) apart.
+__device__ __forceinline__ int work_class(uint32_t c)
+{
+    return c == 0 ? 0 : min(255, 1 + (int)(8.0f * __log2f((float)c)));
+}
+
+// Split mode: the backward's work items and their launch order.  The segment
+// length G is the multiple of kSplit nearest above the frame's work (the sum
+// of the tiles' largest last_contributor) over slots x kSplitItemsPerSlot
+// items; a tile whose largest last_contributor is c gets ceil(c / G) items
+// (tile, 0), (tile, 1), ...  item_cost holds each item's number of positions,
+// nitems[0] their total and nitems[1] = G; order lists the items with the
+// most positions first (a counting sort over logarithmic classes).  One block
+// of 1024 threads.
+__global__ void __launch_bounds__(1024)
+k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint2 *__restrict__ items,
+           uint32_t *__restrict__ item_cost, uint32_t *__restrict__ order, uint32_t *__restrict__ nitems)
+{
+    grid_dependency_begin();
+    __shared__ uint32_t s_warp[32];
+    __shared__ uint32_t s_carry;
+    __shared__ uint32_t s_hist[256];
+    __shared__ unsigned long long s_work;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        s_carry = 0;
+        s_work = 0;
+    }
+    __syncthreads();
+    unsigned long long work = 0;
+    for (int t = threadIdx.x; t < num_tiles; t += 1024) work += cost[t];
+    atomicAdd(&s_work, work);
+    __syncthreads();
+    const unsigned long long per = s_work / ((unsigned long long)slots * kSplitItemsPerSlot);
+    const unsigned long long g = max((per + kSplit - 1) / kSplit * kSplit, kSplitMinSegment);
+    const uint32_t G = (uint32_t)min(g, 0x40000000ull);
+    for (int base = 0; base < num_tiles; base += 1024) {
+        const int t = base + threadIdx.x;
+        const uint32_t c = t < num_tiles ? cost[t] : 0u;
+        const uint32_t nseg = (c + G - 1) / G;
+        uint32_t incl = nseg;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        uint32_t before = s_carry, total = s_carry;
+        for (int w = 0; w < 32; ++w) {
+            const uint32_t v = s_warp[w];
+            if (w < warp) before += v;
+            total += v;
+        }
+        const uint32_t off = before + incl - nseg;
+        for (uint32_t k = 0; k < nseg; ++k) {
+            items[off + k] = make_uint2((uint32_t)t, k);
+            item_cost[off + k] = min(G, c - k * G);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) s_carry = total;
+        __syncthreads();
+    }
+    const uint32_t n = s_carry;
+    if (threadIdx.x == 0) {
+        nitems[0] = n;
+        nitems[1] = G;
+    }
+    // The launch order: histogram of the classes, then each class's start
+    // counted from the largest class down, then the items placed.
+    if (threadIdx.x < 256) s_hist[threadIdx.x] = 0;
+    __syncthreads();
+    for (uint32_t w = threadIdx.x; w < n; w += 1024) atomicAdd(&s_hist[work_class(item_cost[w])], 1u);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        uint32_t local[8], sum = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            local[k] = s_hist[255 - (8 * lane + k)];
+            sum += local[k];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        uint32_t run = incl - sum;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            s_hist[255 - (8 * lane + k)] = run;
+            run += local[k];
+        }
+    }
+    __syncthreads();
+    for (uint32_t w = threadIdx.x; w < n; w += 1024) order[atomicAdd(&s_hist[work_class(item_cost[w])], 1u)] = w;
+}
+
 }  // namespace
+
+// The pair count of bins, or its bound (the arena's capacity) when it stayed
+// on the device.
+static uint64_t pairs_bound(const gsr_ctx *ctx, const gsr_bins *bins)
+{
+    return bins->num_pairs == GSR_PAIRS_ON_DEVICE ? (uint64_t)ctx->cap_pairs : (uint64_t)bins->num_pairs;
+}
 
 int rasterize_forward(gsr_ctx *ctx, const float *splats, const gsr_bins *bins, float *out_rgbw,
                       float *final_T, uint32_t *last_contrib, cudaStream_t stream)
 {
     const int num_tiles = bins->tiles_x * bins->tiles_y;
+    // The boundary states the split backward starts its segments from: one
+    // slot of 256 pixels per kSplit pairs, grown with the pairs.
+    float4 *bnd = nullptr;
+    ctx->fwd_bnd_valid = false;
+    if (ctx->opt_split) {
+        const uint64_t bound = pairs_bound(ctx, bins);
+        const size_t slots = (size_t)(bound / kSplit) + 1;
+        if (slots > ctx->cap_bnd || !ctx->bnd) {
+            if (ctx->bnd) {
+                // queued work of an earlier call may still use the old buffer
+                if (int rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize")) return rc;
+                cudaFree(ctx->bnd);
+            }
+            ctx->bnd = nullptr;
+            ctx->cap_bnd = 0;
+            if (device_alloc(ctx, (void **)&ctx->bnd, slots * kTilePixels * sizeof(float4)) != cudaSuccess) {
+                cudaGetLastError();
+                ctx->bnd = nullptr;
+                return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the segment boundary states");
+            }
+            ctx->cap_bnd = slots;
+        }
+        bnd = ctx->bnd;
+    }
     auto go = [&](auto kernel) {
         return launch_kernel(ctx, kernel, dim3(num_tiles), dim3(kTilePixels), stream, splats, bins->sorted_idx,
                              reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->tile_order, bins->width,
                              bins->height, bins->tiles_x, reinterpret_cast<float4 *>(out_rgbw), final_T,
-                             last_contrib);
+                             last_contrib, bnd);
     };
-    return cuda_check(ctx, ctx->opt_warp_cull ? go(k_forward<true>) : go(k_forward<false>), "forward launch");
+    int rc = cuda_check(ctx, ctx->opt_warp_cull ? go(k_forward<true>) : go(k_forward<false>), "forward launch");
+    if (rc == GSR_OK && bnd) {
+        ctx->fwd_bnd_valid = true;
+        ctx->fwd_bin_call = ctx->bin_calls;
+        ctx->fwd_final_T = final_T;
+        ctx->fwd_last = last_contrib;
+        ctx->fwd_pairs_bound = pairs_bound(ctx, bins);
+    }
+    return rc;
 }
 
 int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_bins *bins,
@@ -940,12 +1153,51 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
         ctx->bwd_tile_order = ctx->bwd_tile_cost + cap;
         ctx->cap_bwd_tiles = cap;
     }
+    // Split mode: long lists run as segments of kSplit positions, each from the
+    // state this context's forward recorded at its end.  Only over the forward
+    // that recorded them: the same bins and the same forward outputs.
+    const bool split = ctx->opt_split && !ctx->opt_bwd_per_splat && ctx->fwd_bnd_valid && ctx->bnd &&
+                       ctx->fwd_bin_call == ctx->bin_calls && ctx->fwd_final_T == final_T &&
+                       ctx->fwd_last == last_contrib;
+    size_t item_bound = 0;
+    if (split) {
+        // at most ceil(len / kSplit) items per tile: num_tiles + pairs / kSplit
+        item_bound = (size_t)num_tiles + (size_t)(ctx->fwd_pairs_bound / kSplit);
+        if (item_bound > ctx->cap_items || !ctx->bwd_items) {
+            if (ctx->bwd_items) {
+                if ((rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize"))) return rc;
+                cudaFree(ctx->bwd_items);
+            }
+            ctx->bwd_items = nullptr;
+            ctx->cap_items = 0;
+            // items (uint2), their costs, their order, the count and the segment length
+            if (device_alloc(ctx, (void **)&ctx->bwd_items, item_bound * (sizeof(uint2) + 2 * sizeof(uint32_t)) +
+                                                                2 * sizeof(uint32_t)) != cudaSuccess) {
+                cudaGetLastError();
+                ctx->bwd_items = nullptr;
+                return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the backward work items");
+            }
+            ctx->cap_items = item_bound;
+            ctx->bwd_item_cost = reinterpret_cast<uint32_t *>(ctx->bwd_items + item_bound);
+            ctx->bwd_item_order = ctx->bwd_item_cost + item_bound;
+        }
+    }
+    uint32_t *nitems = split ? ctx->bwd_item_order + ctx->cap_items : nullptr;
     if ((rc = cuda_check(ctx, launch_kernel(ctx, k_tile_cost, dim3((num_tiles + 7) / 8), dim3(256), stream,
                                             last_contrib, bins->width, bins->height, bins->tiles_x, num_tiles,
                                             ctx->bwd_tile_cost),
-                         "tile cost launch")) ||
-        (rc = launch_tile_order(ctx, nullptr, ctx->bwd_tile_cost, num_tiles, ctx->bwd_tile_order, stream)))
+                         "tile cost launch")))
         return rc;
+    if (split) {
+        if ((rc = cuda_check(ctx, launch_kernel(ctx, k_bwd_plan, dim3(1), dim3(1024), stream,
+                                                (const uint32_t *)ctx->bwd_tile_cost, num_tiles,
+                                                ctx->num_sms * GSR_BWD_MIN_BLOCKS, ctx->bwd_items,
+                                                ctx->bwd_item_cost, ctx->bwd_item_order, nitems),
+                             "backward plan launch")))
+            return rc;
+    } else if ((rc = launch_tile_order(ctx, nullptr, ctx->bwd_tile_cost, num_tiles, ctx->bwd_tile_order, stream))) {
+        return rc;
+    }
     // Deterministic mode: the maxima and the per-splat fixed-point exponents.
     const uint2 *escale = nullptr;
     if (ctx->opt_deterministic) {
@@ -981,8 +1233,10 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
         escale = ctx->det_escale;
     }
     ctx->grad_acc_zero = false;
-    if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins, ctx->bwd_tile_order, dl_dout, final_T,
-                                              last_contrib, ctx->grad_acc, escale),
+    const SplitItems sp = {split ? ctx->bwd_items : nullptr, nitems, split ? ctx->bnd : nullptr};
+    if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins,
+                                              split ? ctx->bwd_item_order : ctx->bwd_tile_order, dl_dout, final_T,
+                                              last_contrib, ctx->grad_acc, escale, sp, (int)item_bound),
                          "backward launch")))
         return rc;
     if (count > 0) {

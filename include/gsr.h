@@ -28,7 +28,8 @@
  *     arrays inside gsr_bins, which belong to the context's arena.
  *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
  *     legacy default stream).  gsr_bin_splats synchronises that stream once to
- *     read the pair count; the raster calls return without synchronising.
+ *     read the pair count, unless the context has a reservation
+ *     (gsr_reserve_pairs); the raster calls return without synchronising.
  *   - The calling thread's current CUDA device is switched to the context's
  *     device for the duration of a call and restored afterwards.
  *   - Every call returns GSR_OK or an error code; gsr_last_error() gives the text.
@@ -112,16 +113,26 @@ enum {
                                      warps add in ("M3 per-splat backward", sections 2 and 4: run-to-run
                                      self-noise).  A non-finite dL/dout makes every gradient NaN.  Not
                                      available to gsr_rasterize_backward_noalloc (GSR_ERR_INVALID_ARG). */
-    GSR_OPT_BWD_PER_SPLAT = 7     /* default 0.  1: the backward runs the transposed loop nest ("M3
+    GSR_OPT_BWD_PER_SPLAT = 7,    /* default 0.  1: the backward runs the transposed loop nest ("M3
                                      per-splat backward", section 1): one warp per tile, one lane per
                                      splat, the tile's pixels met in diagonal order, each lane's sums
                                      kept in registers and added once per (tile, splat).  Same
                                      gradients within float rounding; it evaluates every pixel of a
                                      tile for every splat, and ran 24 times slower than the default
                                      backward on an 800x800 image of 409,660 splats. */
+    GSR_OPT_SPLIT = 8             /* default 1.  The forward records each pixel's transmittance and the
+                                     colour behind every 512th position of a tile's list, and the
+                                     backward that follows it on the same context (the same bins, the
+                                     same final_T and last_contrib buffers) runs a long list as
+                                     segments of a multiple of 512 positions, sized from the frame's
+                                     work, each its own CTA from those states, so a crowded tile no
+                                     longer runs on alone at the end of the launch.  0: one CTA per
+                                     tile (same results within float rounding). */
 };
 
 typedef struct gsr_ctx gsr_ctx;
+
+#define GSR_PAIRS_ON_DEVICE 0xffffffffu  /* gsr_bins.num_pairs: the count stayed on the device */
 
 /* Result of gsr_bin_splats.  The device arrays live in the context's arena and
  * stay valid until the next gsr_bin_splats or gsr_destroy on that context. */
@@ -134,7 +145,12 @@ typedef struct gsr_bins {
     const uint32_t *tile_order;  /* device, [tiles_x * tiles_y]: every tile index once, longest
                                     lists first (by classes of pair count); the forward
                                     launches its CTAs in this order.  NULL: tile order. */
-    uint32_t num_pairs;          /* host copy of the pair count */
+    const uint32_t *num_pairs_dev; /* device, [2]: the pair count (saturated at 0xffffffff) and the
+                                    binning's status, GSR_OK or GSR_ERR_TOO_MANY_PAIRS (the count
+                                    exceeded the reserved capacity: every tile range is {0, 0});
+                                    valid once the binning's work has run */
+    uint32_t num_pairs;          /* host copy of the pair count, or GSR_PAIRS_ON_DEVICE when the
+                                    binning did not read it back (gsr_reserve_pairs) */
     int32_t n;                   /* splat count the bins were built from */
     int32_t width, height;       /* image size in pixels */
     int32_t tiles_x, tiles_y;    /* ceil(width / 16), ceil(height / 16) */
@@ -169,12 +185,41 @@ uint64_t gsr_launch_count(const gsr_ctx *ctx);
  * clamped to the grid; it emits nothing when a field or its depth is not
  * finite, depth <= 0, a <= 0 or det <= 0, or its box misses the image.  The
  * arena grows (never shrinks) to max(65536, 16 n, 1.5 x previous pairs) pairs
- * as needed.  n == 0 is valid and gives empty bins.
+ * as needed: the call reads the pair count back (one synchronisation of
+ * `stream`) unless the context has a reservation (gsr_reserve_pairs), with
+ * which it reads nothing back.  n == 0 is valid and gives empty bins.
  * Errors: GSR_ERR_INVALID_ARG (null ctx/out, n < 0 or > GSR_MAX_SPLATS,
  * width/height outside [1, GSR_MAX_IMAGE_SIDE], null splats/depths with n > 0),
  * GSR_ERR_TOO_MANY_PAIRS, GSR_ERR_OOM, GSR_ERR_CUDA. */
 int gsr_bin_splats(gsr_ctx *ctx, const gsr_splat2d *splats, const float *depths, int32_t n,
                    int32_t width, int32_t height, void *stream, gsr_bins *out);
+
+/* Reserves arena capacity for max_pairs tile pairs and switches the context's
+ * binning to a mode that reads nothing back to the host
+ * ("C0 resident arena + C1 pass skip", section 2 table, C0: the arena grows and
+ * is reused; here it is sized ahead so that no call needs the count on the
+ * host).  From the next gsr_bin_splats on:
+ *   - the call does not synchronise: the arena holds max(max_pairs, 16 n,
+ *     65536) pairs (grown at that call if smaller, which does synchronise),
+ *     every kernel takes its key counts from the device, and the radix passes
+ *     decide on the device which digits to skip;
+ *   - bins->num_pairs is GSR_PAIRS_ON_DEVICE and bins->num_pairs_dev holds the
+ *     count and the status once the work has run;
+ *   - a call whose pairs exceed the capacity emits nothing: its status is
+ *     GSR_ERR_TOO_MANY_PAIRS, every tile range is {0, 0} (the forward then
+ *     gives final_T = 1 and no colour, the backward zero gradients), and
+ *     gsr_num_pairs reports the count that was needed;
+ *   - once the arena has its size, a call allocates nothing and can be
+ *     captured in a CUDA graph together with the raster calls.
+ * max_pairs = 0 returns to the default mode (the count is read back and the
+ * arena grown to it).  GSR_ERR_INVALID_ARG for max_pairs > GSR_MAX_PAIRS. */
+int gsr_reserve_pairs(gsr_ctx *ctx, uint64_t max_pairs);
+
+/* The pair count of the last gsr_bin_splats on this context: waits for that
+ * call's stream, then reads the count from the device.  GSR_ERR_TOO_MANY_PAIRS
+ * (with *out the count that was needed) when that binning exceeded its
+ * reservation. */
+int gsr_num_pairs(gsr_ctx *ctx, uint32_t *out);
 
 /* Forward rasterization over bins made by gsr_bin_splats from the same splats
  * ("forward/adam audit", sections (a), (b), 3; "A.9 f16 forward", snippet;

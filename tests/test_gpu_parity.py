@@ -37,8 +37,10 @@ def ctx(gsr):
 
 
 # The most gradient components per config allowed to need the 8u sum|t| term
-# (sums whose terms cancel; measured counts with the forced replays applied).
-COND_CAPS = {"tiny": 0, "small": 0, "lego_early": 4, "lego_final": 4, "stress": 100}
+# (sums whose terms cancel), with the forced replays applied.  Measured on
+# GB300: tiny 0, small 0, lego_early 2 (of 0.75M), lego_final 0 (of 3.7M),
+# stress 24 (of 9M); the caps leave room for the order of the atomic adds.
+COND_CAPS = {"tiny": 0, "small": 0, "lego_early": 4, "lego_final": 2, "stress": 32}
 
 
 def _full(gsr, ctx, wl, backward=True, cond_cap=None):
