@@ -436,26 +436,24 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
            const uint2 *__restrict__ ranges, const uint32_t *__restrict__ order, int width, int height,
            int tiles_x, const float4 *__restrict__ dl_dout, const float *__restrict__ final_T,
            const uint32_t *__restrict__ last_in, double *__restrict__ grad_acc, const uint2 *__restrict__ escale,
-           const uint2 *__restrict__ items, const uint32_t *__restrict__ nitems, const float4 *__restrict__ bnd)
+           const uint2 *__restrict__ items, const uint32_t *__restrict__ queue, const float4 *__restrict__ bnd)
 {
     grid_dependency_begin();
-    // Split mode (items set): CTA i takes work item items[order[i]] = (tile,
-    // segment), the positions [segment G, (segment + 1) G) of the tile's list,
-    // G = nitems[1] (a multiple of kSplit); otherwise CTA i takes tile
-    // order[i] (or i), all of it.
-    uint2 item = make_uint2(0u, 0u);
-    uint32_t seg_len = 0;
-    if (items) {
-        if (blockIdx.x >= __ldg(nitems)) return;
-        item = items[order[blockIdx.x]];
-        seg_len = __ldg(nitems + 1);
-    }
     __shared__ StagedBatchT<kBwdBatch> sb;
     __shared__ uint2 s_esc[kDet ? kBwdBatch : 1];   // fixed-point exponents (deterministic mode)
     __shared__ uint32_t s_wmax[kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t wbit = 1u << warp;
-    const int tile = items ? (int)item.x : (order ? (int)order[blockIdx.x] : (int)blockIdx.x);
+    // CTA w takes work item w.  Split mode (items set): item w is
+    // items[order[w]] = (tile, segment), the positions [segment G,
+    // (segment + 1) G) of the tile's list, with queue[0] items (the grid holds
+    // a bound on their number) and G = queue[1] (a multiple of kSplit);
+    // otherwise item w is tile order[w] (or w), all of it.
+    const uint32_t w = blockIdx.x;
+    if (items && w >= __ldg(queue)) return;
+    const uint32_t seg_len = items ? __ldg(queue + 1) : 0u;
+    const uint2 item = items ? items[order[w]] : make_uint2(order ? order[w] : w, 0u);
+    const int tile = (int)item.x;
     const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
     const int x = x0 + pixel_x(threadIdx.x);
     const int y = y0 + pixel_y(threadIdx.x);
@@ -876,24 +874,27 @@ __global__ void __launch_bounds__(256) k_grad_to_float_det(long long *__restrict
     }
 }
 
-// Work items of the split backward (all null: one CTA per tile).
-struct SplitItems {
+// Work items of the backward: items null, one CTA per tile; else the split's
+// (tile, segment) items, queue holding their number and the segment length,
+// and bound the most there can be (the grid: CTAs past the number exit).
+struct WorkItems {
     const uint2 *items;
-    const uint32_t *nitems;
+    const uint32_t *queue;
     const float4 *bnd;
+    uint32_t bound;
 };
 
 template <bool kSkip, bool kLc>
 cudaError_t launch_backward_cull(gsr_ctx *ctx, bool cull, int grid, cudaStream_t stream, const float *splats,
                                  const gsr_bins *bins, const uint32_t *order, const float *dl_dout,
                                  const float *final_T, const uint32_t *last_contrib, double *acc,
-                                 const uint2 *escale, SplitItems sp)
+                                 const uint2 *escale, WorkItems wi)
 {
     auto go = [&](auto kernel) {
         return launch_kernel(ctx, kernel, dim3(grid), dim3(kTilePixels), stream, splats, bins->sorted_idx,
                              reinterpret_cast<const uint2 *>(bins->tile_ranges), order, bins->width,
                              bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
-                             last_contrib, acc, escale, sp.items, sp.nitems, sp.bnd);
+                             last_contrib, acc, escale, wi.items, wi.queue, wi.bnd);
     };
     if (escale) return cull ? go(k_backward<kSkip, kLc, true, true>) : go(k_backward<kSkip, kLc, false, true>);
     return cull ? go(k_backward<kSkip, kLc, true, false>) : go(k_backward<kSkip, kLc, false, false>);
@@ -904,12 +905,13 @@ cudaError_t launch_backward_cull(gsr_ctx *ctx, bool cull, int grid, cudaStream_t
 cudaError_t launch_backward(gsr_ctx *ctx, cudaStream_t stream, const float *splats, const gsr_bins *bins,
                             const uint32_t *order, const float *dl_dout, const float *final_T,
                             const uint32_t *last_contrib, double *acc, const uint2 *escale,
-                            SplitItems sp = {nullptr, nullptr, nullptr}, int split_grid = 0)
+                            WorkItems wi = {nullptr, nullptr, nullptr, 0})
 {
-    const int grid = sp.items ? split_grid : bins->tiles_x * bins->tiles_y;
+    const int num_tiles = bins->tiles_x * bins->tiles_y;
+    const int grid = wi.items ? (int)wi.bound : num_tiles;
     if (ctx->opt_bwd_per_splat) {
-        auto go = [&](auto kernel) {
-            return launch_kernel(ctx, kernel, dim3(grid), dim3(32), stream, splats, bins->sorted_idx,
+        auto go = [&](auto kernel) {   // one CTA per tile
+            return launch_kernel(ctx, kernel, dim3(num_tiles), dim3(32), stream, splats, bins->sorted_idx,
                                  reinterpret_cast<const uint2 *>(bins->tile_ranges), order, bins->width,
                                  bins->height, bins->tiles_x, reinterpret_cast<const float4 *>(dl_dout), final_T,
                                  last_contrib, acc, escale);
@@ -919,15 +921,15 @@ cudaError_t launch_backward(gsr_ctx *ctx, cudaStream_t stream, const float *spla
     const bool cull = ctx->opt_warp_cull != 0;
     if (ctx->opt_warp_skip && ctx->opt_last_contrib)
         return launch_backward_cull<true, true>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                                last_contrib, acc, escale, sp);
+                                                last_contrib, acc, escale, wi);
     if (ctx->opt_warp_skip)
         return launch_backward_cull<true, false>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                                 last_contrib, acc, escale, sp);
+                                                 last_contrib, acc, escale, wi);
     if (ctx->opt_last_contrib)
         return launch_backward_cull<false, true>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                                 last_contrib, acc, escale, sp);
+                                                 last_contrib, acc, escale, wi);
     return launch_backward_cull<false, false>(ctx, cull, grid, stream, splats, bins, order, dl_dout, final_T,
-                                              last_contrib, acc, escale, sp);
+                                              last_contrib, acc, escale, wi);
 }
 
 // Per tile: the largest last_contributor of its pixels (one warp per tile), the
@@ -962,12 +964,12 @@ __device__ __forceinline__ int work_class(uint32_t c)
 // of the tiles' largest last_contributor) over slots x kSplitItemsPerSlot
 // items; a tile whose largest last_contributor is c gets ceil(c / G) items
 // (tile, 0), (tile, 1), ...  item_cost holds each item's number of positions,
-// nitems[0] their total and nitems[1] = G; order lists the items with the
+// queue[0] their total and queue[1] = G; order lists the items with the
 // most positions first (a counting sort over logarithmic classes).  One block
 // of 1024 threads.
 __global__ void __launch_bounds__(1024)
-k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint2 *__restrict__ items,
-           uint32_t *__restrict__ item_cost, uint32_t *__restrict__ order, uint32_t *__restrict__ nitems)
+k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint32_t bound, uint2 *__restrict__ items,
+           uint32_t *__restrict__ item_cost, uint32_t *__restrict__ order, uint32_t *__restrict__ queue)
 {
     grid_dependency_begin();
     __shared__ uint32_t s_warp[32];
@@ -982,9 +984,12 @@ k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint2 *_
     __syncthreads();
     unsigned long long work = 0;
     for (int t = threadIdx.x; t < num_tiles; t += 1024) work += cost[t];
-    atomicAdd(&s_work, work);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) work += __shfl_xor_sync(kFull, work, o);
+    if (lane == 0) atomicAdd(&s_work, work);   // one shared atomic per warp
     __syncthreads();
-    const unsigned long long per = s_work / ((unsigned long long)slots * kSplitItemsPerSlot);
+    const unsigned long long items_wanted = (unsigned long long)slots * kSplitItemsPerSlot;
+    const unsigned long long per = (s_work + items_wanted - 1) / items_wanted;
     const unsigned long long g = max((per + kSplit - 1) / kSplit * kSplit, kSplitMinSegment);
     const uint32_t G = (uint32_t)min(g, 0x40000000ull);
     for (int base = 0; base < num_tiles; base += 1024) {
@@ -1006,7 +1011,7 @@ k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint2 *_
             total += v;
         }
         const uint32_t off = before + incl - nseg;
-        for (uint32_t k = 0; k < nseg; ++k) {
+        for (uint32_t k = 0; k < nseg && off + k < bound; ++k) {   // (the bound holds by construction)
             items[off + k] = make_uint2((uint32_t)t, k);
             item_cost[off + k] = min(G, c - k * G);
         }
@@ -1014,16 +1019,24 @@ k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint2 *_
         if (threadIdx.x == 0) s_carry = total;
         __syncthreads();
     }
-    const uint32_t n = s_carry;
+    const uint32_t n = min(s_carry, bound);
     if (threadIdx.x == 0) {
-        nitems[0] = n;
-        nitems[1] = G;
+        queue[0] = n;
+        queue[1] = G;
     }
     // The launch order: histogram of the classes, then each class's start
-    // counted from the largest class down, then the items placed.
+    // counted from the largest class down, then the items placed.  Many items
+    // share a class (full segments): the lanes of a warp with the same class
+    // make one shared atomic together.
     if (threadIdx.x < 256) s_hist[threadIdx.x] = 0;
     __syncthreads();
-    for (uint32_t w = threadIdx.x; w < n; w += 1024) atomicAdd(&s_hist[work_class(item_cost[w])], 1u);
+    const uint32_t lanes_below = (1u << lane) - 1u;
+    for (uint32_t base = 0; base < n; base += 1024) {
+        const uint32_t w = base + threadIdx.x;
+        const int cls = w < n ? work_class(item_cost[w]) : -1;
+        const uint32_t peers = __match_any_sync(kFull, cls);
+        if (cls >= 0 && (peers & lanes_below) == 0) atomicAdd(&s_hist[cls], (uint32_t)__popc(peers));
+    }
     __syncthreads();
     if (threadIdx.x < 32) {
         uint32_t local[8], sum = 0;
@@ -1046,7 +1059,16 @@ k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint2 *_
         }
     }
     __syncthreads();
-    for (uint32_t w = threadIdx.x; w < n; w += 1024) order[atomicAdd(&s_hist[work_class(item_cost[w])], 1u)] = w;
+    for (uint32_t base = 0; base < n; base += 1024) {
+        const uint32_t w = base + threadIdx.x;
+        const int cls = w < n ? work_class(item_cost[w]) : -1;
+        const uint32_t peers = __match_any_sync(kFull, cls);
+        const int leader = __ffs(peers) - 1;
+        uint32_t first = 0;
+        if (cls >= 0 && lane == leader) first = atomicAdd(&s_hist[cls], (uint32_t)__popc(peers));
+        first = __shfl_sync(kFull, first, leader);
+        if (cls >= 0) order[first + __popc(peers & lanes_below)] = w;
+    }
 }
 
 }  // namespace
@@ -1145,7 +1167,9 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
         ctx->bwd_tile_cost = ctx->bwd_tile_order = nullptr;
         ctx->cap_bwd_tiles = 0;
         const size_t cap = std::max<size_t>((size_t)num_tiles, 1);
-        if (device_alloc(ctx, (void **)&ctx->bwd_tile_cost, 2 * cap * sizeof(uint32_t)) != cudaSuccess) {
+        // per tile its cost and the launch order, then the split's item count
+        // and segment length
+        if (device_alloc(ctx, (void **)&ctx->bwd_tile_cost, (2 * cap + 2) * sizeof(uint32_t)) != cudaSuccess) {
             cudaGetLastError();
             ctx->bwd_tile_cost = nullptr;
             return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the backward tile order");
@@ -1153,16 +1177,22 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
         ctx->bwd_tile_order = ctx->bwd_tile_cost + cap;
         ctx->cap_bwd_tiles = cap;
     }
-    // Split mode: long lists run as segments of kSplit positions, each from the
-    // state this context's forward recorded at its end.  Only over the forward
-    // that recorded them: the same bins and the same forward outputs.
+    uint32_t *queue = ctx->bwd_tile_order + ctx->cap_bwd_tiles;
+    // Split mode: long lists run as segments of a multiple of kSplit positions,
+    // each from the state this context's forward recorded at its end.  Only
+    // over the forward that recorded them: the same bins and the same forward
+    // outputs.
     const bool split = ctx->opt_split && !ctx->opt_bwd_per_splat && ctx->fwd_bnd_valid && ctx->bnd &&
                        ctx->fwd_bin_call == ctx->bin_calls && ctx->fwd_final_T == final_T &&
                        ctx->fwd_last == last_contrib;
     size_t item_bound = 0;
     if (split) {
-        // at most ceil(len / kSplit) items per tile: num_tiles + pairs / kSplit
-        item_bound = (size_t)num_tiles + (size_t)(ctx->fwd_pairs_bound / kSplit);
+        // at most ceil(len / kSplit) items per tile (num_tiles + pairs / kSplit),
+        // and at most num_tiles + slots x kSplitItemsPerSlot with segments of
+        // at least the frame's work over that many items
+        item_bound = (size_t)num_tiles + std::min<size_t>((size_t)(ctx->fwd_pairs_bound / kSplit),
+                                                          (size_t)ctx->num_sms * GSR_BWD_MIN_BLOCKS *
+                                                              kSplitItemsPerSlot);
         if (item_bound > ctx->cap_items || !ctx->bwd_items) {
             if (ctx->bwd_items) {
                 if ((rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize"))) return rc;
@@ -1170,9 +1200,9 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
             }
             ctx->bwd_items = nullptr;
             ctx->cap_items = 0;
-            // items (uint2), their costs, their order, the count and the segment length
-            if (device_alloc(ctx, (void **)&ctx->bwd_items, item_bound * (sizeof(uint2) + 2 * sizeof(uint32_t)) +
-                                                                2 * sizeof(uint32_t)) != cudaSuccess) {
+            // items (uint2), their costs, their order
+            if (device_alloc(ctx, (void **)&ctx->bwd_items, item_bound * (sizeof(uint2) + 2 * sizeof(uint32_t))) !=
+                cudaSuccess) {
                 cudaGetLastError();
                 ctx->bwd_items = nullptr;
                 return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the backward work items");
@@ -1182,7 +1212,6 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
             ctx->bwd_item_order = ctx->bwd_item_cost + item_bound;
         }
     }
-    uint32_t *nitems = split ? ctx->bwd_item_order + ctx->cap_items : nullptr;
     if ((rc = cuda_check(ctx, launch_kernel(ctx, k_tile_cost, dim3((num_tiles + 7) / 8), dim3(256), stream,
                                             last_contrib, bins->width, bins->height, bins->tiles_x, num_tiles,
                                             ctx->bwd_tile_cost),
@@ -1191,8 +1220,8 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
     if (split) {
         if ((rc = cuda_check(ctx, launch_kernel(ctx, k_bwd_plan, dim3(1), dim3(1024), stream,
                                                 (const uint32_t *)ctx->bwd_tile_cost, num_tiles,
-                                                ctx->num_sms * GSR_BWD_MIN_BLOCKS, ctx->bwd_items,
-                                                ctx->bwd_item_cost, ctx->bwd_item_order, nitems),
+                                                ctx->num_sms * GSR_BWD_MIN_BLOCKS, (uint32_t)item_bound, ctx->bwd_items,
+                                                ctx->bwd_item_cost, ctx->bwd_item_order, queue),
                              "backward plan launch")))
             return rc;
     } else if ((rc = launch_tile_order(ctx, nullptr, ctx->bwd_tile_cost, num_tiles, ctx->bwd_tile_order, stream))) {
@@ -1233,10 +1262,11 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
         escale = ctx->det_escale;
     }
     ctx->grad_acc_zero = false;
-    const SplitItems sp = {split ? ctx->bwd_items : nullptr, nitems, split ? ctx->bnd : nullptr};
+    const WorkItems wi = {split ? ctx->bwd_items : nullptr, queue, split ? ctx->bnd : nullptr,
+                          (uint32_t)item_bound};
     if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins,
                                               split ? ctx->bwd_item_order : ctx->bwd_tile_order, dl_dout, final_T,
-                                              last_contrib, ctx->grad_acc, escale, sp, (int)item_bound),
+                                              last_contrib, ctx->grad_acc, escale, wi),
                          "backward launch")))
         return rc;
     if (count > 0) {
