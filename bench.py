@@ -109,11 +109,13 @@ def parse_args(argv=None):
                    help="also time the whole step (binning, forward, backward) replayed as one captured CUDA graph")
     p.add_argument("--no-split", action="store_true",
                    help="run the backward as one CTA per tile (no segments of long lists)")
-    p.add_argument("--read-back", action="store_true",
-                   help="bin in the default mode, which reads the pair count back to the host every call, "
-                        "instead of with a reserved arena")
+    p.add_argument("--reserved", action="store_true",
+                   help="time the step with the binning of a context that has a reservation (no host read-back) "
+                        "instead of the default binning, which reads the pair count back every call")
     p.add_argument("--no-projection", action="store_true",
                    help="skip the separate timing of the projection kernels")
+    p.add_argument("--no-alu-peaks", action="store_true",
+                   help="skip the FP32/SFU rate kernels (profiling runs; the roofline is then not reported)")
     p.add_argument("--min-warm-s", type=float, default=1.5,
                    help="keep warming up until this many seconds passed (clock sampling)")
     return p.parse_args(argv)
@@ -288,8 +290,9 @@ def bench_config(wl, args, pairs, world):
             "backward_accumulation": "fixed point (deterministic)" if args.deterministic else "double atomics",
             "backward_loop_nest": "per splat (diagonal)" if args.bwd_per_splat else "per pixel",
             "long_lists": "one CTA per tile" if args.no_split else "backward segments of 2,048 positions",
-            "binning": "pair count read back every call" if args.read_back
-            else "reserved arena (1.5 x the pair count), no host read-back"}
+            "binning": "reserved arena (1.5 x the pair count), no host read-back" if args.reserved
+            else "pair count read back every call",
+            "e2e_binning": "reserved arena (1.5 x the pair count), no host read-back"}
 
 
 def reference_arm(args):
@@ -440,9 +443,10 @@ def time_projection(gsr, ctx, dev, stream, flush, steps, warmup, peaks):
 
 
 def time_graph(gsr, ctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush, steps):
-    """The whole step (binning with the context's reservation, forward,
-    backward) replayed from one captured CUDA graph, against the same step
-    with direct calls, alternating, between L2 flushes; medians."""
+    """The whole step (binning with a reservation, forward, backward) replayed
+    from one captured CUDA graph, against the same step with direct calls on
+    the same context, alternating, between L2 flushes; medians.  ctx must have
+    a reservation (a graph cannot hold the default binning's read-back)."""
     import torch
 
     def direct():
@@ -504,7 +508,6 @@ def gpu_arm(args):
     if args.no_split:
         ctx.set_option("split", False)
     stream = torch.cuda.current_stream(dev)
-    reserve = 0
 
     sp = torch.from_numpy(wl.splats).to(dev)
     dp = torch.from_numpy(wl.depths).to(dev)
@@ -515,10 +518,11 @@ def gpu_arm(args):
     last = torch.empty((npx,), dtype=torch.int32, device=dev)
     grad = torch.empty((wl.n, 9), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    if not args.read_back:
-        # One binning that reads its count back sizes the reservation (setup,
-        # outside any timing); the timed steps then read nothing back.
-        reserve = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height).num_pairs * 3 // 2
+    # One binning that reads its count back sizes the reservations (setup,
+    # outside any timing) of the contexts that read nothing back: the e2e
+    # contexts, the graph's, and the timed one with --reserved.
+    reserve = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height).num_pairs * 3 // 2
+    if args.reserved:
         ctx.reserve_pairs(reserve)
 
     def step(evs):
@@ -582,9 +586,8 @@ def gpu_arm(args):
         h_dl = torch.from_numpy(wl.dl_dout).pin_memory()
         slots = []
         for k in range(2):
-            c2 = ctx if k == 0 else gsr.Context(local)
-            if reserve:
-                c2.reserve_pairs(reserve)
+            c2 = gsr.Context(local)
+            c2.reserve_pairs(reserve)
             if args.deterministic:
                 c2.set_option("deterministic", True)
             if args.bwd_per_splat:
@@ -682,8 +685,16 @@ def gpu_arm(args):
                "two_threads_ms_per_iter": e2e_two_ms / args.steps}
 
     graph = None
-    if args.graph and not args.read_back:
-        graph = time_graph(gsr, ctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush, max(args.steps, 20))
+    if args.graph:
+        gctx = gsr.Context(local)
+        gctx.reserve_pairs(reserve)
+        for flag, name in ((args.deterministic, "deterministic"), (args.bwd_per_splat, "bwd_per_splat")):
+            if flag:
+                gctx.set_option(name, True)
+        if args.no_split:
+            gctx.set_option("split", False)
+        graph = time_graph(gsr, gctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush, max(args.steps, 20))
+        gctx.close()
     peaks = measured_peaks()
     # Binning against HBM: N·40 B of splats and depths read, each pair's 12-byte
     # key and index written once and read and written by every executed pair
@@ -705,7 +716,7 @@ def gpu_arm(args):
         projection = time_projection(gsr, ctx, dev, stream, flush, max(args.steps, 20), max(args.warmup, 3),
                                      peaks)
 
-    alu = measure_alu_peaks(gsr, ctx, dev, stream)
+    alu = None if args.no_alu_peaks else measure_alu_peaks(gsr, ctx, dev, stream)
     rows = sampler.stop()
     clocks = ClockSampler.summarize(rows)
 
@@ -732,7 +743,7 @@ def gpu_arm(args):
     if graph:
         line["graph"] = graph
 
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and alu:
         cb = cpu_baseline(wl)
         line["cpu_baseline"] = {"value": cb["ms"], "unit": "ms/iter", "cores": 1, "kind": "oracle",
                                 "sample": "the whole workload once (binning, forward, backward), "

@@ -851,20 +851,12 @@ k_tile_order(const uint2 *__restrict__ ranges, const uint32_t *__restrict__ cost
     if (threadIdx.x < 256) s_hist[threadIdx.x] = 0;
     __syncthreads();
     auto cost_of = [&](int t) { return ranges ? ranges[t].y - ranges[t].x : costs[t]; };
-    // Tiles of the same class in a warp make one shared atomic together (many
-    // tiles share a class: empty ones, and lists of like length).
-    const int lane = threadIdx.x & 31;
-    const uint32_t lanes_below = (1u << lane) - 1u;
-    for (int base = 0; base < num_tiles; base += blockDim.x) {
-        const int t = base + threadIdx.x;
-        const int cls = t < num_tiles ? cost_class(cost_of(t)) : -1;
-        const uint32_t peers = __match_any_sync(kFull, cls);
-        if (cls >= 0 && (peers & lanes_below) == 0) atomicAdd(&s_hist[cls], (uint32_t)__popc(peers));
-    }
+    for (int t = threadIdx.x; t < num_tiles; t += blockDim.x) atomicAdd(&s_hist[cost_class(cost_of(t))], 1u);
     __syncthreads();
     if (threadIdx.x < 32) {
         // Exclusive scan over the classes from the largest down: lane l owns
         // classes 255 - 8l down to 248 - 8l.
+        const int lane = threadIdx.x;
         uint32_t local[8], sum = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -885,16 +877,8 @@ k_tile_order(const uint2 *__restrict__ ranges, const uint32_t *__restrict__ cost
         }
     }
     __syncthreads();
-    for (int base = 0; base < num_tiles; base += blockDim.x) {
-        const int t = base + threadIdx.x;
-        const int cls = t < num_tiles ? cost_class(cost_of(t)) : -1;
-        const uint32_t peers = __match_any_sync(kFull, cls);
-        const int leader = __ffs(peers) - 1;
-        uint32_t first = 0;
-        if (cls >= 0 && lane == leader) first = atomicAdd(&s_cursor[cls], (uint32_t)__popc(peers));
-        first = __shfl_sync(kFull, first, leader);
-        if (cls >= 0) order[first + __popc(peers & lanes_below)] = (uint32_t)t;
-    }
+    for (int t = threadIdx.x; t < num_tiles; t += blockDim.x)
+        order[atomicAdd(&s_cursor[cost_class(cost_of(t))], 1u)] = (uint32_t)t;
 }
 
 int bits_for(uint64_t v)

@@ -68,6 +68,8 @@ static_assert(kSplit % kBatch == 0 && kSplit % kBwdBatch == 0, "segments hold wh
 #define GSR_SPLIT_MIN_SEGMENT 512
 #endif
 constexpr int kSplitItemsPerSlot = GSR_SPLIT_ITEMS_PER_SLOT;
+// The segment field of the work item of a tile that is not split.
+constexpr uint32_t kWholeList = 0xffffffffu;
 constexpr unsigned long long kSplitMinSegment = GSR_SPLIT_MIN_SEGMENT;   // a multiple of kSplit
 // ln(255) plus a margin far above the rounding of the exponent path: a lane whose
 // sigma exceeds ln(color_a) + this cannot reach alpha >= 1/255.
@@ -444,14 +446,17 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
     __shared__ uint32_t s_wmax[kWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t wbit = 1u << warp;
-    // CTA w takes work item w.  Split mode (items set): item w is
-    // items[order[w]] = (tile, segment), the positions [segment G,
-    // (segment + 1) G) of the tile's list, with queue[0] items (the grid holds
-    // a bound on their number) and G = queue[1] (a multiple of kSplit);
-    // otherwise item w is tile order[w] (or w), all of it.
-    const uint32_t w = blockIdx.x;
-    if (items && w >= __ldg(queue)) return;
+    // CTA b takes work items b, b + gridDim.x, ...  Split mode (items set):
+    // item w is items[order[w]] = (tile, segment), the positions
+    // [segment G, (segment + 1) G) of the tile's list (or all of it), with
+    // queue[0] items and G = queue[1] (a multiple of kSplit); the grid holds
+    // one CTA per tile, so a CTA takes a second item only when the split
+    // makes more items than tiles.  Otherwise CTA b takes tile order[b] (or
+    // b), all of it.
+    const uint32_t n = items ? __ldg(queue) : 0u;
     const uint32_t seg_len = items ? __ldg(queue + 1) : 0u;
+    for (uint32_t w = blockIdx.x; !items || w < n; w += gridDim.x) {
+    if (items && w > blockIdx.x) __syncthreads();   // the previous item's shared state is read
     const uint2 item = items ? items[order[w]] : make_uint2(order ? order[w] : w, 0u);
     const int tile = (int)item.x;
     const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
@@ -461,8 +466,9 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
     const float px = (float)x, py = (float)y;
     const uint2 range = ranges[tile];
     const uint32_t len = range.y - range.x;
-    const uint32_t s0 = items ? item.y * seg_len : 0u;
-    const uint32_t s1 = items ? min(len, s0 + seg_len) : len;
+    const bool whole = !items || item.y == kWholeList;
+    const uint32_t s0 = whole ? 0u : item.y * seg_len;
+    const uint32_t s1 = whole ? len : min(len, s0 + seg_len);
 
     float T = 1.0f;
     uint32_t L = 0;
@@ -568,6 +574,8 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
                                        kDet ? s_esc[j] : make_uint2(0u, 0u));
             }
         }
+    }
+    if (!items) break;
     }
 }
 
@@ -876,7 +884,7 @@ __global__ void __launch_bounds__(256) k_grad_to_float_det(long long *__restrict
 
 // Work items of the backward: items null, one CTA per tile; else the split's
 // (tile, segment) items, queue holding their number and the segment length,
-// and bound the most there can be (the grid: CTAs past the number exit).
+// and bound the most there can be.
 struct WorkItems {
     const uint2 *items;
     const uint32_t *queue;
@@ -908,7 +916,7 @@ cudaError_t launch_backward(gsr_ctx *ctx, cudaStream_t stream, const float *spla
                             WorkItems wi = {nullptr, nullptr, nullptr, 0})
 {
     const int num_tiles = bins->tiles_x * bins->tiles_y;
-    const int grid = wi.items ? (int)wi.bound : num_tiles;
+    const int grid = num_tiles;   // one CTA per tile, in both modes
     if (ctx->opt_bwd_per_splat) {
         auto go = [&](auto kernel) {   // one CTA per tile
             return launch_kernel(ctx, kernel, dim3(num_tiles), dim3(32), stream, splats, bins->sorted_idx,
@@ -959,17 +967,21 @@ __device__ __forceinline__ int work_class(uint32_t c)
     return c == 0 ? 0 : min(255, 1 + (int)(8.0f * __log2f((float)c)));
 }
 
-// Split mode: the backward's work items and their launch order.  The segment
-// length G is the multiple of kSplit nearest above the frame's work (the sum
-// of the tiles' largest last_contributor) over slots x kSplitItemsPerSlot
-// items; a tile whose largest last_contributor is c gets ceil(c / G) items
-// (tile, 0), (tile, 1), ...  item_cost holds each item's number of positions,
-// queue[0] their total and queue[1] = G; order lists the items with the
-// most positions first (a counting sort over logarithmic classes).  One block
-// of 1024 threads.
+// Split mode: the backward's work items and their launch order.  A tile is
+// split when its largest last_contributor c exceeds a CTA slot's fair share of
+// the frame's work (the sum of the tiles' c over the slots): it then gets
+// ceil(c / G) items (tile, 0), (tile, 1), ..., G the multiple of kSplit
+// nearest above the frame's work over slots x kSplitItemsPerSlot items; any
+// other tile with work gets the one item (tile, 0) with G covering it.  In a
+// frame without crowded tiles nothing splits.  queue[0] holds the items'
+// total and queue[1] = G.
+// order lists the items tile by tile, the tiles of larger c first (a counting
+// sort over logarithmic classes of c, each class counting its tiles' items).
+// first (num_tiles entries) receives each tile's first item.  One block of
+// 1024 threads.
 __global__ void __launch_bounds__(1024)
 k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint32_t bound, uint2 *__restrict__ items,
-           uint32_t *__restrict__ item_cost, uint32_t *__restrict__ order, uint32_t *__restrict__ queue)
+           uint32_t *__restrict__ first, uint32_t *__restrict__ order, uint32_t *__restrict__ queue)
 {
     grid_dependency_begin();
     __shared__ uint32_t s_warp[32];
@@ -981,6 +993,7 @@ k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint32_t
         s_carry = 0;
         s_work = 0;
     }
+    if (threadIdx.x < 256) s_hist[threadIdx.x] = 0;
     __syncthreads();
     unsigned long long work = 0;
     for (int t = threadIdx.x; t < num_tiles; t += 1024) work += cost[t];
@@ -992,10 +1005,15 @@ k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint32_t
     const unsigned long long per = (s_work + items_wanted - 1) / items_wanted;
     const unsigned long long g = max((per + kSplit - 1) / kSplit * kSplit, kSplitMinSegment);
     const uint32_t G = (uint32_t)min(g, 0x40000000ull);
+    const unsigned long long share = (s_work + slots - 1) / slots;   // a slot's fair share
+    // segments of a tile: one unless its work exceeds the share
+    auto segments = [&](uint32_t c) -> uint32_t { return c > share ? (c + G - 1) / G : (c ? 1u : 0u); };
+    // Items tile by tile (an exclusive scan of the segment counts), and each
+    // class's item count.
     for (int base = 0; base < num_tiles; base += 1024) {
         const int t = base + threadIdx.x;
         const uint32_t c = t < num_tiles ? cost[t] : 0u;
-        const uint32_t nseg = (c + G - 1) / G;
+        const uint32_t nseg = segments(c);
         uint32_t incl = nseg;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -1011,9 +1029,13 @@ k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint32_t
             total += v;
         }
         const uint32_t off = before + incl - nseg;
-        for (uint32_t k = 0; k < nseg && off + k < bound; ++k) {   // (the bound holds by construction)
-            items[off + k] = make_uint2((uint32_t)t, k);
-            item_cost[off + k] = min(G, c - k * G);
+        if (t < num_tiles) {
+            first[t] = off;
+            // (the bound holds by construction); an unsplit tile's item is
+            // marked as the whole list
+            for (uint32_t k = 0; k < nseg && off + k < bound; ++k)
+                items[off + k] = make_uint2((uint32_t)t, nseg == 1 ? kWholeList : k);
+            if (nseg) atomicAdd(&s_hist[work_class(c)], nseg);
         }
         __syncthreads();
         if (threadIdx.x == 0) s_carry = total;
@@ -1024,20 +1046,7 @@ k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint32_t
         queue[0] = n;
         queue[1] = G;
     }
-    // The launch order: histogram of the classes, then each class's start
-    // counted from the largest class down, then the items placed.  Many items
-    // share a class (full segments): the lanes of a warp with the same class
-    // make one shared atomic together.
-    if (threadIdx.x < 256) s_hist[threadIdx.x] = 0;
-    __syncthreads();
-    const uint32_t lanes_below = (1u << lane) - 1u;
-    for (uint32_t base = 0; base < n; base += 1024) {
-        const uint32_t w = base + threadIdx.x;
-        const int cls = w < n ? work_class(item_cost[w]) : -1;
-        const uint32_t peers = __match_any_sync(kFull, cls);
-        if (cls >= 0 && (peers & lanes_below) == 0) atomicAdd(&s_hist[cls], (uint32_t)__popc(peers));
-    }
-    __syncthreads();
+    // Each class's first place, counted from the largest class down.
     if (threadIdx.x < 32) {
         uint32_t local[8], sum = 0;
 #pragma unroll
@@ -1059,15 +1068,14 @@ k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint32_t
         }
     }
     __syncthreads();
-    for (uint32_t base = 0; base < n; base += 1024) {
-        const uint32_t w = base + threadIdx.x;
-        const int cls = w < n ? work_class(item_cost[w]) : -1;
-        const uint32_t peers = __match_any_sync(kFull, cls);
-        const int leader = __ffs(peers) - 1;
-        uint32_t first = 0;
-        if (cls >= 0 && lane == leader) first = atomicAdd(&s_hist[cls], (uint32_t)__popc(peers));
-        first = __shfl_sync(kFull, first, leader);
-        if (cls >= 0) order[first + __popc(peers & lanes_below)] = w;
+    // A tile's items go together to its class's next places.
+    for (int t = threadIdx.x; t < num_tiles; t += 1024) {
+        const uint32_t c = cost[t];
+        const uint32_t nseg = segments(c);
+        if (!nseg) continue;
+        const uint32_t place = atomicAdd(&s_hist[work_class(c)], nseg);
+        const uint32_t f = first[t];
+        for (uint32_t k = 0; k < nseg && place + k < bound && f + k < bound; ++k) order[place + k] = f + k;
     }
 }
 
@@ -1187,12 +1195,14 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
                        ctx->fwd_last == last_contrib;
     size_t item_bound = 0;
     if (split) {
-        // at most ceil(len / kSplit) items per tile (num_tiles + pairs / kSplit),
-        // and at most num_tiles + slots x kSplitItemsPerSlot with segments of
-        // at least the frame's work over that many items
+        // at most ceil(len / kSplit) items per tile (num_tiles + pairs / kSplit);
+        // and with segments of at least the frame's work W over slots x
+        // kSplitItemsPerSlot items, split only in tiles whose work exceeds
+        // W / slots (at most slots of them), at most num_tiles + slots x
+        // (kSplitItemsPerSlot + 1)
         item_bound = (size_t)num_tiles + std::min<size_t>((size_t)(ctx->fwd_pairs_bound / kSplit),
                                                           (size_t)ctx->num_sms * GSR_BWD_MIN_BLOCKS *
-                                                              kSplitItemsPerSlot);
+                                                              (kSplitItemsPerSlot + 1));
         if (item_bound > ctx->cap_items || !ctx->bwd_items) {
             if (ctx->bwd_items) {
                 if ((rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize"))) return rc;
@@ -1200,7 +1210,7 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
             }
             ctx->bwd_items = nullptr;
             ctx->cap_items = 0;
-            // items (uint2), their costs, their order
+            // items (uint2), each tile's first item, the items' order
             if (device_alloc(ctx, (void **)&ctx->bwd_items, item_bound * (sizeof(uint2) + 2 * sizeof(uint32_t))) !=
                 cudaSuccess) {
                 cudaGetLastError();
@@ -1208,8 +1218,8 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
                 return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the backward work items");
             }
             ctx->cap_items = item_bound;
-            ctx->bwd_item_cost = reinterpret_cast<uint32_t *>(ctx->bwd_items + item_bound);
-            ctx->bwd_item_order = ctx->bwd_item_cost + item_bound;
+            ctx->bwd_item_first = reinterpret_cast<uint32_t *>(ctx->bwd_items + item_bound);
+            ctx->bwd_item_order = ctx->bwd_item_first + item_bound;
         }
     }
     if ((rc = cuda_check(ctx, launch_kernel(ctx, k_tile_cost, dim3((num_tiles + 7) / 8), dim3(256), stream,
@@ -1221,7 +1231,7 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
         if ((rc = cuda_check(ctx, launch_kernel(ctx, k_bwd_plan, dim3(1), dim3(1024), stream,
                                                 (const uint32_t *)ctx->bwd_tile_cost, num_tiles,
                                                 ctx->num_sms * GSR_BWD_MIN_BLOCKS, (uint32_t)item_bound, ctx->bwd_items,
-                                                ctx->bwd_item_cost, ctx->bwd_item_order, queue),
+                                                ctx->bwd_item_first, ctx->bwd_item_order, queue),
                              "backward plan launch")))
             return rc;
     } else if ((rc = launch_tile_order(ctx, nullptr, ctx->bwd_tile_cost, num_tiles, ctx->bwd_tile_order, stream))) {
