@@ -77,9 +77,7 @@ struct gsr_ctx {
     size_t cap_bnd = 0;
     float4 *bnd = nullptr;                      // [cap_bnd * 256] boundary states (S, T)
     size_t cap_items = 0;
-    uint2 *bwd_items = nullptr;                 // [cap_items] (tile, segment) work items
-    uint32_t *bwd_item_first = nullptr;         // after bwd_items: [cap_items] each tile's first item
-    uint32_t *bwd_item_order = nullptr;         // then [cap_items] launch order, then the item count
+    uint2 *bwd_items = nullptr;                 // [cap_items] (tile, segment) work items in launch order
     // The forward whose boundary states bnd holds (the backward splits only
     // over the same bins and the same forward outputs).
     bool fwd_bnd_valid = false;

@@ -447,7 +447,7 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t wbit = 1u << warp;
     // CTA b takes work items b, b + gridDim.x, ...  Split mode (items set):
-    // item w is items[order[w]] = (tile, segment), the positions
+    // item w is items[w] = (tile, segment), the positions
     // [segment G, (segment + 1) G) of the tile's list (or all of it), with
     // queue[0] items and G = queue[1] (a multiple of kSplit); the grid holds
     // one CTA per tile, so a CTA takes a second item only when the split
@@ -457,7 +457,7 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
     const uint32_t seg_len = items ? __ldg(queue + 1) : 0u;
     for (uint32_t w = blockIdx.x; !items || w < n; w += gridDim.x) {
     if (items && w > blockIdx.x) __syncthreads();   // the previous item's shared state is read
-    const uint2 item = items ? items[order[w]] : make_uint2(order ? order[w] : w, 0u);
+    const uint2 item = items ? items[w] : make_uint2(order ? order[w] : w, 0u);
     const int tile = (int)item.x;
     const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
     const int x = x0 + pixel_x(threadIdx.x);
@@ -967,31 +967,29 @@ __device__ __forceinline__ int work_class(uint32_t c)
     return c == 0 ? 0 : min(255, 1 + (int)(8.0f * __log2f((float)c)));
 }
 
-// Split mode: the backward's work items and their launch order.  A tile is
-// split when its largest last_contributor c exceeds a CTA slot's fair share of
-// the frame's work (the sum of the tiles' c over the slots): it then gets
+// Split mode: the backward's work items in launch order.  A tile is split
+// when its largest last_contributor c exceeds a CTA slot's fair share of the
+// frame's work (the sum of the tiles' c over the slots): it then gets
 // ceil(c / G) items (tile, 0), (tile, 1), ..., G the multiple of kSplit
 // nearest above the frame's work over slots x kSplitItemsPerSlot items; any
-// other tile with work gets the one item (tile, 0) with G covering it.  In a
-// frame without crowded tiles nothing splits.  queue[0] holds the items'
-// total and queue[1] = G.
-// order lists the items tile by tile, the tiles of larger c first (a counting
-// sort over logarithmic classes of c, each class counting its tiles' items).
-// first (num_tiles entries) receives each tile's first item.  One block of
-// 1024 threads.
+// other tile with work gets the one item (tile, kWholeList).  In a frame
+// without crowded tiles nothing splits.  The items are written in launch
+// order, tile by tile, the tiles of larger c first: a counting sort over
+// logarithmic classes of c, each class counting its tiles' items.
+// queue[0] receives the items' total and queue[1] = G.  One block of 1024
+// threads.
 __global__ void __launch_bounds__(1024)
 k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint32_t bound, uint2 *__restrict__ items,
-           uint32_t *__restrict__ first, uint32_t *__restrict__ order, uint32_t *__restrict__ queue)
+           uint32_t *__restrict__ queue)
 {
     grid_dependency_begin();
-    __shared__ uint32_t s_warp[32];
-    __shared__ uint32_t s_carry;
     __shared__ uint32_t s_hist[256];
     __shared__ unsigned long long s_work;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __shared__ uint32_t s_items;
+    const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        s_carry = 0;
         s_work = 0;
+        s_items = 0;
     }
     if (threadIdx.x < 256) s_hist[threadIdx.x] = 0;
     __syncthreads();
@@ -1008,42 +1006,19 @@ k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint32_t
     const unsigned long long share = (s_work + slots - 1) / slots;   // a slot's fair share
     // segments of a tile: one unless its work exceeds the share
     auto segments = [&](uint32_t c) -> uint32_t { return c > share ? (c + G - 1) / G : (c ? 1u : 0u); };
-    // Items tile by tile (an exclusive scan of the segment counts), and each
-    // class's item count.
-    for (int base = 0; base < num_tiles; base += 1024) {
-        const int t = base + threadIdx.x;
-        const uint32_t c = t < num_tiles ? cost[t] : 0u;
+    // Each class's item count, and the total.
+    uint32_t mine = 0;
+    for (int t = threadIdx.x; t < num_tiles; t += 1024) {
+        const uint32_t c = cost[t];
         const uint32_t nseg = segments(c);
-        uint32_t incl = nseg;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) s_warp[warp] = incl;
-        __syncthreads();
-        uint32_t before = s_carry, total = s_carry;
-        for (int w = 0; w < 32; ++w) {
-            const uint32_t v = s_warp[w];
-            if (w < warp) before += v;
-            total += v;
-        }
-        const uint32_t off = before + incl - nseg;
-        if (t < num_tiles) {
-            first[t] = off;
-            // (the bound holds by construction); an unsplit tile's item is
-            // marked as the whole list
-            for (uint32_t k = 0; k < nseg && off + k < bound; ++k)
-                items[off + k] = make_uint2((uint32_t)t, nseg == 1 ? kWholeList : k);
-            if (nseg) atomicAdd(&s_hist[work_class(c)], nseg);
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) s_carry = total;
-        __syncthreads();
+        if (nseg) atomicAdd(&s_hist[work_class(c)], nseg);
+        mine += nseg;
     }
-    const uint32_t n = min(s_carry, bound);
+    mine = __reduce_add_sync(kFull, mine);
+    if (lane == 0 && mine) atomicAdd(&s_items, mine);
+    __syncthreads();
     if (threadIdx.x == 0) {
-        queue[0] = n;
+        queue[0] = min(s_items, bound);
         queue[1] = G;
     }
     // Each class's first place, counted from the largest class down.
@@ -1068,14 +1043,15 @@ k_bwd_plan(const uint32_t *__restrict__ cost, int num_tiles, int slots, uint32_t
         }
     }
     __syncthreads();
-    // A tile's items go together to its class's next places.
+    // A tile's items go together to its class's next places (the bound holds
+    // by construction; the test keeps the writes inside the buffer regardless).
     for (int t = threadIdx.x; t < num_tiles; t += 1024) {
         const uint32_t c = cost[t];
         const uint32_t nseg = segments(c);
         if (!nseg) continue;
         const uint32_t place = atomicAdd(&s_hist[work_class(c)], nseg);
-        const uint32_t f = first[t];
-        for (uint32_t k = 0; k < nseg && place + k < bound && f + k < bound; ++k) order[place + k] = f + k;
+        for (uint32_t k = 0; k < nseg && place + k < bound; ++k)
+            items[place + k] = make_uint2((uint32_t)t, nseg == 1 ? kWholeList : k);
     }
 }
 
@@ -1210,16 +1186,13 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
             }
             ctx->bwd_items = nullptr;
             ctx->cap_items = 0;
-            // items (uint2), each tile's first item, the items' order
-            if (device_alloc(ctx, (void **)&ctx->bwd_items, item_bound * (sizeof(uint2) + 2 * sizeof(uint32_t))) !=
+            if (device_alloc(ctx, (void **)&ctx->bwd_items, item_bound * sizeof(uint2)) !=
                 cudaSuccess) {
                 cudaGetLastError();
                 ctx->bwd_items = nullptr;
                 return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the backward work items");
             }
             ctx->cap_items = item_bound;
-            ctx->bwd_item_first = reinterpret_cast<uint32_t *>(ctx->bwd_items + item_bound);
-            ctx->bwd_item_order = ctx->bwd_item_first + item_bound;
         }
     }
     if ((rc = cuda_check(ctx, launch_kernel(ctx, k_tile_cost, dim3((num_tiles + 7) / 8), dim3(256), stream,
@@ -1231,7 +1204,7 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
         if ((rc = cuda_check(ctx, launch_kernel(ctx, k_bwd_plan, dim3(1), dim3(1024), stream,
                                                 (const uint32_t *)ctx->bwd_tile_cost, num_tiles,
                                                 ctx->num_sms * GSR_BWD_MIN_BLOCKS, (uint32_t)item_bound, ctx->bwd_items,
-                                                ctx->bwd_item_first, ctx->bwd_item_order, queue),
+                                                queue),
                              "backward plan launch")))
             return rc;
     } else if ((rc = launch_tile_order(ctx, nullptr, ctx->bwd_tile_cost, num_tiles, ctx->bwd_tile_order, stream))) {
@@ -1275,7 +1248,7 @@ int rasterize_backward(gsr_ctx *ctx, const float *splats, int32_t n, const gsr_b
     const WorkItems wi = {split ? ctx->bwd_items : nullptr, queue, split ? ctx->bnd : nullptr,
                           (uint32_t)item_bound};
     if ((rc = cuda_check(ctx, launch_backward(ctx, stream, splats, bins,
-                                              split ? ctx->bwd_item_order : ctx->bwd_tile_order, dl_dout, final_T,
+                                              split ? nullptr : ctx->bwd_tile_order, dl_dout, final_T,
                                               last_contrib, ctx->grad_acc, escale, wi),
                          "backward launch")))
         return rc;
