@@ -108,10 +108,14 @@ def parse_args(argv=None):
     p.add_argument("--graph", action="store_true",
                    help="also time the whole step (binning, forward, backward) replayed as one captured CUDA graph")
     p.add_argument("--no-split", action="store_true",
-                   help="run the backward as one CTA per tile (no segments of long lists)")
+                   help="run forward and backward as one CTA per tile (no chunks or segments of long lists)")
+    p.add_argument("--no-split-forward", action="store_true",
+                   help="run the forward as one CTA per tile (the backward still splits long lists)")
     p.add_argument("--reserved", action="store_true",
                    help="time the step with the binning of a context that has a reservation (no host read-back) "
                         "instead of the default binning, which reads the pair count back every call")
+    p.add_argument("--no-other-configs", action="store_true",
+                   help="skip the lines of the other frames timed beside the headline one")
     p.add_argument("--no-projection", action="store_true",
                    help="skip the separate timing of the projection kernels")
     p.add_argument("--no-alu-peaks", action="store_true",
@@ -282,6 +286,26 @@ def band_workload(wl, band, bands):
     return gen.from_arrays(f"{wl.name}[rows {y0}:{y1}]", wl.width, y1 - y0, s, wl.depths, dl), y1 - y0
 
 
+def long_lists_label(args) -> str:
+    if args.no_split:
+        return "one CTA per tile"
+    bwd = "backward: segments of tiles above a CTA slot's share of the work"
+    if args.no_split_forward:
+        return "forward: one CTA per tile; " + bwd
+    return "forward: 512-position chunks past a head of max(2048, pairs / CTA slots); " + bwd
+
+
+def apply_options(c, args):
+    """The bench's variant switches on context c."""
+    for flag, name in ((args.deterministic, "deterministic"), (args.bwd_per_splat, "bwd_per_splat")):
+        if flag:
+            c.set_option(name, True)
+    if args.no_split:
+        c.set_option("split", False)
+    if args.no_split_forward:
+        c.set_option("split_forward", False)
+
+
 def bench_config(wl, args, pairs, world):
     """The `config` object of the JSON line; both arms print the same one."""
     return {"workload": workload_label(wl), "splats": wl.n, "width": wl.width, "height": wl.height,
@@ -289,7 +313,7 @@ def bench_config(wl, args, pairs, world):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "backward_accumulation": "fixed point (deterministic)" if args.deterministic else "double atomics",
             "backward_loop_nest": "per splat (diagonal)" if args.bwd_per_splat else "per pixel",
-            "long_lists": "one CTA per tile" if args.no_split else "backward segments of 2,048 positions",
+            "long_lists": long_lists_label(args),
             "binning": "reserved arena (1.5 x the pair count), no host read-back" if args.reserved
             else "pair count read back every call",
             "e2e_binning": "reserved arena (1.5 x the pair count), no host read-back"}
@@ -488,6 +512,49 @@ def time_graph(gsr, ctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush
                     f"{steps} steps"}
 
 
+# Frames timed beside the headline one (same step, same L2 flush): the pages'
+# pair density, and a close-up whose crowded tiles the split serves.
+OTHER_CONFIGS = ("lego_pages", "lego_far")
+
+
+def time_other_config(gsr, name, args, dev, stream, flush, steps, warmup):
+    import torch
+    wl = gen.make(name)
+    ctx = gsr.Context(dev.index or 0)
+    apply_options(ctx, args)
+    sp, dp, dl = (torch.from_numpy(a).to(dev) for a in (wl.splats, wl.depths, wl.dl_dout))
+    npx = wl.width * wl.height
+    out = torch.empty((npx, 4), dtype=torch.float32, device=dev)
+    fT = torch.empty((npx,), dtype=torch.float32, device=dev)
+    last = torch.empty((npx,), dtype=torch.int32, device=dev)
+    grad = torch.empty((wl.n, 9), dtype=torch.float32, device=dev)
+
+    def step(evs):
+        evs[0].record(stream)
+        bins = gsr.bin_splats(ctx, sp, dp, wl.width, wl.height)
+        evs[1].record(stream)
+        gsr.rasterize_forward(ctx, sp, bins, out, fT, last)
+        evs[2].record(stream)
+        gsr.rasterize_backward(ctx, sp, bins, dl, fT, last, grad)
+        evs[3].record(stream)
+
+    for k in range(warmup):
+        flush.fill_(float(k))
+        step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(float(i))
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    t = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(3)] + [e[0].elapsed_time(e[3])] for e in evs])
+    pairs = ctx.num_pairs()
+    ctx.close()
+    return {"workload": workload_label(wl), "splats": wl.n, "pairs": int(pairs),
+            "pairs_per_splat": pairs / wl.n, "steps": steps, "ms_per_step": float(t[:, 3].mean()),
+            "stages_ms": {"bin": float(t[:, 0].mean()), "forward": float(t[:, 1].mean()),
+                          "backward": float(t[:, 2].mean())}}
+
+
 def gpu_arm(args):
     import torch
 
@@ -501,12 +568,7 @@ def gpu_arm(args):
     dev = torch.device("cuda", local)
     wl = gen.make(args.config)
     ctx = gsr.Context(local)
-    if args.deterministic:
-        ctx.set_option("deterministic", True)
-    if args.bwd_per_splat:
-        ctx.set_option("bwd_per_splat", True)
-    if args.no_split:
-        ctx.set_option("split", False)
+    apply_options(ctx, args)
     stream = torch.cuda.current_stream(dev)
 
     sp = torch.from_numpy(wl.splats).to(dev)
@@ -588,12 +650,7 @@ def gpu_arm(args):
         for k in range(2):
             c2 = gsr.Context(local)
             c2.reserve_pairs(reserve)
-            if args.deterministic:
-                c2.set_option("deterministic", True)
-            if args.bwd_per_splat:
-                c2.set_option("bwd_per_splat", True)
-            if args.no_split:
-                c2.set_option("split", False)
+            apply_options(c2, args)
             slots.append({
                 "ctx": c2, "stream": torch.cuda.Stream(dev),
                 "sp": torch.empty_like(sp), "dp": torch.empty_like(dp), "dl": torch.empty_like(dl),
@@ -688,13 +745,13 @@ def gpu_arm(args):
     if args.graph:
         gctx = gsr.Context(local)
         gctx.reserve_pairs(reserve)
-        for flag, name in ((args.deterministic, "deterministic"), (args.bwd_per_splat, "bwd_per_splat")):
-            if flag:
-                gctx.set_option(name, True)
-        if args.no_split:
-            gctx.set_option("split", False)
+        apply_options(gctx, args)
         graph = time_graph(gsr, gctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush, max(args.steps, 20))
         gctx.close()
+    others = None
+    if not args.no_other_configs and args.config == "lego_final" and world == 1:
+        others = {name: time_other_config(gsr, name, args, dev, stream, flush, max(args.steps, 20),
+                                          max(args.warmup, 3)) for name in OTHER_CONFIGS}
     peaks = measured_peaks()
     # Binning against HBM: N·40 B of splats and depths read, each pair's 12-byte
     # key and index written once and read and written by every executed pair
@@ -742,6 +799,8 @@ def gpu_arm(args):
     line["alu_peaks"] = alu
     if graph:
         line["graph"] = graph
+    if others:
+        line["other_configs"] = others
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline and alu:
         cb = cpu_baseline(wl)

@@ -18,7 +18,7 @@ LIB_PATH = os.environ.get("GSR_LIBRARY") or os.path.join(_PKG, "lib", "libgsr.so
 GSR_OK, GSR_ERR_INVALID_ARG, GSR_ERR_CUDA, GSR_ERR_OOM, GSR_ERR_TOO_MANY_PAIRS = range(5)
 GSR_PAIRS_ON_DEVICE = 0xFFFFFFFF
 OPTIONS = {"bwd_warp_skip": 1, "bwd_last_contrib": 2, "warp_cull": 3, "pdl": 4, "fail_next_alloc": 5,
-           "deterministic": 6, "bwd_per_splat": 7, "split": 8}
+           "deterministic": 6, "bwd_per_splat": 7, "split": 8, "split_forward": 9}
 
 
 class GsrError(RuntimeError):

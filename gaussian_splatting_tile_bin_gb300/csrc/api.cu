@@ -123,6 +123,7 @@ void gsr_destroy(gsr_ctx *ctx)
         cudaFree(ctx->det_escale);
         cudaFree(ctx->bnd);
         cudaFree(ctx->bwd_items);
+        cudaFree(ctx->fwd_items);
         if (ctx->host_total) cudaFreeHost(ctx->host_total);
     }
     delete ctx;
@@ -143,6 +144,7 @@ int gsr_set_option(gsr_ctx *ctx, int option, int value)
     case GSR_OPT_DETERMINISTIC: ctx->opt_deterministic = value; return GSR_OK;
     case GSR_OPT_BWD_PER_SPLAT: ctx->opt_bwd_per_splat = value; return GSR_OK;
     case GSR_OPT_SPLIT: ctx->opt_split = value; return GSR_OK;
+    case GSR_OPT_SPLIT_FORWARD: ctx->opt_split_forward = value; return GSR_OK;
     default: return fail(ctx, GSR_ERR_INVALID_ARG, "unknown option " + std::to_string(option));
     }
 }

@@ -38,6 +38,7 @@ struct gsr_ctx {
     int opt_deterministic = 0;
     int opt_bwd_per_splat = 0;
     int opt_split = 1;
+    int opt_split_forward = 1;
     int fail_next_alloc = 0;                    // test hook: the next device allocation fails
     int num_sms = 0;                            // multiprocessors of the device (read by gsr_create)
 
@@ -76,6 +77,15 @@ struct gsr_ctx {
     // long list as its own CTA from that state.
     size_t cap_bnd = 0;
     float4 *bnd = nullptr;                      // [cap_bnd * 256] boundary states (S, T)
+    float4 *bnd_chunk = nullptr;                // after bnd: [cap_bnd * 256] the forward split's chunk states
+    uint32_t *bnd_last = nullptr;               // then [cap_bnd * 256] their last composites
+    // Forward split (raster.cu): chunks past the head of crowded lists.
+    size_t cap_fwd_items = 0;
+    uint2 *fwd_items = nullptr;                 // [cap_fwd_items] (tile, chunk)
+    size_t cap_fwd_tickets = 0;
+    uint32_t *fwd_queue = nullptr;              // after fwd_items: item count, replay ticket, then a
+                                                // ticket per tile ([cap_fwd_tickets]); zero between calls
+    bool fwd_queue_dirty = false;               // a forward failed between queueing and clearing
     size_t cap_items = 0;
     uint2 *bwd_items = nullptr;                 // [cap_items] (tile, segment) work items in launch order
     // The forward whose boundary states bnd holds (the backward splits only

@@ -70,6 +70,27 @@ static_assert(kSplit % kBatch == 0 && kSplit % kBwdBatch == 0, "segments hold wh
 constexpr int kSplitItemsPerSlot = GSR_SPLIT_ITEMS_PER_SLOT;
 // The segment field of the work item of a tile that is not split.
 constexpr uint32_t kWholeList = 0xffffffffu;
+// The shortest head after which the forward splits a list.
+#ifndef GSR_FWD_HEAD_MIN
+#define GSR_FWD_HEAD_MIN 2048
+#endif
+constexpr uint32_t kFwdHeadMin = GSR_FWD_HEAD_MIN;   // a multiple of kSplit
+// CTAs per SM of the chunk and replay grids (each loops over the queued items).
+#ifndef GSR_FWD_CHUNK_CTAS_PER_SM
+#define GSR_FWD_CHUNK_CTAS_PER_SM GSR_FWD_MIN_BLOCKS
+#endif
+#ifndef GSR_FWD_REPLAY_CTAS_PER_SM
+#define GSR_FWD_REPLAY_CTAS_PER_SM (GSR_FWD_MIN_BLOCKS - 1)
+#endif
+// The head as a fraction of a CTA slot's fair share of the frame's pairs.
+#ifndef GSR_FWD_HEAD_SHARE_NUM
+#define GSR_FWD_HEAD_SHARE_NUM 1
+#endif
+#ifndef GSR_FWD_HEAD_SHARE_DEN
+#define GSR_FWD_HEAD_SHARE_DEN 1
+#endif
+constexpr unsigned long long kFwdHeadShareNum = GSR_FWD_HEAD_SHARE_NUM;
+constexpr unsigned long long kFwdHeadShareDen = GSR_FWD_HEAD_SHARE_DEN;
 constexpr unsigned long long kSplitMinSegment = GSR_SPLIT_MIN_SEGMENT;   // a multiple of kSplit
 // ln(255) plus a margin far above the rounding of the exponent path: a lane whose
 // sigma exceeds ln(color_a) + this cannot reach alpha >= 1/255.
@@ -229,12 +250,147 @@ __device__ __forceinline__ float splat_alpha(float sigma, float o, float &e, flo
 
 // --- forward ---------------------------------------------------------------
 
+// Slot of the per-pixel record at position pos of a tile's list, for pos a
+// multiple of kSplit with 0 < pos < the list's length: (list start + pos) /
+// kSplit.  Two such positions of different lists are more than kSplit apart,
+// so their slots differ, and a buffer of pairs / kSplit + 1 slots holds them
+// all.  Boundary states live at their boundary's slot; the forward split's
+// chunk records at the slot of the chunk's start.
+__device__ __forceinline__ size_t bnd_slot(uint32_t list_start, uint32_t pos)
+{
+    return (size_t)((list_start + pos) / kSplit);
+}
+
+// The forward split of crowded tiles.  A list longer than a head of H
+// positions stops there in k_forward; if some pixel of the tile is still
+// compositing, the rest of the list runs as chunks of kSplit positions, each
+// its own CTA, composited from T = 1 (k_forward_chunk), and k_forward_replay
+// then finds each pixel's stop from the chunks' transmittance products,
+// replays the chunk holding it from the true transmittance, and assembles the
+// tile.  H is a CTA slot's fair share of the frame's pairs, rounded up to a
+// multiple of kSplit, and at least kFwdHeadMin: a tile within its share never
+// splits.
+struct FwdSplit {
+    float4 *chunk;             // [slots x 256]: per chunk (colour, transmittance product) from T = 1
+    uint32_t *last;            // [slots x 256]: per chunk its last composite (0: none); at the head's
+                               // end the pixel's stop: kStopInHead, kNoStop or the chunk that holds it
+    uint2 *items;              // (tile, chunk) of every chunk past the head of an unfinished tile
+    uint32_t *queue;           // [0] the items' count, [1] replay CTAs finished (both cleared after)
+    uint32_t *ticket;          // [tiles] items of the tile finished (cleared after each kernel)
+    const uint32_t *pairs_dev; // the frame's pair count on the device, or nullptr
+    uint32_t pairs_host;       // the count when pairs_dev is nullptr
+    uint32_t bound;            // capacity of items
+    int slots;                 // CTA slots of the forward (SMs x resident CTAs)
+};
+
+constexpr uint32_t kStopInHead = 0xffffffffu;   // the pixel stopped within the head
+constexpr uint32_t kNoStop = 0xfffffffeu;       // the pixel composites to the list's end
+
+// The pixel's stop state lives in the chunk-last record of the head's final
+// chunk, which no chunk item uses (chunk items start at the head).
+__device__ __forceinline__ size_t head_state_slot(uint32_t list_start, uint32_t head)
+{
+    return bnd_slot(list_start, head - kSplit);
+}
+
+__device__ __forceinline__ uint32_t forward_head(const FwdSplit &fs)
+{
+    const unsigned long long P = fs.pairs_dev ? (unsigned long long)*fs.pairs_dev : fs.pairs_host;
+    const unsigned long long share = (P * kFwdHeadShareNum + (unsigned long long)fs.slots * kFwdHeadShareDen - 1) /
+                                     ((unsigned long long)fs.slots * kFwdHeadShareDen);
+    const unsigned long long h = max((share + kSplit - 1) / kSplit * kSplit, (unsigned long long)kFwdHeadMin);
+    return (uint32_t)min(h, 0x80000000ull);
+}
+
+// How composite_batch treats the threshold on the transmittance (the forward's
+// own loop, in k_forward, is the rule of kReplay with t_in = 1).
+enum CompositeMode {
+    kChunkProduct,    // a chunk from T = 1 with no stop of its own: T runs down as the chunk's
+                      // transmittance product; a pixel leaves once t_in (a bound on its
+                      // transmittance at the chunk's start) times the product falls below the
+                      // threshold (the pixel then stops at or before that splat), the product
+                      // then including that splat
+    kReplay           // the forward's rule, on the transmittance t_in times the running product:
+                      // a splat whose next transmittance would fall below the threshold is not
+                      // composited and the pixel stops
+};
+
+// Composites the staged splats 0..cnt-1 of sb in order into one pixel (T, C,
+// last = 1 + the position, offset by pos0, of its last composite).
+template <int kMode>
+__device__ __forceinline__ void composite_batch(const StagedBatch &sb, int cnt, uint32_t wbit, int lane, float px,
+                                                float py, float t_in, float &T, float3 &C, uint32_t &last,
+                                                uint32_t pos0, bool &done)
+{
+    for (int c0 = 0; c0 < cnt; c0 += 32) {
+        GSR_CANARY(3);
+        uint32_t m = __ballot_sync(kFull, c0 + lane < cnt && (sb.mask[c0 + lane] & wbit));
+        while (m) {
+            const int j = c0 + __ffs(m) - 1;
+            m &= m - 1;
+            // Straight-line: every lane evaluates the splat and the predicates
+            // take the pixel's skip, stop and composite decisions.
+            const float4 geo = sb.geo[j];
+            const float4 aux = sb.aux[j];
+            const float4 c = sb.rgb[j];
+            float dx, dy;
+            const float sigma = splat_sigma(geo, aux.x, px, py, dx, dy);
+            const bool in_range = !done && sigma >= 0.0f && sigma < aux.z;
+            if (!__any_sync(kFull, in_range)) continue;   // no lane can composite: skip the exponential
+            float e, raw;
+            const float alpha = splat_alpha(in_range ? sigma : 0.0f, aux.y, e, raw);
+            const bool ok = in_range && alpha >= kAlphaMin;
+            const float next_T = __fmul_rn(T, __fsub_rn(1.0f, alpha));
+            const bool stop = ok && __fmul_rn(t_in, next_T) < kTMin;
+            const bool comp = ok && !stop;
+            const float w = __fmul_rn(alpha, T);
+            if (comp) {
+                C.x = __fadd_rn(C.x, __fmul_rn(c.x, w));
+                C.y = __fadd_rn(C.y, __fmul_rn(c.y, w));
+                C.z = __fadd_rn(C.z, __fmul_rn(c.z, w));
+                last = pos0 + (uint32_t)j + 1u;
+            }
+            if (comp || (kMode == kChunkProduct && stop)) T = next_T;
+            done = done || stop;
+        }
+        if (__all_sync(kFull, done)) break;
+    }
+}
+
+// The colour behind every boundary 1..top of a tile's list (slot(m) = the
+// pixel's record at boundary m): each record holds the colour of the segment
+// that ends there and the transmittance there; C enters as the colour of the
+// part after boundary top.  Turns the colours into suffix sums from the back
+// (as the backward accumulates its S) and returns the pixel's colour.  Loads
+// go kGroup records at a time ahead of their stores, so a long list does not
+// wait for one round trip per boundary.
+template <uint32_t kGroup, typename SlotOf>
+__device__ __forceinline__ float3 suffix_colours(float4 *bnd, uint32_t top, float3 C, SlotOf slot)
+{
+    for (uint32_t m = top; m >= 1;) {
+        const uint32_t g = min(m, kGroup);
+        float4 r[kGroup];
+#pragma unroll
+        for (uint32_t i = 0; i < kGroup; ++i)
+            if (i < g) r[i] = __ldcg(bnd + slot(m - i));
+#pragma unroll
+        for (uint32_t i = 0; i < kGroup; ++i) {
+            if (i < g) {
+                bnd[slot(m - i)] = make_float4(C.x, C.y, C.z, r[i].w);
+                C = make_float3(__fadd_rn(C.x, r[i].x), __fadd_rn(C.y, r[i].y), __fadd_rn(C.z, r[i].z));
+            }
+        }
+        m -= g;
+    }
+    return C;
+}
+
 template <bool kCull>
 __global__ void __launch_bounds__(kTilePixels, GSR_FWD_MIN_BLOCKS)
 k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
           const uint2 *__restrict__ ranges, const uint32_t *__restrict__ order, int width, int height,
           int tiles_x, float4 *__restrict__ out_rgbw, float *__restrict__ final_T, uint32_t *__restrict__ last_out,
-          float4 *__restrict__ bnd)
+          float4 *__restrict__ bnd, FwdSplit fs)
 {
     grid_dependency_begin();
     __shared__ StagedBatch sb;
@@ -252,6 +408,9 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
     // only: it is stored and restarted at each boundary, and the pixel's
     // colour is the sum of its segments' colours, formed at the end.
     const bool record = bnd && range.y - range.x > kSplit;
+    // Forward split: a list longer than the head stops after it (the head is
+    // recomputed after the loop rather than kept live through it).
+    const uint32_t end = fs.items ? range.x + min(range.y - range.x, forward_head(fs)) : range.y;
 
     float T = 1.0f;
     float3 C = make_float3(0.0f, 0.0f, 0.0f);
@@ -259,15 +418,13 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
     bool done = !inside;
     uint32_t bounds = 0;   // segment boundaries whose state this CTA recorded
 
-    for (uint32_t bstart = range.x; bstart < range.y; bstart += kBatch) {
+    for (uint32_t bstart = range.x; bstart < end; bstart += kBatch) {
         // Every pixel of the tile has stopped: no later splat can change it.
         if (__syncthreads_count(done) == kTilePixels) break;
         // At every multiple of kSplit positions inside the list: the pixel's
-        // transmittance and the colour of the segment that ends there (slot
-        // (list start + position) / kSplit: boundaries of different tiles are
-        // more than kSplit apart).
+        // transmittance and the colour of the segment that ends there.
         if (record && bstart > range.x && (bstart - range.x) % kSplit == 0) {
-            bnd[(size_t)(bstart / kSplit) * kTilePixels + threadIdx.x] = make_float4(C.x, C.y, C.z, T);
+            bnd[bnd_slot(range.x, bstart - range.x) * kTilePixels + threadIdx.x] = make_float4(C.x, C.y, C.z, T);
             C = make_float3(0.0f, 0.0f, 0.0f);
             ++bounds;
         }
@@ -276,11 +433,11 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
         for (int q = 0; q < GSR_STAGE_PER_THREAD; ++q) {
             const int slot = q * kTilePixels + threadIdx.x;
             const uint32_t pos = bstart + slot;
-            if (pos < range.y) stage_splat<kCull>(sb, slot, splats, __ldg(sorted_idx + pos), x0, y0);
+            if (pos < end) stage_splat<kCull>(sb, slot, splats, __ldg(sorted_idx + pos), x0, y0);
         }
         GSR_CANARY(2);
         __syncthreads();
-        const int cnt = (int)min(range.y - bstart, (uint32_t)kBatch);
+        const int cnt = (int)min(end - bstart, (uint32_t)kBatch);
         if (__all_sync(kFull, done)) continue;
         for (int c0 = 0; c0 < cnt; c0 += 32) {
             GSR_CANARY(3);
@@ -316,22 +473,248 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
             if (__all_sync(kFull, done)) break;
         }
     }
+    // (the tile and its list's end are recomputed rather than kept live
+    // through the loop)
+    const int tile_id = (y0 / kTile) * tiles_x + x0 / kTile;
+    const uint32_t list_end = ranges[tile_id].y;
+    if (end != list_end && __syncthreads_count(done) < kTilePixels) {
+        // Some pixel still composites at the head's end: record its state
+        // there, queue the chunks of the rest of the list, and leave the
+        // outputs to the replay.
+        const uint32_t len = list_end - range.x, head = end - range.x;
+        bnd[bnd_slot(range.x, head) * kTilePixels + threadIdx.x] = make_float4(C.x, C.y, C.z, T);
+        fs.last[head_state_slot(range.x, head) * kTilePixels + threadIdx.x] = done ? kStopInHead : 0u;
+        if (inside) last_out[(size_t)y * width + x] = last;
+        if (threadIdx.x == 0) {
+            const uint32_t first = head / kSplit, nch = (len + kSplit - 1) / kSplit - first;
+            const uint32_t base = atomicAdd(fs.queue, nch);
+            for (uint32_t k = 0; k < nch && base + k < fs.bound; ++k)
+                fs.items[base + k] = make_uint2((uint32_t)tile_id, first + k);
+        }
+        return;
+    }
     // The backward of a segment needs the colour of the splats behind its
     // end: S at a boundary is the sum of the colours of the segments after
     // it, added from the back (as the backward itself accumulates S; a
     // difference of running sums would lose S's digits deep in a long list).
     // The sum over all segments is the pixel's colour.
-    for (uint32_t k = bounds; k >= 1; --k) {
-        float4 &b = bnd[(size_t)((range.x + k * kSplit) / kSplit) * kTilePixels + threadIdx.x];
-        const float4 c = b;   // the colour of the segment before boundary k
-        b = make_float4(C.x, C.y, C.z, c.w);
-        C = make_float3(__fadd_rn(C.x, c.x), __fadd_rn(C.y, c.y), __fadd_rn(C.z, c.z));
-    }
+    if (bounds)
+        C = suffix_colours<4>(bnd, bounds, C, [&](uint32_t m) {
+            return bnd_slot(range.x, m * kSplit) * kTilePixels + threadIdx.x;
+        });
     if (inside) {
         const size_t p = (size_t)y * width + x;
         out_rgbw[p] = make_float4(C.x, C.y, C.z, __fsub_rn(1.0f, T));
         final_T[p] = T;
         last_out[p] = last;
+    }
+}
+
+// Once every chunk of a split tile is composited: per pixel, the
+// transmittance runs from the head's end through the chunk products; the
+// pixel stops inside the first chunk at whose end it falls below the
+// threshold.  Each chunk before that gets its colour (its colour from T = 1
+// times its start transmittance) and the transmittance at its end in the
+// boundary record at its end; the head state records the stop, last_out the
+// last composite before it.  A pixel that never stops gets its final colour
+// part (the last chunk's) and transmittance in out_rgbw and final_T.  The
+// loads do not depend on the stop, so they run ahead of the arithmetic.
+__device__ __forceinline__ void prepare_split_pixel(uint2 range, int tile, uint32_t head, size_t p,
+                                                    float4 *__restrict__ bnd, const float4 *__restrict__ chunk,
+                                                    uint32_t *__restrict__ clast, float4 *__restrict__ out_rgbw,
+                                                    float *__restrict__ final_T, uint32_t *__restrict__ last_out)
+{
+    const uint32_t len = range.y - range.x;
+    const uint32_t first = head / kSplit, nchunks = (len + kSplit - 1) / kSplit;
+    const size_t hs = head_state_slot(range.x, head) * kTilePixels + threadIdx.x;
+    float T = __ldcg(&bnd[bnd_slot(range.x, head) * kTilePixels + threadIdx.x].w);
+    if (__ldcg(clast + hs) == kStopInHead) {
+        out_rgbw[p] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        final_T[p] = T;
+        return;
+    }
+    uint32_t last = __ldcg(last_out + p);
+    uint32_t stop = kNoStop;
+    float3 tail = make_float3(0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+    for (uint32_t k = first; k < nchunks; ++k) {
+        const size_t s = bnd_slot(range.x, k * kSplit) * kTilePixels + threadIdx.x;   // the chunk's start
+        const float4 r = __ldcg(chunk + s);
+        const uint32_t lc = __ldcg(clast + s);
+        if (stop == kNoStop) {
+            const float Tn = __fmul_rn(T, r.w);
+            if (Tn < kTMin) {
+                stop = k;
+            } else {
+                tail = make_float3(__fmul_rn(T, r.x), __fmul_rn(T, r.y), __fmul_rn(T, r.z));
+                if (lc) last = k * kSplit + lc;
+                T = Tn;
+                if (k + 1 < nchunks)   // the boundary at the chunk's end, inside the list
+                    bnd[bnd_slot(range.x, (k + 1) * kSplit) * kTilePixels + threadIdx.x] =
+                        make_float4(tail.x, tail.y, tail.z, T);
+            }
+        }
+    }
+    clast[hs] = stop;
+    last_out[p] = last;
+    if (stop == kNoStop) {
+        out_rgbw[p] = make_float4(tail.x, tail.y, tail.z, 0.0f);
+        final_T[p] = T;
+    }
+}
+
+// The tile's items finished so far, counted after this CTA's writes are
+// published; true for the CTA that completes the tile (which clears the count).
+__device__ __forceinline__ bool tile_item_done(uint32_t *ticket, int tile, uint32_t items_of_tile, int *s_flag)
+{
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t n = atomicAdd(ticket + tile, 1u) + 1u;
+        *s_flag = n == items_of_tile;
+        if (n == items_of_tile) ticket[tile] = 0;
+    }
+    __syncthreads();
+    const bool last = *s_flag != 0;
+    if (last) __threadfence();
+    return last;
+}
+
+// One chunk past the head of each queued item, composited from T = 1: its
+// colour and transmittance product per pixel and its last composite.  The
+// last chunk of a tile to finish prepares the tile's replays.
+template <bool kCull>
+__global__ void __launch_bounds__(kTilePixels, GSR_FWD_MIN_BLOCKS)
+k_forward_chunk(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
+                const uint2 *__restrict__ ranges, int width, int height, int tiles_x,
+                float4 *__restrict__ out_rgbw, float *__restrict__ final_T, uint32_t *__restrict__ last_out,
+                float4 *__restrict__ bnd, FwdSplit fs)
+{
+    grid_dependency_begin();
+    __shared__ StagedBatch sb;
+    __shared__ int s_flag;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t wbit = 1u << warp;
+    const uint32_t n = min(fs.queue[0], fs.bound);
+    const uint32_t head = forward_head(fs), first = head / kSplit;
+    for (uint32_t w = blockIdx.x; w < n; w += gridDim.x) {
+        if (w > blockIdx.x) __syncthreads();   // the previous item's batch is read
+        const uint2 item = fs.items[w];
+        const int tile = (int)item.x;
+        const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
+        const int x = x0 + pixel_x(threadIdx.x);
+        const int y = y0 + pixel_y(threadIdx.x);
+        const bool inside = x < width && y < height;
+        const uint2 range = ranges[tile];
+        const uint32_t s0 = range.x + item.y * kSplit;
+        const int cnt = (int)min(range.y - s0, kSplit);
+#pragma unroll
+        for (int q = 0; q < GSR_STAGE_PER_THREAD; ++q) {
+            const int slot = q * kTilePixels + threadIdx.x;
+            if (slot < cnt) stage_splat<kCull>(sb, slot, splats, __ldg(sorted_idx + s0 + slot), x0, y0);
+        }
+        __syncthreads();
+        // The pixel's transmittance at the head's end bounds it at the chunk's
+        // start (every later factor is at most 1, and rounding is monotonic);
+        // a pixel that stopped within the head has nothing to composite.
+        const float t_head = bnd[bnd_slot(range.x, head) * kTilePixels + threadIdx.x].w;
+        float T = 1.0f;
+        float3 C = make_float3(0.0f, 0.0f, 0.0f);
+        uint32_t last = 0;
+        bool done = !inside || fs.last[head_state_slot(range.x, head) * kTilePixels + threadIdx.x] == kStopInHead;
+        if (!__all_sync(kFull, done))
+            composite_batch<kChunkProduct>(sb, cnt, wbit, lane, (float)x, (float)y, t_head, T, C, last, 0u, done);
+        const size_t s = bnd_slot(range.x, item.y * kSplit) * kTilePixels + threadIdx.x;   // the chunk's start
+        fs.chunk[s] = make_float4(C.x, C.y, C.z, T);
+        fs.last[s] = last;
+        const uint32_t nch = (range.y - range.x + kSplit - 1) / kSplit - first;
+        if (tile_item_done(fs.ticket, tile, nch, &s_flag) && inside)
+            prepare_split_pixel(range, tile, head, (size_t)y * width + x, bnd, fs.chunk, fs.last, out_rgbw,
+                                final_T, last_out);
+    }
+}
+
+// Per queued chunk: the pixels that stop inside it replay it from their
+// transmittance at its start with the forward's rule, on that start times the
+// running product.  The running product repeats the chunk kernel's
+// arithmetic splat for splat and rounding is monotonic, so the tested
+// transmittance never exceeds the start times the chunk's stored product,
+// which fell below the threshold: the replay stops inside the chunk.  The
+// last item of a tile to finish assembles the tile's pixels (the suffix pass
+// of the forward over all the list's boundaries), and the last CTA of the
+// launch clears the queue for the next forward.  No CTA waits on another.
+template <bool kCull>
+__global__ void __launch_bounds__(kTilePixels, GSR_FWD_MIN_BLOCKS - 1)
+k_forward_replay(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
+                 const uint2 *__restrict__ ranges, int width, int height, int tiles_x,
+                 float4 *__restrict__ out_rgbw, float *__restrict__ final_T, uint32_t *__restrict__ last_out,
+                 float4 *__restrict__ bnd, FwdSplit fs)
+{
+    grid_dependency_begin();
+    __shared__ StagedBatch sb;
+    __shared__ int s_flag;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t wbit = 1u << warp;
+    const uint32_t n = min(fs.queue[0], fs.bound);
+    const uint32_t head = forward_head(fs), first = head / kSplit;
+    for (uint32_t w = blockIdx.x; w < n; w += gridDim.x) {
+        if (w > blockIdx.x) __syncthreads();   // the previous item's batch is read
+        const uint2 item = fs.items[w];
+        const int tile = (int)item.x;
+        const uint32_t chunk = item.y;
+        const int x0 = (tile % tiles_x) * kTile, y0 = (tile / tiles_x) * kTile;
+        const int x = x0 + pixel_x(threadIdx.x);
+        const int y = y0 + pixel_y(threadIdx.x);
+        const bool inside = x < width && y < height;
+        const size_t p = (size_t)y * width + x;
+        const uint2 range = ranges[tile];
+        const size_t hs = head_state_slot(range.x, head) * kTilePixels + threadIdx.x;
+        const bool mine = inside && fs.last[hs] == chunk;
+        if (__syncthreads_count(mine) > 0) {
+            // the transmittance at the chunk's start: the record at its start
+            // boundary (the head's own for the first chunk)
+            const float t_in = bnd[bnd_slot(range.x, chunk * kSplit) * kTilePixels + threadIdx.x].w;
+            const uint32_t s0 = range.x + chunk * kSplit;
+            const int cnt = (int)min(range.y - s0, kSplit);
+#pragma unroll
+            for (int q = 0; q < GSR_STAGE_PER_THREAD; ++q) {
+                const int slot = q * kTilePixels + threadIdx.x;
+                if (slot < cnt) stage_splat<kCull>(sb, slot, splats, __ldg(sorted_idx + s0 + slot), x0, y0);
+            }
+            __syncthreads();
+            float P = 1.0f;
+            float3 C = make_float3(0.0f, 0.0f, 0.0f);
+            uint32_t last = 0;
+            bool done = !mine;
+            if (!__all_sync(kFull, done))
+                composite_batch<kReplay>(sb, cnt, wbit, lane, (float)x, (float)y, t_in, P, C, last, 0u, done);
+            if (mine) {
+                out_rgbw[p] = make_float4(__fmul_rn(t_in, C.x), __fmul_rn(t_in, C.y), __fmul_rn(t_in, C.z), 0.0f);
+                final_T[p] = __fmul_rn(t_in, P);
+                if (last) last_out[p] = chunk * kSplit + last;
+            }
+        }
+        const uint32_t nch = (range.y - range.x + kSplit - 1) / kSplit - first;
+        if (tile_item_done(fs.ticket, tile, nch, &s_flag) && inside) {
+            const uint32_t stop = __ldcg(fs.last + hs);
+            const uint32_t nchunks = (range.y - range.x + kSplit - 1) / kSplit;
+            const uint32_t top = stop == kStopInHead ? first : stop == kNoStop ? nchunks - 1 : stop;
+            const float4 o = __ldcg(out_rgbw + p);
+            const float T = __ldcg(final_T + p);
+            const float3 C = suffix_colours<4>(bnd, top, make_float3(o.x, o.y, o.z), [&](uint32_t m) {
+                return bnd_slot(range.x, m * kSplit) * kTilePixels + threadIdx.x;
+            });
+            out_rgbw[p] = make_float4(C.x, C.y, C.z, __fsub_rn(1.0f, T));
+        }
+    }
+    // The last CTA of the launch clears the queue for the next forward.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(fs.queue + 1, 1u) + 1u == gridDim.x) {
+            fs.queue[0] = 0;
+            fs.queue[1] = 0;
+        }
     }
 }
 
@@ -481,7 +864,7 @@ k_backward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted
         if (L > s1) {
             // The pixel composites splats past this segment: start from the
             // state the forward recorded at the segment's end.
-            const float4 b = bnd[(size_t)((range.x + s1) / kSplit) * kTilePixels + threadIdx.x];
+            const float4 b = bnd[bnd_slot(range.x, s1) * kTilePixels + threadIdx.x];
             S = make_float3(b.x, b.y, b.z);
             T = b.w;
             L = s1;
@@ -1068,37 +1451,109 @@ int rasterize_forward(gsr_ctx *ctx, const float *splats, const gsr_bins *bins, f
                       float *final_T, uint32_t *last_contrib, cudaStream_t stream)
 {
     const int num_tiles = bins->tiles_x * bins->tiles_y;
-    // The boundary states the split backward starts its segments from: one
-    // slot of 256 pixels per kSplit pairs, grown with the pairs.
+    // The boundary states the split backward starts its segments from, and
+    // the forward split's chunk states: a slot of 256 pixels per kSplit pairs
+    // and one per tile, grown with the pairs.
     float4 *bnd = nullptr;
+    FwdSplit fs = {};
     ctx->fwd_bnd_valid = false;
+    int rc;
     if (ctx->opt_split) {
         const uint64_t bound = pairs_bound(ctx, bins);
         const size_t slots = (size_t)(bound / kSplit) + 1;
         if (slots > ctx->cap_bnd || !ctx->bnd) {
             if (ctx->bnd) {
                 // queued work of an earlier call may still use the old buffer
-                if (int rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize")) return rc;
+                if ((rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize"))) return rc;
                 cudaFree(ctx->bnd);
             }
-            ctx->bnd = nullptr;
+            ctx->bnd = ctx->bnd_chunk = nullptr;
+            ctx->bnd_last = nullptr;
             ctx->cap_bnd = 0;
-            if (device_alloc(ctx, (void **)&ctx->bnd, slots * kTilePixels * sizeof(float4)) != cudaSuccess) {
+            // boundary states, the forward split's chunk states, their last composites
+            if (device_alloc(ctx, (void **)&ctx->bnd, slots * kTilePixels * (2 * sizeof(float4) + sizeof(uint32_t))) !=
+                cudaSuccess) {
                 cudaGetLastError();
                 ctx->bnd = nullptr;
                 return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the segment boundary states");
             }
+            ctx->bnd_chunk = ctx->bnd + slots * kTilePixels;
+            ctx->bnd_last = reinterpret_cast<uint32_t *>(ctx->bnd_chunk + slots * kTilePixels);
             ctx->cap_bnd = slots;
         }
         bnd = ctx->bnd;
+        if (ctx->opt_split_forward) {
+            // At most one item per chunk past a head: fewer than slots.
+            if (slots > ctx->cap_fwd_items || (size_t)num_tiles > ctx->cap_fwd_tickets || !ctx->fwd_items) {
+                if (ctx->fwd_items) {
+                    if ((rc = cuda_check(ctx, cudaDeviceSynchronize(), "cudaDeviceSynchronize"))) return rc;
+                    cudaFree(ctx->fwd_items);
+                }
+                ctx->fwd_items = nullptr;
+                ctx->fwd_queue = nullptr;
+                ctx->cap_fwd_items = ctx->cap_fwd_tickets = 0;
+                const size_t tickets = std::max<size_t>((size_t)num_tiles, 1);
+                if (device_alloc(ctx, (void **)&ctx->fwd_items, slots * sizeof(uint2) + (2 + tickets) * sizeof(uint32_t)) !=
+                    cudaSuccess) {
+                    cudaGetLastError();
+                    ctx->fwd_items = nullptr;
+                    return fail(ctx, GSR_ERR_OOM, "cudaMalloc failed for the forward split queue");
+                }
+                ctx->fwd_queue = reinterpret_cast<uint32_t *>(ctx->fwd_items + slots);
+                ctx->cap_fwd_items = slots;
+                ctx->cap_fwd_tickets = tickets;
+                ctx->fwd_queue_dirty = true;
+            }
+            if (ctx->fwd_queue_dirty) {
+                if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->fwd_queue, 0, (2 + ctx->cap_fwd_tickets) * sizeof(uint32_t),
+                                                          stream),
+                                     "forward split queue clear")))
+                    return rc;
+                ctx->fwd_queue_dirty = false;
+            }
+            const bool on_device = bins->num_pairs == GSR_PAIRS_ON_DEVICE;
+            fs.chunk = ctx->bnd_chunk;
+            fs.last = ctx->bnd_last;
+            fs.items = ctx->fwd_items;
+            fs.queue = ctx->fwd_queue;
+            fs.ticket = ctx->fwd_queue + 2;
+            fs.pairs_dev = on_device ? bins->num_pairs_dev : nullptr;
+            fs.pairs_host = on_device ? 0u : bins->num_pairs;
+            fs.bound = (uint32_t)std::min<size_t>(ctx->cap_fwd_items, 0xffffffffu);
+            fs.slots = ctx->num_sms * GSR_FWD_MIN_BLOCKS;
+        }
     }
+    const uint2 *ranges = reinterpret_cast<const uint2 *>(bins->tile_ranges);
+    float4 *out4 = reinterpret_cast<float4 *>(out_rgbw);
     auto go = [&](auto kernel) {
-        return launch_kernel(ctx, kernel, dim3(num_tiles), dim3(kTilePixels), stream, splats, bins->sorted_idx,
-                             reinterpret_cast<const uint2 *>(bins->tile_ranges), bins->tile_order, bins->width,
-                             bins->height, bins->tiles_x, reinterpret_cast<float4 *>(out_rgbw), final_T,
-                             last_contrib, bnd);
+        return launch_kernel(ctx, kernel, dim3(num_tiles), dim3(kTilePixels), stream, splats, bins->sorted_idx, ranges,
+                             bins->tile_order, bins->width, bins->height, bins->tiles_x, out4, final_T, last_contrib,
+                             bnd, fs);
     };
-    int rc = cuda_check(ctx, ctx->opt_warp_cull ? go(k_forward<true>) : go(k_forward<false>), "forward launch");
+    rc = cuda_check(ctx, ctx->opt_warp_cull ? go(k_forward<true>) : go(k_forward<false>), "forward launch");
+    if (rc == GSR_OK && fs.items) {
+        // The chunks past the heads, then their replays: grids of one wave of
+        // CTA slots, looping over the queued items.
+        auto wave = [&](int per_sm) {
+            return (int)std::max<size_t>(std::min<size_t>(ctx->cap_fwd_items, (size_t)ctx->num_sms * per_sm), 1);
+        };
+        ctx->fwd_queue_dirty = true;
+        auto split_kernel = [&](auto kernel, int grid) {
+            return launch_kernel(ctx, kernel, dim3(grid), dim3(kTilePixels), stream, splats, bins->sorted_idx, ranges,
+                                 bins->width, bins->height, bins->tiles_x, out4, final_T, last_contrib, bnd, fs);
+        };
+        const int chunk_grid = wave(GSR_FWD_CHUNK_CTAS_PER_SM), replay_grid = wave(GSR_FWD_REPLAY_CTAS_PER_SM);
+        rc = cuda_check(ctx,
+                        ctx->opt_warp_cull ? split_kernel(k_forward_chunk<true>, chunk_grid)
+                                           : split_kernel(k_forward_chunk<false>, chunk_grid),
+                        "forward chunk launch");
+        if (rc == GSR_OK)
+            rc = cuda_check(ctx,
+                            ctx->opt_warp_cull ? split_kernel(k_forward_replay<true>, replay_grid)
+                                               : split_kernel(k_forward_replay<false>, replay_grid),
+                            "forward replay launch");
+        if (rc == GSR_OK) ctx->fwd_queue_dirty = false;
+    }
     if (rc == GSR_OK && bnd) {
         ctx->fwd_bnd_valid = true;
         ctx->fwd_bin_call = ctx->bin_calls;

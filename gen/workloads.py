@@ -150,6 +150,14 @@ def lego_final(seed: int = 3) -> Workload:
     return _lego("lego_final", seed, 409_660, 2.5, 1.0, LEGO_FINAL_TAIL)
 
 
+def lego_pages(seed: int = 3) -> Workload:
+    """lego_final's splat count and opacity mix at the pages' pair density:
+    their final checkpoint binned 969,838 pairs for 407,267 splats (2.38 per
+    splat); smaller footprints, std LN(ln 1.15, 0.6), give 983,065 pairs for
+    409,660 splats (2.40 per splat)."""
+    return _lego("lego_pages", seed, 409_660, 1.15, 0.6, LEGO_FINAL_TAIL)
+
+
 def stress(seed: int = 4) -> Workload:
     rng = np.random.Generator(np.random.PCG64(seed))
     n, w, h = 1_000_000, 1920, 1080
@@ -190,6 +198,7 @@ CONFIGS = {
     "lego_final": lego_final,
     "stress": stress,
     "lego_far": lego_far,
+    "lego_pages": lego_pages,
 }
 
 

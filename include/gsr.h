@@ -120,7 +120,7 @@ enum {
                                      gradients within float rounding; it evaluates every pixel of a
                                      tile for every splat, and ran 24 times slower than the default
                                      backward on an 800x800 image of 409,660 splats. */
-    GSR_OPT_SPLIT = 8             /* default 1.  The forward records each pixel's transmittance and the
+    GSR_OPT_SPLIT = 8,            /* default 1.  The forward records each pixel's transmittance and the
                                      colour behind every 512th position of a tile's list, and the
                                      backward that follows it on the same context (the same bins, the
                                      same final_T and last_contrib buffers) runs a long list as
@@ -128,6 +128,16 @@ enum {
                                      work, each its own CTA from those states, so a crowded tile no
                                      longer runs on alone at the end of the launch.  0: one CTA per
                                      tile (same results within float rounding). */
+    GSR_OPT_SPLIT_FORWARD = 9     /* default 1 (with GSR_OPT_SPLIT).  The forward stops a list longer than
+                                     a head of max(2048, pairs / CTA slots rounded up to a multiple of
+                                     512) positions there; if a pixel of the tile still composites, the
+                                     rest of the list runs as 512-position chunks, each its own CTA
+                                     composited from transmittance 1, and each pixel's stop is found
+                                     from the chunks' transmittance products and replayed from the
+                                     true transmittance in the chunk that holds it.  Transmittance past
+                                     the head rounds as a product of chunk products, so final_T and the
+                                     colour differ from the unsplit forward by float rounding, and a
+                                     stop may move where next_T lies within that rounding of 1e-4. */
 };
 
 typedef struct gsr_ctx gsr_ctx;

@@ -62,3 +62,14 @@ def test_lego_far_crowds_a_few_tiles():
     share = cost.sum() / 608.0
     assert cost.max() > 10.0 * share
     assert len(keys) < len(oracle.bin_splats(near.splats, near.depths, 800, 800)[0])
+
+
+def test_lego_pages_matches_the_pages_pair_density():
+    """lego_final's splats with smaller footprints: about 2.4 pairs per splat,
+    the density of the pages' final checkpoint (969,838 pairs for 407,267
+    splats, "forward/adam audit" section 3, staging read)."""
+    wl = gen.make("lego_pages")
+    assert (wl.width, wl.height, wl.n) == (800, 800, 409_660)
+    keys, idx, ranges = oracle.bin_splats(wl.splats, wl.depths, wl.width, wl.height)
+    assert 2.3 <= len(keys) / wl.n <= 2.5
+    assert abs(len(keys) / wl.n - 969_838 / 407_267) < 0.05
