@@ -109,8 +109,8 @@ def parse_args(argv=None):
                    help="also time the whole step (binning, forward, backward) replayed as one captured CUDA graph")
     p.add_argument("--no-split", action="store_true",
                    help="run forward and backward as one CTA per tile (no chunks or segments of long lists)")
-    p.add_argument("--no-split-forward", action="store_true",
-                   help="run the forward as one CTA per tile (the backward still splits long lists)")
+    p.add_argument("--split-forward", action="store_true",
+                   help="split the forward's crowded lists too (GSR_OPT_SPLIT_FORWARD)")
     p.add_argument("--reserved", action="store_true",
                    help="time the step with the binning of a context that has a reservation (no host read-back) "
                         "instead of the default binning, which reads the pair count back every call")
@@ -290,9 +290,9 @@ def long_lists_label(args) -> str:
     if args.no_split:
         return "one CTA per tile"
     bwd = "backward: segments of tiles above a CTA slot's share of the work"
-    if args.no_split_forward:
-        return "forward: one CTA per tile; " + bwd
-    return "forward: 512-position chunks past a head of max(2048, pairs / CTA slots); " + bwd
+    if args.split_forward:
+        return "forward: 512-position chunks past a head of max(2048, pairs / CTA slots); " + bwd
+    return "forward: one CTA per tile; " + bwd
 
 
 def apply_options(c, args):
@@ -302,8 +302,8 @@ def apply_options(c, args):
             c.set_option(name, True)
     if args.no_split:
         c.set_option("split", False)
-    if args.no_split_forward:
-        c.set_option("split_forward", False)
+    if args.split_forward:
+        c.set_option("split_forward", True)
 
 
 def bench_config(wl, args, pairs, world):
@@ -513,15 +513,18 @@ def time_graph(gsr, ctx, wl, sp, dp, dl, out, fT, last, grad, dev, stream, flush
 
 
 # Frames timed beside the headline one (same step, same L2 flush): the pages'
-# pair density, and a close-up whose crowded tiles the split serves.
-OTHER_CONFIGS = ("lego_pages", "lego_far")
+# pair density, and a close-up whose crowded tiles the split serves, with and
+# without the forward's split.
+OTHER_CONFIGS = (("lego_pages", {}), ("lego_far", {}), ("lego_far", {"split_forward": True}))
 
 
-def time_other_config(gsr, name, args, dev, stream, flush, steps, warmup):
+def time_other_config(gsr, name, options, args, dev, stream, flush, steps, warmup):
     import torch
     wl = gen.make(name)
     ctx = gsr.Context(dev.index or 0)
     apply_options(ctx, args)
+    for opt, value in options.items():
+        ctx.set_option(opt, value)
     sp, dp, dl = (torch.from_numpy(a).to(dev) for a in (wl.splats, wl.depths, wl.dl_dout))
     npx = wl.width * wl.height
     out = torch.empty((npx, 4), dtype=torch.float32, device=dev)
@@ -549,7 +552,7 @@ def time_other_config(gsr, name, args, dev, stream, flush, steps, warmup):
     t = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(3)] + [e[0].elapsed_time(e[3])] for e in evs])
     pairs = ctx.num_pairs()
     ctx.close()
-    return {"workload": workload_label(wl), "splats": wl.n, "pairs": int(pairs),
+    return {"workload": workload_label(wl), "options": options, "splats": wl.n, "pairs": int(pairs),
             "pairs_per_splat": pairs / wl.n, "steps": steps, "ms_per_step": float(t[:, 3].mean()),
             "stages_ms": {"bin": float(t[:, 0].mean()), "forward": float(t[:, 1].mean()),
                           "backward": float(t[:, 2].mean())}}
@@ -750,8 +753,9 @@ def gpu_arm(args):
         gctx.close()
     others = None
     if not args.no_other_configs and args.config == "lego_final" and world == 1:
-        others = {name: time_other_config(gsr, name, args, dev, stream, flush, max(args.steps, 20),
-                                          max(args.warmup, 3)) for name in OTHER_CONFIGS}
+        others = {name + "".join("+" + k for k in opts): time_other_config(
+                      gsr, name, opts, args, dev, stream, flush, max(args.steps, 20), max(args.warmup, 3))
+                  for name, opts in OTHER_CONFIGS}
     peaks = measured_peaks()
     # Binning against HBM: N·40 B of splats and depths read, each pair's 12-byte
     # key and index written once and read and written by every executed pair

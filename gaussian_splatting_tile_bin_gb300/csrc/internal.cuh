@@ -38,7 +38,7 @@ struct gsr_ctx {
     int opt_deterministic = 0;
     int opt_bwd_per_splat = 0;
     int opt_split = 1;
-    int opt_split_forward = 1;
+    int opt_split_forward = 0;
     int fail_next_alloc = 0;                    // test hook: the next device allocation fails
     int num_sms = 0;                            // multiprocessors of the device (read by gsr_create)
 

@@ -385,7 +385,9 @@ __device__ __forceinline__ float3 suffix_colours(float4 *bnd, uint32_t top, floa
     return C;
 }
 
-template <bool kCull>
+// kCut: lists longer than the forward split's head stop there (fs is used);
+// otherwise every list runs to its end and fs is ignored.
+template <bool kCull, bool kCut>
 __global__ void __launch_bounds__(kTilePixels, GSR_FWD_MIN_BLOCKS)
 k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_idx,
           const uint2 *__restrict__ ranges, const uint32_t *__restrict__ order, int width, int height,
@@ -408,9 +410,8 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
     // only: it is stored and restarted at each boundary, and the pixel's
     // colour is the sum of its segments' colours, formed at the end.
     const bool record = bnd && range.y - range.x > kSplit;
-    // Forward split: a list longer than the head stops after it (the head is
-    // recomputed after the loop rather than kept live through it).
-    const uint32_t end = fs.items ? range.x + min(range.y - range.x, forward_head(fs)) : range.y;
+    // Forward split: a list longer than the head stops after it.
+    const uint32_t end = kCut ? range.x + min(range.y - range.x, forward_head(fs)) : range.y;
 
     float T = 1.0f;
     float3 C = make_float3(0.0f, 0.0f, 0.0f);
@@ -473,35 +474,39 @@ k_forward(const float *__restrict__ splats, const uint32_t *__restrict__ sorted_
             if (__all_sync(kFull, done)) break;
         }
     }
-    // (the tile and its list's end are recomputed rather than kept live
-    // through the loop)
-    const int tile_id = (y0 / kTile) * tiles_x + x0 / kTile;
-    const uint32_t list_end = ranges[tile_id].y;
-    if (end != list_end && __syncthreads_count(done) < kTilePixels) {
-        // Some pixel still composites at the head's end: record its state
-        // there, queue the chunks of the rest of the list, and leave the
-        // outputs to the replay.
-        const uint32_t len = list_end - range.x, head = end - range.x;
-        bnd[bnd_slot(range.x, head) * kTilePixels + threadIdx.x] = make_float4(C.x, C.y, C.z, T);
-        fs.last[head_state_slot(range.x, head) * kTilePixels + threadIdx.x] = done ? kStopInHead : 0u;
-        if (inside) last_out[(size_t)y * width + x] = last;
-        if (threadIdx.x == 0) {
-            const uint32_t first = head / kSplit, nch = (len + kSplit - 1) / kSplit - first;
-            const uint32_t base = atomicAdd(fs.queue, nch);
-            for (uint32_t k = 0; k < nch && base + k < fs.bound; ++k)
-                fs.items[base + k] = make_uint2((uint32_t)tile_id, first + k);
+    if constexpr (kCut) {
+        // (the tile and its list's end are recomputed rather than kept live
+        // through the loop)
+        const int tile_id = (y0 / kTile) * tiles_x + x0 / kTile;
+        const uint32_t list_end = ranges[tile_id].y;
+        if (end != list_end && __syncthreads_count(done) < kTilePixels) {
+            // Some pixel still composites at the head's end: record its state
+            // there, queue the chunks of the rest of the list, and leave the
+            // outputs to the replay.
+            const uint32_t len = list_end - range.x, head = end - range.x;
+            bnd[bnd_slot(range.x, head) * kTilePixels + threadIdx.x] = make_float4(C.x, C.y, C.z, T);
+            fs.last[head_state_slot(range.x, head) * kTilePixels + threadIdx.x] = done ? kStopInHead : 0u;
+            if (inside) last_out[(size_t)y * width + x] = last;
+            if (threadIdx.x == 0) {
+                const uint32_t first = head / kSplit, nch = (len + kSplit - 1) / kSplit - first;
+                const uint32_t base = atomicAdd(fs.queue, nch);
+                for (uint32_t k = 0; k < nch && base + k < fs.bound; ++k)
+                    fs.items[base + k] = make_uint2((uint32_t)tile_id, first + k);
+            }
+            return;
         }
-        return;
     }
     // The backward of a segment needs the colour of the splats behind its
     // end: S at a boundary is the sum of the colours of the segments after
     // it, added from the back (as the backward itself accumulates S; a
     // difference of running sums would lose S's digits deep in a long list).
     // The sum over all segments is the pixel's colour.
-    if (bounds)
-        C = suffix_colours<4>(bnd, bounds, C, [&](uint32_t m) {
-            return bnd_slot(range.x, m * kSplit) * kTilePixels + threadIdx.x;
-        });
+    for (uint32_t k = bounds; k >= 1; --k) {
+        float4 &b = bnd[bnd_slot(range.x, k * kSplit) * kTilePixels + threadIdx.x];
+        const float4 c = b;   // the colour of the segment before boundary k
+        b = make_float4(C.x, C.y, C.z, c.w);
+        C = make_float3(__fadd_rn(C.x, c.x), __fadd_rn(C.y, c.y), __fadd_rn(C.z, c.z));
+    }
     if (inside) {
         const size_t p = (size_t)y * width + x;
         out_rgbw[p] = make_float4(C.x, C.y, C.z, __fsub_rn(1.0f, T));
@@ -1530,7 +1535,11 @@ int rasterize_forward(gsr_ctx *ctx, const float *splats, const gsr_bins *bins, f
                              bins->tile_order, bins->width, bins->height, bins->tiles_x, out4, final_T, last_contrib,
                              bnd, fs);
     };
-    rc = cuda_check(ctx, ctx->opt_warp_cull ? go(k_forward<true>) : go(k_forward<false>), "forward launch");
+    const bool cut = fs.items != nullptr;
+    rc = cuda_check(ctx,
+                    ctx->opt_warp_cull ? (cut ? go(k_forward<true, true>) : go(k_forward<true, false>))
+                                       : (cut ? go(k_forward<false, true>) : go(k_forward<false, false>)),
+                    "forward launch");
     if (rc == GSR_OK && fs.items) {
         // The chunks past the heads, then their replays: grids of one wave of
         // CTA slots, looping over the queued items.

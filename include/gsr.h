@@ -128,7 +128,7 @@ enum {
                                      work, each its own CTA from those states, so a crowded tile no
                                      longer runs on alone at the end of the launch.  0: one CTA per
                                      tile (same results within float rounding). */
-    GSR_OPT_SPLIT_FORWARD = 9     /* default 1 (with GSR_OPT_SPLIT).  The forward stops a list longer than
+    GSR_OPT_SPLIT_FORWARD = 9     /* default 0; takes effect with GSR_OPT_SPLIT.  1: the forward stops a list longer than
                                      a head of max(2048, pairs / CTA slots rounded up to a multiple of
                                      512) positions there; if a pixel of the tile still composites, the
                                      rest of the list runs as 512-position chunks, each its own CTA
@@ -137,7 +137,10 @@ enum {
                                      true transmittance in the chunk that holds it.  Transmittance past
                                      the head rounds as a product of chunk products, so final_T and the
                                      colour differ from the unsplit forward by float rounding, and a
-                                     stop may move where next_T lies within that rounding of 1e-4. */
+                                     stop may move where next_T lies within that rounding of 1e-4.  It
+                                     pays on frames with a few crowded tiles (an 800x800 close-up whose
+                                     longest list holds 33,000 pairs: forward 0.30 -> 0.20 ms) and costs
+                                     about 10 us on an 800x800 frame without them. */
 };
 
 typedef struct gsr_ctx gsr_ctx;

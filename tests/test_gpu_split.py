@@ -1,4 +1,5 @@
-"""The split of crowded tiles (GSR_OPT_SPLIT, GSR_OPT_SPLIT_FORWARD).
+"""The split of crowded tiles (GSR_OPT_SPLIT, on by default, and
+GSR_OPT_SPLIT_FORWARD, off by default).
 
 Forward: a list longer than a head of max(2048, pairs / CTA slots) positions
 stops there; the rest of an unfinished tile runs as 512-position chunks
@@ -49,14 +50,17 @@ def test_crowded_tiles_parity(gsr, ctx, distance):
     wl = gen.lego_far(distance=distance)
     o = run_oracle(wl)
     assert int(np.max(o["ranges"][:, 1] - o["ranges"][:, 0])) > 8 * 512      # lists that split
-    for det in (False, True):
+    for det, fwd in ((False, False), (True, False), (False, True), (True, True)):
         ctx.set_option("deterministic", det)
+        ctx.set_option("split_forward", fwd)
         g = run_gpu(gsr, ctx, wl)
         check_bins(g, o)
         fs = check_forward(g, o)
         bs = check_backward(g, o)
-        record_stats(f"lego_far x{distance:g}{' det' if det else ''}", forward=fs, backward=bs)
+        record_stats(f"lego_far x{distance:g}{' det' if det else ''}{' split fwd' if fwd else ''}",
+                     forward=fs, backward=bs)
     ctx.set_option("deterministic", False)
+    ctx.set_option("split_forward", False)
 
 
 def crowded_fixture(seed=11, n=6000, width=40, height=20):
@@ -82,14 +86,18 @@ def test_forward_split_fixture_parity(gsr, ctx):
     T, last = o["fwd"]["final_T"], o["fwd"]["last"]
     stopped = T < 3e-4
     assert np.any(stopped & (last < 2048)) and np.any(stopped & (last > 2048)) and np.any(~stopped)
-    for det in (False, True):
-        ctx.set_option("deterministic", det)
-        g = run_gpu(gsr, ctx, wl)
-        check_bins(g, o)
-        fs = check_forward(g, o)
-        bs = check_backward(g, o)
-        record_stats(f"crowded fixture{' det' if det else ''}", forward=fs, backward=bs)
-    ctx.set_option("deterministic", False)
+    ctx.set_option("split_forward", True)
+    try:
+        for det in (False, True):
+            ctx.set_option("deterministic", det)
+            g = run_gpu(gsr, ctx, wl)
+            check_bins(g, o)
+            fs = check_forward(g, o)
+            bs = check_backward(g, o)
+            record_stats(f"crowded fixture{' det' if det else ''}", forward=fs, backward=bs)
+    finally:
+        ctx.set_option("deterministic", False)
+        ctx.set_option("split_forward", False)
 
 
 def _runs(gsr, ctx, wl, settings):
@@ -99,7 +107,7 @@ def _runs(gsr, ctx, wl, settings):
         ctx.set_option("split_forward", fwd)
         runs[name] = run_gpu(gsr, ctx, wl)
     ctx.set_option("split", True)
-    ctx.set_option("split_forward", True)
+    ctx.set_option("split_forward", False)
     return runs
 
 
@@ -149,6 +157,7 @@ def test_repeated_forwards_give_the_same_bits(gsr, ctx):
     of split and unsplit frames in any order give the same bits."""
     far, early = gen.lego_far(), gen.lego_early()
     ctx.set_option("deterministic", True)
+    ctx.set_option("split_forward", True)
     try:
         first = run_gpu(gsr, ctx, far)
         run_gpu(gsr, ctx, early, backward=False)
@@ -156,6 +165,7 @@ def test_repeated_forwards_give_the_same_bits(gsr, ctx):
         again2 = run_gpu(gsr, ctx, far)
     finally:
         ctx.set_option("deterministic", False)
+        ctx.set_option("split_forward", False)
     for r in (again, again2):
         _same_bits(r, first, ("out", "final_T", "last", "grad"))
 

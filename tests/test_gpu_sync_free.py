@@ -131,13 +131,16 @@ def test_read_back_and_reserved_modes_give_the_same_bits(gsr):
         b.close()
 
 
-def test_whole_step_replays_from_one_graph(gsr):
+@pytest.mark.parametrize("name,split_forward", [("lego_early", False), ("lego_far", True)])
+def test_whole_step_replays_from_one_graph(gsr, name, split_forward):
     """Binning, forward and backward captured in one CUDA graph: the replays
-    give the direct calls' bits, and pick up new inputs written in place."""
-    wl = gen.lego_early()
-    ctx = _sync_free_ctx(gsr, 3_000_000)
+    give the direct calls' bits, and pick up new inputs written in place
+    (with the forward split too: its chunk queue lives on the device)."""
+    wl = gen.make(name)
+    ctx = _sync_free_ctx(gsr, 3_000_000)    # lego_early emits 2,320,479 pairs, lego_far 876,855
     try:
         ctx.set_option("deterministic", True)
+        ctx.set_option("split_forward", split_forward)
         sp, dp, dl = to_dev(wl.splats), to_dev(wl.depths), to_dev(wl.dl_dout)
         npx = wl.width * wl.height
         out = torch.empty((npx, 4), dtype=torch.float32, device="cuda:0")
