@@ -60,16 +60,16 @@ RASTER_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/raster.cu",
                   "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
 PROJECT_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/project.cu",
                    "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
-RASTER_SHA256 = "a3f1a5eca56b101f6534dd8df3a16432326d3a51b635af0190f52b5ceaa1ebaf"
-PROJECT_SHA256 = "5f49acc944f050d6510d0e9b291b1aa2b607e9cecd5cd46094bc8b7b3000ab42"
+RASTER_SHA256 = "86347478a6507a5081a51356e754c123656472b868e7e22edc5227bd571068ec"
+PROJECT_SHA256 = "175bb9e55f6c1b3360e8b68de16750f83fbafe5efbb2c04b03160fcf883f5192"
 NCU_TRAFFIC = {
-    "forward": {"bytes": 22_276_864 + 5_376, "workload": "lego_final", "sources": RASTER_SOURCES,
+    "forward": {"bytes": 22_278_144 + 120_576, "workload": "lego_final", "sources": RASTER_SOURCES,
                 "sha256": RASTER_SHA256},
-    "backward": {"bytes": 50_592_000 + 114_432, "workload": "lego_final", "sources": RASTER_SOURCES,
+    "backward": {"bytes": 49_740_032 + 68_352, "workload": "lego_final", "sources": RASTER_SOURCES,
                  "sha256": RASTER_SHA256},
-    "project_forward": {"bytes": 22_961_152 + 0, "workload": "lego_scene", "sources": PROJECT_SOURCES,
+    "project_forward": {"bytes": 22_960_128 + 1_024, "workload": "lego_scene", "sources": PROJECT_SOURCES,
                         "sha256": PROJECT_SHA256},
-    "project_backward": {"bytes": 37_724_416 + 272_384, "workload": "lego_scene", "sources": PROJECT_SOURCES,
+    "project_backward": {"bytes": 37_718_528 + 136_960, "workload": "lego_scene", "sources": PROJECT_SOURCES,
                          "sha256": PROJECT_SHA256},
 }
 
@@ -291,7 +291,7 @@ def long_lists_label(args) -> str:
         return "one CTA per tile"
     bwd = "backward: segments of tiles above a CTA slot's share of the work"
     if args.split_forward:
-        return "forward: 512-position chunks past a head of max(2048, pairs / CTA slots); " + bwd
+        return "forward: 512-position chunks past a head of max(1024, half the pairs per CTA slot); " + bwd
     return "forward: one CTA per tile; " + bwd
 
 

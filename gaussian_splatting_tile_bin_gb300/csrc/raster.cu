@@ -72,9 +72,11 @@ constexpr int kSplitItemsPerSlot = GSR_SPLIT_ITEMS_PER_SLOT;
 constexpr uint32_t kWholeList = 0xffffffffu;
 // The shortest head after which the forward splits a list.
 #ifndef GSR_FWD_HEAD_MIN
-#define GSR_FWD_HEAD_MIN 2048
+#define GSR_FWD_HEAD_MIN 1024
 #endif
 constexpr uint32_t kFwdHeadMin = GSR_FWD_HEAD_MIN;   // a multiple of kSplit
+// (the head's last chunk, which starts inside the list, holds the pixel's stop state)
+static_assert(kFwdHeadMin % kSplit == 0 && kFwdHeadMin >= 2 * kSplit, "the head holds two chunks at least");
 // CTAs per SM of the chunk and replay grids (each loops over the queued items).
 #ifndef GSR_FWD_CHUNK_CTAS_PER_SM
 #define GSR_FWD_CHUNK_CTAS_PER_SM GSR_FWD_MIN_BLOCKS
@@ -87,7 +89,7 @@ constexpr uint32_t kFwdHeadMin = GSR_FWD_HEAD_MIN;   // a multiple of kSplit
 #define GSR_FWD_HEAD_SHARE_NUM 1
 #endif
 #ifndef GSR_FWD_HEAD_SHARE_DEN
-#define GSR_FWD_HEAD_SHARE_DEN 1
+#define GSR_FWD_HEAD_SHARE_DEN 2
 #endif
 constexpr unsigned long long kFwdHeadShareNum = GSR_FWD_HEAD_SHARE_NUM;
 constexpr unsigned long long kFwdHeadShareDen = GSR_FWD_HEAD_SHARE_DEN;
@@ -267,9 +269,8 @@ __device__ __forceinline__ size_t bnd_slot(uint32_t list_start, uint32_t pos)
 // its own CTA, composited from T = 1 (k_forward_chunk), and k_forward_replay
 // then finds each pixel's stop from the chunks' transmittance products,
 // replays the chunk holding it from the true transmittance, and assembles the
-// tile.  H is a CTA slot's fair share of the frame's pairs, rounded up to a
-// multiple of kSplit, and at least kFwdHeadMin: a tile within its share never
-// splits.
+// tile.  H is half a CTA slot's fair share of the frame's pairs, rounded up
+// to a multiple of kSplit, and at least kFwdHeadMin.
 struct FwdSplit {
     float4 *chunk;             // [slots x 256]: per chunk (colour, transmittance product) from T = 1
     uint32_t *last;            // [slots x 256]: per chunk its last composite (0: none); at the head's
