@@ -60,7 +60,7 @@ RASTER_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/raster.cu",
                   "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
 PROJECT_SOURCES = ("gaussian_splatting_tile_bin_gb300/csrc/project.cu",
                    "gaussian_splatting_tile_bin_gb300/csrc/internal.cuh")
-RASTER_SHA256 = "86347478a6507a5081a51356e754c123656472b868e7e22edc5227bd571068ec"
+RASTER_SHA256 = "01ed77677abb61440974f4d52d7aa690e31651757e8d5622f336866995f58d85"
 PROJECT_SHA256 = "175bb9e55f6c1b3360e8b68de16750f83fbafe5efbb2c04b03160fcf883f5192"
 NCU_TRAFFIC = {
     "forward": {"bytes": 22_278_144 + 120_576, "workload": "lego_final", "sources": RASTER_SOURCES,
