@@ -350,7 +350,7 @@ __device__ __forceinline__ const uint32_t *depth_sorted(const DepthBuffers &b, c
 {
     if (!depth_and_or) return b.v[1];
     int executed;
-    field_pass(__ldcg(depth_and_or) ^ __ldcg(depth_and_or + 1), 0, 32, -1, &executed);
+    field_pass(__ldg(depth_and_or) ^ __ldg(depth_and_or + 1), 0, 32, -1, &executed);
     return executed ? b.v[1] : b.v[0];
 }
 
@@ -363,7 +363,7 @@ k_sorted_sums(DepthBuffers dbufs, const uint2 *__restrict__ rects, int n, int m_
     grid_dependency_begin();
     __shared__ unsigned long long ws[8];
     // the emitting count: m_host when the host knows it, else the device's
-    const int m = m_host >= 0 ? m_host : (int)min(__ldcg(scalars + kScalarEmitting), (unsigned long long)n);
+    const int m = m_host >= 0 ? m_host : (int)min(__ldg(scalars + kScalarEmitting), (unsigned long long)n);
     const uint32_t *__restrict__ sorted_idx = depth_sorted(dbufs, depth_and_or);
     const int k = blockIdx.x * kBinBlock + threadIdx.x;
     const uint32_t c = k < m ? rect_count(rects[sorted_idx[k]]) : 0u;
@@ -394,7 +394,7 @@ k_emit(const uint2 *__restrict__ rects, const float *__restrict__ depths, DepthB
        const unsigned long long *__restrict__ depth_and_or)
 {
     grid_dependency_begin();
-    const int m = m_host >= 0 ? m_host : (int)min(__ldcg(scalars + kScalarEmitting), (unsigned long long)n);
+    const int m = m_host >= 0 ? m_host : (int)min(__ldg(scalars + kScalarEmitting), (unsigned long long)n);
     const uint32_t *__restrict__ sorted_idx = depth_sorted(dbufs, depth_and_or);
     if ((int)(blockIdx.x * kBinBlock) >= m) {
         // no splat of this block emits; its part of the keys' AND / OR is empty
@@ -554,9 +554,13 @@ struct PassSpec {
     int stride;                      // radix tiles per digit row of counts / offsets
 };
 
+// Counts and plans that earlier kernels left on the device are read through
+// the read-only path (__ldg): every thread reads the same word, and the cache
+// serves a warp's and the SM's requests at once, where L2-only loads would
+// send every warp's request to the same L2 slice.
 __device__ __forceinline__ uint32_t pass_num(const PassSpec &p)
 {
-    return p.num ? (uint32_t)min(__ldcg(p.num), (unsigned long long)p.num_max) : p.num_max;
+    return p.num ? (uint32_t)min(__ldg(p.num), (unsigned long long)p.num_max) : p.num_max;
 }
 
 // Geometry of pass `field` of `executed` varying digits, whose position among
@@ -578,7 +582,7 @@ __device__ __forceinline__ bool pass_geom(const PassSpec &p, PassGeom &g)
         return true;
     }
     int executed;
-    const int j = field_pass(p.and_or[0] ^ p.and_or[1], p.key_lo, p.key_hi, p.field, &executed);
+    const int j = field_pass(__ldg(p.and_or) ^ __ldg(p.and_or + 1), p.key_lo, p.key_hi, p.field, &executed);
     if (j < 0) return false;
     g = plan_geom(p.key_lo, p.key_hi, p.field, j, executed);
     return true;
@@ -788,7 +792,7 @@ k_extract_ranges(PairBuffers bufs, const unsigned long long *__restrict__ num_de
                  uint32_t *__restrict__ ranges, const unsigned long long *__restrict__ and_or, int key_lo, int key_hi)
 {
     grid_dependency_begin();
-    const uint32_t num = num_dev ? (uint32_t)min(__ldcg(num_dev), (unsigned long long)num_max) : num_max;
+    const uint32_t num = num_dev ? (uint32_t)min(__ldg(num_dev), (unsigned long long)num_max) : num_max;
     // A tile sort that ran no pass (every key shares its tile bits) left the
     // emitted order, already sorted, in buffer 0: copy it to the result.
     const uint64_t *__restrict__ keys = bufs.k[1];
