@@ -329,11 +329,14 @@ k_count(const float *__restrict__ splats, const float *__restrict__ depths, int 
 __global__ void __launch_bounds__(kBinBlock)
 k_compact(const uint2 *__restrict__ rects, const float *__restrict__ depths, int n,
           const unsigned long long *__restrict__ blk_emit_offs, uint32_t *__restrict__ dkeys,
-          uint32_t *__restrict__ didx)
+          uint32_t *__restrict__ didx, uint32_t *__restrict__ ranges, uint32_t range_words)
 {
     grid_dependency_begin();
     __shared__ uint32_t ws[8];
     const int i = blockIdx.x * kBinBlock + threadIdx.x;
+    // Every tile's range starts empty ({0, 0}); the extraction writes the
+    // tiles that get pairs.
+    for (uint32_t w = (uint32_t)i; w < range_words; w += gridDim.x * kBinBlock) ranges[w] = 0u;
     const bool emits = i < n && rect_count(rects[i]) > 0;
     uint32_t total;
     const uint32_t excl = block_exclusive_scan_256<uint32_t>(emits ? 1u : 0u, ws, &total);
@@ -1138,14 +1141,16 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
             return rc;
     }
 
-    if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->ranges, 0, num_tiles * 2 * sizeof(uint32_t), stream),
-                         "cudaMemsetAsync")))
-        return rc;
-
-    if (num_max > 0 && m_max > 0) {
-        // 3. depth sort of the emitting splats.
+    if (num_max == 0 || m_max == 0) {
+        // nothing to sort: every tile's range is empty
+        if ((rc = cuda_check(ctx, cudaMemsetAsync(ctx->ranges, 0, num_tiles * 2 * sizeof(uint32_t), stream),
+                             "cudaMemsetAsync")))
+            return rc;
+    } else {
+        // 3. depth sort of the emitting splats (k_compact also empties every
+        //    tile's range).
         GSR_LAUNCH(ctx, k_compact, dim3(nblk), dim3(kBinBlock), stream, ctx->rects, depths, n, blk_emit,
-                   ctx->depth.k[0], ctx->depth.v[0]);
+                   ctx->depth.k[0], ctx->depth.v[0], ctx->ranges, (uint32_t)(num_tiles * 2));
         if ((rc = radix_sort<uint32_t, kRtItemsDepth>(ctx, ctx->depth,
                                                       sync_free ? ctx->scalars + kScalarEmitting : nullptr, m_max, 0, 32,
                                                       ctx->scalars + kScalarDepthAnd,

@@ -123,26 +123,26 @@ enum {
     GSR_OPT_SPLIT = 8,            /* default 1.  The forward records each pixel's transmittance and the
                                      colour behind every 512th position of a tile's list, and the
                                      backward that follows it on the same context (the same bins, the
-                                     same final_T and last_contrib buffers) runs a long list as
-                                     segments of a multiple of 512 positions, sized from the frame's
-                                     work, each its own CTA from those states, so a crowded tile no
-                                     longer runs on alone at the end of the launch.  0: one CTA per
-                                     tile (same results within float rounding). */
-    GSR_OPT_SPLIT_FORWARD = 9     /* default 0; takes effect with GSR_OPT_SPLIT.  1: the forward stops a list longer than
-                                     a head of max(1024, half the pairs per CTA slot rounded up to a
-                                     multiple of 512) positions there; if a pixel of the tile still composites, the
-                                     rest of the list runs as 512-position chunks, each its own CTA
-                                     composited from transmittance 1, and each pixel's stop is found
-                                     from the chunks' transmittance products and replayed from the
-                                     true transmittance in the chunk that holds it.  Transmittance past
-                                     the head rounds as a product of chunk products, so final_T and the
-                                     colour differ from the unsplit forward by float rounding, and a
-                                     stop may move where next_T lies within that rounding of 1e-4.  It
-                                     pays on frames with a few crowded tiles (an 800x800 close-up whose
-                                     longest list holds 33,000 pairs: forward 0.25 -> 0.18 ms) and costs
-                                     on frames without them, where the chunks past the heads are mostly
-                                     behind every pixel's stop (800x800, 409,660 splats, 3.7M pairs:
-                                     0.118 -> 0.148 ms). */
+                                     same final_T and last_contrib buffers) runs each tile whose work
+                                     exceeds a CTA slot's share of the frame's work as segments of a
+                                     multiple of 512 positions, each its own CTA from those states, so a
+                                     crowded tile no longer runs on alone at the end of the launch.
+                                     0: one CTA per tile (same results within float rounding). */
+    GSR_OPT_SPLIT_FORWARD = 9     /* default 0; takes effect with GSR_OPT_SPLIT.  1: the forward stops
+                                     a list longer than a head of max(1024, half the pairs per CTA slot,
+                                     rounded up to a multiple of 512) positions there; if a pixel of the
+                                     tile still composites, the rest of the list runs as 512-position
+                                     chunks, each its own CTA composited from transmittance 1, and each
+                                     pixel's stop is found from the chunks' transmittance products and
+                                     replayed from the true transmittance in the chunk that holds it.
+                                     Transmittance past the head rounds as a product of chunk products,
+                                     so final_T and the colour differ from the unsplit forward by float
+                                     rounding, and a stop may move where next_T lies within that
+                                     rounding of 1e-4.  It pays on frames with a few crowded tiles (an
+                                     800x800 close-up whose longest list holds 33,000 pairs: forward
+                                     0.25 -> 0.18 ms) and costs on frames without them, where the chunks
+                                     past the heads are mostly behind every pixel's stop (800x800,
+                                     409,660 splats, 3.7M pairs: 0.118 -> 0.148 ms). */
 };
 
 typedef struct gsr_ctx gsr_ctx;
