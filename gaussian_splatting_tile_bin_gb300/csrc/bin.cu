@@ -149,6 +149,29 @@ __device__ __forceinline__ void block_and_or_into(unsigned long long a, unsigned
     }
 }
 
+// The block's AND / OR of (a, o), valid in thread 0.
+__device__ __forceinline__ void block_and_or(unsigned long long &a, unsigned long long &o, unsigned long long *s_and,
+                                             unsigned long long *s_or)
+{
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) {
+        a &= __shfl_xor_sync(kFull, a, k);
+        o |= __shfl_xor_sync(kFull, o, k);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s_and[threadIdx.x >> 5] = a;
+        s_or[threadIdx.x >> 5] = o;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < 8; ++w) {
+            a &= s_and[w];
+            o |= s_or[w];
+        }
+    }
+    __syncthreads();
+}
+
 // Lanes in `members` whose kWidth-bit digit equals this lane's, from one
 // ballot per bit.  Every lane of the warp calls this together.
 template <int kWidth>
@@ -207,16 +230,6 @@ __host__ __device__ __forceinline__ int field_pass(unsigned long long diff, int 
 }
 
 // Clears the binning's scalars and the radix digit totals of both sorts.
-__global__ void k_init_scalars(unsigned long long *__restrict__ scalars, uint32_t *__restrict__ radix_totals,
-                               int ntotals)
-{
-    grid_dependency_begin();
-    for (int i = threadIdx.x; i < ntotals; i += blockDim.x) radix_totals[i] = 0u;
-    if (threadIdx.x != 0) return;
-    for (int k = 0; k < kScalarCount; ++k) scalars[k] = 0ull;
-    scalars[kScalarDepthAnd] = ~0ull;
-    scalars[kScalarKeyAnd] = ~0ull;
-}
 
 // True in the one block that finishes last: every block calls this after it has
 // written its per-block results, and the last block then reads all of them
@@ -263,10 +276,20 @@ __device__ unsigned long long block_scan_inplace_256(unsigned long long *__restr
 __global__ void __launch_bounds__(kBinBlock)
 k_count(const float *__restrict__ splats, const float *__restrict__ depths, int n, int tiles_x,
         int tiles_y, uint2 *__restrict__ rects, unsigned long long *__restrict__ blk_pairs,
-        unsigned long long *__restrict__ blk_emitting, unsigned long long *__restrict__ scalars,
-        unsigned long long capacity)
+        unsigned long long *__restrict__ blk_emitting, unsigned long long *__restrict__ blk_and,
+        unsigned long long *__restrict__ blk_or, unsigned long long *__restrict__ scalars,
+        uint32_t *__restrict__ radix_totals, int ntotals, unsigned long long capacity)
 {
     grid_dependency_begin();
+    // Block 0 clears what the binning's later kernels accumulate into.
+    if (blockIdx.x == 0) {
+        for (int k = threadIdx.x; k < ntotals; k += kBinBlock) radix_totals[k] = 0u;
+        if (threadIdx.x == 0) {
+            scalars[kScalarTicketSums] = 0ull;
+            scalars[kScalarKeyAnd] = ~0ull;
+            scalars[kScalarKeyOr] = 0ull;
+        }
+    }
     __shared__ float s_rec[kBinBlock * 9];
     __shared__ unsigned long long s_and[8], s_or[8];
     __shared__ unsigned long long ws[8];
@@ -300,18 +323,30 @@ k_count(const float *__restrict__ splats, const float *__restrict__ depths, int 
         blk_pairs[blockIdx.x] = pairs_total;
         blk_emitting[blockIdx.x] = emit_total;
     }
-    block_and_or_into(c > 0 ? (unsigned long long)db : ~0ull, c > 0 ? (unsigned long long)db : 0ull,
-                      s_and, s_or, scalars + kScalarDepthAnd);
-    // The last block: the pair total (a plain sum) and the exclusive scan of the
-    // per-block emitting counts with their total.
+    unsigned long long da = c > 0 ? (unsigned long long)db : ~0ull, dor = c > 0 ? (unsigned long long)db : 0ull;
+    block_and_or(da, dor, s_and, s_or);
+    if (threadIdx.x == 0) {
+        blk_and[blockIdx.x] = da;
+        blk_or[blockIdx.x] = dor;
+    }
+    // The last block: the pair total (a plain sum), the exclusive scan of the
+    // per-block emitting counts with their total, and the depth bits' AND / OR.
     if (last_block_done(scalars + kScalarTicketCount)) {
-        unsigned long long s = 0;
-        for (int b = threadIdx.x; b < (int)gridDim.x; b += kBinBlock) s += __ldcg(blk_pairs + b);
+        unsigned long long s = 0, a = ~0ull, o = 0ull;
+        for (int b = threadIdx.x; b < (int)gridDim.x; b += kBinBlock) {
+            s += __ldcg(blk_pairs + b);
+            a &= __ldcg(blk_and + b);
+            o |= __ldcg(blk_or + b);
+        }
         unsigned long long t;
         block_exclusive_scan_256<unsigned long long>(s, ws, &t);
         __syncthreads();
+        block_and_or(a, o, s_and, s_or);
         const unsigned long long m = block_scan_inplace_256(blk_emitting, (int)gridDim.x, ws);
         if (threadIdx.x == 0) {
+            scalars[kScalarDepthAnd] = a;
+            scalars[kScalarDepthOr] = o;
+            scalars[kScalarTicketCount] = 0ull;   // for the next binning
             // More pairs than the arena holds (or than 32-bit indices reach):
             // nothing is emitted, sorted or ranged, and every tile stays empty.
             const bool fits = t <= capacity && t <= (unsigned long long)GSR_MAX_PAIRS;
@@ -1054,10 +1089,18 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         cudaGetLastError();
         return fail(ctx, GSR_ERR_OOM, std::string("cudaMalloc failed for ") + what);
     };
-    if (!ctx->scalars &&
-        (rc = alloc_failed(device_alloc(ctx, (void **)&ctx->scalars, kScalarCount * sizeof(unsigned long long)),
-                           "binning scalars")))
-        return rc;
+    if (!ctx->scalars) {
+        if ((rc = alloc_failed(device_alloc(ctx, (void **)&ctx->scalars, kScalarCount * sizeof(unsigned long long)),
+                               "binning scalars")))
+            return rc;
+        // k_count's ticket starts at zero; k_count resets it after each use
+        if ((rc = cuda_check(ctx, cudaMemset(ctx->scalars, 0, kScalarCount * sizeof(unsigned long long)),
+                             "cudaMemset"))) {
+            cudaFree(ctx->scalars);
+            ctx->scalars = nullptr;
+            return rc;
+        }
+    }
     if (!ctx->host_total &&
         (rc = alloc_failed(cudaHostAlloc(&ctx->host_total, 4 * sizeof(unsigned long long), cudaHostAllocDefault),
                            "pinned pair count")))
@@ -1073,12 +1116,15 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
         ctx->cap_splats = 0;  // regrow the rectangles below to the same capacity
         if ((rc = grow(ctx, &ctx->rects, &ctx->cap_splats, cap, 1, "tile rectangles"))) return rc;
     }
-    // Three per-block arrays: [0, c) pair sums, [c, 2c) emitting counts then
-    // offsets, [2c, 3c) pair sums in depth order then offsets.
-    if ((rc = grow(ctx, &ctx->blk_sums, &ctx->cap_blocks, (size_t)nblk, 3, "block sums"))) return rc;
+    // Five per-block arrays: [0, c) pair sums, [c, 2c) emitting counts then
+    // offsets, [2c, 3c) pair sums in depth order then offsets, [3c, 5c) the
+    // AND / OR of the emitting splats' depth bits.
+    if ((rc = grow(ctx, &ctx->blk_sums, &ctx->cap_blocks, (size_t)std::max(nblk, 1), 5, "block sums"))) return rc;
     unsigned long long *blk_pairs = ctx->blk_sums;
     unsigned long long *blk_emit = ctx->blk_sums + ctx->cap_blocks;
     unsigned long long *blk_sorted = ctx->blk_sums + 2 * ctx->cap_blocks;
+    unsigned long long *blk_and = ctx->blk_sums + 3 * ctx->cap_blocks;
+    unsigned long long *blk_or = ctx->blk_sums + 4 * ctx->cap_blocks;
     // Per tile: {start, end}, then the launch order after all tiles' ranges.
     if ((rc = grow(ctx, &ctx->ranges, &ctx->cap_tiles, num_tiles, 3, "tile ranges"))) return rc;
     ctx->tile_order = ctx->ranges + 2 * ctx->cap_tiles;
@@ -1104,11 +1150,11 @@ int bin_splats(gsr_ctx *ctx, const float *splats, const float *depths, int32_t n
     // 1. counts, totals; without a reservation, read the pair total, the
     //    emitting count and the depth bits' AND / OR (the one host sync).
     uint64_t total = 0, emitting = 0;
-    GSR_LAUNCH(ctx, k_init_scalars, dim3(1), dim3(256), stream, ctx->scalars, ctx->radix_totals, 2 * 4 * 256);
+    // (with no splats, one block still writes the zero counts)
+    GSR_LAUNCH(ctx, k_count, dim3(std::max(nblk, 1)), dim3(kBinBlock), stream, splats, depths, n, tiles_x, tiles_y,
+               ctx->rects, blk_pairs, blk_emit, blk_and, blk_or, ctx->scalars, ctx->radix_totals, 2 * 4 * 256,
+               sync_free ? (unsigned long long)ctx->cap_pairs : (unsigned long long)GSR_MAX_PAIRS);
     if (n > 0) {
-        GSR_LAUNCH(ctx, k_count, dim3(nblk), dim3(kBinBlock), stream, splats, depths, n, tiles_x, tiles_y,
-                   ctx->rects, blk_pairs, blk_emit, ctx->scalars,
-                   sync_free ? (unsigned long long)ctx->cap_pairs : (unsigned long long)GSR_MAX_PAIRS);
         if (!sync_free) {
             // Pair total, emitting count and the AND / OR of the emitting
             // splats' depth bits (scalar slots 0..3).
