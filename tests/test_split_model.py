@@ -1,16 +1,19 @@
-"""A CPU model of the heavy-tile split of the forward (not a kernel yet),
-against the oracle.
+"""A CPU model of the heavy-tile split, against the oracle.
 
-Splitting one tile's list across CTAs ("next" row 3: several CTAs per long
-list, merged through the (C, T) state) has to keep the early stop
-(T < 1e-4).  A segment cannot know the transmittance in front of it, so the
-model's segments composite from T = 1 without stopping and record their colour
-C_k, their transmittance product P_k and their last composite.  A merge then
-walks each pixel's segments in order.  While T_in P_k stays at or above 1e-4,
-no stop can fall inside segment k (the running product only decreases), so
-(C, T) <- (C + T_in C_k, T_in P_k).  Otherwise the pixel stops inside segment
-k, and the merge replays that segment from (T_in, C) with the sequential
-arithmetic.
+Splitting one tile's list across CTAs has to keep the early stop (T < 1e-4).
+A chunk cannot know the transmittance in front of it, so chunks composite
+from T = 1 without stopping and record their colour C_k, their transmittance
+product P_k and their last composite.  A merge then walks each pixel's chunks
+in order.  While T_in P_k stays at or above 1e-4, no stop can fall inside
+chunk k (the running product only decreases), so (C, T) <- (C + T_in C_k,
+T_in P_k).  Otherwise the pixel stops inside chunk k, which is replayed.
+
+Two models: the design study (`_split_forward`: segments of any length from
+the list's start, the stopping segment replayed with the sequential
+arithmetic) and the algorithm the split forward kernels run
+(`_kernel_split_forward`: k_forward's exact head, k_forward_chunk's chunks of
+512 with the head's transmittance bounding their start, k_forward_replay's
+replay on T_in times the running product, and the assembly).
 
 Every step is float32 in the oracle's operation order, vectorised over a
 tile's 256 pixels.  The model reproduces the oracle bit for bit when it does
@@ -106,6 +109,94 @@ def _split_forward(splats, lst, px, py, inside, seg_len, bounds=None):
     return C, T, last, replays
 
 
+def _kernel_split_forward(splats, lst, px, py, inside, head, chunk=512):
+    """The split forward as its kernels compute it, for one tile whose list
+    is longer than `head` (a multiple of `chunk`): returns (C, T, last, the
+    stop chunk per pixel or -1)."""
+    n = px.size
+    # k_forward: the exact head
+    C = np.zeros((3, n), F)
+    T = np.ones(n, F)
+    last = np.zeros(n, np.int64)
+    done = ~inside
+    _sequential(splats, lst[:head], 0, px, py, C, T, last, done)
+    t_head = T.copy()
+    nchunks = (len(lst) + chunk - 1) // chunk
+    first = head // chunk
+    # k_forward_chunk: every chunk past the head from T = 1, a pixel leaving
+    # once t_head times its product falls below the threshold
+    Ck, Pk, Lk = [], [], []
+    for k in range(first, nchunks):
+        seg = lst[k * chunk:(k + 1) * chunk]
+        c = np.zeros((3, n), F)
+        P = np.ones(n, F)
+        lk = np.zeros(n, np.int64)
+        gone = done.copy()
+        for j, i in enumerate(seg):
+            s = splats[i]
+            alpha, ok = _alpha(s, px, py)
+            ok &= ~gone
+            nxt = (P * (F(1) - alpha)).astype(F)
+            stop = ok & ((t_head * nxt).astype(F) < T_MIN)
+            comp = ok & ~stop
+            w = (alpha * P).astype(F)
+            for ch in range(3):
+                c[ch] = np.where(comp, c[ch] + s[5 + ch] * w, c[ch]).astype(F)
+            P = np.where(comp | stop, nxt, P)
+            lk = np.where(comp, j + 1, lk)
+            gone |= stop
+        Ck.append(c)
+        Pk.append(P)
+        Lk.append(lk)
+    # the chunks' prepare: the first chunk at whose end the product chain
+    # falls below the threshold holds the stop
+    stop_chunk = np.full(n, -1, np.int64)
+    T_at = np.zeros((nchunks - first, n), F)
+    Tr = t_head.copy()
+    live = ~done
+    for q, k in enumerate(range(first, nchunks)):
+        T_at[q] = Tr
+        Tn = (Tr * Pk[q]).astype(F)
+        st = live & (Tn < T_MIN)
+        stop_chunk = np.where(st, k, stop_chunk)
+        adv = live & ~st
+        for ch in range(3):
+            C[ch] = np.where(adv, C[ch] + (Tr * Ck[q][ch]).astype(F), C[ch]).astype(F)
+        last = np.where(adv & (Lk[q] > 0), k * chunk + Lk[q], last)
+        Tr = np.where(adv, Tn, Tr)
+        live &= ~st
+    T = np.where(~done, Tr, T)
+    # k_forward_replay: the stopping chunk from its start transmittance, on
+    # t_in times the running product
+    for k in np.unique(stop_chunk[stop_chunk >= 0]):
+        mine = stop_chunk == k
+        t_in = T_at[k - first]
+        seg = lst[k * chunk:(k + 1) * chunk]
+        c = np.zeros((3, n), F)
+        P = np.ones(n, F)
+        lr = np.zeros(n, np.int64)
+        gone = ~mine
+        for j, i in enumerate(seg):
+            s = splats[i]
+            alpha, ok = _alpha(s, px, py)
+            ok &= ~gone
+            nxt = (P * (F(1) - alpha)).astype(F)
+            stop = ok & ((t_in * nxt).astype(F) < T_MIN)
+            comp = ok & ~stop
+            w = (alpha * P).astype(F)
+            for ch in range(3):
+                c[ch] = np.where(comp, c[ch] + s[5 + ch] * w, c[ch]).astype(F)
+            P = np.where(comp, nxt, P)
+            lr = np.where(comp, j + 1, lr)
+            gone |= stop
+        assert gone[mine].all(), "a replay must stop inside its chunk"
+        for ch in range(3):
+            C[ch] = np.where(mine, C[ch] + (t_in * c[ch]).astype(F), C[ch]).astype(F)
+        T = np.where(mine, (t_in * P).astype(F), T)
+        last = np.where(mine & (lr > 0), k * chunk + lr, last)
+    return C, T, last, stop_chunk
+
+
 def _heavy_tiles(ranges, count):
     lengths = ranges[:, 1].astype(np.int64) - ranges[:, 0].astype(np.int64)
     return np.argsort(-lengths, kind="stable")[:count]
@@ -163,6 +254,34 @@ def test_split_forward_matches_the_oracle(lego_final, seg_len):
         assert not (bad & ~knife).any(), (tile, np.nonzero(bad & ~knife)[0][:5])
         assert d[inside & ~knife].max() <= 1e-5
     assert total_replays > 0    # the stop fell inside a segment somewhere
+
+
+@pytest.mark.parametrize("name,tiles", [("lego_far", 3), ("lego_final", 2)])
+def test_kernel_split_forward_matches_the_oracle(name, tiles):
+    """The split forward's algorithm with a 1,024-position head and 512-position
+    chunks on the longest lists of the crowded close-up and of the Lego-final
+    set: within the forward tolerance of the oracle, last_contrib moved only at
+    knife-edges, and the replays always find the stop inside their chunk."""
+    wl = gen.make(name)
+    _, idx, ranges = oracle.bin_splats(wl.splats, wl.depths, wl.width, wl.height)
+    ranges = ranges.reshape(-1, 2)
+    f = oracle.forward(wl.splats, idx, ranges, wl.width, wl.height, eps_alpha=EPS_ALPHA, sigma_ulps=0.0)
+    splats = wl.splats.astype(F)
+    stops = 0
+    for tile in _heavy_tiles(ranges, tiles):
+        tile = int(tile)
+        px, py, inside, p = _tile_pixels(wl, tile)
+        lst = idx[ranges[tile, 0]:ranges[tile, 1]]
+        assert len(lst) > 1024 + 512
+        C, T, last, stop_chunk = _kernel_split_forward(splats, lst, px, py, inside, 1024)
+        stops += int((stop_chunk >= 0).sum())
+        ref_c, ref_t = f["out"][p, :3], f["final_T"][p]
+        d = np.maximum(np.abs(C.T - ref_c).max(axis=1), np.abs(T - ref_t))
+        knife = f["margin"][p] < 1.0
+        bad = inside & ((d > 1e-5) | (last != f["last"][p].astype(np.int64)))
+        assert not (bad & ~knife).any(), (tile, np.nonzero(bad & ~knife)[0][:5])
+        assert d[inside & ~knife].max() <= 1e-5
+    assert stops > 0    # some pixels stop past their head, inside a chunk
 
 
 # --- backward ------------------------------------------------------------------
