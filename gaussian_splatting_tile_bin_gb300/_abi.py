@@ -119,6 +119,10 @@ class Context:
             raise GsrError(rc, lib.gsr_last_error(self._h).decode())
 
     def set_option(self, name: str, value: bool):
+        """Sets a GSR_OPT_* switch by its name in OPTIONS (the header documents
+        each): "split" (backward segments of crowded tiles, on by default),
+        "split_forward" (the forward's chunks past a head, off by default),
+        "deterministic", "bwd_per_splat", and the A/B switches."""
         self._check(lib.gsr_set_option(self._h, OPTIONS[name], int(bool(value))))
 
     def launch_count(self) -> int:
